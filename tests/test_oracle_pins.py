@@ -1,0 +1,348 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself.
+
+* fp16 conversion: every one of the 65 536 bit patterns against numpy's
+  float16 decoding, round trips, numpy's float64->float16 rounding on random
+  and exactly-halfway values, and hand-worked IEEE-754 binary16 cases.
+* GELU: textbook standard-normal CDF values (tests/golden), a numerical
+  integral of the normal density (independent of erf), the odd-part identity
+  GELU(x) - GELU(-x) = x, and the large-|x| limits.
+* GEMM: closed forms (identity, permutation, rank-1, zero K tail, small
+  integers where every step is exact), numpy's fp64 matmul, and a brute-force
+  pure-Python triple loop on tiny shapes.
+* Planted mistakes (a transposed operand, a dropped bias) must fail the
+  closed forms.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- fp16 conversion
+
+def test_half_to_double_exhaustive(oracle_mod):
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    got = oracle_mod.half_to_double(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # signs of zeros and infinities
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_half_round_trip_identity(oracle_mod):
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    vals = bits.view(np.float16).astype(np.float64)
+    keep = ~np.isnan(vals)
+    back = oracle_mod.double_to_half(vals[keep])
+    assert np.array_equal(back, bits[keep])
+
+
+def test_double_to_half_matches_numpy_random(oracle_mod):
+    rng = np.random.default_rng(7)
+    x = np.concatenate([
+        rng.standard_normal(200_000) * 10.0 ** rng.integers(-9, 6, 200_000),
+        rng.uniform(-70000, 70000, 50_000),
+        rng.uniform(-1e-6, 1e-6, 50_000),           # subnormal range
+    ])
+    got = oracle_mod.double_to_half(x)
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_double_to_half_exact_halfway_points(oracle_mod):
+    # midpoints between consecutive finite fp16 values must tie to even
+    bits = np.arange(0, 0x7bff, dtype=np.uint16)            # positive finite, < max
+    lo = bits.view(np.float16).astype(np.float64)
+    hi = (bits + 1).view(np.float16).astype(np.float64)
+    mid = (lo + hi) / 2.0                                     # exact in double
+    got = oracle_mod.double_to_half(mid)
+    even = np.where(bits % 2 == 0, bits, bits + 1).astype(np.uint16)
+    assert np.array_equal(got, even)
+    assert np.array_equal(oracle_mod.double_to_half(-mid), even | np.uint16(0x8000))
+    # and numpy agrees
+    assert np.array_equal(got, mid.astype(np.float16).view(np.uint16))
+
+
+@pytest.mark.parametrize("x, expect", [
+    (1.0 + 2.0 ** -11, 0x3C00),          # tie -> even (1.0)
+    (1.0 + 3 * 2.0 ** -11, 0x3C02),      # tie -> even (1 + 2^-9)
+    (65504.0, 0x7BFF),                   # max finite
+    (65519.999, 0x7BFF),
+    (65520.0, 0x7C00),                   # tie at the top rounds to infinity
+    (-1e6, 0xFC00),
+    (2.0 ** -24, 0x0001),                # smallest subnormal
+    (2.0 ** -25, 0x0000),                # tie between 0 and 2^-24 -> even (0)
+    (3 * 2.0 ** -26, 0x0001),            # 0.75 quantum -> 1 quantum
+    (2.0 ** -14, 0x0400),                # smallest normal
+    (2.0 ** -14 - 2.0 ** -25, 0x0400),   # tie between 0x03ff and 0x0400 -> even
+    (-0.0, 0x8000),
+    (float("inf"), 0x7C00),
+])
+def test_double_to_half_hand_cases(oracle_mod, x, expect):
+    assert int(oracle_mod.double_to_half(np.array([x]))[0]) == expect
+
+
+def test_nan_maps_to_nan(oracle_mod):
+    h = int(oracle_mod.double_to_half(np.array([float("nan")]))[0])
+    assert (h & 0x7C00) == 0x7C00 and (h & 0x03FF) != 0
+
+
+# ---------------------------------------------------------------- epilogues
+
+def _golden_phi():
+    rows = []
+    with open(os.path.join(GOLDEN, "normal_cdf_table.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                x, p = line.split()
+                rows.append((float(x), float(p)))
+    return rows
+
+
+def test_gelu_textbook_phi_values(oracle_mod):
+    for x, phi in _golden_phi():
+        assert oracle_mod.epilogue_scalar(x, "bias_gelu_erf") == pytest.approx(x * phi, abs=1e-13)
+
+
+def _simpson(f, a, b, n):
+    h = (b - a) / n
+    s = 0.0
+    for i in range(n + 1):
+        w = 1 if i in (0, n) else (4 if i % 2 else 2)
+        s += w * f(a + i * h)
+    return s * h / 3.0
+
+
+def _phi_by_simpson(x, n=40000):
+    # Phi(x) from the normal density phi(t) = exp(-t^2/2)/sqrt(2 pi) alone:
+    # x >= 0: 1/2 + integral_0^x phi; x < 0: integral_{x-30}^x phi (no cancellation)
+    phi = lambda t: math.exp(-0.5 * t * t) / math.sqrt(2.0 * math.pi)
+    if x >= 0:
+        return 0.5 + _simpson(phi, 0.0, x, n)
+    return _simpson(phi, x - 30.0, x, 4 * n)
+
+
+@pytest.mark.parametrize("x", [-5.0, -2.7, -1.3, -0.4, 0.1, 0.77, 1.5, 3.3, 6.0])
+def test_gelu_against_normal_density_integral(oracle_mod, x):
+    assert oracle_mod.epilogue_scalar(x, "bias_gelu_erf") == pytest.approx(
+        x * _phi_by_simpson(x), rel=1e-11, abs=1e-14)
+
+
+def test_gelu_identities(oracle_mod):
+    g = lambda v: oracle_mod.epilogue_scalar(v, "bias_gelu_erf")
+    assert g(0.0) == 0.0
+    for x in np.linspace(-8, 8, 161):
+        assert g(x) - g(-x) == pytest.approx(x, abs=1e-14)
+    # GELU(x) -> x above ~6 and -> 0 below ~-6, exactly once rounded to fp16
+    xs = np.array([6.0, 7.5, 12.0, 100.0])
+    ys = np.array([g(v) for v in xs])
+    assert np.array_equal(oracle_mod.double_to_half(ys), xs.astype(np.float16).view(np.uint16))
+    assert abs(g(-9.0)) < 1e-17
+
+
+def test_relu_and_identity_epilogues(oracle_mod):
+    for x in (-3.5, -1e-30, 0.0, 2.25, 1e6):
+        assert oracle_mod.epilogue_scalar(x, "bias_relu") == max(x, 0.0)
+        assert oracle_mod.epilogue_scalar(x, "bias") == x
+        assert oracle_mod.epilogue_scalar(x, "none") == x
+    assert math.isnan(oracle_mod.epilogue_scalar(float("nan"), "bias_relu"))
+
+
+# ---------------------------------------------------------------- GEMM closed forms
+
+def _rand16(rng, shape, scale=1.0):
+    return (rng.standard_normal(shape) * scale).astype(np.float16)
+
+
+def test_identity_B(oracle_mod):
+    rng = np.random.default_rng(1)
+    M, K = 37, 40
+    A = _rand16(rng, (M, K), 3.0)
+    eye = np.eye(K, dtype=np.float16)
+    bias = _rand16(rng, (K,))
+    assert np.array_equal(oracle_mod.gemm(A, eye, None, "none").view(np.uint16), A.view(np.uint16))
+    ref = (A.astype(np.float64) + bias.astype(np.float64)).astype(np.float16)
+    assert np.array_equal(oracle_mod.gemm(A, eye, bias, "bias").view(np.uint16), ref.view(np.uint16))
+
+
+def test_permutation_B(oracle_mod):
+    rng = np.random.default_rng(2)
+    M, K = 19, 33
+    A = _rand16(rng, (M, K))
+    perm = rng.permutation(K)
+    P = np.zeros((K, K), np.float16)
+    P[perm, np.arange(K)] = 1.0           # C[i, j] = A[i, perm[j]]
+    C = oracle_mod.gemm(A, P, None, "none")
+    assert np.array_equal(C.view(np.uint16), A[:, perm].view(np.uint16))
+
+
+def test_rank1(oracle_mod):
+    rng = np.random.default_rng(3)
+    M, N, K = 21, 45, 17
+    u, v = _rand16(rng, M), _rand16(rng, N)
+    A = np.zeros((M, K), np.float16)
+    B = np.zeros((K, N), np.float16)
+    A[:, 0] = u
+    B[0, :] = v
+    ref = np.outer(u.astype(np.float64), v.astype(np.float64)).astype(np.float16)  # products exact
+    assert np.array_equal(oracle_mod.gemm(A, B, None, "none").view(np.uint16), ref.view(np.uint16))
+
+
+def test_zero_k_tail(oracle_mod):
+    rng = np.random.default_rng(4)
+    M, N, K = 13, 29, 24
+    A, B, bias = _rand16(rng, (M, K)), _rand16(rng, (K, N)), _rand16(rng, N)
+    A2 = np.concatenate([A, np.zeros((M, 9), np.float16)], axis=1)
+    B2 = np.concatenate([B, np.zeros((9, N), np.float16)], axis=0)
+    for epi in ("none", "bias", "bias_relu", "bias_gelu_erf"):
+        b = None if epi == "none" else bias
+        assert np.array_equal(oracle_mod.gemm(A, B, b, epi).view(np.uint16),
+                              oracle_mod.gemm(A2, B2, b, epi).view(np.uint16))
+
+
+@pytest.mark.parametrize("epi", ["none", "bias", "bias_relu"])
+def test_integer_inputs_exact(oracle_mod, epi):
+    rng = np.random.default_rng(5)
+    M, N, K = 40, 56, 300
+    Ai = rng.integers(-2, 3, (M, K))
+    Bi = rng.integers(-2, 3, (K, N))
+    bi = rng.integers(-8, 9, N)
+    ref = Ai @ Bi + (0 if epi == "none" else bi)
+    if epi == "bias_relu":
+        ref = np.maximum(ref, 0)
+    assert np.abs(ref).max() <= 2048
+    C = oracle_mod.gemm(Ai.astype(np.float16), Bi.astype(np.float16),
+                        None if epi == "none" else bi.astype(np.float16), epi)
+    assert np.array_equal(C.astype(np.int64), ref)
+
+
+def test_matches_numpy_fp64_matmul(oracle_mod):
+    rng = np.random.default_rng(6)
+    M, N, K = 64, 96, 200
+    A, B, bias = _rand16(rng, (M, K)), _rand16(rng, (K, N)), _rand16(rng, N)
+    _, y = oracle_mod.gemm(A, B, bias, "bias", want_f64=True)
+    ref = A.astype(np.float64) @ B.astype(np.float64) + bias.astype(np.float64)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def _brute(A, B, bias, epi):
+    M, K = A.shape
+    N = B.shape[1]
+    out = np.zeros((M, N), np.float64)
+    for i in range(M):
+        for j in range(N):
+            s = 0.0
+            for k in range(K):
+                s += float(A[i, k]) * float(B[k, j])
+            x = s + (float(bias[j]) if epi != "none" else 0.0)
+            if epi == "bias_relu":
+                x = max(x, 0.0)
+            elif epi == "bias_gelu_erf":
+                x = 0.5 * x * (1.0 + math.erf(x / math.sqrt(2.0)))
+            out[i, j] = x
+    return out.astype(np.float16)
+
+
+def test_brute_force_tiny(oracle_mod):
+    rng = np.random.default_rng(8)
+    epis = ["none", "bias", "bias_relu", "bias_gelu_erf"]
+    n = 0
+    for M in (1, 2, 3, 5, 8):
+        for N in (1, 2, 4, 7):
+            for K in (1, 3, 6, 8):
+                epi = epis[n % 4]
+                n += 1
+                A, B, bias = _rand16(rng, (M, K)), _rand16(rng, (K, N)), _rand16(rng, N)
+                b = None if epi == "none" else bias
+                got = oracle_mod.gemm(A, B, b, epi)
+                assert np.array_equal(got.view(np.uint16), _brute(A, B, bias, epi).view(np.uint16)), (M, N, K, epi)
+
+
+def test_rows_and_elems_agree(oracle_mod):
+    rng = np.random.default_rng(9)
+    M, N, K = 50, 70, 130
+    A, B, bias = _rand16(rng, (M, K)), _rand16(rng, (K, N)), _rand16(rng, N)
+    full = oracle_mod.gemm(A, B, bias, "bias_gelu_erf")
+    ii, jj = workloads.sample_coords(11, M, N, 300)
+    el = oracle_mod.gemm_elems(A, B, bias, "bias_gelu_erf", ii, jj)
+    assert np.array_equal(el.view(np.uint16), full[ii, jj].view(np.uint16))
+    rows = np.array([0, 17, 49])
+    assert np.array_equal(oracle_mod.gemm_rows(A, B, bias, "bias_gelu_erf", rows).view(np.uint16),
+                          full[rows].view(np.uint16))
+
+
+def test_k_zero_is_epilogue_of_bias(oracle_mod):
+    bias = np.array([-2.0, -0.5, 0.0, 1.0, 3.0], np.float16)
+    A = np.zeros((3, 0), np.float16)
+    B = np.zeros((0, 5), np.float16)
+    C = oracle_mod.gemm(A, B, bias, "bias_relu")
+    assert np.array_equal(C, np.tile(np.maximum(bias, 0), (3, 1)))
+    assert np.all(oracle_mod.gemm(A, B, None, "none") == 0)
+
+
+def test_bad_arguments_rejected(oracle_mod):
+    A = np.zeros((2, 3), np.float16)
+    B = np.zeros((3, 4), np.float16)
+    with pytest.raises(ValueError):
+        oracle_mod.gemm(A, B, None, "bias")            # bias missing
+    with pytest.raises(ValueError):
+        oracle_mod.gemm_rows(A, B, None, "none", [5])   # row out of range
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+def test_planted_transpose_is_caught(oracle_mod):
+    # feeding B^T (a transposed operand) must break the permutation closed form
+    rng = np.random.default_rng(10)
+    K = 24
+    A = _rand16(rng, (6, K))
+    perm = rng.permutation(K)
+    P = np.zeros((K, K), np.float16)
+    P[perm, np.arange(K)] = 1.0
+    C = oracle_mod.gemm(A, np.ascontiguousarray(P.T), None, "none")
+    assert not np.array_equal(C.view(np.uint16), A[:, perm].view(np.uint16))
+
+
+def test_planted_dropped_bias_is_caught(oracle_mod):
+    rng = np.random.default_rng(11)
+    A = _rand16(rng, (4, 8))
+    eye = np.eye(8, dtype=np.float16)
+    bias = np.full(8, 0.5, np.float16)
+    ref = (A.astype(np.float64) + 0.5).astype(np.float16)
+    dropped = oracle_mod.gemm(A, eye, bias, "none")      # "none" ignores the bias
+    assert not np.array_equal(dropped.view(np.uint16), ref.view(np.uint16))
+
+
+# ---------------------------------------------------------------- input generator
+
+def test_generator_is_deterministic_and_shaped():
+    w = workloads.WORKLOADS["gemm256"]
+    A1, B1, b1 = w.make()
+    A2, B2, b2 = w.make()
+    assert A1.dtype == np.float16 and A1.shape == (256, 256) and b1.shape == (256,)
+    assert np.array_equal(A1.view(np.uint16), A2.view(np.uint16))
+    assert np.array_equal(B1.view(np.uint16), B2.view(np.uint16))
+    assert not np.array_equal(A1.view(np.uint16), B1.view(np.uint16))
+    # N(0,1)/16 statistics
+    a = A1.astype(np.float64).ravel()
+    assert abs(a.mean()) < 0.002 and abs(a.std() - 1 / 16) < 0.002
+    u = workloads.fp16_tensor((100000,), "uniform", 1.0, 4, 2).astype(np.float64)
+    assert u.min() >= -1 and u.max() <= 1 and abs(u.mean()) < 0.01 and abs(u.var() - 1 / 3) < 0.01
+
+
+def test_generator_is_counter_based():
+    # any slice of a stream equals the same slice of a longer draw
+    full = workloads.raw_draws(3, 1, 0, 1000)
+    assert np.array_equal(full[500:600], workloads.raw_draws(3, 1, 500, 100))
+    # first splitmix64 output for state 0 is the published value
+    z = workloads._mix(np.array([0x9E3779B97F4A7C15], dtype=np.uint64))[0]
+    assert int(z) == 0xE220A8397B1DCDAF
