@@ -1,0 +1,127 @@
+"""Fused fp16 tensor-core GEMM for GB300:  C = epilogue(A @ B + bias).
+
+A thin ctypes binding over the C ABI in include/gemm_f16.h.  It only
+marshals arguments (device pointers, sizes, the current CUDA stream); every
+step of the computation runs in the library's CUDA kernels.  PyTorch serves
+for device memory and streams.  There is no fallback: if the compiled
+library is missing, importing this package fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libgemm_f16.so")
+
+GEMM_EPI_NONE, GEMM_EPI_BIAS, GEMM_EPI_BIAS_RELU, GEMM_EPI_BIAS_GELU_ERF = 0, 1, 2, 3
+EPILOGUES = {"none": GEMM_EPI_NONE, "bias": GEMM_EPI_BIAS, "bias_relu": GEMM_EPI_BIAS_RELU,
+             "bias_gelu_erf": GEMM_EPI_BIAS_GELU_ERF}
+GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED_DEVICE, GEMM_ERR_MISALIGNED = 0, 1, 2, 3
+GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT, GEMM_ERR_NO_MEMORY = 4, 5, 6
+
+EXPORTS = ("gemm_f16", "gemm_f16_status_string", "gemm_f16_last_cuda_error", "gemm_f16_debug_status",
+           "gemm_f16_release_workspace", "gemm_f16_plan", "gemm_f16_selftest_timeout")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
+                      "or `python dense_fp16_tensor_tma_gb300/build.py`")
+
+lib = ctypes.CDLL(LIB_PATH)
+_vp, _i64, _int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+lib.gemm_f16.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
+lib.gemm_f16.restype = _int
+lib.gemm_f16_status_string.argtypes = [_int]
+lib.gemm_f16_status_string.restype = ctypes.c_char_p
+lib.gemm_f16_last_cuda_error.restype = _int
+lib.gemm_f16_debug_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
+lib.gemm_f16_debug_status.restype = _int
+lib.gemm_f16_release_workspace.restype = _int
+lib.gemm_f16_plan.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, ctypes.POINTER(ctypes.c_int64)]
+lib.gemm_f16_plan.restype = _int
+lib.gemm_f16_selftest_timeout.argtypes = [_vp, ctypes.c_uint32]
+lib.gemm_f16_selftest_timeout.restype = _int
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, where: str = "gemm_f16"):
+        self.status = status
+        msg = gemm_f16_status_string(status)
+        if status == GEMM_ERR_CUDA:
+            msg += f" (cudaError {lib.gemm_f16_last_cuda_error()})"
+        super().__init__(f"{where}: {msg}")
+
+
+def gemm_f16_status_string(status: int) -> str:
+    return lib.gemm_f16_status_string(int(status)).decode()
+
+
+def _epi(epilogue) -> int:
+    return EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def gemm_f16_ptr(a_ptr: int, b_ptr: int, bias_ptr: int, c_ptr: int, M: int, N: int, K: int,
+                 epilogue=GEMM_EPI_NONE, stream: int = 0) -> int:
+    """Raw C-ABI call: device addresses as integers; returns the status code."""
+    return lib.gemm_f16(a_ptr or None, b_ptr or None, bias_ptr or None, c_ptr or None,
+                        int(M), int(N), int(K), _epi(epilogue), stream or None)
+
+
+def gemm_f16(A, B, bias, C, epilogue="none", stream=None):
+    """C = epilogue(A @ B + bias) into the preallocated fp16 CUDA tensor C.
+
+    A [M,K], B [K,N], C [M,N] and bias [N] (or None for "none") are
+    contiguous torch.float16 CUDA tensors on the current device.  Enqueued on
+    `stream` (default: torch's current stream); raises GemmError on a nonzero
+    status.
+    """
+    import torch
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError(f"shape mismatch: A {tuple(A.shape)}, B {tuple(B.shape)}, C {tuple(C.shape)}")
+    for name, t in (("A", A), ("B", B), ("C", C)) + ((("bias", bias),) if bias is not None else ()):
+        if t.dtype != torch.float16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float16 CUDA tensor")
+    if bias is not None and tuple(bias.shape) != (N,):
+        raise ValueError(f"bias must have shape ({N},)")
+    st = lib.gemm_f16(A.data_ptr() or None, B.data_ptr() or None,
+                      bias.data_ptr() if bias is not None else None, C.data_ptr() or None,
+                      M, N, K, _epi(epilogue), _stream_handle(stream))
+    if st != GEMM_OK:
+        raise GemmError(st)
+    return C
+
+
+def gemm_f16_plan(M, N, K, epilogue="none", num_sms=152, a_addr=256, b_addr=256, c_addr=256,
+                  bias_addr=256):
+    """Host-only: the plan gemm_f16 would pick (dict), without touching a device."""
+    out = (ctypes.c_int64 * 8)()
+    st = lib.gemm_f16_plan(a_addr or None, b_addr or None, bias_addr or None, c_addr or None,
+                           int(M), int(N), int(K), _epi(epilogue), int(num_sms), out)
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_f16_plan")
+    keys = ("path", "tile_m", "tile_n", "stages", "ctas", "pack_a", "pack_b", "vec_store")
+    return dict(zip(keys, list(out)))
+
+
+def gemm_f16_debug_status(stream=None):
+    """Synchronise the stream; (status, raw device status word)."""
+    word = ctypes.c_uint32(0)
+    st = lib.gemm_f16_debug_status(_stream_handle(stream), ctypes.byref(word))
+    return st, word.value
+
+
+def gemm_f16_release_workspace() -> int:
+    return lib.gemm_f16_release_workspace()
+
+
+def gemm_f16_selftest_timeout(timeout_us: int = 1000, stream=None) -> int:
+    return lib.gemm_f16_selftest_timeout(_stream_handle(stream), int(timeout_us))

@@ -1,0 +1,336 @@
+// Fused fp16 GEMM kernels for sm_103a:  C = epilogue(A.B + bias).
+//
+// The method: "writing-tilelang-kernels", Kernel Anatomy / GEMM (Minimal)
+// (tile loop over K with global->shared copies of an A tile and a B tile and
+// a tensor-core tile product into a float accumulator, then one write-back),
+// and "TileLang: Write, Autotune, and Ship Fused Tensor-Core Kernels from
+// Python", Why tile-level control matters (bias + activation applied to the
+// on-chip accumulator before the single write of C).
+//
+// GB300 design (not the pages' Ampere/Hopper templates):
+//   * persistent CTAs, one per SM, walking output tiles in grouped order so
+//     that concurrently running CTAs share A row-panels and B column-panels
+//     in L2;
+//   * warp 0: TMA producer filling a STAGES-deep ring of (A, B) tiles with
+//     128-byte-swizzled boxes; OOB elements of ragged M/N/K tails arrive as
+//     zeros;
+//   * warp 1: allocates tensor memory and issues tcgen05.mma (M=128, N=BN,
+//     K=16) from one thread into one of two TMEM accumulators;
+//   * warps 2..5: epilogue, reading the accumulator with tcgen05.ld while the
+//     MMA warp already fills the other accumulator for the next tile.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace gemm_f16_dev {
+
+enum : int { EPI_NONE = 0, EPI_BIAS = 1, EPI_BIAS_RELU = 2, EPI_BIAS_GELU_ERF = 3 };
+
+__device__ unsigned int g_status;  // bounded-wait status word, read by the host
+
+constexpr int kBM = 128;                 // tile rows = MMA M = TMEM lanes
+constexpr int kBK = 64;                  // K per stage: one 128-byte swizzle row of fp16
+constexpr int kUMMA_K = 16;              // K per tcgen05.mma kind::f16
+constexpr int kThreads = 192;            // 6 warps
+constexpr uint32_t kATileBytes = kBM * kBK * 2;  // 16 KiB
+constexpr uint32_t kBBoxBytes = 64 * kBK * 2;    // one 64(N) x 64(K) box, 8 KiB
+
+template <int BN, int STAGES>
+struct SmemPlan {
+    static constexpr uint32_t kBTileBytes = BN * kBK * 2;
+    static constexpr uint32_t kA = 0;                                   // STAGES A tiles
+    static constexpr uint32_t kB = kA + STAGES * kATileBytes;           // STAGES B tiles
+    static constexpr uint32_t kBias = kB + STAGES * kBTileBytes;        // 4 warps x BN floats
+    static constexpr uint32_t kBars = kBias + 4 * BN * 4;               // mbarriers (8 B each)
+    static constexpr uint32_t kNumBars = 2 * STAGES + 2 + 2 + 1;        // full, empty, acc_full, acc_empty, drain
+    static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
+    static constexpr uint32_t kAbort = kTmemSlot + 4;
+    static constexpr uint32_t kEnd = kAbort + 4;
+    static constexpr uint32_t kDynamicBytes = kEnd + 1024;             // + alignment slack
+    static_assert(kBTileBytes % 1024 == 0 && kATileBytes % 1024 == 0, "swizzle atoms need 1 KiB alignment");
+};
+
+struct TileCoord { int m0, n0; };
+
+// Grouped rasterisation: `group_m` consecutive tile-rows are walked column by
+// column, so a wave of CTAs covers a compact group_m x (wave/group_m) block.
+__device__ __forceinline__ TileCoord tile_coord(int t, int tiles_m, int tiles_n, int group_m, int BN) {
+    const int per_group = group_m * tiles_n;
+    const int g = t / per_group;
+    const int first_m = g * group_m;
+    const int rows = min(tiles_m - first_m, group_m);
+    const int r = t - g * per_group;
+    TileCoord c;
+    c.m0 = (first_m + r % rows) * kBM;
+    c.n0 = (r / rows) * BN;
+    return c;
+}
+
+__device__ __forceinline__ float apply_act(float x, int epi) {
+    if (epi == EPI_BIAS_RELU) return fmaxf(x, 0.0f);
+    if (epi == EPI_BIAS_GELU_ERF) return 0.5f * x * (1.0f + erff(x * 0.70710678118654752440f));
+    return x;
+}
+
+struct GemmParams {
+    __half* C;
+    const __half* bias;
+    int M, N, K;
+    int ldc;
+    int epi;
+    int vec_store;       // C base 16-byte aligned and ldc % 8 == 0
+    int group_m;
+    uint64_t timeout_ns;
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+    using SP = SmemPlan<BN, STAGES>;
+    constexpr int kBoxesB = BN / 64;
+    constexpr uint32_t kIdesc = idesc_f16_f32(kBM, BN, /*b_mn_major=*/true);
+    constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators, power of two >= 32
+
+    extern __shared__ uint8_t smem_raw[];
+    // 1 KiB alignment of the shared-window address (128-byte swizzle atoms).
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t* base = smem_raw + (base_s - raw_s);
+
+    const uint32_t sA = base_s + SP::kA;
+    const uint32_t sB = base_s + SP::kB;
+    float* bias_s = reinterpret_cast<float*>(base + SP::kBias);
+    const uint32_t bars = base_s + SP::kBars;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
+    auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bars + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + SP::kTmemSlot);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + SP::kAbort);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int tiles_m = (p.M + kBM - 1) / kBM;
+    const int tiles_n = (p.N + BN - 1) / BN;
+    const int num_tiles = tiles_m * tiles_n;
+    const int kblocks = (p.K + kBK - 1) / kBK;
+    unsigned int* status = &g_status;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+                const TileCoord tc = tile_coord(t, tiles_m, tiles_n, p.group_m, BN);
+                // B boxes entirely right of N are skipped: the stale smem they
+                // leave only feeds accumulator columns >= N, which are never stored.
+                const int live_boxes = min(kBoxesB, (p.N - tc.n0 + 63) / 64);
+                const uint32_t bytes = kATileBytes + static_cast<uint32_t>(live_boxes) * kBBoxBytes;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, status,
+                                           ROLE_PRODUCER, BAR_EMPTY)) { ok = false; break; }
+                    mbar_arrive_expect_tx(full_bar(stage), bytes);
+                    tma_load_2d(sA + stage * kATileBytes, &tmA, full_bar(stage), kb * kBK, tc.m0);
+                    for (int c = 0; c < live_boxes; ++c)
+                        tma_load_2d(sB + stage * SP::kBTileBytes + c * kBBoxBytes, &tmB, full_bar(stage),
+                                    tc.n0 + 64 * c, kb * kBK);
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // Let the last (up to STAGES) loads land before the CTA can exit:
+            // earlier ones were consumed, which the empty-barrier waits proved.
+            const int pending = min(issued, STAGES);
+            for (int i = 0; i < pending; ++i) {
+                if (--stage < 0) { stage = STAGES - 1; phase ^= 1u; }
+                mbar_wait_bounded(full_bar(stage), phase, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_FULL);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+                if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag, status,
+                                       ROLE_MMA, BAR_ACC_EMPTY)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, p.timeout_ns, abort_flag, status,
+                                           ROLE_MMA, BAR_FULL)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a0 = sA + stage * kATileBytes;
+                    const uint32_t b0 = sB + stage * SP::kBTileBytes;
+#pragma unroll
+                    for (int k = 0; k < kBK / kUMMA_K; ++k) {
+                        // A: K-major, 128-byte rows, 8-row atoms 1 KiB apart; a K step
+                        //    of 16 fp16 = 32 bytes inside the swizzled row.
+                        // B: N-major, 64-column boxes 8 KiB apart (LBO), 8-row K
+                        //    groups 1 KiB apart (SBO); a K step of 16 rows = 2 KiB.
+                        const uint64_t adesc = smem_desc_sw128(a0 + k * 32, 0, 1024);
+                        const uint64_t bdesc = smem_desc_sw128(b0 + k * 2048, kBBoxBytes, 1024);
+                        tc_mma_f16(d_tmem, adesc, bdesc, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(empty_bar(stage));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit(accf_bar(acc));
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            // Every MMA issued has completed before the accumulator is freed.
+            tc_commit(drain_bar);
+            mbar_wait_bounded(drain_bar, 0, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_DRAIN);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;            // TMEM lane quarter this warp may access
+        const int ew = warp - 2;           // private bias slice
+        float* my_bias = bias_s + ew * BN;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        const bool has_bias = p.epi != EPI_NONE;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            const TileCoord tc = tile_coord(t, tiles_m, tiles_n, p.group_m, BN);
+            __syncwarp();
+            if (has_bias) {
+                for (int i = lane; i < BN; i += 32) {
+                    const int n = tc.n0 + i;
+                    my_bias[i] = n < p.N ? __half2float(p.bias[n]) : 0.0f;
+                }
+            }
+            __syncwarp();
+            // tcgen05.ld is warp-collective: the go/no-go decision must be warp-uniform.
+            const bool ready = mbar_wait_bounded(accf_bar(acc), acc_phase, p.timeout_ns, abort_flag, status,
+                                                 ROLE_EPILOGUE, BAR_ACC_FULL);
+            if (!__all_sync(0xffffffffu, ready)) break;
+            tc_fence_after();
+            const int row = tc.m0 + 32 * q + lane;
+            const bool row_ok = row < p.M;
+            __half* crow = p.C + static_cast<int64_t>(row) * p.ldc;
+            const uint32_t t_base = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(32 * q) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_base + 32u * c, r);
+                tmem_wait_ld();
+                const int col0 = tc.n0 + 32 * c;
+                if (row_ok && col0 < p.N) {
+                    uint32_t h[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        float x0 = __uint_as_float(r[2 * j]);
+                        float x1 = __uint_as_float(r[2 * j + 1]);
+                        if (has_bias) {
+                            x0 += my_bias[32 * c + 2 * j];
+                            x1 += my_bias[32 * c + 2 * j + 1];
+                        }
+                        x0 = apply_act(x0, p.epi);
+                        x1 = apply_act(x1, p.epi);
+                        const __half2 hv = __floats2half2_rn(x0, x1);
+                        h[j] = *reinterpret_cast<const uint32_t*>(&hv);
+                    }
+                    if (p.vec_store && col0 + 32 <= p.N) {
+                        uint4* dst = reinterpret_cast<uint4*>(crow + col0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            if (col0 + j < p.N) {
+                                const uint16_t bits = static_cast<uint16_t>((h[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+                                reinterpret_cast<uint16_t*>(crow)[col0 + j] = bits;
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar(acc));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// K == 0: C = epilogue(bias) (zeros for NONE).
+__global__ void gemm_f16_bias_only_kernel(__half* C, const __half* bias, int64_t M, int64_t N, int64_t ldc, int epi) {
+    const int64_t total = M * N;
+    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t i = e / N, j = e - i * N;
+        const float x = epi == EPI_NONE ? 0.0f : __half2float(bias[j]);
+        C[i * ldc + j] = __float2half_rn(apply_act(x, epi));
+    }
+}
+
+// Row repack: dst[r, 0:cols] = src[r, 0:cols] with a 16-byte-multiple pitch,
+// so the tensor map can describe the copy (columns >= cols are left as is;
+// the tensor map's extent stops at `cols`, so TMA never reads them).
+__global__ void gemm_f16_repack_kernel(uint16_t* __restrict__ dst, const uint16_t* __restrict__ src,
+                                       int64_t rows, int64_t cols, int64_t ld_src, int64_t ld_dst) {
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y)
+        for (int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; c < cols;
+             c += static_cast<int64_t>(gridDim.x) * blockDim.x)
+            dst[r * ld_dst + c] = src[r * ld_src + c];
+}
+
+// One CTA, one thread waits on a barrier nobody arrives on.
+__global__ void gemm_f16_selftest_timeout_kernel(uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbarrier_init();
+        mbar_wait_bounded(smem_u32(&bar), 0, timeout_ns, nullptr, &g_status, ROLE_SELFTEST, BAR_TEST);
+    }
+}
+
+}  // namespace gemm_f16_dev

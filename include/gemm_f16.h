@@ -1,0 +1,126 @@
+/*
+ * gemm_f16.h -- C ABI of the fused fp16 tensor-core GEMM for GB300 (sm_103a).
+ *
+ *   C[M,N] = epilogue(A[M,K] . B[K,N] + bias[N])
+ *
+ * The operation: "writing-tilelang-kernels", Kernel Anatomy and GEMM (Minimal)
+ * (A an (M,K) fp16 tensor, B a (K,N) fp16 tensor, C an (M,N) fp16 tensor,
+ * float accumulator, one write-back of C); the same page's Pre-flight
+ * Checklist ("GEMM + fusion": an activation epilogue after the GEMM); and
+ * "TileLang: Write, Autotune, and Ship Fused Tensor-Core Kernels from
+ * Python", Why tile-level control matters (bias add and GELU applied while
+ * the accumulator is on chip, C written once, no M x N intermediate in HBM).
+ *
+ * Numerics: A and B are fp16; products are accumulated in fp32 in tensor
+ * memory; bias is added and the activation applied in fp32; C is rounded
+ * once to fp16 (round to nearest even).  GELU is the exact form
+ * 0.5 x (1 + erf(x / sqrt 2)).
+ *
+ * Layout: all matrices are dense row-major (lda = K, ldb = N, ldc = N),
+ * element type IEEE binary16 passed as raw pointers.  bias is a length-N
+ * vector broadcast over the rows of C.
+ *
+ * Pointers: A, B, bias and C are DEVICE pointers on the current CUDA device.
+ * The caller owns them; the library never frees or retains them.  C must not
+ * overlap A, B or bias.  Every pointer must be at least 2-byte aligned.
+ * Operands whose base is not 16-byte aligned, or whose row pitch in bytes is
+ * not a multiple of 16 (K % 8 != 0 for A, N % 8 != 0 for B), are repacked
+ * into a library-owned, stream-ordered scratch buffer before the GEMM.
+ *
+ * Streams: every call is asynchronous on `cuda_stream` (a cudaStream_t, or
+ * NULL for the legacy default stream) and returns once the work is enqueued.
+ * Errors detected while the kernel runs appear at the caller's next
+ * synchronisation; gemm_f16_debug_status reports bounded-wait timeouts.
+ */
+#ifndef GEMM_F16_H
+#define GEMM_F16_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Epilogue applied to x = acc + bias[n] (bias ignored for NONE). */
+typedef enum {
+    GEMM_EPI_NONE = 0,          /* C = acc                              */
+    GEMM_EPI_BIAS = 1,          /* C = acc + bias                       */
+    GEMM_EPI_BIAS_RELU = 2,     /* C = max(acc + bias, 0)               */
+    GEMM_EPI_BIAS_GELU_ERF = 3  /* C = 0.5 x (1 + erf(x/sqrt2)), x = acc + bias */
+} gemm_epilogue_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,        /* negative size, bad epilogue, null pointer, overflow */
+    GEMM_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not compute capability 10.3 */
+    GEMM_ERR_MISALIGNED = 3,         /* a pointer is not 2-byte aligned */
+    GEMM_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed; see gemm_f16_last_cuda_error */
+    GEMM_ERR_TIMEOUT = 5,            /* a kernel's bounded wait ran out (reported by gemm_f16_debug_status) */
+    GEMM_ERR_NO_MEMORY = 6           /* the repack scratch buffer could not be allocated */
+} gemm_status_t;
+
+/*
+ * gemm_f16 -- C = epilogue(A.B + bias) on the current device.
+ *
+ *   A        device pointer, fp16 [M, K] row-major
+ *   B        device pointer, fp16 [K, N] row-major
+ *   bias     device pointer, fp16 [N]; required for epilogue >= GEMM_EPI_BIAS,
+ *            ignored (may be NULL) for GEMM_EPI_NONE
+ *   C        device pointer, fp16 [M, N] row-major, written (never read)
+ *   M, N, K  sizes, each >= 0 and < 2^31; M*N, M*K, K*N < 2^62
+ *   epilogue a gemm_epilogue_t value
+ *   cuda_stream  cudaStream_t to enqueue on (NULL = legacy default stream)
+ *
+ * Returns GEMM_OK once enqueued.  M == 0 or N == 0 is a no-op; K == 0 writes
+ * C = epilogue(bias) (zeros for NONE).  Argument errors return before any
+ * CUDA call and enqueue nothing.
+ */
+int gemm_f16(const void* A, const void* B, const void* bias, void* C,
+             int64_t M, int64_t N, int64_t K, int epilogue, void* cuda_stream);
+
+/* Static, human-readable name of a status code. */
+const char* gemm_f16_status_string(int status);
+
+/* cudaError_t value behind the calling thread's most recent GEMM_ERR_CUDA. */
+int gemm_f16_last_cuda_error(void);
+
+/*
+ * Synchronises `cuda_stream`, then reads and clears the device-side status
+ * word of the current device.  Returns GEMM_ERR_TIMEOUT if any kernel of
+ * this library gave up a bounded wait since the last call, GEMM_ERR_CUDA if
+ * the synchronisation failed, GEMM_OK otherwise.  `detail` (nullable)
+ * receives the raw status word (role and barrier of the first timeout).
+ */
+int gemm_f16_debug_status(void* cuda_stream, uint32_t* detail);
+
+/* Returns the library's cached repack scratch memory on the current device
+ * to the system (the scratch is stream-ordered; call after synchronising). */
+int gemm_f16_release_workspace(void);
+
+/*
+ * Host-only planning query (no device access): the execution plan that
+ * gemm_f16 would choose for these sizes and base addresses on a device with
+ * `num_sms` SMs.  plan[0..7] receive: path (0 none, 1 bias-only K==0,
+ * 2 tiled tensor-core kernel, 3 swap-AB skinny kernel), tile_m, tile_n,
+ * pipeline stages, CTAs launched, repack A (0/1), repack B (0/1), vector
+ * stores of C (0/1).  Returns a status code like gemm_f16 (argument errors
+ * only).  Diagnostic; it has no counterpart on the pages.
+ */
+int gemm_f16_plan(const void* A, const void* B, const void* bias, const void* C,
+                  int64_t M, int64_t N, int64_t K, int epilogue, int num_sms,
+                  int64_t plan[8]);
+
+/*
+ * Diagnostic for the bounded-wait machinery (no counterpart on the pages):
+ * launches one CTA that waits on an mbarrier nothing ever arrives on, with a
+ * limit of `timeout_us` microseconds, and returns what gemm_f16_debug_status
+ * then reports (GEMM_ERR_TIMEOUT when the limit worked).  The context stays
+ * usable afterwards.
+ */
+int gemm_f16_selftest_timeout(void* cuda_stream, uint32_t timeout_us);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_F16_H */

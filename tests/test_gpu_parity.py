@@ -1,0 +1,262 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Bar: relative Frobenius error <= 1e-3 and |err| <= 1e-2 (1 + |ref|) per
+element (oracle/compare.py); bit-exact where every step is exact (small
+integer operands).  Inputs come from workloads.py (seeded, shared by both
+sides).
+"""
+import numpy as np
+import pytest
+
+import workloads
+from oracle.compare import parity
+
+pytestmark = pytest.mark.gpu
+
+EPIS = ("none", "bias", "bias_relu", "bias_gelu_erf")
+
+
+@pytest.fixture(scope="module")
+def torch_dev():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch, torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def g(torch_dev):
+    import dense_fp16_tensor_tma_gb300 as mod
+    return mod
+
+
+def _dev(torch, x, dev):
+    return None if x is None else torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+
+def run(g, torch_dev, A, B, bias, epi, check_status=True):
+    torch, dev = torch_dev
+    M, K = A.shape
+    N = B.shape[1]
+    C = torch.full((M, N), float("nan"), dtype=torch.float16, device=dev)
+    g.gemm_f16(_dev(torch, A, dev), _dev(torch, B, dev), _dev(torch, bias, dev) if epi != "none" else None, C, epi)
+    if check_status:
+        st, word = g.gemm_f16_debug_status()
+        assert st == 0, f"device status {st} word {word:#x}"
+    return C.cpu().numpy()
+
+
+def rand16(rng, shape, scale=1.0):
+    return (rng.standard_normal(shape) * scale).astype(np.float16)
+
+
+def assert_parity(got, ref, what=""):
+    res = parity(got, ref)
+    assert res["ok"], f"{what}: {res}"
+    return res
+
+
+# ---------------------------------------------------------------- exact (integer) cases first
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (128, 64, 64), (256, 512, 128), (200, 300, 136), (129, 257, 65)])
+@pytest.mark.parametrize("epi", ["none", "bias", "bias_relu"])
+def test_integer_inputs_bit_exact(g, torch_dev, oracle_mod, M, N, K, epi):
+    rng = np.random.default_rng(M * 7 + N * 3 + K)
+    A = rng.integers(-2, 3, (M, K)).astype(np.float16)
+    B = rng.integers(-2, 3, (K, N)).astype(np.float16)
+    bias = rng.integers(-8, 9, N).astype(np.float16)
+    got = run(g, torch_dev, A, B, bias, epi)
+    ref = oracle_mod.gemm(A, B, bias, epi)
+    assert np.array_equal(got, ref), f"max diff {np.nanmax(np.abs(got.astype(np.float64) - ref.astype(np.float64)))}"
+
+
+def test_identity_and_permutation_B(g, torch_dev, oracle_mod):
+    rng = np.random.default_rng(12)
+    K = 320
+    A = rand16(rng, (300, K))
+    eye = np.eye(K, dtype=np.float16)
+    assert np.array_equal(run(g, torch_dev, A, eye, None, "none").view(np.uint16), A.view(np.uint16))
+    perm = rng.permutation(K)
+    P = np.zeros((K, K), np.float16)
+    P[perm, np.arange(K)] = 1.0
+    assert np.array_equal(run(g, torch_dev, A, P, None, "none").view(np.uint16), A[:, perm].view(np.uint16))
+
+
+# ---------------------------------------------------------------- the five workloads
+
+def _check_full(g, torch_dev, oracle_mod, w, epi):
+    A, B, bias = w.make()
+    got = run(g, torch_dev, A, B, bias, epi)
+    ref = oracle_mod.gemm(A, B, bias if epi != "none" else None, epi)
+    return assert_parity(got, ref, f"{w.name} {epi}")
+
+
+@pytest.mark.parametrize("epi", ["none", "bias_gelu_erf"])
+def test_workload_gemm256(g, torch_dev, oracle_mod, epi):
+    _check_full(g, torch_dev, oracle_mod, workloads.WORKLOADS["gemm256"], epi)
+
+
+def test_workload_gemm1024(g, torch_dev, oracle_mod):
+    _check_full(g, torch_dev, oracle_mod, workloads.WORKLOADS["gemm1024"], "none")
+
+
+def test_workload_ragged_3001x5003x1000(g, torch_dev, oracle_mod):
+    _check_full(g, torch_dev, oracle_mod, workloads.WORKLOADS["ragged3001x5003x1000"], "bias_relu")
+
+
+def test_workload_skinny_16x8192x8192(g, torch_dev, oracle_mod):
+    _check_full(g, torch_dev, oracle_mod, workloads.WORKLOADS["skinny16x8192x8192"], "none")
+
+
+def _check_sampled(g, torch_dev, oracle_mod, w, epi, n_rows_extra=0):
+    A, B, bias = w.make()
+    got = run(g, torch_dev, A, B, bias, epi)
+    b = bias if epi != "none" else None
+    rows = [0, w.M - 1] + list(workloads.sample_coords(w.seed + 1000, w.M, 1, n_rows_extra)[0])
+    ref_rows = oracle_mod.gemm_rows(A, B, b, epi, rows)
+    assert_parity(got[rows], ref_rows, f"{w.name} rows")
+    ii, jj = workloads.sample_coords(w.seed, w.M, w.N, workloads.SAMPLED_ELEMS)
+    ref_el = oracle_mod.gemm_elems(A, B, b, epi, ii, jj)
+    assert_parity(got[ii, jj], ref_el, f"{w.name} elems")
+    assert np.all(np.isfinite(got))
+
+
+def test_workload_fused4096(g, torch_dev, oracle_mod):
+    _check_sampled(g, torch_dev, oracle_mod, workloads.WORKLOADS["fused4096"], "bias_gelu_erf", n_rows_extra=62)
+
+
+def test_workload_fused8192(g, torch_dev, oracle_mod):
+    _check_sampled(g, torch_dev, oracle_mod, workloads.WORKLOADS["fused8192"], "bias_gelu_erf")
+
+
+# ---------------------------------------------------------------- tails, epilogues, paths
+
+SHAPES = [(1, 1, 1), (1, 15, 8), (15, 16, 16), (16, 17, 63), (17, 127, 64), (127, 128, 65),
+          (128, 129, 1000), (129, 255, 16), (255, 257, 8), (257, 1, 63), (64, 1000, 200),
+          (300, 520, 77), (513, 384, 128), (33, 4097, 24)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_shape_sweep(g, torch_dev, oracle_mod, M, N, K):
+    rng = np.random.default_rng(M * 1009 + N * 17 + K)
+    A, B, bias = rand16(rng, (M, K), 0.5), rand16(rng, (K, N), 0.5), rand16(rng, N)
+    epi = EPIS[(M + N + K) % 4]
+    got = run(g, torch_dev, A, B, bias, epi)
+    assert_parity(got, oracle_mod.gemm(A, B, bias if epi != "none" else None, epi), f"{M}x{N}x{K} {epi}")
+
+
+@pytest.mark.parametrize("epi", EPIS)
+def test_each_epilogue_multi_tile(g, torch_dev, oracle_mod, epi):
+    rng = np.random.default_rng(99)
+    M, N, K = 384, 768, 320
+    A, B, bias = rand16(rng, (M, K), 0.3), rand16(rng, (K, N), 0.3), rand16(rng, N)
+    got = run(g, torch_dev, A, B, bias, epi)
+    assert_parity(got, oracle_mod.gemm(A, B, bias if epi != "none" else None, epi), epi)
+
+
+def test_large_tiles_persistent_many_waves(g, torch_dev, oracle_mod):
+    # > 2 tiles per CTA on the 128x256 configuration, every tile checked on sampled rows
+    rng = np.random.default_rng(5)
+    M, N, K = 2048, 4096, 256
+    A, B, bias = rand16(rng, (M, K), 0.2), rand16(rng, (K, N), 0.2), rand16(rng, N)
+    got = run(g, torch_dev, A, B, bias, "bias_gelu_erf")
+    rows = np.arange(0, M, 37)
+    assert_parity(got[rows], oracle_mod.gemm_rows(A, B, bias, "bias_gelu_erf", rows), "rows")
+
+
+def test_unaligned_pointers_use_repack_and_narrow_stores(g, torch_dev, oracle_mod):
+    torch, dev = torch_dev
+    rng = np.random.default_rng(6)
+    M, N, K = 200, 136, 96
+    A, B, bias = rand16(rng, (M, K)), rand16(rng, (K, N)), rand16(rng, N)
+    # offset every operand by one element inside a larger buffer: 2-byte but not 16-byte aligned
+    def offset(x):
+        buf = torch.zeros(x.size + 8, dtype=torch.float16, device=dev)
+        buf[1:1 + x.size] = torch.from_numpy(x.ravel()).to(dev)
+        return buf, buf[1:1 + x.size]
+    _, a1 = offset(A)
+    _, b1 = offset(B)
+    _, bias1 = offset(bias)
+    cbuf = torch.full((M * N + 8,), -7.0, dtype=torch.float16, device=dev)
+    c1 = cbuf[1:1 + M * N]
+    assert g.gemm_f16_ptr(a1.data_ptr(), b1.data_ptr(), bias1.data_ptr(), c1.data_ptr(), M, N, K,
+                          "bias_gelu_erf", torch.cuda.current_stream().cuda_stream) == 0
+    got = c1.view(M, N).cpu().numpy()
+    assert_parity(got, oracle_mod.gemm(A, B, bias, "bias_gelu_erf"))
+    c = cbuf.cpu().numpy()
+    assert c[0] == -7.0 and np.all(c[1 + M * N:] == -7.0)
+
+
+def test_odd_k_repacks_a(g, torch_dev, oracle_mod):
+    rng = np.random.default_rng(7)
+    M, N, K = 150, 264, 77
+    A, B, bias = rand16(rng, (M, K)), rand16(rng, (K, N)), rand16(rng, N)
+    assert g.gemm_f16_plan(M, N, K, "bias")["pack_a"] == 1
+    assert_parity(run(g, torch_dev, A, B, bias, "bias"), oracle_mod.gemm(A, B, bias, "bias"))
+
+
+def test_guard_zones_untouched(g, torch_dev, oracle_mod):
+    torch, dev = torch_dev
+    rng = np.random.default_rng(8)
+    M, N, K = 130, 264, 72
+    A, B, bias = rand16(rng, (M, K)), rand16(rng, (K, N)), rand16(rng, N)
+    pad = 4096
+    sentinel = np.float16(-12345.0)
+    buf = torch.full((pad + M * N + pad,), float(sentinel), dtype=torch.float16, device=dev)
+    C = buf[pad:pad + M * N].view(M, N)
+    tA, tB, tb = _dev(torch, A, dev), _dev(torch, B, dev), _dev(torch, bias, dev)
+    g.gemm_f16(tA, tB, tb, C, "bias_relu")
+    torch.cuda.synchronize()
+    host = buf.cpu().numpy()
+    assert np.all(host[:pad] == sentinel) and np.all(host[pad + M * N:] == sentinel)
+    assert_parity(host[pad:pad + M * N].reshape(M, N), oracle_mod.gemm(A, B, bias, "bias_relu"))
+    # inputs unchanged
+    assert np.array_equal(tA.cpu().numpy().view(np.uint16), A.view(np.uint16))
+    assert np.array_equal(tB.cpu().numpy().view(np.uint16), B.view(np.uint16))
+
+
+def test_deterministic(g, torch_dev):
+    rng = np.random.default_rng(9)
+    A, B, bias = rand16(rng, (777, 999)), rand16(rng, (999, 1234)), rand16(rng, 1234)
+    c1 = run(g, torch_dev, A, B, bias, "bias_gelu_erf")
+    c2 = run(g, torch_dev, A, B, bias, "bias_gelu_erf")
+    assert np.array_equal(c1.view(np.uint16), c2.view(np.uint16))
+
+
+def test_k_zero_and_empty(g, torch_dev):
+    torch, dev = torch_dev
+    bias = np.array([-2.0, -0.5, 0.0, 1.0, 3.0, 0.25, -1.0, 2.0], np.float16)
+    tb = _dev(torch, bias, dev)
+    C = torch.full((5, 8), 9.0, dtype=torch.float16, device=dev)
+    empty_a = torch.empty((5, 0), dtype=torch.float16, device=dev)
+    empty_b = torch.empty((0, 8), dtype=torch.float16, device=dev)
+    g.gemm_f16(empty_a, empty_b, tb, C, "bias_relu")
+    assert np.array_equal(C.cpu().numpy(), np.tile(np.maximum(bias, 0), (5, 1)))
+    g.gemm_f16(empty_a, empty_b, None, C, "none")
+    assert np.all(C.cpu().numpy() == 0)
+    C0 = torch.empty((0, 8), dtype=torch.float16, device=dev)
+    g.gemm_f16(torch.empty((0, 4), dtype=torch.float16, device=dev),
+               torch.empty((4, 8), dtype=torch.float16, device=dev), None, C0, "none")
+
+
+def test_runs_on_a_side_stream(g, torch_dev, oracle_mod):
+    torch, dev = torch_dev
+    rng = np.random.default_rng(10)
+    A, B, bias = rand16(rng, (256, 512)), rand16(rng, (512, 384)), rand16(rng, 384)
+    s = torch.cuda.Stream()
+    tA, tB, tb = _dev(torch, A, dev), _dev(torch, B, dev), _dev(torch, bias, dev)
+    C = torch.empty((256, 384), dtype=torch.float16, device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g.gemm_f16(tA, tB, tb, C, "bias")
+    s.synchronize()
+    assert_parity(C.cpu().numpy(), oracle_mod.gemm(A, B, bias, "bias"))
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(g, torch_dev, oracle_mod):
+    # a barrier nothing arrives on: the wait gives up after 2 ms and reports it
+    assert g.gemm_f16_selftest_timeout(2000) == g.GEMM_ERR_TIMEOUT
+    assert g.gemm_f16_debug_status()[0] == g.GEMM_OK          # cleared
+    rng = np.random.default_rng(11)
+    A, B = rand16(rng, (128, 64)), rand16(rng, (64, 128))
+    assert_parity(run(g, torch_dev, A, B, None, "none"), oracle_mod.gemm(A, B, None, "none"))
