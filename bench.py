@@ -1,0 +1,420 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused fp16 GEMM  C = GELU(A @ B + bias)  at M = N = K = 8192.
+
+One step = one call of gemm_f16 (the whole path: TMA loads, tcgen05 MMA into
+tensor memory, fused bias + erf-GELU epilogue, one fp16 write of C) on
+seeded synthetic inputs already resident in HBM.  Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-cpu-baseline]
+
+--impl reference times the CPU oracle (fp64, all host cores) on bounded row
+samples of the same workload: the comparison arm.  N > 1 runs independent
+replicas, one per GPU (weak scaling; no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "TFLOP/s and % of GB300 fp16 tensor peak for fused bias+GELU GEMM"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "fused8192"
+L2_BYTES = 129 * 10 ** 6
+FALLBACK_TENSOR_TFLOPS = 1900.0
+FP16_PER_BF16 = 1.0          # nominal dense fp16 rate / dense bf16 rate
+KERNEL_SOURCES = ("dense_fp16_tensor_tma_gb300/csrc/gemm_kernels.cuh",
+                  "dense_fp16_tensor_tma_gb300/csrc/ptx.cuh",
+                  "dense_fp16_tensor_tma_gb300/csrc/gemm_f16.cu")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def workload_config(w, epi):
+    return {
+        "workload": f"{w.name}: M={w.M} N={w.N} K={w.K} epilogue={epi}, fp16 row-major A,B "
+                    f"~{w.ab_dist}*{w.ab_scale}, bias ~{w.bias_dist}, seed {w.seed}",
+        "M": w.M, "N": w.N, "K": w.K, "epilogue": epi, "seed": w.seed,
+        "accumulate": "f32", "flops_per_step": w.flops(), "alg_bytes_per_step": w.alg_bytes(),
+        "l2": ("inputs larger than L2 (no flush)" if w.alg_bytes() > L2_BYTES
+               else "L2 flushed between steps (256 MiB write)"),
+    }
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]) * FP16_PER_BF16, "measured", pk
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_TENSOR_TFLOPS, "fallback", None
+
+
+def committed_traffic(workload_name):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload_name)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid=None, interval_ms=100):
+        self.proc = None
+        self.lines = []
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", str(interval_ms)]
+        if gpu_uuid:
+            cmd += ["-i", gpu_uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        self.t_start = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        return [l for l in out.splitlines() if l.strip()]
+
+    @staticmethod
+    def parse(lines):
+        """[(unix_time, sm_mhz, sm_max_mhz, set(active reasons))]"""
+        out = []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                sm, smax = float(parts[2]), float(parts[3])
+            except (ValueError, IndexError):
+                continue
+            out.append((ts, sm, smax, {n for n, v in zip(names, parts[6:10]) if v.lower() == "active"}))
+        return out
+
+    @staticmethod
+    def summarize(samples, t0=None, t1=None, pad_s=0.25):
+        """Median SM clock and throttle reasons of the samples inside [t0-pad, t1+pad];
+        when the window holds none (a short run), the samples of the whole run."""
+        window = "timed"
+        sel = samples
+        if t0 is not None and t1 is not None:
+            sel = [s for s in samples if t0 - pad_s <= s[0] <= t1 + pad_s]
+            if not sel:
+                sel, window = samples, "whole run (timed window shorter than the sampling interval)"
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": window}
+        reasons = set().union(*[s[3] for s in sel])
+        return {"sm_mhz": statistics.median(s[1] for s in sel), "sm_max_mhz": sel[-1][2],
+                "reasons": sorted(reasons), "samples": len(sel), "window": window}
+
+
+# ------------------------------------------------------------------ distributed (replicas)
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(world, x: float) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def oracle_rows_timing(w, epi, A, B, bias, target_s):
+    """Time the oracle on a bounded sample of full rows; returns (tflops, seconds, rows, threads)."""
+    import oracle
+    b = bias if epi != "none" else None
+    threads = oracle.default_threads()
+    # two probes separate the per-call operand conversion from the per-row cost
+    p1 = max(1, min(w.M, threads))
+    p2 = max(p1, min(w.M, 4 * threads))
+    t0 = time.perf_counter()
+    oracle.gemm_rows(A, B, b, epi, np.arange(p1))
+    t1 = time.perf_counter()
+    oracle.gemm_rows(A, B, b, epi, np.arange(p2))
+    t2 = time.perf_counter()
+    per_row = max((t2 - t1) - (t1 - t0), 1e-6) / max(1, p2 - p1)
+    rows = int(min(w.M, max(p2, target_s / per_row)))
+    rows = min(w.M, max(threads, rows // threads * threads))
+    t0 = time.perf_counter()
+    oracle.gemm_rows(A, B, b, epi, np.arange(rows))
+    dt = time.perf_counter() - t0
+    return 2.0 * rows * w.N * w.K / dt / 1e12, dt, rows, threads
+
+
+def run_reference(args, w, epi):
+    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    A, B, bias = w.make()
+    b = bias if epi != "none" else None
+    threads = oracle.default_threads()
+    # calibrate rows per step so the whole run stays within a few minutes
+    t0 = time.perf_counter()
+    oracle.gemm_rows(A, B, b, epi, np.arange(min(w.M, threads)))
+    per_row = (time.perf_counter() - t0) / min(w.M, threads)
+    budget_s = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    rows_per_step = int(min(w.M, max(1, budget_s / max(per_row, 1e-9))))
+    rows_per_step = max(1, min(w.M, rows_per_step // threads * threads or rows_per_step))
+    for i in range(args.warmup):
+        oracle.gemm_rows(A, B, b, epi, (np.arange(rows_per_step) + i * rows_per_step) % w.M)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.gemm_rows(A, B, b, epi, (np.arange(rows_per_step) + i * rows_per_step) % w.M)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows_per_step * w.N * w.K * args.steps
+    value = flops / dt / 1e12
+    sample = (f"{rows_per_step} of {w.M} output rows per step (full K={w.K} dot products, all N={w.N} "
+              f"columns, epilogue {epi}), fp64 C++ oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, epi),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args, w, epi):
+    import torch
+    world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import dense_fp16_tensor_tma_gb300 as g
+
+    props = torch.cuda.get_device_properties(dev)
+    # replicas: each rank owns an independent problem of the same shape
+    wr = w if world == 1 else workloads.Workload(**{**w.__dict__, "seed": w.seed + 1000 * rank})
+    t_gen = time.perf_counter()
+    A, B, bias = wr.make()
+    log(f"[rank {rank}] inputs generated in {time.perf_counter() - t_gen:.1f}s")
+    b_np = bias if epi != "none" else None
+    tA = torch.from_numpy(A).to(dev)
+    tB = torch.from_numpy(B).to(dev)
+    tb = torch.from_numpy(b_np).to(dev) if b_np is not None else None
+    C = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    flush = None
+    if w.alg_bytes() <= L2_BYTES:
+        flush = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
+    plan = g.gemm_f16_plan(w.M, w.N, w.K, epi, num_sms=props.multi_processor_count,
+                           a_addr=tA.data_ptr(), b_addr=tB.data_ptr(), c_addr=C.data_ptr(),
+                           bias_addr=tb.data_ptr() if tb is not None else 0)
+    launches_per_step = 1 + plan["pack_a"] + plan["pack_b"]
+
+    def step():
+        if flush is not None:
+            flush.fill_(1.0)
+        st = g.gemm_f16_ptr(tA.data_ptr(), tB.data_ptr(), tb.data_ptr() if tb is not None else 0,
+                            C.data_ptr(), w.M, w.N, w.K, epi, sh)
+        if st != 0:
+            raise g.GemmError(st)
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    stream.synchronize()
+    st, word = g.gemm_f16_debug_status(stream)
+    if st != 0:
+        raise SystemExit(f"device status {st} ({word:#x}) after warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    dist_barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    dist_barrier(world)
+    clock_lines = sampler.stop()
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    elapsed_ms = starts[0].elapsed_time(ends[-1])
+    elapsed_ms = dist_max(world, elapsed_ms)
+    st, word = g.gemm_f16_debug_status(stream)
+    if st != 0:
+        raise SystemExit(f"device status {st} ({word:#x}) after timed steps")
+
+    flops = w.flops()
+    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    avg_launch_ms = statistics.mean(per_launch_ms)
+    achieved = flops / (avg_launch_ms * 1e-3) / 1e12
+    peak, peak_src, _ = read_peaks()
+    traffic = committed_traffic(w.name)
+
+    # ---- end to end: pinned host buffers through the C ABI, copies inside the timed region
+    hA = torch.from_numpy(A).pin_memory()
+    hB = torch.from_numpy(B).pin_memory()
+    hb = torch.from_numpy(b_np).pin_memory() if b_np is not None else None
+    hC = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+    h2d = hA.numel() * 2 + hB.numel() * 2 + (hb.numel() * 2 if hb is not None else 0)
+    d2h = hC.numel() * 2
+
+    def e2e_step():
+        tA.copy_(hA, non_blocking=True)
+        tB.copy_(hB, non_blocking=True)
+        if hb is not None:
+            tb.copy_(hb, non_blocking=True)
+        step()
+        hC.copy_(C, non_blocking=True)
+
+    e2e_steps = args.steps
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+    stream.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_barrier(world)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = dist_max(world, ev0.elapsed_time(ev1))
+    dist_barrier(world)
+    e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tfl, secs, rows, threads = oracle_rows_timing(w, epi, A, B, bias, target_s=args.cpu_seconds)
+        cpu = {"value": tfl, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{rows} of {w.M} output rows (full N, full K), fp64 C++ oracle, {secs:.1f}s"}
+
+    if rank == 0:
+        clocks = ClockSampler.summarize(ClockSampler.parse(clock_lines), t_wall0, t_wall1)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": elapsed_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic",
+            "config": {**workload_config(w, epi), "parallelism": f"replicas{world}" if world > 1 else "single"},
+            "pct_of_peak": 100.0 * achieved / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_src} (bf16 burst x fp16/bf16 ratio {FP16_PER_BF16})",
+                         "kernel": "gemm_f16_tc_kernel", "avg_launch_ms": avg_launch_ms},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms / e2e_steps},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                       "reasons": clocks["reasons"], "samples": clocks["samples"],
+                       "window": clocks["window"], "window_s": round(t_wall1 - t_wall0, 3)},
+            "cpu_baseline": cpu,
+            "plan": plan,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--epilogue", default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.steps < 1:
+        raise SystemExit("--steps must be >= 1")
+    w = workloads.WORKLOADS[args.workload]
+    epi = args.epilogue or w.epilogues[-1]
+    if args.impl == "reference":
+        return run_reference(args, w, epi)
+    return run_ours(args, w, epi)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
