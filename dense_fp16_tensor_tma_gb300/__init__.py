@@ -18,10 +18,10 @@ GEMM_EPI_NONE, GEMM_EPI_BIAS, GEMM_EPI_BIAS_RELU, GEMM_EPI_BIAS_GELU_ERF = 0, 1,
 EPILOGUES = {"none": GEMM_EPI_NONE, "bias": GEMM_EPI_BIAS, "bias_relu": GEMM_EPI_BIAS_RELU,
              "bias_gelu_erf": GEMM_EPI_BIAS_GELU_ERF}
 GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED_DEVICE, GEMM_ERR_MISALIGNED = 0, 1, 2, 3
-GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT, GEMM_ERR_NO_MEMORY = 4, 5, 6
+GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT, GEMM_ERR_NO_MEMORY, GEMM_ERR_SCRATCH_LIMIT = 4, 5, 6, 7
 
 EXPORTS = ("gemm_f16", "gemm_f16_status_string", "gemm_f16_last_cuda_error", "gemm_f16_debug_status",
-           "gemm_f16_release_workspace", "gemm_f16_plan", "gemm_f16_selftest_timeout")
+           "gemm_f16_release_workspace", "gemm_f16_plan", "gemm_f16_selftest_timeout", "gemm_f16_noalloc")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
@@ -41,6 +41,8 @@ lib.gemm_f16_plan.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, 
 lib.gemm_f16_plan.restype = _int
 lib.gemm_f16_selftest_timeout.argtypes = [_vp, ctypes.c_uint32]
 lib.gemm_f16_selftest_timeout.restype = _int
+lib.gemm_f16_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
+lib.gemm_f16_noalloc.restype = _int
 
 
 class GemmError(RuntimeError):
@@ -125,3 +127,18 @@ def gemm_f16_release_workspace() -> int:
 
 def gemm_f16_selftest_timeout(timeout_us: int = 1000, stream=None) -> int:
     return lib.gemm_f16_selftest_timeout(_stream_handle(stream), int(timeout_us))
+
+
+def gemm_f16_noalloc_ptr(a_ptr: int, b_ptr: int, bias_ptr: int, c_ptr: int, M: int, N: int, K: int,
+                         epilogue=GEMM_EPI_NONE, stream: int = 0) -> int:
+    """Raw call of gemm_f16_noalloc, the variant that never allocates device memory.
+
+    For callers that cannot allocate (a host framework owns the device memory,
+    a serving loop must not synchronise the device through cudaMalloc, or
+    allocation after start-up is forbidden).  Any operand repack goes to a
+    fixed 32 MiB buffer inside the library; larger repacks return
+    GEMM_ERR_SCRATCH_LIMIT.  Calls overlapping on the GPU share that buffer and
+    race.  Returns the status code.
+    """
+    return lib.gemm_f16_noalloc(a_ptr or None, b_ptr or None, bias_ptr or None, c_ptr or None,
+                                int(M), int(N), int(K), _epi(epilogue), stream or None)

@@ -196,6 +196,71 @@ int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& pr
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
 
+// ---------------------------------------------------------------- no-alloc variant
+// Fixed repack buffer for gemm_f16_noalloc, part of the module image: every
+// device that loads this library holds it until the process exits.  In host
+// code `g_noalloc_scratch` names a host-side stand-in, never the device
+// buffer; its device address comes from cudaGetSymbolAddress in
+// init_device_noalloc and is what the kernels and tensor maps receive.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocState {
+    bool ready = false;
+    int status = GEMM_OK;
+    int num_sms = 0;
+    uint8_t* scratch = nullptr;   // device address of g_noalloc_scratch on this device
+};
+NoAllocState g_noalloc[kMaxDevices];
+
+// Per-device set-up of the no-alloc path: device check, tensor-map encoder,
+// kernel attributes and the scratch address.  Allocates nothing.
+int init_device_noalloc(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    NoAllocState& st = g_noalloc[dev];
+    if (st.ready) return st.status;
+    int major = 0, minor = 0, sms = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (major != 10 || minor != 3) {
+        st.ready = true;
+        st.status = GEMM_ERR_UNSUPPORTED_DEVICE;
+        return st.status;
+    }
+    if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return cuda_fail(e != cudaSuccess ? e : cudaErrorSymbolNotFound);
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    e = cudaFuncSetAttribute(gemm_f16_tc_kernel<256, kStages256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SmemPlan<256, kStages256>::kDynamicBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_f16_tc_kernel<128, kStages128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SmemPlan<128, kStages128>::kDynamicBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_f16_tc_kernel<64, kStages64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SmemPlan<64, kStages64>::kDynamicBytes);
+    if (e != cudaSuccess) return cuda_fail(e);
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || ptr == nullptr) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+    if (const char* env = std::getenv("GEMM_F16_TIMEOUT_MS")) {
+        const long ms = std::strtol(env, nullptr, 10);
+        if (ms > 0) g_timeout_ns = static_cast<uint64_t>(ms) * 1000000ull;
+    }
+    st.scratch = static_cast<uint8_t*>(ptr);
+    st.num_sms = sms;
+    st.ready = true;
+    st.status = GEMM_OK;
+    return GEMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -209,6 +274,8 @@ const char* gemm_f16_status_string(int status) {
         case GEMM_ERR_CUDA: return "CUDA error";
         case GEMM_ERR_TIMEOUT: return "device-side bounded wait timed out";
         case GEMM_ERR_NO_MEMORY: return "out of device memory for repack scratch";
+        case GEMM_ERR_SCRATCH_LIMIT:
+            return "repack needs more than the 32 MiB fixed buffer of gemm_f16_noalloc (use gemm_f16)";
         default: return "unknown status";
     }
 }
@@ -305,6 +372,65 @@ int gemm_f16(const void* A, const void* B, const void* bias, void* C, int64_t M,
         if (e != cudaSuccess && st == GEMM_OK) st = cuda_fail(e);
     }
     return st;
+}
+
+int gemm_f16_noalloc(const void* A, const void* B, const void* bias, void* C, int64_t M, int64_t N, int64_t K,
+                     int epilogue, void* cuda_stream) {
+    int st = check_args(A, B, bias, C, M, N, K, epilogue);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    st = init_device_noalloc(dev);
+    if (st != GEMM_OK) return st;
+    const NoAllocState& ns = g_noalloc[dev];
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    const Plan pl = make_plan(A, B, C, M, N, K, ns.num_sms);
+    const __half* biasp = epilogue == GEMM_EPI_NONE ? nullptr : static_cast<const __half*>(bias);
+
+    if (pl.path == 1) {
+        gemm_f16_bias_only_kernel<<<pl.ctas, 256, 0, s>>>(static_cast<__half*>(C), biasp, M, N, N, epilogue);
+        e = cudaGetLastError();
+        return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+    }
+
+    // Same repack layout as gemm_f16 (A first, 256-byte aligned, then B), but
+    // inside the fixed buffer; nothing in it has to start at zero because the
+    // tensor maps stop at the true extents.
+    size_t a_bytes = pl.pack_a ? static_cast<size_t>(M * pl.lda_packed * 2) : 0;
+    const size_t b_bytes = pl.pack_b ? static_cast<size_t>(K * pl.ldb_packed * 2) : 0;
+    a_bytes = (a_bytes + 255) & ~size_t(255);
+    if (a_bytes + b_bytes > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
+    const void* a_src = A;
+    const void* b_src = B;
+    if (pl.pack_a) {
+        st = launch_repack(reinterpret_cast<uint16_t*>(ns.scratch), A, M, K, K, pl.lda_packed, s);
+        a_src = ns.scratch;
+    }
+    if (st == GEMM_OK && pl.pack_b) {
+        uint16_t* bdst = reinterpret_cast<uint16_t*>(ns.scratch + a_bytes);
+        st = launch_repack(bdst, B, K, N, N, pl.ldb_packed, s);
+        b_src = bdst;
+    }
+    CUtensorMap ta, tb;
+    if (st == GEMM_OK) st = encode_2d(&ta, a_src, K, M, pl.lda_packed, kBK, kBM);
+    if (st == GEMM_OK) st = encode_2d(&tb, b_src, N, K, pl.ldb_packed, 64, kBK);
+    if (st != GEMM_OK) return st;
+    GemmParams prm;
+    prm.C = static_cast<__half*>(C);
+    prm.bias = biasp;
+    prm.M = static_cast<int>(M);
+    prm.N = static_cast<int>(N);
+    prm.K = static_cast<int>(K);
+    prm.ldc = static_cast<int>(N);
+    prm.epi = epilogue;
+    prm.vec_store = pl.vec_store ? 1 : 0;
+    prm.group_m = 8;
+    prm.timeout_ns = g_timeout_ns;
+    if (pl.tile_n == 256) return launch_tc<256, kStages256>(ta, tb, prm, pl.ctas, s);
+    if (pl.tile_n == 128) return launch_tc<128, kStages128>(ta, tb, prm, pl.ctas, s);
+    return launch_tc<64, kStages64>(ta, tb, prm, pl.ctas, s);
 }
 
 int gemm_f16_debug_status(void* cuda_stream, uint32_t* detail) {

@@ -56,7 +56,8 @@ typedef enum {
     GEMM_ERR_MISALIGNED = 3,         /* a pointer is not 2-byte aligned */
     GEMM_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed; see gemm_f16_last_cuda_error */
     GEMM_ERR_TIMEOUT = 5,            /* a kernel's bounded wait ran out (reported by gemm_f16_debug_status) */
-    GEMM_ERR_NO_MEMORY = 6           /* the repack scratch buffer could not be allocated */
+    GEMM_ERR_NO_MEMORY = 6,          /* the repack scratch buffer could not be allocated */
+    GEMM_ERR_SCRATCH_LIMIT = 7       /* gemm_f16_noalloc: repack needs more than its fixed buffer */
 } gemm_status_t;
 
 /*
@@ -118,6 +119,42 @@ int gemm_f16_plan(const void* A, const void* B, const void* bias, const void* C,
  * usable afterwards.
  */
 int gemm_f16_selftest_timeout(void* cuda_stream, uint32_t timeout_us);
+
+/*
+ * gemm_f16_noalloc -- the same operation as gemm_f16, for callers that must
+ * not allocate device memory.  The paper has no counterpart; this entry
+ * point exists for the library's users.
+ *
+ * Who needs it: code that runs inside a host framework which owns the
+ * device memory (its caching allocator has reserved nearly all of it, so a
+ * plugin's own cudaMalloc fails or fragments that pool), latency-critical
+ * serving loops where cudaMalloc/cudaFree would synchronise the device and
+ * stall every other stream, and deployments whose rules forbid dynamic
+ * allocation after start-up.
+ *
+ * Arguments, layout, ownership and asynchrony are those of gemm_f16; the
+ * caller still passes A, B, bias and C.  The only difference: when an operand
+ * must be repacked (base not 16-byte aligned, or K % 8 != 0 for A,
+ * N % 8 != 0 for B), the repacked copy goes into a fixed 32 MiB buffer that
+ * is part of the library's device image (a static __device__ array, so every
+ * GPU that loads the library holds it until the process exits) instead of
+ * memory obtained from the allocator.  This function calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ *   - Sizes: the repack needs 2*M*round8(K) bytes for A (rounded up to 256)
+ *     plus 2*K*round8(N) bytes for B; a problem needing more than 32 MiB
+ *     returns GEMM_ERR_SCRATCH_LIMIT and enqueues nothing.  Problems that
+ *     need no repack have no size limit.
+ *   - Set-up: the first call on each device (with that device current) looks
+ *     up the buffer's device address and sets kernel attributes; make that
+ *     first call before any stream capture.
+ *   - Sharing: every call on a device uses the same buffer, which keeps the
+ *     previous call's contents (nothing in it needs to start at zero).  Calls
+ *     whose GPU work overlaps (e.g. on two streams without ordering between
+ *     them) race on the buffer; order them on one stream or with events.
+ */
+int gemm_f16_noalloc(const void* A, const void* B, const void* bias, void* C,
+                     int64_t M, int64_t N, int64_t K, int epilogue, void* cuda_stream);
 
 #ifdef __cplusplus
 }
