@@ -38,6 +38,7 @@ L2_BYTES = 129 * 10 ** 6
 FALLBACK_TENSOR_TFLOPS = 1900.0
 FP16_PER_BF16 = 1.0          # nominal dense fp16 rate / dense bf16 rate
 KERNEL_SOURCES = ("dense_fp16_tensor_tma_gb300/csrc/gemm_kernels.cuh",
+                  "dense_fp16_tensor_tma_gb300/csrc/gemm_kernels_pair.cuh",
                   "dense_fp16_tensor_tma_gb300/csrc/ptx.cuh",
                   "dense_fp16_tensor_tma_gb300/csrc/gemm_f16.cu")
 

@@ -21,7 +21,9 @@ GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED_DEVICE, GEMM_ERR_MISALIGNED 
 GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT, GEMM_ERR_NO_MEMORY, GEMM_ERR_SCRATCH_LIMIT = 4, 5, 6, 7
 
 EXPORTS = ("gemm_f16", "gemm_f16_status_string", "gemm_f16_last_cuda_error", "gemm_f16_debug_status",
-           "gemm_f16_release_workspace", "gemm_f16_plan", "gemm_f16_selftest_timeout", "gemm_f16_noalloc")
+           "gemm_f16_release_workspace", "gemm_f16_plan", "gemm_f16_selftest_timeout", "gemm_f16_noalloc",
+           "gemm_f16_force_config")
+CONFIGS = {"auto": 0, "pair256x256": 1, "128x256": 2, "128x128": 3, "128x64": 4}
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
@@ -43,6 +45,8 @@ lib.gemm_f16_selftest_timeout.argtypes = [_vp, ctypes.c_uint32]
 lib.gemm_f16_selftest_timeout.restype = _int
 lib.gemm_f16_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
 lib.gemm_f16_noalloc.restype = _int
+lib.gemm_f16_force_config.argtypes = [_int]
+lib.gemm_f16_force_config.restype = _int
 
 
 class GemmError(RuntimeError):
@@ -123,6 +127,16 @@ def gemm_f16_debug_status(stream=None):
 
 def gemm_f16_release_workspace() -> int:
     return lib.gemm_f16_release_workspace()
+
+
+def gemm_f16_force_config(config) -> int:
+    """Pin the kernel configuration ("auto", "pair256x256", "128x256", "128x128",
+    "128x64" or its number) for later calls; returns the previous setting."""
+    c = CONFIGS[config] if isinstance(config, str) else int(config)
+    prev = lib.gemm_f16_force_config(c)
+    if prev < 0:
+        raise ValueError(f"unknown configuration {config!r}")
+    return prev
 
 
 def gemm_f16_selftest_timeout(timeout_us: int = 1000, stream=None) -> int:

@@ -1,11 +1,13 @@
 // C-ABI boundary of the fused fp16 GEMM (declared in include/gemm_f16.h):
 // argument checks, device check, execution plan, TMA tensor-map encoding,
-// stream-ordered repack scratch, and kernel launch on the caller's stream.
+// operand repack into scratch (stream-ordered pool, or the fixed buffer of
+// the no-alloc entry point), and kernel launch on the caller's stream.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -13,6 +15,7 @@
 
 #include "gemm_f16.h"
 #include "gemm_kernels.cuh"
+#include "gemm_kernels_pair.cuh"
 
 namespace {
 
@@ -20,8 +23,11 @@ using namespace gemm_f16_dev;
 
 thread_local int t_last_cuda_error = 0;
 
-// Tile configurations (tile_n, stages): 128 x 256 is the throughput shape;
-// narrower tiles give small problems more CTAs.
+// Kernel configurations.  The CTA pair (256 x 256 per pair, 6 x 32 KiB ring
+// per CTA) is the throughput shape; single-CTA tiles of 128 x {256,128,64}
+// give small problems more CTAs.
+enum Config : int { CFG_AUTO = 0, CFG_PAIR_256 = 1, CFG_128x256 = 2, CFG_128x128 = 3, CFG_128x64 = 4 };
+constexpr int kStagesPair = 6;
 constexpr int kStages256 = 4;   // 4 x 48 KiB ring
 constexpr int kStages128 = 6;   // 6 x 32 KiB
 constexpr int kStages64 = 8;    // 8 x 24 KiB
@@ -34,15 +40,19 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 struct DeviceState {
     bool ready = false;
-    int status = GEMM_OK;      // result of the one-time checks
+    int status = GEMM_OK;        // result of the one-time checks
     int num_sms = 0;
-    cudaMemPool_t pool = nullptr;
+    int pair_clusters = 0;       // CTA pairs of the pair kernel that fit on the device at once
+    cudaMemPool_t pool = nullptr;  // repack scratch of gemm_f16, created on first use
+    bool noalloc_ready = false;
+    uint8_t* noalloc_scratch = nullptr;
 };
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 EncodeTiledFn g_encode = nullptr;
 uint64_t g_timeout_ns = 2000000000ull;   // 2 s per bounded wait
+std::atomic<int> g_force_config{CFG_AUTO};
 
 int cuda_fail(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
@@ -51,9 +61,11 @@ int cuda_fail(cudaError_t e) {
 
 struct Plan {
     int path = 0;          // 0 none, 1 bias-only, 2 tiled tensor-core kernel
-    int tile_n = 0, stages = 0, ctas = 0;
+    int cfg = CFG_AUTO;
+    int tile_m = 0, tile_n = 0, stages = 0, ctas = 0;
     bool pack_a = false, pack_b = false, vec_store = false;
     int64_t lda_packed = 0, ldb_packed = 0;
+    size_t a_scratch = 0, b_scratch = 0;   // repack bytes (A rounded to 256)
 };
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -72,10 +84,13 @@ int check_args(const void* A, const void* B, const void* bias, const void* C, in
     if (!aligned(C, 2) || (K > 0 && (!aligned(A, 2) || !aligned(B, 2))) ||
         (epilogue != GEMM_EPI_NONE && !aligned(bias, 2)))
         return GEMM_ERR_MISALIGNED;
+    // every tile index of the smallest tile shape must fit an int
+    if (((M + 127) / 128) * ((N + 63) / 64) >= (int64_t(1) << 31)) return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
 }
 
-Plan make_plan(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K, int num_sms) {
+Plan make_plan(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K, int num_sms,
+               int pair_clusters, int force) {
     Plan pl;
     if (M == 0 || N == 0) return pl;
     if (K == 0) {
@@ -88,23 +103,50 @@ Plan make_plan(const void* A, const void* B, const void* C, int64_t M, int64_t N
     pl.pack_b = !(aligned(B, 16) && N % 8 == 0);
     pl.lda_packed = pl.pack_a ? round_up(K, 8) : K;
     pl.ldb_packed = pl.pack_b ? round_up(N, 8) : N;
+    pl.a_scratch = pl.pack_a ? ((static_cast<size_t>(M * pl.lda_packed * 2) + 255) & ~size_t(255)) : 0;
+    pl.b_scratch = pl.pack_b ? static_cast<size_t>(K * pl.ldb_packed * 2) : 0;
     pl.vec_store = aligned(C, 16) && N % 8 == 0;
-    const int64_t tiles_m = (M + kBM - 1) / kBM;
-    // Widest tile that still gives every SM work; otherwise the narrowest.
-    pl.tile_n = 64;
-    for (int bn : {256, 128}) {
-        if (tiles_m * ((N + bn - 1) / bn) >= num_sms) { pl.tile_n = bn; break; }
+    const int64_t tiles_m = (M + 127) / 128;
+    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    int cfg = force;
+    if (cfg == CFG_AUTO) {
+        if (pair_tiles >= pair_clusters) {
+            cfg = CFG_PAIR_256;
+        } else {
+            // widest single-CTA tile that still gives every SM a tile; else the narrowest
+            cfg = CFG_128x64;
+            if (tiles_m * ((N + 255) / 256) >= num_sms) cfg = CFG_128x256;
+            else if (tiles_m * ((N + 127) / 128) >= num_sms) cfg = CFG_128x128;
+        }
     }
-    pl.stages = pl.tile_n == 256 ? kStages256 : (pl.tile_n == 128 ? kStages128 : kStages64);
-    const int64_t tiles = tiles_m * ((N + pl.tile_n - 1) / pl.tile_n);
-    pl.ctas = static_cast<int>(std::min<int64_t>(tiles, num_sms));
+    pl.cfg = cfg;
+    switch (cfg) {
+        case CFG_PAIR_256:
+            pl.tile_m = 256; pl.tile_n = 256; pl.stages = kStagesPair;
+            pl.ctas = 2 * static_cast<int>(std::min<int64_t>(pair_tiles, std::max(1, pair_clusters)));
+            break;
+        case CFG_128x256: pl.tile_m = 128; pl.tile_n = 256; pl.stages = kStages256; break;
+        case CFG_128x128: pl.tile_m = 128; pl.tile_n = 128; pl.stages = kStages128; break;
+        default: pl.tile_m = 128; pl.tile_n = 64; pl.stages = kStages64; break;
+    }
+    if (cfg != CFG_PAIR_256)
+        pl.ctas = static_cast<int>(std::min<int64_t>(tiles_m * ((N + pl.tile_n - 1) / pl.tile_n), num_sms));
     return pl;
 }
 
-int init_device(int dev) {
-    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
-    std::lock_guard<std::mutex> lk(g_mu);
-    DeviceState& st = g_dev[dev];
+cudaLaunchConfig_t launch_config(int ctas, uint32_t smem, cudaStream_t s) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    return cfg;
+}
+
+// One-time per-device checks and kernel attributes (allocates nothing).
+// Called with g_mu held.
+int init_common_locked(int dev, DeviceState& st) {
     if (st.ready) return st.status;
     int major = 0, minor = 0, sms = 0;
     cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
@@ -124,8 +166,11 @@ int init_device(int dev) {
             return cuda_fail(e != cudaSuccess ? e : cudaErrorSymbolNotFound);
         g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    e = cudaFuncSetAttribute(gemm_f16_tc_kernel<256, kStages256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SmemPlan<256, kStages256>::kDynamicBytes);
+    e = cudaFuncSetAttribute(gemm_f16_tc2_kernel<kStagesPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SmemPlanPair<kStagesPair>::kDynamicBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_f16_tc_kernel<256, kStages256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SmemPlan<256, kStages256>::kDynamicBytes);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gemm_f16_tc_kernel<128, kStages128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SmemPlan<128, kStages128>::kDynamicBytes);
@@ -133,17 +178,24 @@ int init_device(int dev) {
         e = cudaFuncSetAttribute(gemm_f16_tc_kernel<64, kStages64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SmemPlan<64, kStages64>::kDynamicBytes);
     if (e != cudaSuccess) return cuda_fail(e);
-    // A library-owned pool keeps repack scratch cached between calls without
-    // changing the device's default pool.
-    cudaMemPoolProps props;
-    std::memset(&props, 0, sizeof(props));
-    props.allocType = cudaMemAllocationTypePinned;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = dev;
-    e = cudaMemPoolCreate(&st.pool, &props);
-    if (e != cudaSuccess) return cuda_fail(e);
-    uint64_t keep = ~0ull;
-    cudaMemPoolSetAttribute(st.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    // How many CTA pairs fit at once decides the persistent grid of the pair kernel.
+    {
+        cudaLaunchConfig_t cfg = launch_config(sms, SmemPlanPair<kStagesPair>::kDynamicBytes, nullptr);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(gemm_f16_tc2_kernel<kStagesPair>),
+                                           &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = sms / 2;
+        }
+        st.pair_clusters = n;
+    }
     if (const char* env = std::getenv("GEMM_F16_TIMEOUT_MS")) {
         const long ms = std::strtol(env, nullptr, 10);
         if (ms > 0) g_timeout_ns = static_cast<uint64_t>(ms) * 1000000ull;
@@ -151,6 +203,33 @@ int init_device(int dev) {
     st.num_sms = sms;
     st.ready = true;
     st.status = GEMM_OK;
+    return GEMM_OK;
+}
+
+int init_device(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    return init_common_locked(dev, g_dev[dev]);
+}
+
+// The library-owned pool for gemm_f16's repack scratch (keeps memory cached
+// between calls without touching the device's default pool).
+int ensure_pool(int dev) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& st = g_dev[dev];
+    if (st.pool != nullptr) return GEMM_OK;
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaError_t e = cudaMemPoolCreate(&st.pool, &props);
+    if (e != cudaSuccess) {
+        st.pool = nullptr;
+        return cuda_fail(e);
+    }
+    uint64_t keep = ~0ull;
+    cudaMemPoolSetAttribute(st.pool, cudaMemPoolAttrReleaseThreshold, &keep);
     return GEMM_OK;
 }
 
@@ -186,13 +265,68 @@ int launch_repack(uint16_t* dst, const void* src, int64_t rows, int64_t cols, in
 
 template <int BN, int STAGES>
 int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& prm, int ctas, cudaStream_t s) {
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = SmemPlan<BN, STAGES>::kDynamicBytes;
-    cfg.stream = s;
+    cudaLaunchConfig_t cfg = launch_config(ctas, SmemPlan<BN, STAGES>::kDynamicBytes, s);
     cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_tc_kernel<BN, STAGES>, ta, tb, prm);
+    return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+}
+
+int launch_tc_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& prm, int ctas, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = launch_config(ctas, SmemPlanPair<kStagesPair>::kDynamicBytes, s);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_kernel<kStagesPair>, ta, tb, prm);
+    return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+}
+
+// Everything after scratch is settled: repack (into `scratch`, which holds
+// pl.a_scratch + pl.b_scratch bytes when a repack is planned), tensor maps,
+// and the tensor-core kernel, all on stream `s`.
+int enqueue_plan(const Plan& pl, const void* A, const void* B, const __half* biasp, void* C, int64_t M, int64_t N,
+                 int64_t K, int epilogue, uint8_t* scratch, cudaStream_t s) {
+    int st = GEMM_OK;
+    const void* a_src = A;
+    const void* b_src = B;
+    if (pl.pack_a) {
+        st = launch_repack(reinterpret_cast<uint16_t*>(scratch), A, M, K, K, pl.lda_packed, s);
+        a_src = scratch;
+    }
+    if (st == GEMM_OK && pl.pack_b) {
+        uint16_t* bdst = reinterpret_cast<uint16_t*>(scratch + pl.a_scratch);
+        st = launch_repack(bdst, B, K, N, N, pl.ldb_packed, s);
+        b_src = bdst;
+    }
+    CUtensorMap ta, tb;
+    if (st == GEMM_OK) st = encode_2d(&ta, a_src, K, M, pl.lda_packed, kBK, kBM);
+    if (st == GEMM_OK) st = encode_2d(&tb, b_src, N, K, pl.ldb_packed, 64, kBK);
+    if (st != GEMM_OK) return st;
+    GemmParams prm;
+    prm.C = static_cast<__half*>(C);
+    prm.bias = biasp;
+    prm.M = static_cast<int>(M);
+    prm.N = static_cast<int>(N);
+    prm.K = static_cast<int>(K);
+    prm.ldc = static_cast<int>(N);
+    prm.epi = epilogue;
+    prm.vec_store = pl.vec_store ? 1 : 0;
+    prm.group_m = 8;
+    prm.timeout_ns = g_timeout_ns;
+    switch (pl.cfg) {
+        case CFG_PAIR_256: return launch_tc_pair(ta, tb, prm, pl.ctas, s);
+        case CFG_128x256: return launch_tc<256, kStages256>(ta, tb, prm, pl.ctas, s);
+        case CFG_128x128: return launch_tc<128, kStages128>(ta, tb, prm, pl.ctas, s);
+        default: return launch_tc<64, kStages64>(ta, tb, prm, pl.ctas, s);
+    }
+}
+
+int enqueue_bias_only(const Plan& pl, const __half* biasp, void* C, int64_t M, int64_t N, int epilogue,
+                      cudaStream_t s) {
+    gemm_f16_bias_only_kernel<<<pl.ctas, 256, 0, s>>>(static_cast<__half*>(C), biasp, M, N, N, epilogue);
+    cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
 
@@ -205,59 +339,20 @@ int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& pr
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-struct NoAllocState {
-    bool ready = false;
-    int status = GEMM_OK;
-    int num_sms = 0;
-    uint8_t* scratch = nullptr;   // device address of g_noalloc_scratch on this device
-};
-NoAllocState g_noalloc[kMaxDevices];
-
-// Per-device set-up of the no-alloc path: device check, tensor-map encoder,
-// kernel attributes and the scratch address.  Allocates nothing.
+// Per-device set-up of the no-alloc path: the common checks plus the device
+// address of the fixed buffer.  Allocates nothing.
 int init_device_noalloc(int dev) {
     if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
     std::lock_guard<std::mutex> lk(g_mu);
-    NoAllocState& st = g_noalloc[dev];
-    if (st.ready) return st.status;
-    int major = 0, minor = 0, sms = 0;
-    cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (major != 10 || minor != 3) {
-        st.ready = true;
-        st.status = GEMM_ERR_UNSUPPORTED_DEVICE;
-        return st.status;
-    }
-    if (g_encode == nullptr) {
-        void* fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
-            return cuda_fail(e != cudaSuccess ? e : cudaErrorSymbolNotFound);
-        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
-    }
-    e = cudaFuncSetAttribute(gemm_f16_tc_kernel<256, kStages256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SmemPlan<256, kStages256>::kDynamicBytes);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemm_f16_tc_kernel<128, kStages128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SmemPlan<128, kStages128>::kDynamicBytes);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemm_f16_tc_kernel<64, kStages64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SmemPlan<64, kStages64>::kDynamicBytes);
-    if (e != cudaSuccess) return cuda_fail(e);
+    DeviceState& st = g_dev[dev];
+    const int s = init_common_locked(dev, st);
+    if (s != GEMM_OK) return s;
+    if (st.noalloc_ready) return GEMM_OK;
     void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
     if (e != cudaSuccess || ptr == nullptr) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
-    if (const char* env = std::getenv("GEMM_F16_TIMEOUT_MS")) {
-        const long ms = std::strtol(env, nullptr, 10);
-        if (ms > 0) g_timeout_ns = static_cast<uint64_t>(ms) * 1000000ull;
-    }
-    st.scratch = static_cast<uint8_t*>(ptr);
-    st.num_sms = sms;
-    st.ready = true;
-    st.status = GEMM_OK;
+    st.noalloc_scratch = static_cast<uint8_t*>(ptr);
+    st.noalloc_ready = true;
     return GEMM_OK;
 }
 
@@ -282,14 +377,19 @@ const char* gemm_f16_status_string(int status) {
 
 int gemm_f16_last_cuda_error(void) { return t_last_cuda_error; }
 
+int gemm_f16_force_config(int config) {
+    if (config < CFG_AUTO || config > CFG_128x64) return -1;
+    return g_force_config.exchange(config);
+}
+
 int gemm_f16_plan(const void* A, const void* B, const void* bias, const void* C, int64_t M, int64_t N, int64_t K,
                   int epilogue, int num_sms, int64_t plan[8]) {
     if (plan == nullptr || num_sms <= 0) return GEMM_ERR_INVALID_ARG;
     const int st = check_args(A, B, bias, C, M, N, K, epilogue);
     if (st != GEMM_OK) return st;
-    const Plan pl = make_plan(A, B, C, M, N, K, num_sms);
+    const Plan pl = make_plan(A, B, C, M, N, K, num_sms, num_sms / 2, g_force_config.load());
     plan[0] = pl.path;
-    plan[1] = pl.path == 2 ? kBM : 0;
+    plan[1] = pl.tile_m;
     plan[2] = pl.tile_n;
     plan[3] = pl.stages;
     plan[4] = pl.ctas;
@@ -309,66 +409,27 @@ int gemm_f16(const void* A, const void* B, const void* bias, void* C, int64_t M,
     if (e != cudaSuccess) return cuda_fail(e);
     st = init_device(dev);
     if (st != GEMM_OK) return st;
-    DeviceState& ds = g_dev[dev];
+    const DeviceState& ds = g_dev[dev];
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-    const Plan pl = make_plan(A, B, C, M, N, K, ds.num_sms);
+    const Plan pl = make_plan(A, B, C, M, N, K, ds.num_sms, ds.pair_clusters, g_force_config.load());
     const __half* biasp = epilogue == GEMM_EPI_NONE ? nullptr : static_cast<const __half*>(bias);
+    if (pl.path == 1) return enqueue_bias_only(pl, biasp, C, M, N, epilogue, s);
 
-    if (pl.path == 1) {
-        gemm_f16_bias_only_kernel<<<pl.ctas, 256, 0, s>>>(static_cast<__half*>(C), biasp, M, N, N, epilogue);
-        e = cudaGetLastError();
-        return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
-    }
-
-    // Repack operands the tensor map cannot describe (unaligned base or row pitch).
-    const void* a_src = A;
-    const void* b_src = B;
     void* scratch = nullptr;
-    size_t a_bytes = pl.pack_a ? static_cast<size_t>(M * pl.lda_packed * 2) : 0;
-    size_t b_bytes = pl.pack_b ? static_cast<size_t>(K * pl.ldb_packed * 2) : 0;
-    a_bytes = (a_bytes + 255) & ~size_t(255);
-    if (a_bytes + b_bytes > 0) {
-        e = cudaMallocFromPoolAsync(&scratch, a_bytes + b_bytes, ds.pool, s);
+    const size_t scratch_bytes = pl.a_scratch + pl.b_scratch;
+    if (scratch_bytes > 0) {
+        st = ensure_pool(dev);
+        if (st != GEMM_OK) return st;
+        e = cudaMallocFromPoolAsync(&scratch, scratch_bytes, ds.pool, s);
         if (e != cudaSuccess) {
             t_last_cuda_error = static_cast<int>(e);
             cudaGetLastError();
             return GEMM_ERR_NO_MEMORY;
         }
-        if (pl.pack_a) {
-            st = launch_repack(static_cast<uint16_t*>(scratch), A, M, K, K, pl.lda_packed, s);
-            a_src = scratch;
-        }
-        if (st == GEMM_OK && pl.pack_b) {
-            uint16_t* bdst = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(scratch) + a_bytes);
-            st = launch_repack(bdst, B, K, N, N, pl.ldb_packed, s);
-            b_src = bdst;
-        }
     }
-
-    CUtensorMap ta, tb;
-    if (st == GEMM_OK) st = encode_2d(&ta, a_src, K, M, pl.lda_packed, kBK, kBM);
-    if (st == GEMM_OK) st = encode_2d(&tb, b_src, N, K, pl.ldb_packed, 64, kBK);
-    if (st == GEMM_OK) {
-        GemmParams prm;
-        prm.C = static_cast<__half*>(C);
-        prm.bias = biasp;
-        prm.M = static_cast<int>(M);
-        prm.N = static_cast<int>(N);
-        prm.K = static_cast<int>(K);
-        prm.ldc = static_cast<int>(N);
-        prm.epi = epilogue;
-        prm.vec_store = pl.vec_store ? 1 : 0;
-        prm.group_m = 8;
-        prm.timeout_ns = g_timeout_ns;
-        if (pl.tile_n == 256)
-            st = launch_tc<256, kStages256>(ta, tb, prm, pl.ctas, s);
-        else if (pl.tile_n == 128)
-            st = launch_tc<128, kStages128>(ta, tb, prm, pl.ctas, s);
-        else
-            st = launch_tc<64, kStages64>(ta, tb, prm, pl.ctas, s);
-    }
+    st = enqueue_plan(pl, A, B, biasp, C, M, N, K, epilogue, static_cast<uint8_t*>(scratch), s);
     if (scratch != nullptr) {
-        e = cudaFreeAsync(scratch, s);   // stream-ordered: freed after the GEMM reads it
+        e = cudaFreeAsync(scratch, s);   // stream-ordered: freed after the GEMM has read it
         if (e != cudaSuccess && st == GEMM_OK) st = cuda_fail(e);
     }
     return st;
@@ -384,53 +445,16 @@ int gemm_f16_noalloc(const void* A, const void* B, const void* bias, void* C, in
     if (e != cudaSuccess) return cuda_fail(e);
     st = init_device_noalloc(dev);
     if (st != GEMM_OK) return st;
-    const NoAllocState& ns = g_noalloc[dev];
+    const DeviceState& ds = g_dev[dev];
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-    const Plan pl = make_plan(A, B, C, M, N, K, ns.num_sms);
+    const Plan pl = make_plan(A, B, C, M, N, K, ds.num_sms, ds.pair_clusters, g_force_config.load());
     const __half* biasp = epilogue == GEMM_EPI_NONE ? nullptr : static_cast<const __half*>(bias);
-
-    if (pl.path == 1) {
-        gemm_f16_bias_only_kernel<<<pl.ctas, 256, 0, s>>>(static_cast<__half*>(C), biasp, M, N, N, epilogue);
-        e = cudaGetLastError();
-        return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
-    }
-
+    if (pl.path == 1) return enqueue_bias_only(pl, biasp, C, M, N, epilogue, s);
     // Same repack layout as gemm_f16 (A first, 256-byte aligned, then B), but
     // inside the fixed buffer; nothing in it has to start at zero because the
     // tensor maps stop at the true extents.
-    size_t a_bytes = pl.pack_a ? static_cast<size_t>(M * pl.lda_packed * 2) : 0;
-    const size_t b_bytes = pl.pack_b ? static_cast<size_t>(K * pl.ldb_packed * 2) : 0;
-    a_bytes = (a_bytes + 255) & ~size_t(255);
-    if (a_bytes + b_bytes > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
-    const void* a_src = A;
-    const void* b_src = B;
-    if (pl.pack_a) {
-        st = launch_repack(reinterpret_cast<uint16_t*>(ns.scratch), A, M, K, K, pl.lda_packed, s);
-        a_src = ns.scratch;
-    }
-    if (st == GEMM_OK && pl.pack_b) {
-        uint16_t* bdst = reinterpret_cast<uint16_t*>(ns.scratch + a_bytes);
-        st = launch_repack(bdst, B, K, N, N, pl.ldb_packed, s);
-        b_src = bdst;
-    }
-    CUtensorMap ta, tb;
-    if (st == GEMM_OK) st = encode_2d(&ta, a_src, K, M, pl.lda_packed, kBK, kBM);
-    if (st == GEMM_OK) st = encode_2d(&tb, b_src, N, K, pl.ldb_packed, 64, kBK);
-    if (st != GEMM_OK) return st;
-    GemmParams prm;
-    prm.C = static_cast<__half*>(C);
-    prm.bias = biasp;
-    prm.M = static_cast<int>(M);
-    prm.N = static_cast<int>(N);
-    prm.K = static_cast<int>(K);
-    prm.ldc = static_cast<int>(N);
-    prm.epi = epilogue;
-    prm.vec_store = pl.vec_store ? 1 : 0;
-    prm.group_m = 8;
-    prm.timeout_ns = g_timeout_ns;
-    if (pl.tile_n == 256) return launch_tc<256, kStages256>(ta, tb, prm, pl.ctas, s);
-    if (pl.tile_n == 128) return launch_tc<128, kStages128>(ta, tb, prm, pl.ctas, s);
-    return launch_tc<64, kStages64>(ta, tb, prm, pl.ctas, s);
+    if (pl.a_scratch + pl.b_scratch > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
+    return enqueue_plan(pl, A, B, biasp, C, M, N, K, epilogue, ds.noalloc_scratch, s);
 }
 
 int gemm_f16_debug_status(void* cuda_stream, uint32_t* detail) {

@@ -1,0 +1,284 @@
+// CTA-pair variant of the fused fp16 GEMM:  C = epilogue(A.B + bias).
+//
+// Same method as gemm_kernels.cuh (tile loop over K, tensor-core tile product
+// into an on-chip fp32 accumulator, fused bias + activation, one write of C:
+// "writing-tilelang-kernels", GEMM (Minimal); "TileLang: Write, Autotune, and
+// Ship Fused Tensor-Core Kernels from Python", Why tile-level control
+// matters), mapped onto two SMs that cooperate on one 256 x 256 output tile:
+//
+//   * a cluster of 2 CTAs; CTA r (r = 0, 1) owns output rows m0 + 128r ..
+//     m0 + 128r + 127 and loads only its own 128 rows of A and its own 128
+//     columns of B per K-block (16 KiB + 16 KiB per stage);
+//   * one thread of CTA 0 issues tcgen05.mma.cta_group::2 (M = 256, N = 256,
+//     K = 16): each SM's tensor core computes its 128 rows against all 256
+//     columns, taking B from both SMs' shared memory, so per SM the operand
+//     traffic is 2/3 of the single-SM 128 x 256 tile for the same FLOPs;
+//   * both CTAs' TMA loads complete on CTA 0's "full" barrier; MMA completion
+//     is multicast to both CTAs' "empty" and "accumulator full" barriers;
+//     both CTAs' epilogues arrive on CTA 0's "accumulator empty" barrier;
+//   * each CTA's epilogue reads its own tensor memory (its 128 rows x 256
+//     fp32 columns, double-buffered) and writes its own rows of C.
+#pragma once
+
+#include "gemm_kernels.cuh"
+
+namespace gemm_f16_dev {
+
+constexpr uint32_t kBHalfBytes = 128 * kBK * 2;   // this CTA's 128 columns of a B stage: 16 KiB
+
+template <int STAGES>
+struct SmemPlanPair {
+    static constexpr uint32_t kA = 0;
+    static constexpr uint32_t kB = kA + STAGES * kATileBytes;
+    static constexpr uint32_t kBias = kB + STAGES * kBHalfBytes;        // 4 warps x 256 floats
+    static constexpr uint32_t kBars = kBias + 4 * 256 * 4;
+    static constexpr uint32_t kNumBars = 2 * STAGES + 2 + 2 + 1;
+    static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
+    static constexpr uint32_t kAbort = kTmemSlot + 4;
+    static constexpr uint32_t kEnd = kAbort + 4;
+    static constexpr uint32_t kDynamicBytes = kEnd + 1024;
+};
+
+__device__ __forceinline__ TileCoord tile_coord_bm(int t, int tiles_m, int tiles_n, int group_m, int BM, int BN) {
+    const int per_group = group_m * tiles_n;
+    const int g = t / per_group;
+    const int first_m = g * group_m;
+    const int rows = min(tiles_m - first_m, group_m);
+    const int r = t - g * per_group;
+    TileCoord c;
+    c.m0 = (first_m + r % rows) * BM;
+    c.n0 = (r / rows) * BN;
+    return c;
+}
+
+template <int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const GemmParams p) {
+    using SP = SmemPlanPair<STAGES>;
+    constexpr int PM = 256;                  // pair tile rows = MMA M
+    constexpr int BN = 256;                  // pair tile columns = MMA N
+    constexpr uint32_t kIdesc = idesc_f16_f32(PM, BN, /*b_mn_major=*/true);
+    constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators of 256 fp32 columns
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;   // identical in both CTAs of the pair
+    uint8_t* base = smem_raw + (base_s - raw_s);
+
+    const uint32_t sA = base_s + SP::kA;
+    const uint32_t sB = base_s + SP::kB;
+    float* bias_s = reinterpret_cast<float*>(base + SP::kBias);
+    const uint32_t bars = base_s + SP::kBars;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
+    auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bars + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + SP::kTmemSlot);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + SP::kAbort);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);      // CTA 0's producer arrives; both CTAs' bytes complete it
+            mbar_init(empty_bar(s), 1);     // one multicast MMA commit
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);      // one multicast MMA commit
+            mbar_init(acce_bar(b), 8);      // 4 epilogue warps x 2 CTAs (used on CTA 0)
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish_pair();
+        tc_fence_before();
+    }
+    __syncthreads();
+    cluster_sync_all();     // both CTAs' barriers exist before any cross-CTA arrive or complete_tx
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int tiles_m = (p.M + PM - 1) / PM;
+    const int tiles_n = (p.N + BN - 1) / BN;
+    const int num_tiles = tiles_m * tiles_n;
+    const int kblocks = (p.K + kBK - 1) / kBK;
+    const int cid = blockIdx.x >> 1;
+    const int nclusters = gridDim.x >> 1;
+    unsigned int* status = &g_status;
+
+    // Boxes each CTA loads for a tile: its A box unless all 128 rows are past
+    // M, and those of its two 64-column B boxes that start before N.  The
+    // skipped ones would only feed accumulator rows / columns that are never
+    // stored.
+    auto a_live = [&](int m0, int r) { return (m0 + 128 * r) < p.M ? 1 : 0; };
+    auto b_live = [&](int n0, int r) { return max(0, min(2, (p.N - (n0 + 128 * r) + 63) / 64)); };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int t = cid; ok && t < num_tiles; t += nclusters) {
+                const TileCoord tc = tile_coord_bm(t, tiles_m, tiles_n, p.group_m, PM, BN);
+                const int my_a = a_live(tc.m0, rank);
+                const int my_b = b_live(tc.n0, rank);
+                const uint32_t pair_bytes =
+                    static_cast<uint32_t>(a_live(tc.m0, 0) + a_live(tc.m0, 1)) * kATileBytes +
+                    static_cast<uint32_t>(b_live(tc.n0, 0) + b_live(tc.n0, 1)) * kBBoxBytes;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_cluster_bounded(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, status,
+                                                   ROLE_PRODUCER, BAR_EMPTY)) { ok = false; break; }
+                    const uint32_t full_leader = mapa_shared(full_bar(stage), 0);
+                    if (leader) mbar_arrive_expect_tx(full_bar(stage), pair_bytes);
+                    if (my_a)
+                        tma_load_2d_pair(sA + stage * kATileBytes, &tmA, full_leader, kb * kBK, tc.m0 + 128 * rank);
+                    for (int c = 0; c < my_b; ++c)
+                        tma_load_2d_pair(sB + stage * kBHalfBytes + c * kBBoxBytes, &tmB, full_leader,
+                                         tc.n0 + 128 * rank + 64 * c, kb * kBK);
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // CTA 0's full barriers count both CTAs' bytes: draining them there
+            // covers every load of the pair still in flight.
+            if (leader) {
+                const int pending = min(issued, STAGES);
+                for (int i = 0; i < pending; ++i) {
+                    if (--stage < 0) { stage = STAGES - 1; phase ^= 1u; }
+                    mbar_wait_cluster_bounded(full_bar(stage), phase, p.timeout_ns, nullptr, status, ROLE_DRAIN,
+                                              BAR_FULL);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (CTA 0 only)
+        if (leader && lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int t = cid; ok && t < num_tiles; t += nclusters) {
+                if (!mbar_wait_cluster_bounded(acce_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag, status,
+                                               ROLE_MMA, BAR_ACC_EMPTY)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_cluster_bounded(full_bar(stage), phase, p.timeout_ns, abort_flag, status,
+                                                   ROLE_MMA, BAR_FULL)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a0 = sA + stage * kATileBytes;
+                    const uint32_t b0 = sB + stage * kBHalfBytes;
+#pragma unroll
+                    for (int k = 0; k < kBK / kUMMA_K; ++k) {
+                        // same layouts as the single-SM kernel; B here is this
+                        // CTA's 128 columns (two 64-column boxes, LBO 8 KiB)
+                        const uint64_t adesc = smem_desc_sw128(a0 + k * 32, 0, 1024);
+                        const uint64_t bdesc = smem_desc_sw128(b0 + k * 2048, kBBoxBytes, 1024);
+                        tc_mma_f16_pair(d_tmem, adesc, bdesc, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    tc_commit_pair_mc(empty_bar(stage), 0x3);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit_pair_mc(accf_bar(acc), 0x3);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            tc_commit_pair_mc(drain_bar, 0x1);
+            mbar_wait_bounded(drain_bar, 0, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_DRAIN);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        const int ew = warp - 2;
+        float* my_bias = bias_s + ew * BN;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        const bool has_bias = p.epi != EPI_NONE;
+        for (int t = cid; t < num_tiles; t += nclusters) {
+            const TileCoord tc = tile_coord_bm(t, tiles_m, tiles_n, p.group_m, PM, BN);
+            __syncwarp();
+            if (has_bias) {
+                for (int i = lane; i < BN; i += 32) {
+                    const int n = tc.n0 + i;
+                    my_bias[i] = n < p.N ? __half2float(p.bias[n]) : 0.0f;
+                }
+            }
+            __syncwarp();
+            const bool ready = mbar_wait_cluster_bounded(accf_bar(acc), acc_phase, p.timeout_ns, abort_flag, status,
+                                                         ROLE_EPILOGUE, BAR_ACC_FULL);
+            if (!__all_sync(0xffffffffu, ready)) break;
+            tc_fence_after();
+            const int row = tc.m0 + 128 * static_cast<int>(rank) + 32 * q + lane;
+            const bool row_ok = row < p.M;
+            __half* crow = p.C + static_cast<int64_t>(row) * p.ldc;
+            const uint32_t t_base = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(32 * q) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_base + 32u * c, r);
+                tmem_wait_ld();
+                const int col0 = tc.n0 + 32 * c;
+                if (row_ok && col0 < p.N) {
+                    uint32_t h[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        float x0 = __uint_as_float(r[2 * j]);
+                        float x1 = __uint_as_float(r[2 * j + 1]);
+                        if (has_bias) {
+                            x0 += my_bias[32 * c + 2 * j];
+                            x1 += my_bias[32 * c + 2 * j + 1];
+                        }
+                        x0 = apply_act(x0, p.epi);
+                        x1 = apply_act(x1, p.epi);
+                        const __half2 hv = __floats2half2_rn(x0, x1);
+                        h[j] = *reinterpret_cast<const uint32_t*>(&hv);
+                    }
+                    if (p.vec_store && col0 + 32 <= p.N) {
+                        uint4* dst = reinterpret_cast<uint4*>(crow + col0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            if (col0 + j < p.N) {
+                                const uint16_t bits = static_cast<uint16_t>((h[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+                                reinterpret_cast<uint16_t*>(crow)[col0 + j] = bits;
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    __syncthreads();
+    cluster_sync_all();     // the peer no longer touches this CTA's shared or tensor memory
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace gemm_f16_dev

@@ -101,8 +101,9 @@ int gemm_f16_release_workspace(void);
 /*
  * Host-only planning query (no device access): the execution plan that
  * gemm_f16 would choose for these sizes and base addresses on a device with
- * `num_sms` SMs.  plan[0..7] receive: path (0 none, 1 bias-only K==0,
- * 2 tiled tensor-core kernel, 3 swap-AB skinny kernel), tile_m, tile_n,
+ * `num_sms` SMs (assuming num_sms/2 co-resident CTA pairs).  plan[0..7]
+ * receive: path (0 none, 1 bias-only K==0, 2 tiled tensor-core kernel),
+ * tile_m (256 for the CTA-pair kernel), tile_n,
  * pipeline stages, CTAs launched, repack A (0/1), repack B (0/1), vector
  * stores of C (0/1).  Returns a status code like gemm_f16 (argument errors
  * only).  Diagnostic; it has no counterpart on the pages.
@@ -110,6 +111,16 @@ int gemm_f16_release_workspace(void);
 int gemm_f16_plan(const void* A, const void* B, const void* bias, const void* C,
                   int64_t M, int64_t N, int64_t K, int epilogue, int num_sms,
                   int64_t plan[8]);
+
+/*
+ * Diagnostic (no counterpart on the pages): pins the kernel configuration
+ * that every later call in this process uses, for tests and tile sweeps.
+ *   0 automatic (the default), 1 CTA pair with a 256 x 256 tile,
+ *   2 single CTA 128 x 256, 3 single CTA 128 x 128, 4 single CTA 128 x 64.
+ * Returns the previous setting, or -1 (nothing changed) for an unknown
+ * value.  Process-wide; set it while no other host thread is calling.
+ */
+int gemm_f16_force_config(int config);
 
 /*
  * Diagnostic for the bounded-wait machinery (no counterpart on the pages):

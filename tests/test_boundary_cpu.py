@@ -70,10 +70,33 @@ def test_argument_errors_need_no_device(g, args, expect):
     assert g.gemm_f16_ptr(a, b, bias, c, M, N, K, epi, 0) == expect
 
 
-def test_plan_large_square_uses_wide_tiles(g):
+def test_plan_large_square_uses_cta_pairs(g):
     p = g.gemm_f16_plan(8192, 8192, 8192, "bias_gelu_erf", num_sms=152)
-    assert p == {"path": 2, "tile_m": 128, "tile_n": 256, "stages": 4, "ctas": 152,
+    assert p == {"path": 2, "tile_m": 256, "tile_n": 256, "stages": 6, "ctas": 152,
                  "pack_a": 0, "pack_b": 0, "vec_store": 1}
+    p = g.gemm_f16_plan(4096, 4096, 4096, "bias_gelu_erf", num_sms=152)
+    assert p["tile_m"] == 256 and p["ctas"] == 152
+
+
+def test_plan_mid_size_uses_single_cta_tiles(g):
+    # 18 pair tiles < 76 pairs: single-CTA 128-row tiles give more CTAs
+    p = g.gemm_f16_plan(1536, 768, 4096, "none", num_sms=152)
+    assert p["tile_m"] == 128 and p["tile_n"] == 64 and p["ctas"] == 144
+
+
+def test_force_config_overrides_and_restores(g):
+    prev = g.gemm_f16_force_config("128x256")
+    try:
+        p = g.gemm_f16_plan(8192, 8192, 8192, "none", num_sms=152)
+        assert (p["tile_m"], p["tile_n"], p["stages"]) == (128, 256, 4)
+        g.gemm_f16_force_config("pair256x256")
+        p = g.gemm_f16_plan(200, 300, 64, "none", num_sms=152)
+        assert (p["tile_m"], p["tile_n"], p["ctas"]) == (256, 256, 4)
+    finally:
+        g.gemm_f16_force_config(prev)
+    with pytest.raises(ValueError):
+        g.gemm_f16_force_config(9)
+    assert g.gemm_f16_plan(8192, 8192, 8192, "none", num_sms=152)["tile_m"] == 256
 
 
 def test_plan_small_problem_uses_narrow_tiles(g):
@@ -86,6 +109,7 @@ def test_plan_small_problem_uses_narrow_tiles(g):
 def test_plan_ragged_n_repacks_b_and_stores_narrow(g):
     p = g.gemm_f16_plan(3001, 5003, 1000, "bias_relu", num_sms=152)
     assert p["pack_b"] == 1 and p["pack_a"] == 0 and p["vec_store"] == 0 and p["path"] == 2
+    assert p["tile_m"] == 256 and p["ctas"] == 152      # 12 x 20 pair tiles
 
 
 def test_plan_unaligned_pointers_repack(g):

@@ -260,3 +260,54 @@ def test_bounded_wait_reports_timeout_and_context_survives(g, torch_dev, oracle_
     rng = np.random.default_rng(11)
     A, B = rand16(rng, (128, 64)), rand16(rng, (64, 128))
     assert_parity(run(g, torch_dev, A, B, None, "none"), oracle_mod.gemm(A, B, None, "none"))
+
+
+# ---------------------------------------------------------------- every kernel configuration
+
+CONFIGS = ["pair256x256", "128x256", "128x128", "128x64"]
+
+
+@pytest.fixture
+def forced(g):
+    prev = g.gemm_f16_force_config("auto")
+    yield g
+    g.gemm_f16_force_config(prev)
+
+
+@pytest.mark.parametrize("cfg", CONFIGS)
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (512, 768, 320), (300, 200, 136), (129, 520, 1000)])
+def test_forced_config_integer_exact(forced, torch_dev, oracle_mod, cfg, M, N, K):
+    g = forced
+    g.gemm_f16_force_config(cfg)
+    rng = np.random.default_rng(M + 3 * N + 7 * K)
+    A = rng.integers(-2, 3, (M, K)).astype(np.float16)
+    B = rng.integers(-2, 3, (K, N)).astype(np.float16)
+    bias = rng.integers(-8, 9, N).astype(np.float16)
+    got = run(g, torch_dev, A, B, bias, "bias")
+    assert np.array_equal(got, oracle_mod.gemm(A, B, bias, "bias"))
+
+
+@pytest.mark.parametrize("cfg", CONFIGS)
+@pytest.mark.parametrize("M,N,K,epi", [(1, 1, 1, "bias_gelu_erf"), (257, 129, 65, "bias_relu"),
+                                       (700, 1100, 333, "bias_gelu_erf"), (2000, 600, 96, "none"),
+                                       (40, 5003, 200, "bias")])
+def test_forced_config_random(forced, torch_dev, oracle_mod, cfg, M, N, K, epi):
+    g = forced
+    g.gemm_f16_force_config(cfg)
+    rng = np.random.default_rng(M * 5 + N + K)
+    A, B, bias = rand16(rng, (M, K), 0.5), rand16(rng, (K, N), 0.5), rand16(rng, N)
+    got = run(g, torch_dev, A, B, bias, epi)
+    assert_parity(got, oracle_mod.gemm(A, B, bias if epi != "none" else None, epi), f"{cfg} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("cfg", CONFIGS)
+def test_forced_config_many_tiles_per_cta(forced, torch_dev, oracle_mod, cfg):
+    # several tiles per persistent CTA (both TMEM accumulators reused repeatedly)
+    g = forced
+    g.gemm_f16_force_config(cfg)
+    rng = np.random.default_rng(17)
+    M, N, K = 4096, 4096, 128
+    A, B, bias = rand16(rng, (M, K), 0.3), rand16(rng, (K, N), 0.3), rand16(rng, N)
+    got = run(g, torch_dev, A, B, bias, "bias_gelu_erf")
+    rows = np.arange(3, M, 61)
+    assert_parity(got[rows], oracle_mod.gemm_rows(A, B, bias, "bias_gelu_erf", rows), cfg)
