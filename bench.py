@@ -66,6 +66,15 @@ def workload_config(w, epi):
     }
 
 
+def kernel_name(plan):
+    """Name of the tensor-core kernel a plan launches."""
+    if plan.get("path") != 2:
+        return "gemm_f16_bias_only_kernel"
+    if plan.get("tile_m") == 256:
+        return f"gemm_f16_tc2_kernel (CTA pair, 256x256, {plan['stages']} stages)"
+    return f"gemm_f16_tc_kernel<{plan['tile_n']}, {plan['stages']}>"
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -380,7 +389,7 @@ def run_ours(args, w, epi):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_src} (bf16 burst x fp16/bf16 ratio {FP16_PER_BF16})",
-                         "kernel": "gemm_f16_tc_kernel", "avg_launch_ms": avg_launch_ms},
+                         "kernel": kernel_name(plan), "avg_launch_ms": avg_launch_ms},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms / e2e_steps},
             "gpu_launches": launches_per_step * args.steps,

@@ -23,14 +23,25 @@ using namespace gemm_f16_dev;
 
 thread_local int t_last_cuda_error = 0;
 
-// Kernel configurations.  The CTA pair (256 x 256 per pair, 6 x 32 KiB ring
-// per CTA) is the throughput shape; single-CTA tiles of 128 x {256,128,64}
-// give small problems more CTAs.
+// Kernel configurations.  The CTA pair (256 x 256 per pair, 3 x 64 KiB ring
+// per CTA, 128-deep K stages) is the throughput shape; single-CTA tiles of
+// 128 x {256,128,64} give small problems more CTAs.
 enum Config : int { CFG_AUTO = 0, CFG_PAIR_256 = 1, CFG_128x256 = 2, CFG_128x128 = 3, CFG_128x64 = 4 };
-constexpr int kStagesPair = 6;
+#ifndef GEMM_F16_PAIR_STAGES
+#define GEMM_F16_PAIR_STAGES 3
+#endif
+#ifndef GEMM_F16_PAIR_KSUB
+#define GEMM_F16_PAIR_KSUB 2
+#endif
+#ifndef GEMM_F16_GROUP_M
+#define GEMM_F16_GROUP_M 8
+#endif
+constexpr int kStagesPair = GEMM_F16_PAIR_STAGES;   // 3 stages x 64 KiB per CTA
+constexpr int kKSubPair = GEMM_F16_PAIR_KSUB;       // 64-deep K sub-blocks per stage
 constexpr int kStages256 = 4;   // 4 x 48 KiB ring
-constexpr int kStages128 = 6;   // 6 x 32 KiB
-constexpr int kStages64 = 8;    // 8 x 24 KiB
+constexpr int kStages128 = 7;   // 7 x 32 KiB
+constexpr int kStages64 = 9;    // 9 x 24 KiB
+constexpr int kGroupM = GEMM_F16_GROUP_M;   // tile-rows per rasterisation group
 
 constexpr int kMaxDevices = 64;
 
@@ -166,8 +177,8 @@ int init_common_locked(int dev, DeviceState& st) {
             return cuda_fail(e != cudaSuccess ? e : cudaErrorSymbolNotFound);
         g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    e = cudaFuncSetAttribute(gemm_f16_tc2_kernel<kStagesPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SmemPlanPair<kStagesPair>::kDynamicBytes);
+    e = cudaFuncSetAttribute(gemm_f16_tc2_kernel<kStagesPair, kKSubPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SmemPlanPair<kStagesPair, kKSubPair>::kDynamicBytes);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gemm_f16_tc_kernel<256, kStages256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SmemPlan<256, kStages256>::kDynamicBytes);
@@ -180,7 +191,7 @@ int init_common_locked(int dev, DeviceState& st) {
     if (e != cudaSuccess) return cuda_fail(e);
     // How many CTA pairs fit at once decides the persistent grid of the pair kernel.
     {
-        cudaLaunchConfig_t cfg = launch_config(sms, SmemPlanPair<kStagesPair>::kDynamicBytes, nullptr);
+        cudaLaunchConfig_t cfg = launch_config(sms, SmemPlanPair<kStagesPair, kKSubPair>::kDynamicBytes, nullptr);
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
@@ -189,7 +200,7 @@ int init_common_locked(int dev, DeviceState& st) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(gemm_f16_tc2_kernel<kStagesPair>),
+        if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(gemm_f16_tc2_kernel<kStagesPair, kKSubPair>),
                                            &cfg) != cudaSuccess || n <= 0) {
             cudaGetLastError();
             n = sms / 2;
@@ -271,7 +282,7 @@ int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& pr
 }
 
 int launch_tc_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& prm, int ctas, cudaStream_t s) {
-    cudaLaunchConfig_t cfg = launch_config(ctas, SmemPlanPair<kStagesPair>::kDynamicBytes, s);
+    cudaLaunchConfig_t cfg = launch_config(ctas, SmemPlanPair<kStagesPair, kKSubPair>::kDynamicBytes, s);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -279,7 +290,7 @@ int launch_tc_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParam
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_kernel<kStagesPair>, ta, tb, prm);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_kernel<kStagesPair, kKSubPair>, ta, tb, prm);
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
 
@@ -313,7 +324,8 @@ int enqueue_plan(const Plan& pl, const void* A, const void* B, const __half* bia
     prm.ldc = static_cast<int>(N);
     prm.epi = epilogue;
     prm.vec_store = pl.vec_store ? 1 : 0;
-    prm.group_m = 8;
+    prm.bias_vec = (biasp != nullptr && aligned(biasp, 16)) ? 1 : 0;
+    prm.group_m = kGroupM;
     prm.timeout_ns = g_timeout_ns;
     switch (pl.cfg) {
         case CFG_PAIR_256: return launch_tc_pair(ta, tb, prm, pl.ctas, s);

@@ -43,8 +43,7 @@ struct SmemPlan {
     static constexpr uint32_t kBTileBytes = BN * kBK * 2;
     static constexpr uint32_t kA = 0;                                   // STAGES A tiles
     static constexpr uint32_t kB = kA + STAGES * kATileBytes;           // STAGES B tiles
-    static constexpr uint32_t kBias = kB + STAGES * kBTileBytes;        // 4 warps x BN floats
-    static constexpr uint32_t kBars = kBias + 4 * BN * 4;               // mbarriers (8 B each)
+    static constexpr uint32_t kBars = kB + STAGES * kBTileBytes;        // mbarriers (8 B each)
     static constexpr uint32_t kNumBars = 2 * STAGES + 2 + 2 + 1;        // full, empty, acc_full, acc_empty, drain
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
@@ -82,9 +81,81 @@ struct GemmParams {
     int ldc;
     int epi;
     int vec_store;       // C base 16-byte aligned and ldc % 8 == 0
+    int bias_vec;        // bias base 16-byte aligned (8-wide bias loads)
     int group_m;
     uint64_t timeout_ns;
 };
+
+// Epilogue of one accumulator: this warp's 32 TMEM lanes (one tile row per
+// thread) x BN fp32 columns starting at TMEM address t_base.  Adds bias[n]
+// (fp16, read straight from global memory: every lane of the warp reads the
+// same 64 bytes, a broadcast that L1 serves after the first tile), applies the
+// activation in fp32, rounds to fp16 and writes the row segment of C with
+// 16-byte stores (2-byte stores at a ragged or unaligned edge).
+template <int BN>
+__device__ __forceinline__ void epilogue_rows(const GemmParams& p, uint32_t t_base, int row, int n0) {
+    const bool row_ok = row < p.M;
+    const bool has_bias = p.epi != EPI_NONE;
+    __half* crow = p.C + static_cast<int64_t>(row) * p.ldc;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_base + 32u * c, r);
+        const int col0 = n0 + 32 * c;
+        float bv[32];
+        if (has_bias) {
+            if (p.bias_vec && col0 + 32 <= p.N) {
+                const uint4* src = reinterpret_cast<const uint4*>(p.bias + col0);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const uint4 w = __ldg(src + v);
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __half2 h2 = *reinterpret_cast<const __half2*>(&ws[e]);
+                        const float2 f2 = __half22float2(h2);
+                        bv[8 * v + 2 * e] = f2.x;
+                        bv[8 * v + 2 * e + 1] = f2.y;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) bv[j] = col0 + j < p.N ? __half2float(p.bias[col0 + j]) : 0.0f;
+            }
+        }
+        tmem_wait_ld();
+        if (row_ok && col0 < p.N) {
+            uint32_t h[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                float x0 = __uint_as_float(r[2 * j]);
+                float x1 = __uint_as_float(r[2 * j + 1]);
+                if (has_bias) {
+                    x0 += bv[2 * j];
+                    x1 += bv[2 * j + 1];
+                }
+                x0 = apply_act(x0, p.epi);
+                x1 = apply_act(x1, p.epi);
+                const __half2 hv = __floats2half2_rn(x0, x1);
+                h[j] = *reinterpret_cast<const uint32_t*>(&hv);
+            }
+            if (p.vec_store && col0 + 32 <= p.N) {
+                uint4* dst = reinterpret_cast<uint4*>(crow + col0);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if (col0 + j < p.N) {
+                        const uint16_t bits = static_cast<uint16_t>((h[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+                        reinterpret_cast<uint16_t*>(crow)[col0 + j] = bits;
+                    }
+                }
+            }
+        }
+    }
+}
 
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -103,7 +174,6 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
     const uint32_t sA = base_s + SP::kA;
     const uint32_t sB = base_s + SP::kB;
-    float* bias_s = reinterpret_cast<float*>(base + SP::kBias);
     const uint32_t bars = base_s + SP::kBars;
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
@@ -226,67 +296,17 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;            // TMEM lane quarter this warp may access
-        const int ew = warp - 2;           // private bias slice
-        float* my_bias = bias_s + ew * BN;
         int acc = 0;
         uint32_t acc_phase = 0;
-        const bool has_bias = p.epi != EPI_NONE;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             const TileCoord tc = tile_coord(t, tiles_m, tiles_n, p.group_m, BN);
-            __syncwarp();
-            if (has_bias) {
-                for (int i = lane; i < BN; i += 32) {
-                    const int n = tc.n0 + i;
-                    my_bias[i] = n < p.N ? __half2float(p.bias[n]) : 0.0f;
-                }
-            }
-            __syncwarp();
             // tcgen05.ld is warp-collective: the go/no-go decision must be warp-uniform.
             const bool ready = mbar_wait_bounded(accf_bar(acc), acc_phase, p.timeout_ns, abort_flag, status,
                                                  ROLE_EPILOGUE, BAR_ACC_FULL);
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
-            const int row = tc.m0 + 32 * q + lane;
-            const bool row_ok = row < p.M;
-            __half* crow = p.C + static_cast<int64_t>(row) * p.ldc;
             const uint32_t t_base = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(32 * q) << 16);
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_base + 32u * c, r);
-                tmem_wait_ld();
-                const int col0 = tc.n0 + 32 * c;
-                if (row_ok && col0 < p.N) {
-                    uint32_t h[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        float x0 = __uint_as_float(r[2 * j]);
-                        float x1 = __uint_as_float(r[2 * j + 1]);
-                        if (has_bias) {
-                            x0 += my_bias[32 * c + 2 * j];
-                            x1 += my_bias[32 * c + 2 * j + 1];
-                        }
-                        x0 = apply_act(x0, p.epi);
-                        x1 = apply_act(x1, p.epi);
-                        const __half2 hv = __floats2half2_rn(x0, x1);
-                        h[j] = *reinterpret_cast<const uint32_t*>(&hv);
-                    }
-                    if (p.vec_store && col0 + 32 <= p.N) {
-                        uint4* dst = reinterpret_cast<uint4*>(crow + col0);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            if (col0 + j < p.N) {
-                                const uint16_t bits = static_cast<uint16_t>((h[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-                                reinterpret_cast<uint16_t*>(crow)[col0 + j] = bits;
-                            }
-                        }
-                    }
-                }
-            }
+            epilogue_rows<BN>(p, t_base, tc.m0 + 32 * q + lane, tc.n0);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(acc));

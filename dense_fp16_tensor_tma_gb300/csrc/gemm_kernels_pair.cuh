@@ -8,7 +8,10 @@
 //
 //   * a cluster of 2 CTAs; CTA r (r = 0, 1) owns output rows m0 + 128r ..
 //     m0 + 128r + 127 and loads only its own 128 rows of A and its own 128
-//     columns of B per K-block (16 KiB + 16 KiB per stage);
+//     columns of B: 16 KiB + 16 KiB per 64-deep K sub-block, KSUB sub-blocks
+//     per pipeline stage (8 MMAs per barrier round trip at KSUB = 2: each
+//     stage hand-over costs the tensor pipe a short bubble, so fewer, deeper
+//     stages keep it busier);
 //   * one thread of CTA 0 issues tcgen05.mma.cta_group::2 (M = 256, N = 256,
 //     K = 16): each SM's tensor core computes its 128 rows against all 256
 //     columns, taking B from both SMs' shared memory, so per SM the operand
@@ -24,14 +27,15 @@
 
 namespace gemm_f16_dev {
 
-constexpr uint32_t kBHalfBytes = 128 * kBK * 2;   // this CTA's 128 columns of a B stage: 16 KiB
+constexpr uint32_t kBHalfSubBytes = 128 * kBK * 2;   // this CTA's 128 columns of a 64-deep K sub-block: 16 KiB
 
-template <int STAGES>
+template <int STAGES, int KSUB>
 struct SmemPlanPair {
+    static constexpr uint32_t kAStage = KSUB * kATileBytes;        // KSUB A boxes
+    static constexpr uint32_t kBStage = KSUB * kBHalfSubBytes;     // KSUB x two 64-column B boxes
     static constexpr uint32_t kA = 0;
-    static constexpr uint32_t kB = kA + STAGES * kATileBytes;
-    static constexpr uint32_t kBias = kB + STAGES * kBHalfBytes;        // 4 warps x 256 floats
-    static constexpr uint32_t kBars = kBias + 4 * 256 * 4;
+    static constexpr uint32_t kB = kA + STAGES * kAStage;
+    static constexpr uint32_t kBars = kB + STAGES * kBStage;
     static constexpr uint32_t kNumBars = 2 * STAGES + 2 + 2 + 1;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
@@ -51,11 +55,12 @@ __device__ __forceinline__ TileCoord tile_coord_bm(int t, int tiles_m, int tiles
     return c;
 }
 
-template <int STAGES>
+template <int STAGES, int KSUB>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams p) {
-    using SP = SmemPlanPair<STAGES>;
+    using SP = SmemPlanPair<STAGES, KSUB>;
+    constexpr int kStageK = KSUB * kBK;      // K per pipeline stage
     constexpr int PM = 256;                  // pair tile rows = MMA M
     constexpr int BN = 256;                  // pair tile columns = MMA N
     constexpr uint32_t kIdesc = idesc_f16_f32(PM, BN, /*b_mn_major=*/true);
@@ -68,7 +73,6 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
     const uint32_t sA = base_s + SP::kA;
     const uint32_t sB = base_s + SP::kB;
-    float* bias_s = reinterpret_cast<float*>(base + SP::kBias);
     const uint32_t bars = base_s + SP::kBars;
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
@@ -113,7 +117,7 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int tiles_m = (p.M + PM - 1) / PM;
     const int tiles_n = (p.N + BN - 1) / BN;
     const int num_tiles = tiles_m * tiles_n;
-    const int kblocks = (p.K + kBK - 1) / kBK;
+    const int kblocks = (p.K + kStageK - 1) / kStageK;   // pipeline stages per tile
     const int cid = blockIdx.x >> 1;
     const int nclusters = gridDim.x >> 1;
     unsigned int* status = &g_status;
@@ -136,19 +140,25 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const TileCoord tc = tile_coord_bm(t, tiles_m, tiles_n, p.group_m, PM, BN);
                 const int my_a = a_live(tc.m0, rank);
                 const int my_b = b_live(tc.n0, rank);
-                const uint32_t pair_bytes =
+                // every sub-block's boxes are issued, also those starting past K
+                // (they arrive as zeros), so each stage carries the same bytes
+                const uint32_t pair_bytes = KSUB * (
                     static_cast<uint32_t>(a_live(tc.m0, 0) + a_live(tc.m0, 1)) * kATileBytes +
-                    static_cast<uint32_t>(b_live(tc.n0, 0) + b_live(tc.n0, 1)) * kBBoxBytes;
+                    static_cast<uint32_t>(b_live(tc.n0, 0) + b_live(tc.n0, 1)) * kBBoxBytes);
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_cluster_bounded(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, status,
                                                    ROLE_PRODUCER, BAR_EMPTY)) { ok = false; break; }
                     const uint32_t full_leader = mapa_shared(full_bar(stage), 0);
                     if (leader) mbar_arrive_expect_tx(full_bar(stage), pair_bytes);
-                    if (my_a)
-                        tma_load_2d_pair(sA + stage * kATileBytes, &tmA, full_leader, kb * kBK, tc.m0 + 128 * rank);
-                    for (int c = 0; c < my_b; ++c)
-                        tma_load_2d_pair(sB + stage * kBHalfBytes + c * kBBoxBytes, &tmB, full_leader,
-                                         tc.n0 + 128 * rank + 64 * c, kb * kBK);
+                    for (int ks = 0; ks < KSUB; ++ks) {
+                        const int k0 = kb * kStageK + ks * kBK;
+                        if (my_a)
+                            tma_load_2d_pair(sA + stage * SP::kAStage + ks * kATileBytes, &tmA, full_leader, k0,
+                                             tc.m0 + 128 * rank);
+                        for (int c = 0; c < my_b; ++c)
+                            tma_load_2d_pair(sB + stage * SP::kBStage + ks * kBHalfSubBytes + c * kBBoxBytes, &tmB,
+                                             full_leader, tc.n0 + 128 * rank + 64 * c, k0);
+                    }
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -182,15 +192,18 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (!mbar_wait_cluster_bounded(full_bar(stage), phase, p.timeout_ns, abort_flag, status,
                                                    ROLE_MMA, BAR_FULL)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a0 = sA + stage * kATileBytes;
-                    const uint32_t b0 = sB + stage * kBHalfBytes;
 #pragma unroll
-                    for (int k = 0; k < kBK / kUMMA_K; ++k) {
-                        // same layouts as the single-SM kernel; B here is this
-                        // CTA's 128 columns (two 64-column boxes, LBO 8 KiB)
-                        const uint64_t adesc = smem_desc_sw128(a0 + k * 32, 0, 1024);
-                        const uint64_t bdesc = smem_desc_sw128(b0 + k * 2048, kBBoxBytes, 1024);
-                        tc_mma_f16_pair(d_tmem, adesc, bdesc, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                    for (int ks = 0; ks < KSUB; ++ks) {
+                        const uint32_t a0 = sA + stage * SP::kAStage + ks * kATileBytes;
+                        const uint32_t b0 = sB + stage * SP::kBStage + ks * kBHalfSubBytes;
+#pragma unroll
+                        for (int k = 0; k < kBK / kUMMA_K; ++k) {
+                            // same layouts as the single-SM kernel; B here is this
+                            // CTA's 128 columns (two 64-column boxes, LBO 8 KiB)
+                            const uint64_t adesc = smem_desc_sw128(a0 + k * 32, 0, 1024);
+                            const uint64_t bdesc = smem_desc_sw128(b0 + k * 2048, kBBoxBytes, 1024);
+                            tc_mma_f16_pair(d_tmem, adesc, bdesc, kIdesc, (kb | ks | k) != 0 ? 1u : 0u);
+                        }
                     }
                     tc_commit_pair_mc(empty_bar(stage), 0x3);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -206,69 +219,21 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int q = warp & 3;
-        const int ew = warp - 2;
-        float* my_bias = bias_s + ew * BN;
         int acc = 0;
         uint32_t acc_phase = 0;
-        const bool has_bias = p.epi != EPI_NONE;
+        const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
+        const uint32_t acce_leader1 = mapa_shared(acce_bar(1), 0);
         for (int t = cid; t < num_tiles; t += nclusters) {
             const TileCoord tc = tile_coord_bm(t, tiles_m, tiles_n, p.group_m, PM, BN);
-            __syncwarp();
-            if (has_bias) {
-                for (int i = lane; i < BN; i += 32) {
-                    const int n = tc.n0 + i;
-                    my_bias[i] = n < p.N ? __half2float(p.bias[n]) : 0.0f;
-                }
-            }
-            __syncwarp();
             const bool ready = mbar_wait_cluster_bounded(accf_bar(acc), acc_phase, p.timeout_ns, abort_flag, status,
                                                          ROLE_EPILOGUE, BAR_ACC_FULL);
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
-            const int row = tc.m0 + 128 * static_cast<int>(rank) + 32 * q + lane;
-            const bool row_ok = row < p.M;
-            __half* crow = p.C + static_cast<int64_t>(row) * p.ldc;
             const uint32_t t_base = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(32 * q) << 16);
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_base + 32u * c, r);
-                tmem_wait_ld();
-                const int col0 = tc.n0 + 32 * c;
-                if (row_ok && col0 < p.N) {
-                    uint32_t h[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        float x0 = __uint_as_float(r[2 * j]);
-                        float x1 = __uint_as_float(r[2 * j + 1]);
-                        if (has_bias) {
-                            x0 += my_bias[32 * c + 2 * j];
-                            x1 += my_bias[32 * c + 2 * j + 1];
-                        }
-                        x0 = apply_act(x0, p.epi);
-                        x1 = apply_act(x1, p.epi);
-                        const __half2 hv = __floats2half2_rn(x0, x1);
-                        h[j] = *reinterpret_cast<const uint32_t*>(&hv);
-                    }
-                    if (p.vec_store && col0 + 32 <= p.N) {
-                        uint4* dst = reinterpret_cast<uint4*>(crow + col0);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            if (col0 + j < p.N) {
-                                const uint16_t bits = static_cast<uint16_t>((h[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-                                reinterpret_cast<uint16_t*>(crow)[col0 + j] = bits;
-                            }
-                        }
-                    }
-                }
-            }
+            epilogue_rows<BN>(p, t_base, tc.m0 + 128 * static_cast<int>(rank) + 32 * q + lane, tc.n0);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
+            if (lane == 0) mbar_arrive_cluster(acc == 0 ? acce_leader0 : acce_leader1);
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
     }
