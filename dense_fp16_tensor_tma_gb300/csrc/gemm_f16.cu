@@ -39,8 +39,8 @@ enum Config : int { CFG_AUTO = 0, CFG_PAIR_256 = 1, CFG_128x256 = 2, CFG_128x128
 constexpr int kStagesPair = GEMM_F16_PAIR_STAGES;   // 3 stages x 64 KiB per CTA
 constexpr int kKSubPair = GEMM_F16_PAIR_KSUB;       // 64-deep K sub-blocks per stage
 constexpr int kStages256 = 4;   // 4 x 48 KiB ring
-constexpr int kStages128 = 7;   // 7 x 32 KiB
-constexpr int kStages64 = 9;    // 9 x 24 KiB
+constexpr int kStages128 = 6;   // 6 x 32 KiB
+constexpr int kStages64 = 8;    // 8 x 24 KiB
 constexpr int kGroupM = GEMM_F16_GROUP_M;   // tile-rows per rasterisation group
 
 constexpr int kMaxDevices = 64;

@@ -16,8 +16,9 @@
 //     zeros;
 //   * warp 1: allocates tensor memory and issues tcgen05.mma (M=128, N=BN,
 //     K=16) from one thread into one of two TMEM accumulators;
-//   * warps 2..5: epilogue, reading the accumulator with tcgen05.ld while the
-//     MMA warp already fills the other accumulator for the next tile.
+//   * warps 2..9: epilogue (two warps per TMEM lane quarter, each taking half
+//     of the columns), reading the accumulator with tcgen05.ld while the MMA
+//     warp already fills the other accumulator for the next tile.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -34,16 +35,23 @@ __device__ unsigned int g_status;  // bounded-wait status word, read by the host
 constexpr int kBM = 128;                 // tile rows = MMA M = TMEM lanes
 constexpr int kBK = 64;                  // K per stage: one 128-byte swizzle row of fp16
 constexpr int kUMMA_K = 16;              // K per tcgen05.mma kind::f16
-constexpr int kThreads = 192;            // 6 warps
+constexpr int kThreads = 320;            // 10 warps: producer, MMA, 8 epilogue
+constexpr int kEpiWarps = 8;             // two per TMEM lane quarter, each half of the columns
 constexpr uint32_t kATileBytes = kBM * kBK * 2;  // 16 KiB
 constexpr uint32_t kBBoxBytes = 64 * kBK * 2;    // one 64(N) x 64(K) box, 8 KiB
+// Per epilogue warp: a 32 x 32 fp16 block, rows padded to 17 words so that
+// both the row-wise writes and the column-wise reads are bank-conflict free.
+constexpr uint32_t kStageRowWords = 17;
+constexpr uint32_t kStageWarpBytes = 32 * kStageRowWords * 4;
+constexpr uint32_t kStageBytes = kEpiWarps * kStageWarpBytes;   // 17 KiB for the eight epilogue warps
 
 template <int BN, int STAGES>
 struct SmemPlan {
     static constexpr uint32_t kBTileBytes = BN * kBK * 2;
     static constexpr uint32_t kA = 0;                                   // STAGES A tiles
     static constexpr uint32_t kB = kA + STAGES * kATileBytes;           // STAGES B tiles
-    static constexpr uint32_t kBars = kB + STAGES * kBTileBytes;        // mbarriers (8 B each)
+    static constexpr uint32_t kStage = kB + STAGES * kBTileBytes;       // epilogue staging (narrow stores)
+    static constexpr uint32_t kBars = kStage + kStageBytes;             // mbarriers (8 B each)
     static constexpr uint32_t kNumBars = 2 * STAGES + 2 + 2 + 1;        // full, empty, acc_full, acc_empty, drain
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
@@ -86,74 +94,108 @@ struct GemmParams {
     uint64_t timeout_ns;
 };
 
-// Epilogue of one accumulator: this warp's 32 TMEM lanes (one tile row per
-// thread) x BN fp32 columns starting at TMEM address t_base.  Adds bias[n]
-// (fp16, read straight from global memory: every lane of the warp reads the
-// same 64 bytes, a broadcast that L1 serves after the first tile), applies the
-// activation in fp32, rounds to fp16 and writes the row segment of C with
-// 16-byte stores (2-byte stores at a ragged or unaligned edge).
-template <int BN>
-__device__ __forceinline__ void epilogue_rows(const GemmParams& p, uint32_t t_base, int row, int n0) {
-    const bool row_ok = row < p.M;
+// Bias, activation and fp16 rounding of one 32-column chunk of this thread's
+// row: r = 32 fp32 accumulator columns, bias of columns col0..col0+31.
+__device__ __forceinline__ void epilogue_math(const GemmParams& p, const uint32_t (&r)[32], int col0,
+                                              uint32_t (&h)[16]) {
     const bool has_bias = p.epi != EPI_NONE;
-    __half* crow = p.C + static_cast<int64_t>(row) * p.ldc;
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_base + 32u * c, r);
-        const int col0 = n0 + 32 * c;
-        float bv[32];
-        if (has_bias) {
-            if (p.bias_vec && col0 + 32 <= p.N) {
-                const uint4* src = reinterpret_cast<const uint4*>(p.bias + col0);
+    uint32_t bw[16];   // bias as packed fp16 pairs
+    if (has_bias) {
+        if (p.bias_vec && col0 + 32 <= p.N) {
+            // every lane reads the same 64 bytes: a broadcast that L1 serves after the first tile
+            const uint4* src = reinterpret_cast<const uint4*>(p.bias + col0);
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const uint4 w = __ldg(src + v);
-                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const __half2 h2 = *reinterpret_cast<const __half2*>(&ws[e]);
-                        const float2 f2 = __half22float2(h2);
-                        bv[8 * v + 2 * e] = f2.x;
-                        bv[8 * v + 2 * e + 1] = f2.y;
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) bv[j] = col0 + j < p.N ? __half2float(p.bias[col0 + j]) : 0.0f;
+            for (int v = 0; v < 4; ++v) {
+                const uint4 w = __ldg(src + v);
+                bw[4 * v] = w.x;
+                bw[4 * v + 1] = w.y;
+                bw[4 * v + 2] = w.z;
+                bw[4 * v + 3] = w.w;
             }
-        }
-        tmem_wait_ld();
-        if (row_ok && col0 < p.N) {
-            uint32_t h[16];
+        } else {
+            const uint16_t* b16 = reinterpret_cast<const uint16_t*>(p.bias);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                float x0 = __uint_as_float(r[2 * j]);
-                float x1 = __uint_as_float(r[2 * j + 1]);
-                if (has_bias) {
-                    x0 += bv[2 * j];
-                    x1 += bv[2 * j + 1];
-                }
-                x0 = apply_act(x0, p.epi);
-                x1 = apply_act(x1, p.epi);
-                const __half2 hv = __floats2half2_rn(x0, x1);
-                h[j] = *reinterpret_cast<const uint32_t*>(&hv);
-            }
-            if (p.vec_store && col0 + 32 <= p.N) {
-                uint4* dst = reinterpret_cast<uint4*>(crow + col0);
-#pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if (col0 + j < p.N) {
-                        const uint16_t bits = static_cast<uint16_t>((h[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-                        reinterpret_cast<uint16_t*>(crow)[col0 + j] = bits;
-                    }
-                }
+                const uint32_t lo = col0 + 2 * j < p.N ? b16[col0 + 2 * j] : 0u;
+                const uint32_t hi = col0 + 2 * j + 1 < p.N ? b16[col0 + 2 * j + 1] : 0u;
+                bw[j] = lo | (hi << 16);
             }
         }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        float x0 = __uint_as_float(r[2 * j]);
+        float x1 = __uint_as_float(r[2 * j + 1]);
+        if (has_bias) {
+            const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&bw[j]));
+            x0 += b2.x;
+            x1 += b2.y;
+        }
+        x0 = apply_act(x0, p.epi);
+        x1 = apply_act(x1, p.epi);
+        const __half2 hv = __floats2half2_rn(x0, x1);
+        h[j] = *reinterpret_cast<const uint32_t*>(&hv);
+    }
+}
+
+// Store one 32 x 32 fp16 block: rows row0..row0+31 (one per lane, h = that
+// lane's 32 columns from col0).  Where C rows are 16-byte aligned and the
+// chunk is whole, each thread writes its own 64-byte row segment with 16-byte
+// stores; otherwise (N % 8 != 0, unaligned C, or the ragged last chunk) the
+// block goes through `stage` (this warp's shared-memory tile) and all 32
+// lanes write one row at a time, 64 contiguous bytes per store.
+__device__ __forceinline__ void epilogue_store(const GemmParams& p, const uint32_t (&h)[16], int row0, int col0,
+                                               uint32_t* stage) {
+    const int lane = threadIdx.x & 31;
+    if (p.vec_store && col0 + 32 <= p.N) {
+        const int row = row0 + lane;
+        if (row < p.M) {
+            uint4* dst = reinterpret_cast<uint4*>(p.C + static_cast<int64_t>(row) * p.ldc + col0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+        }
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) stage[lane * kStageRowWords + j] = h[j];
+    __syncwarp();
+    const bool col_ok = col0 + lane < p.N;
+    uint16_t* cbase = reinterpret_cast<uint16_t*>(p.C + static_cast<int64_t>(row0) * p.ldc + col0 + lane);
+    if (row0 + 32 <= p.M) {
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr) {
+            const uint32_t w = stage[rr * kStageRowWords + (lane >> 1)];
+            if (col_ok) cbase[static_cast<int64_t>(rr) * p.ldc] = static_cast<uint16_t>(w >> (16 * (lane & 1)));
+        }
+    } else {
+        const int rows_here = p.M - row0;   // may be <= 0: nothing to store
+        for (int rr = 0; rr < rows_here; ++rr) {
+            const uint32_t w = stage[rr * kStageRowWords + (lane >> 1)];
+            if (col_ok) cbase[static_cast<int64_t>(rr) * p.ldc] = static_cast<uint16_t>(w >> (16 * (lane & 1)));
+        }
+    }
+    __syncwarp();
+}
+
+// Epilogue of NCOL accumulator columns for this warp's 32 TMEM lanes (tile
+// rows row0..row0+31, one per thread), starting at TMEM address t_base and
+// output column n0.  Latency of the TMEM loads is hidden by the second
+// epilogue warp on the same SM sub-partition (each sub-partition's register
+// file holds at most 168 registers per thread for 10 warps, too few for two
+// chunks in flight per warp).
+template <int NCOL>
+__device__ __forceinline__ void epilogue_rows(const GemmParams& p, uint32_t t_base, int row0, int n0,
+                                              uint32_t* stage) {
+#pragma unroll 1
+    for (int c = 0; c < NCOL / 32; ++c) {
+        const int col0 = n0 + 32 * c;
+        if (col0 >= p.N) break;   // warp-uniform: the remaining chunks are right of N
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_base + 32u * c, r);
+        tmem_wait_ld(r);
+        uint32_t h[16];
+        epilogue_math(p, r, col0, h);
+        epilogue_store(p, h, row0, col0, stage);
     }
 }
 
@@ -193,7 +235,7 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), 4);
+            mbar_init(acce_bar(b), kEpiWarps);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -305,8 +347,11 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                                                  ROLE_EPILOGUE, BAR_ACC_FULL);
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
-            const uint32_t t_base = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(32 * q) << 16);
-            epilogue_rows<BN>(p, t_base, tc.m0 + 32 * q + lane, tc.n0);
+            const int half = (warp - 2) >> 2;   // which half of the tile's columns
+            const uint32_t t_base = tmem_base + static_cast<uint32_t>(acc * BN + half * (BN / 2)) +
+                                    (static_cast<uint32_t>(32 * q) << 16);
+            epilogue_rows<BN / 2>(p, t_base, tc.m0 + 32 * q, tc.n0 + half * (BN / 2),
+                                  reinterpret_cast<uint32_t*>(base + SP::kStage + (warp - 2) * kStageWarpBytes));
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(acc));

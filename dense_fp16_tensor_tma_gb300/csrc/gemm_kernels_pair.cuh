@@ -35,7 +35,8 @@ struct SmemPlanPair {
     static constexpr uint32_t kBStage = KSUB * kBHalfSubBytes;     // KSUB x two 64-column B boxes
     static constexpr uint32_t kA = 0;
     static constexpr uint32_t kB = kA + STAGES * kAStage;
-    static constexpr uint32_t kBars = kB + STAGES * kBStage;
+    static constexpr uint32_t kStage = kB + STAGES * kBStage;   // epilogue staging (narrow stores)
+    static constexpr uint32_t kBars = kStage + kStageBytes;
     static constexpr uint32_t kNumBars = 2 * STAGES + 2 + 2 + 1;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
@@ -94,7 +95,7 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);      // one multicast MMA commit
-            mbar_init(acce_bar(b), 8);      // 4 epilogue warps x 2 CTAs (used on CTA 0)
+            mbar_init(acce_bar(b), 2 * kEpiWarps);   // epilogue warps of both CTAs (used on CTA 0)
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -229,8 +230,11 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                                                          ROLE_EPILOGUE, BAR_ACC_FULL);
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
-            const uint32_t t_base = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(32 * q) << 16);
-            epilogue_rows<BN>(p, t_base, tc.m0 + 128 * static_cast<int>(rank) + 32 * q + lane, tc.n0);
+            const int half = (warp - 2) >> 2;   // which half of the tile's columns
+            const uint32_t t_base = tmem_base + static_cast<uint32_t>(acc * BN + half * (BN / 2)) +
+                                    (static_cast<uint32_t>(32 * q) << 16);
+            epilogue_rows<BN / 2>(p, t_base, tc.m0 + 128 * static_cast<int>(rank) + 32 * q, tc.n0 + half * (BN / 2),
+                                  reinterpret_cast<uint32_t*>(base + SP::kStage + (warp - 2) * kStageWarpBytes));
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acc == 0 ? acce_leader0 : acce_leader1);
