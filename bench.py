@@ -39,6 +39,7 @@ FALLBACK_TENSOR_TFLOPS = 1900.0
 FP16_PER_BF16 = 1.0          # nominal dense fp16 rate / dense bf16 rate
 KERNEL_SOURCES = ("dense_fp16_tensor_tma_gb300/csrc/gemm_kernels.cuh",
                   "dense_fp16_tensor_tma_gb300/csrc/gemm_kernels_pair.cuh",
+                  "dense_fp16_tensor_tma_gb300/csrc/gemm_kernels_swap.cuh",
                   "dense_fp16_tensor_tma_gb300/csrc/ptx.cuh",
                   "dense_fp16_tensor_tma_gb300/csrc/gemm_f16.cu")
 
@@ -68,6 +69,8 @@ def workload_config(w, epi):
 
 def kernel_name(plan):
     """Name of the tensor-core kernel a plan launches."""
+    if plan.get("path") == 3:
+        return f"gemm_f16_swap_kernel<{plan['tile_m']}, {plan['stages']}> (swap-AB)"
     if plan.get("path") != 2:
         return "gemm_f16_bias_only_kernel"
     if plan.get("tile_m") == 256:

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libgemm_f16.so")
 SOURCES = ["gemm_f16.cu"]
-DEPS = ["gemm_f16.cu", "gemm_kernels.cuh", "gemm_kernels_pair.cuh", "ptx.cuh"]
+DEPS = ["gemm_f16.cu", "gemm_kernels.cuh", "gemm_kernels_pair.cuh", "gemm_kernels_swap.cuh", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

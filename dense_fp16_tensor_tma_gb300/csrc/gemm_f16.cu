@@ -16,6 +16,7 @@
 #include "gemm_f16.h"
 #include "gemm_kernels.cuh"
 #include "gemm_kernels_pair.cuh"
+#include "gemm_kernels_swap.cuh"
 
 namespace {
 
@@ -25,8 +26,9 @@ thread_local int t_last_cuda_error = 0;
 
 // Kernel configurations.  The CTA pair (256 x 256 per pair, 3 x 64 KiB ring
 // per CTA, 128-deep K stages) is the throughput shape; single-CTA tiles of
-// 128 x {256,128,64} give small problems more CTAs.
-enum Config : int { CFG_AUTO = 0, CFG_PAIR_256 = 1, CFG_128x256 = 2, CFG_128x128 = 3, CFG_128x64 = 4 };
+// 128 x {256,128,64} give small problems more CTAs; the swap-AB kernel
+// (C^T = B^T A^T, tiles of 128 columns x 16/32/64 rows) serves short A.
+enum Config : int { CFG_AUTO = 0, CFG_PAIR_256 = 1, CFG_128x256 = 2, CFG_128x128 = 3, CFG_128x64 = 4, CFG_SWAP = 5 };
 #ifndef GEMM_F16_PAIR_STAGES
 #define GEMM_F16_PAIR_STAGES 3
 #endif
@@ -42,6 +44,9 @@ constexpr int kStages256 = 4;   // 4 x 48 KiB ring
 constexpr int kStages128 = 6;   // 6 x 32 KiB
 constexpr int kStages64 = 8;    // 8 x 24 KiB
 constexpr int kGroupM = GEMM_F16_GROUP_M;   // tile-rows per rasterisation group
+constexpr int kStagesSwap16 = 12;   // 12 x 18 KiB
+constexpr int kStagesSwap32 = 11;   // 11 x 20 KiB
+constexpr int kStagesSwap64 = 9;    //  9 x 24 KiB
 
 constexpr int kMaxDevices = 64;
 
@@ -71,13 +76,18 @@ int cuda_fail(cudaError_t e) {
 }
 
 struct Plan {
-    int path = 0;          // 0 none, 1 bias-only, 2 tiled tensor-core kernel
+    int path = 0;          // 0 none, 1 bias-only, 2 tiled tensor-core kernel, 3 swap-AB kernel
     int cfg = CFG_AUTO;
     int tile_m = 0, tile_n = 0, stages = 0, ctas = 0;
     bool pack_a = false, pack_b = false, vec_store = false;
     int64_t lda_packed = 0, ldb_packed = 0;
-    size_t a_scratch = 0, b_scratch = 0;   // repack bytes (A rounded to 256)
+    int splits = 1;                        // split-K parts per tile (swap-AB kernel)
+    // scratch layout: [A repack][B repack][split-K partials][split-K counters], each 256-aligned
+    size_t a_scratch = 0, b_scratch = 0, p_scratch = 0, c_scratch = 0;
+    size_t scratch_bytes() const { return a_scratch + b_scratch + p_scratch + c_scratch; }
 };
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -101,7 +111,7 @@ int check_args(const void* A, const void* B, const void* bias, const void* C, in
 }
 
 Plan make_plan(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K, int num_sms,
-               int pair_clusters, int force) {
+               int pair_clusters, int force, bool allow_split = true) {
     Plan pl;
     if (M == 0 || N == 0) return pl;
     if (K == 0) {
@@ -114,14 +124,16 @@ Plan make_plan(const void* A, const void* B, const void* C, int64_t M, int64_t N
     pl.pack_b = !(aligned(B, 16) && N % 8 == 0);
     pl.lda_packed = pl.pack_a ? round_up(K, 8) : K;
     pl.ldb_packed = pl.pack_b ? round_up(N, 8) : N;
-    pl.a_scratch = pl.pack_a ? ((static_cast<size_t>(M * pl.lda_packed * 2) + 255) & ~size_t(255)) : 0;
-    pl.b_scratch = pl.pack_b ? static_cast<size_t>(K * pl.ldb_packed * 2) : 0;
+    pl.a_scratch = pl.pack_a ? align256(static_cast<size_t>(M * pl.lda_packed * 2)) : 0;
+    pl.b_scratch = pl.pack_b ? align256(static_cast<size_t>(K * pl.ldb_packed * 2)) : 0;
     pl.vec_store = aligned(C, 16) && N % 8 == 0;
     const int64_t tiles_m = (M + 127) / 128;
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     int cfg = force;
     if (cfg == CFG_AUTO) {
-        if (pair_tiles >= pair_clusters) {
+        if (M <= 64) {
+            cfg = CFG_SWAP;
+        } else if (pair_tiles >= pair_clusters) {
             cfg = CFG_PAIR_256;
         } else {
             // widest single-CTA tile that still gives every SM a tile; else the narrowest
@@ -136,12 +148,35 @@ Plan make_plan(const void* A, const void* B, const void* C, int64_t M, int64_t N
             pl.tile_m = 256; pl.tile_n = 256; pl.stages = kStagesPair;
             pl.ctas = 2 * static_cast<int>(std::min<int64_t>(pair_tiles, std::max(1, pair_clusters)));
             break;
+        case CFG_SWAP:
+            pl.path = 3;
+            pl.tile_m = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+            pl.tile_n = 128;
+            pl.stages = pl.tile_m == 16 ? kStagesSwap16 : (pl.tile_m == 32 ? kStagesSwap32 : kStagesSwap64);
+            break;
         case CFG_128x256: pl.tile_m = 128; pl.tile_n = 256; pl.stages = kStages256; break;
         case CFG_128x128: pl.tile_m = 128; pl.tile_n = 128; pl.stages = kStages128; break;
         default: pl.tile_m = 128; pl.tile_n = 64; pl.stages = kStages64; break;
     }
-    if (cfg != CFG_PAIR_256)
-        pl.ctas = static_cast<int>(std::min<int64_t>(tiles_m * ((N + pl.tile_n - 1) / pl.tile_n), num_sms));
+    if (cfg != CFG_PAIR_256) {
+        const int64_t tiles = ((M + pl.tile_m - 1) / pl.tile_m) * ((N + pl.tile_n - 1) / pl.tile_n);
+        if (cfg == CFG_SWAP && allow_split && tiles < num_sms) {
+            // a CTA streams HBM at a bounded rate: spread each tile's K over
+            // more CTAs, keeping at least 8 K-blocks (512) per part
+            const int64_t kblocks = (K + kBK - 1) / kBK;
+            int64_t S = std::min<int64_t>({num_sms / tiles, kblocks / 8, 16});
+            if (S > 1) {
+                const int64_t kb_per = (kblocks + S - 1) / S;
+                S = (kblocks + kb_per - 1) / kb_per;   // no empty part
+            }
+            pl.splits = static_cast<int>(std::max<int64_t>(1, S));
+        }
+        if (pl.splits > 1) {
+            pl.p_scratch = align256(static_cast<size_t>(tiles) * pl.splits * pl.tile_m * pl.tile_n * 4);
+            pl.c_scratch = align256(static_cast<size_t>(tiles) * 4 * 4);
+        }
+        pl.ctas = static_cast<int>(std::min<int64_t>(tiles * pl.splits, num_sms));
+    }
     return pl;
 }
 
@@ -188,6 +223,15 @@ int init_common_locked(int dev, DeviceState& st) {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gemm_f16_tc_kernel<64, kStages64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SmemPlan<64, kStages64>::kDynamicBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_f16_swap_kernel<16, kStagesSwap16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SmemPlanSwap<16, kStagesSwap16>::kDynamicBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_f16_swap_kernel<32, kStagesSwap32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SmemPlanSwap<32, kStagesSwap32>::kDynamicBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_f16_swap_kernel<64, kStagesSwap64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SmemPlanSwap<64, kStagesSwap64>::kDynamicBytes);
     if (e != cudaSuccess) return cuda_fail(e);
     // How many CTA pairs fit at once decides the persistent grid of the pair kernel.
     {
@@ -281,6 +325,14 @@ int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& pr
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
 
+template <int MT, int STAGES>
+int launch_swap(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& prm, int ctas, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = launch_config(ctas, SmemPlanSwap<MT, STAGES>::kDynamicBytes, s);
+    cfg.blockDim = dim3(kSwapThreads);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_swap_kernel<MT, STAGES>, ta, tb, prm);
+    return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+}
+
 int launch_tc_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& prm, int ctas, cudaStream_t s) {
     cudaLaunchConfig_t cfg = launch_config(ctas, SmemPlanPair<kStagesPair, kKSubPair>::kDynamicBytes, s);
     cudaLaunchAttribute attr[1];
@@ -311,8 +363,17 @@ int enqueue_plan(const Plan& pl, const void* A, const void* B, const __half* bia
         st = launch_repack(bdst, B, K, N, N, pl.ldb_packed, s);
         b_src = bdst;
     }
+    float* partials = nullptr;
+    unsigned int* counters = nullptr;
+    if (st == GEMM_OK && pl.splits > 1) {
+        partials = reinterpret_cast<float*>(scratch + pl.a_scratch + pl.b_scratch);
+        counters = reinterpret_cast<unsigned int*>(scratch + pl.a_scratch + pl.b_scratch + pl.p_scratch);
+        const cudaError_t e = cudaMemsetAsync(counters, 0, pl.c_scratch, s);   // every slice starts at zero parts
+        if (e != cudaSuccess) st = cuda_fail(e);
+    }
     CUtensorMap ta, tb;
-    if (st == GEMM_OK) st = encode_2d(&ta, a_src, K, M, pl.lda_packed, kBK, kBM);
+    // A boxes are 64 K x 128 rows, or 64 K x MT rows for the swap-AB kernel
+    if (st == GEMM_OK) st = encode_2d(&ta, a_src, K, M, pl.lda_packed, kBK, pl.path == 3 ? pl.tile_m : kBM);
     if (st == GEMM_OK) st = encode_2d(&tb, b_src, N, K, pl.ldb_packed, 64, kBK);
     if (st != GEMM_OK) return st;
     GemmParams prm;
@@ -327,8 +388,15 @@ int enqueue_plan(const Plan& pl, const void* A, const void* B, const __half* bia
     prm.bias_vec = (biasp != nullptr && aligned(biasp, 16)) ? 1 : 0;
     prm.group_m = kGroupM;
     prm.timeout_ns = g_timeout_ns;
+    prm.splits = pl.splits;
+    prm.partials = partials;
+    prm.counters = counters;
     switch (pl.cfg) {
         case CFG_PAIR_256: return launch_tc_pair(ta, tb, prm, pl.ctas, s);
+        case CFG_SWAP:
+            if (pl.tile_m == 16) return launch_swap<16, kStagesSwap16>(ta, tb, prm, pl.ctas, s);
+            if (pl.tile_m == 32) return launch_swap<32, kStagesSwap32>(ta, tb, prm, pl.ctas, s);
+            return launch_swap<64, kStagesSwap64>(ta, tb, prm, pl.ctas, s);
         case CFG_128x256: return launch_tc<256, kStages256>(ta, tb, prm, pl.ctas, s);
         case CFG_128x128: return launch_tc<128, kStages128>(ta, tb, prm, pl.ctas, s);
         default: return launch_tc<64, kStages64>(ta, tb, prm, pl.ctas, s);
@@ -390,12 +458,12 @@ const char* gemm_f16_status_string(int status) {
 int gemm_f16_last_cuda_error(void) { return t_last_cuda_error; }
 
 int gemm_f16_force_config(int config) {
-    if (config < CFG_AUTO || config > CFG_128x64) return -1;
+    if (config < CFG_AUTO || config > CFG_SWAP) return -1;
     return g_force_config.exchange(config);
 }
 
 int gemm_f16_plan(const void* A, const void* B, const void* bias, const void* C, int64_t M, int64_t N, int64_t K,
-                  int epilogue, int num_sms, int64_t plan[8]) {
+                  int epilogue, int num_sms, int64_t plan[10]) {
     if (plan == nullptr || num_sms <= 0) return GEMM_ERR_INVALID_ARG;
     const int st = check_args(A, B, bias, C, M, N, K, epilogue);
     if (st != GEMM_OK) return st;
@@ -408,6 +476,8 @@ int gemm_f16_plan(const void* A, const void* B, const void* bias, const void* C,
     plan[5] = pl.pack_a;
     plan[6] = pl.pack_b;
     plan[7] = pl.vec_store;
+    plan[8] = pl.splits;
+    plan[9] = static_cast<int64_t>(pl.scratch_bytes());
     return GEMM_OK;
 }
 
@@ -428,7 +498,7 @@ int gemm_f16(const void* A, const void* B, const void* bias, void* C, int64_t M,
     if (pl.path == 1) return enqueue_bias_only(pl, biasp, C, M, N, epilogue, s);
 
     void* scratch = nullptr;
-    const size_t scratch_bytes = pl.a_scratch + pl.b_scratch;
+    const size_t scratch_bytes = pl.scratch_bytes();
     if (scratch_bytes > 0) {
         st = ensure_pool(dev);
         if (st != GEMM_OK) return st;
@@ -459,13 +529,16 @@ int gemm_f16_noalloc(const void* A, const void* B, const void* bias, void* C, in
     if (st != GEMM_OK) return st;
     const DeviceState& ds = g_dev[dev];
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-    const Plan pl = make_plan(A, B, C, M, N, K, ds.num_sms, ds.pair_clusters, g_force_config.load());
+    Plan pl = make_plan(A, B, C, M, N, K, ds.num_sms, ds.pair_clusters, g_force_config.load());
     const __half* biasp = epilogue == GEMM_EPI_NONE ? nullptr : static_cast<const __half*>(bias);
     if (pl.path == 1) return enqueue_bias_only(pl, biasp, C, M, N, epilogue, s);
-    // Same repack layout as gemm_f16 (A first, 256-byte aligned, then B), but
-    // inside the fixed buffer; nothing in it has to start at zero because the
-    // tensor maps stop at the true extents.
-    if (pl.a_scratch + pl.b_scratch > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
+    // Same scratch layout as gemm_f16, inside the fixed buffer.  The repacks
+    // need no zeroed memory (the tensor maps stop at the true extents); the
+    // split-K counters are zeroed by a stream-ordered memset in enqueue_plan.
+    // Without room for split-K partials the plan runs unsplit.
+    if (pl.scratch_bytes() > kNoAllocScratchBytes)
+        pl = make_plan(A, B, C, M, N, K, ds.num_sms, ds.pair_clusters, g_force_config.load(), false);
+    if (pl.scratch_bytes() > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
     return enqueue_plan(pl, A, B, biasp, C, M, N, K, epilogue, ds.noalloc_scratch, s);
 }
 

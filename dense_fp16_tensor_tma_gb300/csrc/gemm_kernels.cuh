@@ -92,6 +92,10 @@ struct GemmParams {
     int bias_vec;        // bias base 16-byte aligned (8-wide bias loads)
     int group_m;
     uint64_t timeout_ns;
+    // split-K (swap-AB kernel): K of every tile divided among `splits` CTAs
+    int splits;
+    float* partials;          // [tile][split][MT][128] fp32 partial sums
+    unsigned int* counters;   // [tile][4]: parts finished per 32-column slice (zero before the launch)
 };
 
 // Bias, activation and fp16 rounding of one 32-column chunk of this thread's

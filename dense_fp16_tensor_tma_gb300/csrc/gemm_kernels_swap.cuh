@@ -1,0 +1,263 @@
+// Swap-AB variant of the fused fp16 GEMM for short A (small M):
+//
+//   C^T = B^T . A^T,   then C = epilogue(C + bias) written transposed back.
+//
+// Same method as gemm_kernels.cuh ("writing-tilelang-kernels", GEMM
+// (Minimal); "TileLang: Write, Autotune, and Ship Fused Tensor-Core Kernels
+// from Python", Why tile-level control matters).  The tensor core's M side
+// must be 128 rows; with M of 64 or less, putting N on that side instead keeps
+// every MMA row useful and keeps the A tile (now the MMA's N side, MT rows)
+// small, so most of shared memory holds B, the operand this shape streams
+// from HBM:
+//
+//   * tile = 128 columns of C (MMA M, one TMEM lane each) x MT rows of C
+//     (MMA N = 16, 32 or 64);
+//   * MMA "A" operand = B^T: the same N-contiguous 64 x 64 boxes as the
+//     regular kernel's B (MN-major, LBO 8 KiB, SBO 1 KiB);
+//   * MMA "B" operand = A^T: an MT x 64 box of A rows (K-major, SBO 1 KiB);
+//   * stage = 16 KiB of B + MT x 128 B of A, 9 to 12 stages deep;
+//   * epilogue: thread = one output column n (its TMEM lane), registers = MT
+//     rows; bias[n] is one value per thread; every store of a warp covers 32
+//     consecutive columns of one row of C (64 contiguous bytes);
+//   * split-K: a CTA streams HBM at a bounded rate (its outstanding TMA
+//     requests), so when there are fewer tiles than SMs each tile's K range
+//     is divided among `splits` CTAs.  Every part writes its fp32 partial
+//     tile to scratch and counts itself in per-slice counters; the last part
+//     of a slice to finish sums all parts in part order (so the result does
+//     not depend on which finished last), then applies bias and activation
+//     and writes C.  No CTA waits for another.
+#pragma once
+
+#include "gemm_kernels.cuh"
+
+namespace gemm_f16_dev {
+
+constexpr int kSwapThreads = 192;   // producer, MMA, 4 epilogue warps
+
+template <int MT, int STAGES>
+struct SmemPlanSwap {
+    static constexpr uint32_t kBtBytes = 2 * kBBoxBytes;       // 128 columns of B x 64 K
+    static constexpr uint32_t kAtBytes = MT * kBK * 2;         // MT rows of A x 64 K
+    static constexpr uint32_t kStage = kBtBytes + kAtBytes;    // multiple of 1 KiB for MT % 8 == 0
+    static constexpr uint32_t kBars = STAGES * kStage;
+    static constexpr uint32_t kNumBars = 2 * STAGES + 2 + 2 + 1;
+    static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
+    static constexpr uint32_t kAbort = kTmemSlot + 4;
+    static constexpr uint32_t kEnd = kAbort + 4;
+    static constexpr uint32_t kDynamicBytes = kEnd + 1024;
+    static_assert(kStage % 1024 == 0, "swizzle atoms need 1 KiB alignment");
+};
+
+template <int MT, int STAGES>
+__global__ void __launch_bounds__(kSwapThreads, 1)
+gemm_f16_swap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const GemmParams p) {
+    using SP = SmemPlanSwap<MT, STAGES>;
+    constexpr int TN = 128;                                      // columns of C per tile
+    constexpr uint32_t kIdesc = idesc_f16_f32(TN, MT, /*b_mn_major=*/false, /*a_mn_major=*/true);
+    constexpr uint32_t kTmemCols = 2 * MT < 32 ? 32 : 2 * MT;    // two accumulators
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t* base = smem_raw + (base_s - raw_s);
+    const uint32_t bars = base_s + SP::kBars;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
+    auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bars + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + SP::kTmemSlot);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + SP::kAbort);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int tiles_m = (p.M + MT - 1) / MT;
+    const int tiles_n = (p.N + TN - 1) / TN;
+    const int num_tiles = tiles_m * tiles_n;
+    const int kblocks = (p.K + kBK - 1) / kBK;
+    const int S = p.splits;                          // >= 1; no part is empty (host guarantees)
+    const int kb_per = (kblocks + S - 1) / S;
+    const int num_units = num_tiles * S;             // unit u: tile u / S, part u % S
+    unsigned int* status = &g_status;
+    // tile t: row block t % tiles_m, column block t / tiles_m (consecutive CTAs share a B panel)
+    auto tile_m0 = [&](int t) { return (t % tiles_m) * MT; };
+    auto tile_n0 = [&](int t) { return (t / tiles_m) * TN; };
+    auto kb_begin = [&](int u) { return (u % S) * kb_per; };
+    auto kb_end = [&](int u) { return min(kblocks, (u % S + 1) * kb_per); };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+                const int t = u / S;
+                const int m0 = tile_m0(t), n0 = tile_n0(t);
+                // a B box wholly right of N is skipped: its stale columns only
+                // reach TMEM lanes that are never stored
+                const int live_b = min(2, (p.N - n0 + 63) / 64);
+                const uint32_t bytes = static_cast<uint32_t>(live_b) * kBBoxBytes + SP::kAtBytes;
+                for (int kb = kb_begin(u); kb < kb_end(u); ++kb) {
+                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, status,
+                                           ROLE_PRODUCER, BAR_EMPTY)) { ok = false; break; }
+                    const uint32_t st = base_s + stage * SP::kStage;
+                    mbar_arrive_expect_tx(full_bar(stage), bytes);
+                    for (int c = 0; c < live_b; ++c)
+                        tma_load_2d(st + c * kBBoxBytes, &tmB, full_bar(stage), n0 + 64 * c, kb * kBK);
+                    tma_load_2d(st + SP::kBtBytes, &tmA, full_bar(stage), kb * kBK, m0);
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            const int pending = min(issued, STAGES);
+            for (int i = 0; i < pending; ++i) {
+                if (--stage < 0) { stage = STAGES - 1; phase ^= 1u; }
+                mbar_wait_bounded(full_bar(stage), phase, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_FULL);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+                if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag, status,
+                                       ROLE_MMA, BAR_ACC_EMPTY)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MT);
+                const int kb0 = kb_begin(u);
+                for (int kb = kb0; kb < kb_end(u); ++kb) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, p.timeout_ns, abort_flag, status,
+                                           ROLE_MMA, BAR_FULL)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t st = base_s + stage * SP::kStage;
+#pragma unroll
+                    for (int k = 0; k < kBK / kUMMA_K; ++k) {
+                        // B^T: N-major boxes, K step of 16 rows = 2 KiB; A^T: K-major rows, K step 32 B
+                        const uint64_t adesc = smem_desc_sw128(st + k * 2048, kBBoxBytes, 1024);
+                        const uint64_t bdesc = smem_desc_sw128(st + SP::kBtBytes + k * 32, 0, 1024);
+                        tc_mma_f16(d_tmem, adesc, bdesc, kIdesc, (kb != kb0 || k != 0) ? 1u : 0u);
+                    }
+                    tc_commit(empty_bar(stage));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit(accf_bar(acc));
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            tc_commit(drain_bar);
+            mbar_wait_bounded(drain_bar, 0, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_DRAIN);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;   // TMEM lane quarter = columns n0 + 32q .. n0 + 32q + 31
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+            const int t = u / S, part = u % S;
+            const int m0 = tile_m0(t), n0 = tile_n0(t);
+            const int nl = 32 * q + lane;                // column within the tile
+            const int n = n0 + nl;
+            const bool col_ok = n < p.N;
+            const bool ready = mbar_wait_bounded(accf_bar(acc), acc_phase, p.timeout_ns, abort_flag, status,
+                                                 ROLE_EPILOGUE, BAR_ACC_FULL);
+            if (!__all_sync(0xffffffffu, ready)) break;
+            tc_fence_after();
+            const uint32_t t_base = tmem_base + static_cast<uint32_t>(acc * MT) + (static_cast<uint32_t>(32 * q) << 16);
+            float v[MT];
+#pragma unroll
+            for (int j = 0; j < MT / 16; ++j) {
+                uint32_t r[16];
+                tmem_ld_32x32b_x16(t_base + 16u * j, r);
+                tmem_wait_ld(r);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[16 * j + i] = __uint_as_float(r[i]);
+            }
+            // the accumulator is in registers now: hand the TMEM buffer back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar(acc));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+
+            bool finish = true;
+            if (S > 1) {
+                float* mine = p.partials + static_cast<int64_t>(u) * MT * TN;
+#pragma unroll
+                for (int i = 0; i < MT; ++i) __stcg(mine + i * TN + nl, v[i]);
+                __threadfence();
+                __syncwarp();
+                unsigned int before = 0;
+                if (lane == 0) before = atomicAdd(p.counters + 4 * t + q, 1u);
+                before = __shfl_sync(0xffffffffu, before, 0);
+                finish = before == static_cast<unsigned int>(S - 1);
+                if (finish) {
+                    __threadfence();
+                    // all parts, in part order: the sum does not depend on arrival order
+                    float sum[MT];
+#pragma unroll
+                    for (int i = 0; i < MT; ++i) sum[i] = 0.0f;
+                    for (int sp = 0; sp < S; ++sp) {
+                        const float* src = p.partials + static_cast<int64_t>(t * S + sp) * MT * TN;
+#pragma unroll
+                        for (int i = 0; i < MT; ++i) sum[i] += sp == part ? v[i] : __ldcg(src + i * TN + nl);
+                    }
+#pragma unroll
+                    for (int i = 0; i < MT; ++i) v[i] = sum[i];
+                    if (lane == 0) p.counters[4 * t + q] = 0u;   // ready for the next launch
+                }
+            }
+            if (finish) {
+                const float b = (p.epi != EPI_NONE && col_ok) ? __half2float(p.bias[n]) : 0.0f;
+#pragma unroll
+                for (int i = 0; i < MT; ++i) {
+                    const int m = m0 + i;
+                    if (col_ok && m < p.M)
+                        p.C[static_cast<int64_t>(m) * p.ldc + n] = __float2half_rn(apply_act(v[i] + b, p.epi));
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace gemm_f16_dev

@@ -102,21 +102,24 @@ int gemm_f16_release_workspace(void);
  * Host-only planning query (no device access): the execution plan that
  * gemm_f16 would choose for these sizes and base addresses on a device with
  * `num_sms` SMs (assuming num_sms/2 co-resident CTA pairs).  plan[0..7]
- * receive: path (0 none, 1 bias-only K==0, 2 tiled tensor-core kernel),
- * tile_m (256 for the CTA-pair kernel), tile_n,
+ * receive: path (0 none, 1 bias-only K==0, 2 tiled tensor-core kernel,
+ * 3 swap-AB kernel for M <= 64), tile_m (256 for the CTA-pair kernel),
+ * tile_n,
  * pipeline stages, CTAs launched, repack A (0/1), repack B (0/1), vector
- * stores of C (0/1).  Returns a status code like gemm_f16 (argument errors
- * only).  Diagnostic; it has no counterpart on the pages.
+ * stores of C (0/1), split-K parts per tile, scratch bytes.  Returns a status
+ * code like gemm_f16 (argument errors only).  Diagnostic; it has no
+ * counterpart on the pages.
  */
 int gemm_f16_plan(const void* A, const void* B, const void* bias, const void* C,
                   int64_t M, int64_t N, int64_t K, int epilogue, int num_sms,
-                  int64_t plan[8]);
+                  int64_t plan[10]);
 
 /*
  * Diagnostic (no counterpart on the pages): pins the kernel configuration
  * that every later call in this process uses, for tests and tile sweeps.
  *   0 automatic (the default), 1 CTA pair with a 256 x 256 tile,
- *   2 single CTA 128 x 256, 3 single CTA 128 x 128, 4 single CTA 128 x 64.
+ *   2 single CTA 128 x 256, 3 single CTA 128 x 128, 4 single CTA 128 x 64,
+ *   5 swap-AB (C^T = B^T A^T; tiles of 128 columns x 16, 32 or 64 rows).
  * Returns the previous setting, or -1 (nothing changed) for an unknown
  * value.  Process-wide; set it while no other host thread is calling.
  */
@@ -152,10 +155,12 @@ int gemm_f16_selftest_timeout(void* cuda_stream, uint32_t timeout_us);
  * memory obtained from the allocator.  This function calls no cudaMalloc,
  * cudaFree or other allocating routine.
  *
- *   - Sizes: the repack needs 2*M*round8(K) bytes for A (rounded up to 256)
- *     plus 2*K*round8(N) bytes for B; a problem needing more than 32 MiB
- *     returns GEMM_ERR_SCRATCH_LIMIT and enqueues nothing.  Problems that
- *     need no repack have no size limit.
+ *   - Sizes: the repack needs 2*M*round8(K) bytes for A plus 2*K*round8(N)
+ *     bytes for B (each rounded up to 256); a problem needing more than
+ *     32 MiB returns GEMM_ERR_SCRATCH_LIMIT and enqueues nothing.  Problems
+ *     that need no repack have no size limit.  The split-K partial sums of
+ *     short-A problems use the same buffer when they fit, and are skipped
+ *     (the problem runs unsplit) when they do not.
  *   - Set-up: the first call on each device (with that device current) looks
  *     up the buffer's device address and sets kernel attributes; make that
  *     first call before any stream capture.

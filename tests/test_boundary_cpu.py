@@ -133,3 +133,14 @@ def test_python_binding_rejects_bad_tensors(g):
         g.gemm_f16(A, B, None, C)            # CPU tensors
     with pytest.raises(ValueError):
         g.gemm_f16(A, B, None, torch.zeros(4, 5, dtype=torch.float16))
+
+
+def test_plan_short_a_uses_swap_ab(g):
+    p = g.gemm_f16_plan(16, 8192, 8192, "none", num_sms=152)
+    # 64 tiles of 128 columns, K split in two: 128 CTAs stream B
+    assert (p["path"], p["tile_m"], p["tile_n"], p["splits"], p["ctas"]) == (3, 16, 128, 2, 128)
+    assert p["scratch"] == 64 * 2 * 16 * 128 * 4 + 1024
+    p = g.gemm_f16_plan(16, 16384, 8192, "none", num_sms=152)
+    assert (p["splits"], p["ctas"], p["scratch"]) == (1, 128, 0)
+    assert g.gemm_f16_plan(33, 1000, 64, "none", num_sms=152)["tile_m"] == 64
+    assert g.gemm_f16_plan(65, 1000, 64, "none", num_sms=152)["path"] == 2

@@ -264,7 +264,7 @@ def test_bounded_wait_reports_timeout_and_context_survives(g, torch_dev, oracle_
 
 # ---------------------------------------------------------------- every kernel configuration
 
-CONFIGS = ["pair256x256", "128x256", "128x128", "128x64"]
+CONFIGS = ["pair256x256", "128x256", "128x128", "128x64", "swap"]
 
 
 @pytest.fixture
@@ -311,3 +311,55 @@ def test_forced_config_many_tiles_per_cta(forced, torch_dev, oracle_mod, cfg):
     got = run(g, torch_dev, A, B, bias, "bias_gelu_erf")
     rows = np.arange(3, M, 61)
     assert_parity(got[rows], oracle_mod.gemm_rows(A, B, bias, "bias_gelu_erf", rows), cfg)
+
+
+# ---------------------------------------------------------------- short A: the swap-AB kernel
+
+@pytest.mark.parametrize("M,N,K,epi", [(1, 128, 64, "bias"), (7, 300, 77, "bias_gelu_erf"), (16, 1024, 512, "none"),
+                                       (17, 5003, 1000, "bias_relu"), (33, 264, 130, "bias_gelu_erf"),
+                                       (64, 2048, 4096, "bias"), (48, 129, 8, "none")])
+def test_short_a_swap_path(g, torch_dev, oracle_mod, M, N, K, epi):
+    assert g.gemm_f16_plan(M, N, K, epi)["path"] == 3
+    rng = np.random.default_rng(M * 31 + N + K)
+    A, B, bias = rand16(rng, (M, K), 0.5), rand16(rng, (K, N), 0.5), rand16(rng, N)
+    got = run(g, torch_dev, A, B, bias, epi)
+    assert_parity(got, oracle_mod.gemm(A, B, bias if epi != "none" else None, epi), f"{M}x{N}x{K} {epi}")
+
+
+@pytest.mark.parametrize("M", [1, 16, 40, 64])
+def test_short_a_integer_exact(g, torch_dev, oracle_mod, M):
+    rng = np.random.default_rng(M)
+    N, K = 520, 264
+    A = rng.integers(-2, 3, (M, K)).astype(np.float16)
+    B = rng.integers(-2, 3, (K, N)).astype(np.float16)
+    bias = rng.integers(-8, 9, N).astype(np.float16)
+    got = run(g, torch_dev, A, B, bias, "bias_relu")
+    assert np.array_equal(got, oracle_mod.gemm(A, B, bias, "bias_relu"))
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 256, 4096), (40, 1000, 2000), (64, 384, 8192), (3, 130, 1024)])
+def test_short_a_split_k_integer_exact(g, torch_dev, oracle_mod, M, N, K):
+    plan = g.gemm_f16_plan(M, N, K, "bias")
+    assert plan["path"] == 3 and plan["splits"] > 1
+    rng = np.random.default_rng(M + N + K)
+    A = rng.integers(-1, 2, (M, K)).astype(np.float16)      # |C| <= K: exact in fp32 and, here, fp16 for K <= 2048
+    B = rng.integers(-1, 2, (K, N)).astype(np.float16)
+    bias = rng.integers(-8, 9, N).astype(np.float16)
+    got = run(g, torch_dev, A, B, bias, "bias")
+    ref = oracle_mod.gemm(A, B, bias, "bias")
+    if K <= 2048:
+        assert np.array_equal(got, ref)
+    else:
+        assert_parity(got, ref, f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("epi", EPIS)
+def test_short_a_split_k_random_and_deterministic(g, torch_dev, oracle_mod, epi):
+    M, N, K = 24, 1536, 6000
+    assert g.gemm_f16_plan(M, N, K, epi)["splits"] > 1
+    rng = np.random.default_rng(21)
+    A, B, bias = rand16(rng, (M, K), 0.1), rand16(rng, (K, N), 0.1), rand16(rng, N)
+    c1 = run(g, torch_dev, A, B, bias, epi)
+    c2 = run(g, torch_dev, A, B, bias, epi)
+    assert np.array_equal(c1.view(np.uint16), c2.view(np.uint16))
+    assert_parity(c1, oracle_mod.gemm(A, B, bias if epi != "none" else None, epi), epi)
