@@ -73,7 +73,7 @@ def test_argument_errors_need_no_device(g, args, expect):
 def test_plan_large_square_uses_cta_pairs(g):
     p = g.gemm_f16_plan(8192, 8192, 8192, "bias_gelu_erf", num_sms=152)
     assert p == {"path": 2, "tile_m": 256, "tile_n": 256, "stages": 3, "ctas": 152,
-                 "pack_a": 0, "pack_b": 0, "vec_store": 1}
+                 "pack_a": 0, "pack_b": 0, "vec_store": 1, "splits": 1, "scratch": 0}
     p = g.gemm_f16_plan(4096, 4096, 4096, "bias_gelu_erf", num_sms=152)
     assert p["tile_m"] == 256 and p["ctas"] == 152
 
