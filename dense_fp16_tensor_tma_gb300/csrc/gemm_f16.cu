@@ -309,9 +309,8 @@ int encode_2d(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int
 
 int launch_repack(uint16_t* dst, const void* src, int64_t rows, int64_t cols, int64_t ld_src, int64_t ld_dst,
                   cudaStream_t s) {
-    dim3 block(256);
-    dim3 grid(static_cast<unsigned>(std::min<int64_t>((cols + 255) / 256, 64)),
-              static_cast<unsigned>(std::min<int64_t>(rows, 65535)));
+    dim3 block(256);   // 8 elements per thread: 2048 per block along a row
+    dim3 grid(static_cast<unsigned>((cols + 2047) / 2048), static_cast<unsigned>(std::min<int64_t>(rows, 65535)));
     gemm_f16_repack_kernel<<<grid, block, 0, s>>>(dst, static_cast<const uint16_t*>(src), rows, cols, ld_src,
                                                   ld_dst);
     cudaError_t e = cudaGetLastError();

@@ -383,13 +383,27 @@ __global__ void gemm_f16_bias_only_kernel(__half* C, const __half* bias, int64_t
 
 // Row repack: dst[r, 0:cols] = src[r, 0:cols] with a 16-byte-multiple pitch,
 // so the tensor map can describe the copy (columns >= cols are left as is;
-// the tensor map's extent stops at `cols`, so TMA never reads them).
+// the tensor map's extent stops at `cols`, so TMA never reads them).  Each
+// thread gathers 8 consecutive source elements (the source rows are only
+// 2-byte aligned) and writes them with one 16-byte store (ld_dst % 8 == 0 and
+// dst is 256-byte aligned).  grid.x covers a row in 2048-element pieces,
+// grid.y strides over rows.
 __global__ void gemm_f16_repack_kernel(uint16_t* __restrict__ dst, const uint16_t* __restrict__ src,
                                        int64_t rows, int64_t cols, int64_t ld_src, int64_t ld_dst) {
-    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y)
-        for (int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; c < cols;
-             c += static_cast<int64_t>(gridDim.x) * blockDim.x)
-            dst[r * ld_dst + c] = src[r * ld_src + c];
+    const int64_t c = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
+    if (c >= cols) return;
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+        const uint16_t* s = src + r * ld_src + c;
+        uint16_t* d = dst + r * ld_dst + c;
+        if (c + 8 <= cols) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) w[j] = static_cast<uint32_t>(s[2 * j]) | (static_cast<uint32_t>(s[2 * j + 1]) << 16);
+            *reinterpret_cast<uint4*>(d) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+            for (int64_t j = 0; j < cols - c; ++j) d[j] = s[j];
+        }
+    }
 }
 
 // One CTA, one thread waits on a barrier nobody arrives on.
