@@ -40,10 +40,13 @@ constexpr int kEpiWarps = 8;             // two per TMEM lane quarter, each half
 constexpr uint32_t kATileBytes = kBM * kBK * 2;  // 16 KiB
 constexpr uint32_t kBBoxBytes = 64 * kBK * 2;    // one 64(N) x 64(K) box, 8 KiB
 // Per epilogue warp: a 32 x 32 fp16 block, rows padded to 17 words so that
-// both the row-wise writes and the column-wise reads are bank-conflict free.
+// both the row-wise writes and the column-wise reads are bank-conflict free,
+// then the bias of the warp's (up to 128) columns as 64 packed fp16 pairs.
 constexpr uint32_t kStageRowWords = 17;
-constexpr uint32_t kStageWarpBytes = 32 * kStageRowWords * 4;
-constexpr uint32_t kStageBytes = kEpiWarps * kStageWarpBytes;   // 17 KiB for the eight epilogue warps
+constexpr uint32_t kStageBlockWords = 32 * kStageRowWords;
+constexpr uint32_t kStageBiasWords = 64;
+constexpr uint32_t kStageWarpBytes = (kStageBlockWords + kStageBiasWords) * 4;
+constexpr uint32_t kStageBytes = kEpiWarps * kStageWarpBytes;   // 19 KiB for the eight epilogue warps
 
 template <int BN, int STAGES>
 struct SmemPlan {
@@ -98,40 +101,34 @@ struct GemmParams {
     unsigned int* counters;   // [tile][4]: parts finished per 32-column slice (zero before the launch)
 };
 
+// Stage the bias of columns n0 .. n0 + ncol - 1 (zero past N) as packed fp16
+// pairs in this warp's shared memory: done before the accumulator wait, so
+// the global loads overlap it.
+__device__ __forceinline__ void stage_bias(const GemmParams& p, uint32_t* bias_w, int n0, int ncol) {
+    const int lane = threadIdx.x & 31;
+    const uint16_t* b16 = reinterpret_cast<const uint16_t*>(p.bias);
+    __syncwarp();
+    for (int i = lane; i < ncol / 2; i += 32) {
+        const int n = n0 + 2 * i;
+        const uint32_t lo = n < p.N ? b16[n] : 0u;
+        const uint32_t hi = n + 1 < p.N ? b16[n + 1] : 0u;
+        bias_w[i] = lo | (hi << 16);
+    }
+    __syncwarp();
+}
+
 // Bias, activation and fp16 rounding of one 32-column chunk of this thread's
-// row: r = 32 fp32 accumulator columns, bias of columns col0..col0+31.
-__device__ __forceinline__ void epilogue_math(const GemmParams& p, const uint32_t (&r)[32], int col0,
+// row: r = 32 fp32 accumulator columns; bw = the chunk's 16 staged bias pairs.
+__device__ __forceinline__ void epilogue_math(const GemmParams& p, const uint32_t (&r)[32], const uint32_t* bw,
                                               uint32_t (&h)[16]) {
     const bool has_bias = p.epi != EPI_NONE;
-    uint32_t bw[16];   // bias as packed fp16 pairs
-    if (has_bias) {
-        if (p.bias_vec && col0 + 32 <= p.N) {
-            // every lane reads the same 64 bytes: a broadcast that L1 serves after the first tile
-            const uint4* src = reinterpret_cast<const uint4*>(p.bias + col0);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const uint4 w = __ldg(src + v);
-                bw[4 * v] = w.x;
-                bw[4 * v + 1] = w.y;
-                bw[4 * v + 2] = w.z;
-                bw[4 * v + 3] = w.w;
-            }
-        } else {
-            const uint16_t* b16 = reinterpret_cast<const uint16_t*>(p.bias);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const uint32_t lo = col0 + 2 * j < p.N ? b16[col0 + 2 * j] : 0u;
-                const uint32_t hi = col0 + 2 * j + 1 < p.N ? b16[col0 + 2 * j + 1] : 0u;
-                bw[j] = lo | (hi << 16);
-            }
-        }
-    }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         float x0 = __uint_as_float(r[2 * j]);
         float x1 = __uint_as_float(r[2 * j + 1]);
         if (has_bias) {
-            const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&bw[j]));
+            const uint32_t w = bw[j];
+            const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&w));
             x0 += b2.x;
             x1 += b2.y;
         }
@@ -166,7 +163,7 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const uint32
     const bool col_ok = col0 + lane < p.N;
     uint16_t* cbase = reinterpret_cast<uint16_t*>(p.C + static_cast<int64_t>(row0) * p.ldc + col0 + lane);
     if (row0 + 32 <= p.M) {
-#pragma unroll
+#pragma unroll 8
         for (int rr = 0; rr < 32; ++rr) {
             const uint32_t w = stage[rr * kStageRowWords + (lane >> 1)];
             if (col_ok) cbase[static_cast<int64_t>(rr) * p.ldc] = static_cast<uint16_t>(w >> (16 * (lane & 1)));
@@ -183,23 +180,35 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const uint32
 
 // Epilogue of NCOL accumulator columns for this warp's 32 TMEM lanes (tile
 // rows row0..row0+31, one per thread), starting at TMEM address t_base and
-// output column n0.  Latency of the TMEM loads is hidden by the second
-// epilogue warp on the same SM sub-partition (each sub-partition's register
-// file holds at most 168 registers per thread for 10 warps, too few for two
-// chunks in flight per warp).
+// output column n0.  `stage` is the warp's shared-memory block, followed by
+// its staged bias (stage_bias).  The TMEM load of chunk c+1 is in flight
+// while chunk c is processed.
 template <int NCOL>
 __device__ __forceinline__ void epilogue_rows(const GemmParams& p, uint32_t t_base, int row0, int n0,
                                               uint32_t* stage) {
+    constexpr int kChunks = NCOL / 32;
+    const uint32_t* bias_w = stage + kStageBlockWords;
+    uint32_t ra[32], rb[32];
+    tmem_ld_32x32b_x32(t_base, ra);
+    tmem_wait_ld(ra);
+    // chunks two at a time: the even one in ra, the odd one in rb
 #pragma unroll 1
-    for (int c = 0; c < NCOL / 32; ++c) {
+    for (int c = 0; c < kChunks; c += 2) {
         const int col0 = n0 + 32 * c;
         if (col0 >= p.N) break;   // warp-uniform: the remaining chunks are right of N
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_base + 32u * c, r);
-        tmem_wait_ld(r);
+        const bool odd = c + 1 < kChunks && col0 + 32 < p.N;
+        if (odd) tmem_ld_32x32b_x32(t_base + 32u * (c + 1), rb);
         uint32_t h[16];
-        epilogue_math(p, r, col0, h);
+        epilogue_math(p, ra, bias_w + 16 * c, h);
         epilogue_store(p, h, row0, col0, stage);
+        if (!odd) break;
+        tmem_wait_ld(rb);
+        const bool even = c + 2 < kChunks && col0 + 64 < p.N;
+        if (even) tmem_ld_32x32b_x32(t_base + 32u * (c + 2), ra);
+        epilogue_math(p, rb, bias_w + 16 * (c + 1), h);
+        epilogue_store(p, h, row0, col0 + 32, stage);
+        if (!even) break;
+        tmem_wait_ld(ra);
     }
 }
 
@@ -346,16 +355,17 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             const TileCoord tc = tile_coord(t, tiles_m, tiles_n, p.group_m, BN);
+            const int half = (warp - 2) >> 2;   // which half of the tile's columns
+            uint32_t* stage = reinterpret_cast<uint32_t*>(base + SP::kStage + (warp - 2) * kStageWarpBytes);
+            if (p.epi != EPI_NONE) stage_bias(p, stage + kStageBlockWords, tc.n0 + half * (BN / 2), BN / 2);
             // tcgen05.ld is warp-collective: the go/no-go decision must be warp-uniform.
             const bool ready = mbar_wait_bounded(accf_bar(acc), acc_phase, p.timeout_ns, abort_flag, status,
                                                  ROLE_EPILOGUE, BAR_ACC_FULL);
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
-            const int half = (warp - 2) >> 2;   // which half of the tile's columns
             const uint32_t t_base = tmem_base + static_cast<uint32_t>(acc * BN + half * (BN / 2)) +
                                     (static_cast<uint32_t>(32 * q) << 16);
-            epilogue_rows<BN / 2>(p, t_base, tc.m0 + 32 * q, tc.n0 + half * (BN / 2),
-                                  reinterpret_cast<uint32_t*>(base + SP::kStage + (warp - 2) * kStageWarpBytes));
+            epilogue_rows<BN / 2>(p, t_base, tc.m0 + 32 * q, tc.n0 + half * (BN / 2), stage);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(acc));

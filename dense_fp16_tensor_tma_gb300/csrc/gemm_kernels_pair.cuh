@@ -226,15 +226,17 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const uint32_t acce_leader1 = mapa_shared(acce_bar(1), 0);
         for (int t = cid; t < num_tiles; t += nclusters) {
             const TileCoord tc = tile_coord_bm(t, tiles_m, tiles_n, p.group_m, PM, BN);
+            const int half = (warp - 2) >> 2;   // which half of the tile's columns
+            uint32_t* stage = reinterpret_cast<uint32_t*>(base + SP::kStage + (warp - 2) * kStageWarpBytes);
+            if (p.epi != EPI_NONE) stage_bias(p, stage + kStageBlockWords, tc.n0 + half * (BN / 2), BN / 2);
             const bool ready = mbar_wait_cluster_bounded(accf_bar(acc), acc_phase, p.timeout_ns, abort_flag, status,
                                                          ROLE_EPILOGUE, BAR_ACC_FULL);
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
-            const int half = (warp - 2) >> 2;   // which half of the tile's columns
             const uint32_t t_base = tmem_base + static_cast<uint32_t>(acc * BN + half * (BN / 2)) +
                                     (static_cast<uint32_t>(32 * q) << 16);
             epilogue_rows<BN / 2>(p, t_base, tc.m0 + 128 * static_cast<int>(rank) + 32 * q, tc.n0 + half * (BN / 2),
-                                  reinterpret_cast<uint32_t*>(base + SP::kStage + (warp - 2) * kStageWarpBytes));
+                                  stage);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acc == 0 ? acce_leader0 : acce_leader1);
