@@ -363,3 +363,37 @@ def test_short_a_split_k_random_and_deterministic(g, torch_dev, oracle_mod, epi)
     c2 = run(g, torch_dev, A, B, bias, epi)
     assert np.array_equal(c1.view(np.uint16), c2.view(np.uint16))
     assert_parity(c1, oracle_mod.gemm(A, B, bias if epi != "none" else None, epi), epi)
+
+
+# ---------------------------------------------------------------- the device GELU itself
+
+def test_device_gelu_on_every_fp16_value_in_range(g, torch_dev, oracle_mod):
+    # C[i, j] = x_i exactly (x_i * 1 + zeros), so the epilogue sees every fp16 value in
+    # [-10, 10].  The device erf (Abramowitz & Stegun 7.1.26, |error| <= 1.5e-7) in fp32:
+    # each result within 1 fp16 ulp of the fp64 definition, or within 3e-7 max(1, |x|)
+    # absolute (the far negative tail, where GELU is a tiny subnormal and any fp32 form of
+    # 1 + erf loses relative accuracy); almost all bit-equal.
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    xs = bits.view(np.float16)
+    xs = xs[np.isfinite(xs)]
+    xs = np.unique(xs[np.abs(xs.astype(np.float64)) <= 10.0])
+    M, N, K = xs.size, 16, 8
+    A = np.zeros((M, K), np.float16)
+    A[:, 0] = xs
+    B = np.zeros((K, N), np.float16)
+    B[0, :] = 1.0
+    bias = np.zeros(N, np.float16)
+    got = run(g, torch_dev, A, B, bias, "bias_gelu_erf")[:, 0]
+    ref = oracle_mod.gemm(A, B, bias, "bias_gelu_erf")[:, 0]
+    gb = got.view(np.uint16).astype(np.int64)
+    rb = ref.view(np.uint16).astype(np.int64)
+    # ulp distance on the sign-magnitude fp16 encoding
+    def ordered(b):
+        return np.where(b & 0x8000, -(b & 0x7FFF), b)
+    dist = np.abs(ordered(gb) - ordered(rb))
+    abs_err = np.abs(got.astype(np.float64) - ref.astype(np.float64))
+    ok = (dist <= 1) | (abs_err <= 3e-7 * np.maximum(1.0, np.abs(xs.astype(np.float64))))
+    assert ok.all(), (xs[~ok][:5], got[~ok][:5], ref[~ok][:5])
+    # where |GELU| >= 2^-10 the fp16 spacing dwarfs the fp32 error: nearly all bit-equal
+    big = np.abs(ref.astype(np.float64)) >= 2.0 ** -10
+    assert (dist[big] == 0).mean() >= 0.995
