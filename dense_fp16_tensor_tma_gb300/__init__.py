@@ -23,7 +23,7 @@ GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT, GEMM_ERR_NO_MEMORY, GEMM_ERR_SCRATCH_LIMIT = 4,
 EXPORTS = ("gemm_f16", "gemm_f16_status_string", "gemm_f16_last_cuda_error", "gemm_f16_debug_status",
            "gemm_f16_release_workspace", "gemm_f16_plan", "gemm_f16_selftest_timeout", "gemm_f16_noalloc",
            "gemm_f16_force_config")
-CONFIGS = {"auto": 0, "pair256x256": 1, "128x256": 2, "128x128": 3, "128x64": 4, "swap": 5}
+CONFIGS = {"auto": 0, "pair256x256": 1, "128x256": 2, "128x128": 3, "128x64": 4, "swap": 5, "pair_whole": 6}
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
@@ -109,12 +109,13 @@ def gemm_f16(A, B, bias, C, epilogue="none", stream=None):
 def gemm_f16_plan(M, N, K, epilogue="none", num_sms=152, a_addr=256, b_addr=256, c_addr=256,
                   bias_addr=256):
     """Host-only: the plan gemm_f16 would pick (dict), without touching a device."""
-    out = (ctypes.c_int64 * 10)()
+    out = (ctypes.c_int64 * 11)()
     st = lib.gemm_f16_plan(a_addr or None, b_addr or None, bias_addr or None, c_addr or None,
                            int(M), int(N), int(K), _epi(epilogue), int(num_sms), out)
     if st != GEMM_OK:
         raise GemmError(st, "gemm_f16_plan")
-    keys = ("path", "tile_m", "tile_n", "stages", "ctas", "pack_a", "pack_b", "vec_store", "splits", "scratch")
+    keys = ("path", "tile_m", "tile_n", "stages", "ctas", "pack_a", "pack_b", "vec_store", "splits", "scratch",
+            "whole_tiles")
     return dict(zip(keys, list(out)))
 
 

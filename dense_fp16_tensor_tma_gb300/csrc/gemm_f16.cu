@@ -28,7 +28,10 @@ thread_local int t_last_cuda_error = 0;
 // per CTA, 128-deep K stages) is the throughput shape; single-CTA tiles of
 // 128 x {256,128,64} give small problems more CTAs; the swap-AB kernel
 // (C^T = B^T A^T, tiles of 128 columns x 16/32/64 rows) serves short A.
-enum Config : int { CFG_AUTO = 0, CFG_PAIR_256 = 1, CFG_128x256 = 2, CFG_128x128 = 3, CFG_128x64 = 4, CFG_SWAP = 5 };
+enum Config : int {
+    CFG_AUTO = 0, CFG_PAIR_256 = 1, CFG_128x256 = 2, CFG_128x128 = 3, CFG_128x64 = 4, CFG_SWAP = 5,
+    CFG_PAIR_256_WHOLE = 6   // the CTA pair without half-tile tail units (diagnostic)
+};
 #ifndef GEMM_F16_PAIR_STAGES
 #define GEMM_F16_PAIR_STAGES 3
 #endif
@@ -82,6 +85,7 @@ struct Plan {
     bool pack_a = false, pack_b = false, vec_store = false;
     int64_t lda_packed = 0, ldb_packed = 0;
     int splits = 1;                        // split-K parts per tile (swap-AB kernel)
+    int dp_tiles = 0, tail_split = 0;      // CTA pair: whole tiles, then half-tile units
     // scratch layout: [A repack][B repack][split-K partials][split-K counters], each 256-aligned
     size_t a_scratch = 0, b_scratch = 0, p_scratch = 0, c_scratch = 0;
     size_t scratch_bytes() const { return a_scratch + b_scratch + p_scratch + c_scratch; }
@@ -130,6 +134,11 @@ Plan make_plan(const void* A, const void* B, const void* C, int64_t M, int64_t N
     const int64_t tiles_m = (M + 127) / 128;
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     int cfg = force;
+    bool tail_halves = true;
+    if (cfg == CFG_PAIR_256_WHOLE) {
+        cfg = CFG_PAIR_256;
+        tail_halves = false;
+    }
     if (cfg == CFG_AUTO) {
         if (M <= 64) {
             cfg = CFG_SWAP;
@@ -144,10 +153,21 @@ Plan make_plan(const void* A, const void* B, const void* C, int64_t M, int64_t N
     }
     pl.cfg = cfg;
     switch (cfg) {
-        case CFG_PAIR_256:
+        case CFG_PAIR_256: {
             pl.tile_m = 256; pl.tile_n = 256; pl.stages = kStagesPair;
-            pl.ctas = 2 * static_cast<int>(std::min<int64_t>(pair_tiles, std::max(1, pair_clusters)));
+            const int64_t G = std::max(1, pair_clusters);
+            // A partial last wave of R tiles (R <= G/2) runs as 2R half tiles
+            // (256 x 128) on the pairs: it then costs half a tile, not a whole one.
+            const int64_t R = pair_tiles % G;
+            pl.dp_tiles = static_cast<int>(pair_tiles);
+            if (tail_halves && R > 0 && 2 * R <= G) {
+                pl.dp_tiles = static_cast<int>(pair_tiles - R);
+                pl.tail_split = 1;
+            }
+            const int64_t units = pl.dp_tiles + (pl.tail_split ? 2 * (pair_tiles - pl.dp_tiles) : 0);
+            pl.ctas = 2 * static_cast<int>(std::min<int64_t>(units, G));
             break;
+        }
         case CFG_SWAP:
             pl.path = 3;
             pl.tile_m = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
@@ -387,6 +407,8 @@ int enqueue_plan(const Plan& pl, const void* A, const void* B, const __half* bia
     prm.bias_vec = (biasp != nullptr && aligned(biasp, 16)) ? 1 : 0;
     prm.group_m = kGroupM;
     prm.timeout_ns = g_timeout_ns;
+    prm.dp_tiles = pl.dp_tiles;
+    prm.tail_split = pl.tail_split;
     prm.splits = pl.splits;
     prm.partials = partials;
     prm.counters = counters;
@@ -457,12 +479,12 @@ const char* gemm_f16_status_string(int status) {
 int gemm_f16_last_cuda_error(void) { return t_last_cuda_error; }
 
 int gemm_f16_force_config(int config) {
-    if (config < CFG_AUTO || config > CFG_SWAP) return -1;
+    if (config < CFG_AUTO || config > CFG_PAIR_256_WHOLE) return -1;
     return g_force_config.exchange(config);
 }
 
 int gemm_f16_plan(const void* A, const void* B, const void* bias, const void* C, int64_t M, int64_t N, int64_t K,
-                  int epilogue, int num_sms, int64_t plan[10]) {
+                  int epilogue, int num_sms, int64_t plan[11]) {
     if (plan == nullptr || num_sms <= 0) return GEMM_ERR_INVALID_ARG;
     const int st = check_args(A, B, bias, C, M, N, K, epilogue);
     if (st != GEMM_OK) return st;
@@ -477,6 +499,7 @@ int gemm_f16_plan(const void* A, const void* B, const void* bias, const void* C,
     plan[7] = pl.vec_store;
     plan[8] = pl.splits;
     plan[9] = static_cast<int64_t>(pl.scratch_bytes());
+    plan[10] = pl.tail_split ? static_cast<int64_t>(pl.dp_tiles) : -1;
     return GEMM_OK;
 }
 

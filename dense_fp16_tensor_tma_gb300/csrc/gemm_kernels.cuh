@@ -119,6 +119,10 @@ struct GemmParams {
     int bias_vec;        // bias base 16-byte aligned (8-wide bias loads)
     int group_m;
     uint64_t timeout_ns;
+    // CTA-pair kernel: tiles [0, dp_tiles) whole; with tail_split the rest are
+    // computed as two 256 x 128 halves each (a partial last wave costs half a tile)
+    int dp_tiles;
+    int tail_split;
     // split-K (swap-AB kernel): K of every tile divided among `splits` CTAs
     int splits;
     float* partials;          // [tile][split][MT][128] fp32 partial sums

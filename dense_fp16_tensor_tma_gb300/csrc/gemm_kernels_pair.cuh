@@ -56,6 +56,39 @@ __device__ __forceinline__ TileCoord tile_coord_bm(int t, int tiles_m, int tiles
     return c;
 }
 
+// One unit of a CTA pair's work: a whole 256 x 256 tile (half < 0) or the
+// 256 x 128 column half `half` of a tile.
+struct PairUnit {
+    int tile, half;
+};
+
+// The units of CTA pair w out of G, in order: whole tiles w, w + G, ...
+// below dp_tiles, then half-tile units w, w + G, ... of the remaining tiles.
+// A partial last wave of R tiles thus becomes 2R half-tiles spread over the
+// pairs (the host splits only when 2R <= G), each worth half a tile.  Every
+// role of both CTAs walks the same sequence.
+struct PairUnitIter {
+    int w, G, D, halves;
+    int t, u;
+    __device__ PairUnitIter(int w_, int G_, int D_, int num_tiles, int split)
+        : w(w_), G(G_), D(D_), halves(split ? 2 * (num_tiles - D_) : 0), t(w_), u(w_) {}
+    __device__ bool next(PairUnit& x) {
+        if (t < D) {
+            x.tile = t;
+            x.half = -1;
+            t += G;
+            return true;
+        }
+        if (u < halves) {
+            x.tile = D + (u >> 1);
+            x.half = u & 1;
+            u += G;
+            return true;
+        }
+        return false;
+    }
+};
+
 template <int STAGES, int KSUB>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -65,6 +98,7 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     constexpr int PM = 256;                  // pair tile rows = MMA M
     constexpr int BN = 256;                  // pair tile columns = MMA N
     constexpr uint32_t kIdesc = idesc_f16_f32(PM, BN, /*b_mn_major=*/true);
+    constexpr uint32_t kIdescHalf = idesc_f16_f32(PM, BN / 2, /*b_mn_major=*/true);   // 256 x 128 units
     constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators of 256 fp32 columns
 
     extern __shared__ uint8_t smem_raw[];
@@ -121,6 +155,7 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int kblocks = (p.K + kStageK - 1) / kStageK;   // pipeline stages per tile
     const int cid = blockIdx.x >> 1;
     const int nclusters = gridDim.x >> 1;
+    auto units = [&]() { return PairUnitIter(cid, nclusters, p.dp_tiles, num_tiles, p.tail_split); };
     unsigned int* status = &g_status;
 
     // Boxes each CTA loads for a tile: its A box unless all 128 rows are past
@@ -137,15 +172,23 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int t = cid; ok && t < num_tiles; t += nclusters) {
-                const TileCoord tc = tile_coord_bm(t, tiles_m, tiles_n, p.group_m, PM, BN);
+            PairUnitIter it = units();
+            PairUnit un;
+            while (ok && it.next(un)) {
+                const TileCoord tc = tile_coord_bm(un.tile, tiles_m, tiles_n, p.group_m, PM, BN);
                 const int my_a = a_live(tc.m0, rank);
-                const int my_b = b_live(tc.n0, rank);
+                // a whole tile: CTA r loads columns n0 + 128r (two boxes); a half
+                // tile h: CTA r loads the one box at n0 + 128h + 64r
+                const int bcol = un.half < 0 ? tc.n0 + 128 * static_cast<int>(rank) : tc.n0 + 128 * un.half + 64 * static_cast<int>(rank);
+                auto live = [&](int r) {
+                    return un.half < 0 ? b_live(tc.n0, r) : (tc.n0 + 128 * un.half + 64 * r < p.N ? 1 : 0);
+                };
+                const int my_b = live(rank);
                 // every sub-block's boxes are issued, also those starting past K
                 // (they arrive as zeros), so each stage carries the same bytes
                 const uint32_t pair_bytes = KSUB * (
                     static_cast<uint32_t>(a_live(tc.m0, 0) + a_live(tc.m0, 1)) * kATileBytes +
-                    static_cast<uint32_t>(b_live(tc.n0, 0) + b_live(tc.n0, 1)) * kBBoxBytes);
+                    static_cast<uint32_t>(live(0) + live(1)) * kBBoxBytes);
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_cluster_bounded(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, status,
                                                    ROLE_PRODUCER, BAR_EMPTY)) { ok = false; break; }
@@ -158,7 +201,7 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                                              tc.m0 + 128 * rank);
                         for (int c = 0; c < my_b; ++c)
                             tma_load_2d_pair(sB + stage * SP::kBStage + ks * kBHalfSubBytes + c * kBBoxBytes, &tmB,
-                                             full_leader, tc.n0 + 128 * rank + 64 * c, k0);
+                                             full_leader, bcol + 64 * c, k0);
                     }
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -184,11 +227,14 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int t = cid; ok && t < num_tiles; t += nclusters) {
+            PairUnitIter it = units();
+            PairUnit un;
+            while (ok && it.next(un)) {
                 if (!mbar_wait_cluster_bounded(acce_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag, status,
                                                ROLE_MMA, BAR_ACC_EMPTY)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                const uint32_t idesc = un.half < 0 ? kIdesc : kIdescHalf;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_cluster_bounded(full_bar(stage), phase, p.timeout_ns, abort_flag, status,
                                                    ROLE_MMA, BAR_FULL)) { ok = false; break; }
@@ -203,7 +249,7 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                             // CTA's 128 columns (two 64-column boxes, LBO 8 KiB)
                             const uint64_t adesc = smem_desc_sw128(a0 + k * 32, 0, 1024);
                             const uint64_t bdesc = smem_desc_sw128(b0 + k * 2048, kBBoxBytes, 1024);
-                            tc_mma_f16_pair(d_tmem, adesc, bdesc, kIdesc, (kb | ks | k) != 0 ? 1u : 0u);
+                            tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | ks | k) != 0 ? 1u : 0u);
                         }
                     }
                     tc_commit_pair_mc(empty_bar(stage), 0x3);
@@ -224,19 +270,26 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         uint32_t acc_phase = 0;
         const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
         const uint32_t acce_leader1 = mapa_shared(acce_bar(1), 0);
-        for (int t = cid; t < num_tiles; t += nclusters) {
-            const TileCoord tc = tile_coord_bm(t, tiles_m, tiles_n, p.group_m, PM, BN);
-            const int half = (warp - 2) >> 2;   // which half of the tile's columns
+        PairUnitIter it = units();
+        PairUnit un;
+        while (it.next(un)) {
+            const TileCoord tc = tile_coord_bm(un.tile, tiles_m, tiles_n, p.group_m, PM, BN);
+            const int half = (warp - 2) >> 2;   // which half of the unit's columns this warp takes
+            const int ucols = un.half < 0 ? BN : BN / 2;                       // the unit's width
+            const int un0 = un.half < 0 ? tc.n0 : tc.n0 + (BN / 2) * un.half;  // its first column
             uint32_t* stage = reinterpret_cast<uint32_t*>(base + SP::kStage + (warp - 2) * kStageWarpBytes);
-            if (p.epi != EPI_NONE) stage_bias(p, stage + kStageBlockWords, tc.n0 + half * (BN / 2), BN / 2);
+            if (p.epi != EPI_NONE) stage_bias(p, stage + kStageBlockWords, un0 + half * (ucols / 2), ucols / 2);
             const bool ready = mbar_wait_cluster_bounded(accf_bar(acc), acc_phase, p.timeout_ns, abort_flag, status,
                                                          ROLE_EPILOGUE, BAR_ACC_FULL);
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
-            const uint32_t t_base = tmem_base + static_cast<uint32_t>(acc * BN + half * (BN / 2)) +
+            const uint32_t t_base = tmem_base + static_cast<uint32_t>(acc * BN + half * (ucols / 2)) +
                                     (static_cast<uint32_t>(32 * q) << 16);
-            epilogue_rows<BN / 2>(p, t_base, tc.m0 + 128 * static_cast<int>(rank) + 32 * q, tc.n0 + half * (BN / 2),
-                                  stage);
+            const int row0 = tc.m0 + 128 * static_cast<int>(rank) + 32 * q;
+            if (un.half < 0)
+                epilogue_rows<BN / 2>(p, t_base, row0, un0 + half * (BN / 2), stage);
+            else
+                epilogue_rows<BN / 4>(p, t_base, row0, un0 + half * (BN / 4), stage);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acc == 0 ? acce_leader0 : acce_leader1);

@@ -106,20 +106,23 @@ int gemm_f16_release_workspace(void);
  * 3 swap-AB kernel for M <= 64), tile_m (256 for the CTA-pair kernel),
  * tile_n,
  * pipeline stages, CTAs launched, repack A (0/1), repack B (0/1), vector
- * stores of C (0/1), split-K parts per tile, scratch bytes.  Returns a status
+ * stores of C (0/1), split-K parts per tile, scratch bytes, and for the CTA
+ * pair the number of whole tiles before the half-tile units (-1: no split).
+ * Returns a status
  * code like gemm_f16 (argument errors only).  Diagnostic; it has no
  * counterpart on the pages.
  */
 int gemm_f16_plan(const void* A, const void* B, const void* bias, const void* C,
                   int64_t M, int64_t N, int64_t K, int epilogue, int num_sms,
-                  int64_t plan[10]);
+                  int64_t plan[11]);
 
 /*
  * Diagnostic (no counterpart on the pages): pins the kernel configuration
  * that every later call in this process uses, for tests and tile sweeps.
  *   0 automatic (the default), 1 CTA pair with a 256 x 256 tile,
  *   2 single CTA 128 x 256, 3 single CTA 128 x 128, 4 single CTA 128 x 64,
- *   5 swap-AB (C^T = B^T A^T; tiles of 128 columns x 16, 32 or 64 rows).
+ *   5 swap-AB (C^T = B^T A^T; tiles of 128 columns x 16, 32 or 64 rows),
+ *   6 CTA pair with whole tiles only (no half-tile units for a partial last wave).
  * Returns the previous setting, or -1 (nothing changed) for an unknown
  * value.  Process-wide; set it while no other host thread is calling.
  */

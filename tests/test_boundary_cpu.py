@@ -72,8 +72,11 @@ def test_argument_errors_need_no_device(g, args, expect):
 
 def test_plan_large_square_uses_cta_pairs(g):
     p = g.gemm_f16_plan(8192, 8192, 8192, "bias_gelu_erf", num_sms=152)
+    # 1024 tiles on 76 pairs: 988 whole tiles, then the last 36 as 72 half tiles
     assert p == {"path": 2, "tile_m": 256, "tile_n": 256, "stages": 3, "ctas": 152,
-                 "pack_a": 0, "pack_b": 0, "vec_store": 1, "splits": 1, "scratch": 0}
+                 "pack_a": 0, "pack_b": 0, "vec_store": 1, "splits": 1, "scratch": 0, "whole_tiles": 988}
+    # an exact number of waves needs no half tiles
+    assert g.gemm_f16_plan(8192, 9728, 8192, "none", num_sms=152)["whole_tiles"] == -1
     p = g.gemm_f16_plan(4096, 4096, 4096, "bias_gelu_erf", num_sms=152)
     assert p["tile_m"] == 256 and p["ctas"] == 152
 
@@ -91,7 +94,8 @@ def test_force_config_overrides_and_restores(g):
         assert (p["tile_m"], p["tile_n"], p["stages"]) == (128, 256, 4)
         g.gemm_f16_force_config("pair256x256")
         p = g.gemm_f16_plan(200, 300, 64, "none", num_sms=152)
-        assert (p["tile_m"], p["tile_n"], p["ctas"]) == (256, 256, 4)
+        # 2 tiles, far fewer than pairs: run as 4 half tiles on 4 pairs
+        assert (p["tile_m"], p["tile_n"], p["ctas"], p["whole_tiles"]) == (256, 256, 8, 0)
     finally:
         g.gemm_f16_force_config(prev)
     with pytest.raises(ValueError):

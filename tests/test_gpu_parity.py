@@ -264,7 +264,7 @@ def test_bounded_wait_reports_timeout_and_context_survives(g, torch_dev, oracle_
 
 # ---------------------------------------------------------------- every kernel configuration
 
-CONFIGS = ["pair256x256", "128x256", "128x128", "128x64", "swap"]
+CONFIGS = ["pair256x256", "pair_whole", "128x256", "128x128", "128x64", "swap"]
 
 
 @pytest.fixture
@@ -397,3 +397,26 @@ def test_device_gelu_on_every_fp16_value_in_range(g, torch_dev, oracle_mod):
     # where |GELU| >= 2^-10 the fp16 spacing dwarfs the fp32 error: nearly all bit-equal
     big = np.abs(ref.astype(np.float64)) >= 2.0 ** -10
     assert (dist[big] == 0).mean() >= 0.995
+
+
+
+# ---------------------------------------------------------------- CTA pair: half-tile units for a partial last wave
+
+@pytest.mark.parametrize("M,N,K", [(2560, 2560, 1920), (2304, 2816, 1536), (4096, 4096, 640), (300, 4003, 200)])
+def test_pair_half_tile_tail_integer_exact(forced, torch_dev, oracle_mod, M, N, K):
+    g = forced
+    g.gemm_f16_force_config("pair256x256")
+    assert g.gemm_f16_plan(M, N, K, "bias")["whole_tiles"] >= 0
+    rng = np.random.default_rng(M + N + K)
+    A = rng.integers(-1, 2, (M, K)).astype(np.float16)   # |C| <= K + 4 <= 1924: exact in fp32 and fp16
+    B = rng.integers(-1, 2, (K, N)).astype(np.float16)
+    bias = rng.integers(-4, 5, N).astype(np.float16)
+    assert np.array_equal(run(g, torch_dev, A, B, bias, "bias"), oracle_mod.gemm(A, B, bias, "bias"))
+
+
+def test_pair_half_tile_tail_gelu(g, torch_dev, oracle_mod):
+    M, N, K = 2816, 2560, 1280
+    assert g.gemm_f16_plan(M, N, K, "bias_gelu_erf")["whole_tiles"] > 0
+    rng = np.random.default_rng(33)
+    A, B, bias = rand16(rng, (M, K), 0.05), rand16(rng, (K, N), 0.05), rand16(rng, N)
+    assert_parity(run(g, torch_dev, A, B, bias, "bias_gelu_erf"), oracle_mod.gemm(A, B, bias, "bias_gelu_erf"))
