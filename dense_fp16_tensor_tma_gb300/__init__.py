@@ -15,8 +15,10 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libgemm_f16.so")
 
 GEMM_EPI_NONE, GEMM_EPI_BIAS, GEMM_EPI_BIAS_RELU, GEMM_EPI_BIAS_GELU_ERF = 0, 1, 2, 3
+GEMM_EPI_BIAS_SIGMOID, GEMM_EPI_BIAS_GELU_TANH = 4, 5
 EPILOGUES = {"none": GEMM_EPI_NONE, "bias": GEMM_EPI_BIAS, "bias_relu": GEMM_EPI_BIAS_RELU,
-             "bias_gelu_erf": GEMM_EPI_BIAS_GELU_ERF}
+             "bias_gelu_erf": GEMM_EPI_BIAS_GELU_ERF, "bias_sigmoid": GEMM_EPI_BIAS_SIGMOID,
+             "bias_gelu_tanh": GEMM_EPI_BIAS_GELU_TANH}
 GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED_DEVICE, GEMM_ERR_MISALIGNED = 0, 1, 2, 3
 GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT, GEMM_ERR_NO_MEMORY, GEMM_ERR_SCRATCH_LIMIT = 4, 5, 6, 7
 

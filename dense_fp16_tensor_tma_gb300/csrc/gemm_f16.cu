@@ -101,7 +101,7 @@ int check_args(const void* A, const void* B, const void* bias, const void* C, in
                int epilogue) {
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return GEMM_ERR_INVALID_ARG;
-    if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_BIAS_GELU_ERF) return GEMM_ERR_INVALID_ARG;
+    if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_BIAS_GELU_TANH) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM_OK;
     if (C == nullptr) return GEMM_ERR_INVALID_ARG;
     if (K > 0 && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_ARG;

@@ -28,7 +28,8 @@
 
 namespace gemm_f16_dev {
 
-enum : int { EPI_NONE = 0, EPI_BIAS = 1, EPI_BIAS_RELU = 2, EPI_BIAS_GELU_ERF = 3 };
+enum : int { EPI_NONE = 0, EPI_BIAS = 1, EPI_BIAS_RELU = 2, EPI_BIAS_GELU_ERF = 3, EPI_BIAS_SIGMOID = 4,
+             EPI_BIAS_GELU_TANH = 5 };
 
 __device__ unsigned int g_status;  // bounded-wait status word, read by the host
 
@@ -103,10 +104,28 @@ __device__ __forceinline__ float gelu_erf(float x) {
     return fmaf(hx, copysignf(e, x), hx);
 }
 
+// 1 / (1 + e^-x): e^-x overflows to +inf for x < -88, giving 0.
+__device__ __forceinline__ float sigmoid_f(float x) {
+    return __fdividef(1.0f, 1.0f + __expf(-x));
+}
+
+// GELU, tanh form: 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3),
+// with 1 + tanh(u) = 2 - 2 / (1 + e^(2u)) (absolute error ~1e-7; exact
+// saturation: e^(2u) = inf gives 2, e^(2u) = 0 gives 0).
+__device__ __forceinline__ float gelu_tanh_f(float x) {
+    const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
+    const float one_plus_t = 2.0f - __fdividef(2.0f, 1.0f + __expf(2.0f * u));
+    return 0.5f * x * one_plus_t;
+}
+
 __device__ __forceinline__ float apply_act(float x, int epi) {
-    if (epi == EPI_BIAS_RELU) return fmaxf(x, 0.0f);
-    if (epi == EPI_BIAS_GELU_ERF) return gelu_erf(x);
-    return x;
+    switch (epi) {
+        case EPI_BIAS_RELU: return fmaxf(x, 0.0f);
+        case EPI_BIAS_GELU_ERF: return gelu_erf(x);
+        case EPI_BIAS_SIGMOID: return sigmoid_f(x);
+        case EPI_BIAS_GELU_TANH: return gelu_tanh_f(x);
+        default: return x;
+    }
 }
 
 struct GemmParams {

@@ -14,7 +14,8 @@
  * Numerics: A and B are fp16; products are accumulated in fp32 in tensor
  * memory; bias is added and the activation applied in fp32; C is rounded
  * once to fp16 (round to nearest even).  GELU is the exact form
- * 0.5 x (1 + erf(x / sqrt 2)).
+ * 0.5 x (1 + erf(x / sqrt 2)); its tanh approximation and the sigmoid (the
+ * checklist's other "GEMM + fusion" activation) are also offered.
  *
  * Layout: all matrices are dense row-major (lda = K, ldb = N, ldc = N),
  * element type IEEE binary16 passed as raw pointers.  bias is a length-N
@@ -46,7 +47,9 @@ typedef enum {
     GEMM_EPI_NONE = 0,          /* C = acc                              */
     GEMM_EPI_BIAS = 1,          /* C = acc + bias                       */
     GEMM_EPI_BIAS_RELU = 2,     /* C = max(acc + bias, 0)               */
-    GEMM_EPI_BIAS_GELU_ERF = 3  /* C = 0.5 x (1 + erf(x/sqrt2)), x = acc + bias */
+    GEMM_EPI_BIAS_GELU_ERF = 3, /* C = 0.5 x (1 + erf(x/sqrt2)), x = acc + bias */
+    GEMM_EPI_BIAS_SIGMOID = 4,  /* C = 1 / (1 + exp(-x))                 */
+    GEMM_EPI_BIAS_GELU_TANH = 5 /* C = 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) */
 } gemm_epilogue_t;
 
 typedef enum {

@@ -24,9 +24,10 @@ import subprocess
 
 import numpy as np
 
-EPI_NONE, EPI_BIAS, EPI_BIAS_RELU, EPI_BIAS_GELU_ERF = 0, 1, 2, 3
+EPI_NONE, EPI_BIAS, EPI_BIAS_RELU, EPI_BIAS_GELU_ERF, EPI_BIAS_SIGMOID, EPI_BIAS_GELU_TANH = 0, 1, 2, 3, 4, 5
 EPILOGUES = {"none": EPI_NONE, "bias": EPI_BIAS, "bias_relu": EPI_BIAS_RELU,
-             "bias_gelu_erf": EPI_BIAS_GELU_ERF}
+             "bias_gelu_erf": EPI_BIAS_GELU_ERF, "bias_sigmoid": EPI_BIAS_SIGMOID,
+             "bias_gelu_tanh": EPI_BIAS_GELU_TANH}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_oracle.cpp")

@@ -11,6 +11,8 @@
 //   y   = x                    epilogue none / bias
 //         max(x, 0)            epilogue bias_relu
 //         0.5 x (1 + erf(x/sqrt 2))   epilogue bias_gelu_erf
+//         1 / (1 + exp(-x))    epilogue bias_sigmoid
+//         0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))   epilogue bias_gelu_tanh
 //   C[i,j] = fp16 round-to-nearest-even of y, straight from double.
 //
 // Sources, by page and section:
@@ -19,7 +21,8 @@
 //     accumulator is float; the PyTorch reference of the Step-by-Step
 //     Workflow is the plain product A @ B.
 //   * same page, Pre-flight Checklist pattern table: "GEMM + fusion" is a
-//     ReLU (or sigmoid) epilogue after the GEMM.
+//     ReLU (or sigmoid) epilogue after the GEMM.  The tanh form of GELU is
+//     the common approximation of the exact one (the pages name GELU only).
 //   * "TileLang: Write, Autotune, and Ship Fused Tensor-Core Kernels from
 //     Python", What you'll see and Why tile-level control matters: the fused
 //     epilogue adds a bias and applies GELU while the accumulator is on chip,
@@ -47,7 +50,8 @@
 
 namespace {
 
-enum { EPI_NONE = 0, EPI_BIAS = 1, EPI_BIAS_RELU = 2, EPI_BIAS_GELU_ERF = 3 };
+enum { EPI_NONE = 0, EPI_BIAS = 1, EPI_BIAS_RELU = 2, EPI_BIAS_GELU_ERF = 3, EPI_BIAS_SIGMOID = 4,
+       EPI_BIAS_GELU_TANH = 5 };
 
 double half_bits_to_double(uint16_t h) {
     const int sign = (h >> 15) & 1;
@@ -102,6 +106,11 @@ double apply_epilogue(double x, int epi) {
             if (std::isnan(x)) return x;
             return x > 0.0 ? x : 0.0;
         case EPI_BIAS_GELU_ERF: return 0.5 * x * (1.0 + std::erf(x / std::sqrt(2.0)));
+        case EPI_BIAS_SIGMOID: return 1.0 / (1.0 + std::exp(-x));
+        case EPI_BIAS_GELU_TANH: {
+            const double u = std::sqrt(2.0 / M_PI) * (x + 0.044715 * x * x * x);
+            return 0.5 * x * (1.0 + std::tanh(u));
+        }
         default: return x;
     }
 }
@@ -130,7 +139,7 @@ int resolve_threads(int nthreads) {
 bool bad_args(const uint16_t* A, const uint16_t* B, const uint16_t* bias,
               int64_t M, int64_t N, int64_t K, int epi) {
     if (M < 0 || N < 0 || K < 0) return true;
-    if (epi < EPI_NONE || epi > EPI_BIAS_GELU_ERF) return true;
+    if (epi < EPI_NONE || epi > EPI_BIAS_GELU_TANH) return true;
     if (epi != EPI_NONE && bias == nullptr) return true;
     if (K > 0 && M > 0 && A == nullptr) return true;
     if (K > 0 && N > 0 && B == nullptr) return true;

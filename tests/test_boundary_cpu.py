@@ -50,7 +50,7 @@ GOOD = 0x10000  # a 16-byte aligned fake device address: never dereferenced on t
     ((GOOD, GOOD, GOOD, GOOD, -1, 8, 8, 0), 1),          # negative M
     ((GOOD, GOOD, GOOD, GOOD, 8, -2, 8, 0), 1),          # negative N
     ((GOOD, GOOD, GOOD, GOOD, 8, 8, -3, 0), 1),          # negative K
-    ((GOOD, GOOD, GOOD, GOOD, 8, 8, 8, 4), 1),           # unknown epilogue
+    ((GOOD, GOOD, GOOD, GOOD, 8, 8, 8, 6), 1),           # unknown epilogue
     ((GOOD, GOOD, GOOD, GOOD, 8, 8, 8, -1), 1),
     ((GOOD, GOOD, GOOD, 0, 8, 8, 8, 0), 1),              # C null
     ((0, GOOD, GOOD, GOOD, 8, 8, 8, 0), 1),              # A null with K > 0

@@ -13,7 +13,7 @@ from oracle.compare import parity
 
 pytestmark = pytest.mark.gpu
 
-EPIS = ("none", "bias", "bias_relu", "bias_gelu_erf")
+EPIS = ("none", "bias", "bias_relu", "bias_gelu_erf", "bias_sigmoid", "bias_gelu_tanh")
 
 
 @pytest.fixture(scope="module")
@@ -140,7 +140,7 @@ SHAPES = [(1, 1, 1), (1, 15, 8), (15, 16, 16), (16, 17, 63), (17, 127, 64), (127
 def test_shape_sweep(g, torch_dev, oracle_mod, M, N, K):
     rng = np.random.default_rng(M * 1009 + N * 17 + K)
     A, B, bias = rand16(rng, (M, K), 0.5), rand16(rng, (K, N), 0.5), rand16(rng, N)
-    epi = EPIS[(M + N + K) % 4]
+    epi = EPIS[(M + N + K) % len(EPIS)]
     got = run(g, torch_dev, A, B, bias, epi)
     assert_parity(got, oracle_mod.gemm(A, B, bias if epi != "none" else None, epi), f"{M}x{N}x{K} {epi}")
 
@@ -367,12 +367,14 @@ def test_short_a_split_k_random_and_deterministic(g, torch_dev, oracle_mod, epi)
 
 # ---------------------------------------------------------------- the device GELU itself
 
-def test_device_gelu_on_every_fp16_value_in_range(g, torch_dev, oracle_mod):
+@pytest.mark.parametrize("epi", ["bias_gelu_erf", "bias_gelu_tanh", "bias_sigmoid"])
+def test_device_activation_on_every_fp16_value_in_range(g, torch_dev, oracle_mod, epi):
     # C[i, j] = x_i exactly (x_i * 1 + zeros), so the epilogue sees every fp16 value in
-    # [-10, 10].  The device erf (Abramowitz & Stegun 7.1.26, |error| <= 1.5e-7) in fp32:
-    # each result within 1 fp16 ulp of the fp64 definition, or within 3e-7 max(1, |x|)
-    # absolute (the far negative tail, where GELU is a tiny subnormal and any fp32 form of
-    # 1 + erf loses relative accuracy); almost all bit-equal.
+    # [-10, 10].  The device activations in fp32 (erf by Abramowitz & Stegun 7.1.26,
+    # |error| <= 1.5e-7; tanh and the sigmoid through the fast exponential): each result
+    # within 1 fp16 ulp of the fp64 definition, or within 3e-7 max(1, |x|) absolute (the
+    # far negative GELU tail, where the value is a tiny subnormal and any fp32 form of
+    # 1 + erf or 1 + tanh loses relative accuracy); almost all bit-equal.
     bits = np.arange(1 << 16, dtype=np.uint16)
     xs = bits.view(np.float16)
     xs = xs[np.isfinite(xs)]
@@ -383,8 +385,8 @@ def test_device_gelu_on_every_fp16_value_in_range(g, torch_dev, oracle_mod):
     B = np.zeros((K, N), np.float16)
     B[0, :] = 1.0
     bias = np.zeros(N, np.float16)
-    got = run(g, torch_dev, A, B, bias, "bias_gelu_erf")[:, 0]
-    ref = oracle_mod.gemm(A, B, bias, "bias_gelu_erf")[:, 0]
+    got = run(g, torch_dev, A, B, bias, epi)[:, 0]
+    ref = oracle_mod.gemm(A, B, bias, epi)[:, 0]
     gb = got.view(np.uint16).astype(np.int64)
     rb = ref.view(np.uint16).astype(np.int64)
     # ulp distance on the sign-magnitude fp16 encoding

@@ -157,6 +157,29 @@ def test_relu_and_identity_epilogues(oracle_mod):
     assert math.isnan(oracle_mod.epilogue_scalar(float("nan"), "bias_relu"))
 
 
+def test_sigmoid_closed_forms(oracle_mod):
+    sg = lambda v: oracle_mod.epilogue_scalar(v, "bias_sigmoid")
+    assert sg(0.0) == 0.5
+    assert sg(math.log(3.0)) == pytest.approx(0.75, abs=1e-15)       # 1 / (1 + 1/3)
+    assert sg(-math.log(4.0)) == pytest.approx(0.2, abs=1e-15)       # 1 / (1 + 4)
+    for x in np.linspace(-20, 20, 81):
+        assert sg(x) + sg(-x) == pytest.approx(1.0, abs=1e-15)
+    assert sg(-800.0) == 0.0 and sg(800.0) == 1.0
+
+
+def test_gelu_tanh_against_exact_gelu(oracle_mod):
+    # the tanh form approximates x Phi(x) to a few 1e-4 everywhere; a dropped cubic
+    # term or a wrong scale is off by > 1e-2 near |x| = 2
+    gt = lambda v: oracle_mod.epilogue_scalar(v, "bias_gelu_tanh")
+    ge = lambda v: oracle_mod.epilogue_scalar(v, "bias_gelu_erf")
+    assert gt(0.0) == 0.0
+    xs = np.linspace(-8, 8, 321)
+    assert max(abs(gt(x) - ge(x)) for x in xs) < 1e-3
+    for x in xs:
+        assert gt(x) - gt(-x) == pytest.approx(x, abs=1e-13)     # tanh odd
+    assert abs(gt(8.0) - 8.0) < 1e-12 and abs(gt(-8.0)) < 1e-12
+
+
 # ---------------------------------------------------------------- GEMM closed forms
 
 def _rand16(rng, shape, scale=1.0):
@@ -248,18 +271,22 @@ def _brute(A, B, bias, epi):
                 x = max(x, 0.0)
             elif epi == "bias_gelu_erf":
                 x = 0.5 * x * (1.0 + math.erf(x / math.sqrt(2.0)))
+            elif epi == "bias_sigmoid":
+                x = 1.0 / (1.0 + math.exp(-x))
+            elif epi == "bias_gelu_tanh":
+                x = 0.5 * x * (1.0 + math.tanh(math.sqrt(2.0 / math.pi) * (x + 0.044715 * x ** 3)))
             out[i, j] = x
     return out.astype(np.float16)
 
 
 def test_brute_force_tiny(oracle_mod):
     rng = np.random.default_rng(8)
-    epis = ["none", "bias", "bias_relu", "bias_gelu_erf"]
+    epis = ["none", "bias", "bias_relu", "bias_gelu_erf", "bias_sigmoid", "bias_gelu_tanh"]
     n = 0
     for M in (1, 2, 3, 5, 8):
         for N in (1, 2, 4, 7):
             for K in (1, 3, 6, 8):
-                epi = epis[n % 4]
+                epi = epis[n % len(epis)]
                 n += 1
                 A, B, bias = _rand16(rng, (M, K)), _rand16(rng, (K, N)), _rand16(rng, N)
                 b = None if epi == "none" else bias
