@@ -6,7 +6,11 @@ tensor memory, fused bias + erf-GELU epilogue, one fp16 write of C) on
 seeded synthetic inputs already resident in HBM.  Prints ONE JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--no-cpu-baseline]
+                  [--workload NAME] [--layout nn|nt|tn|tt] [--no-cpu-baseline]
+
+--layout stores A (first letter) and/or B (second) transposed in HBM, e.g.
+"nt" = B held as N x K like a Linear layer's weight; the call is then
+gemm_f16_ex with the matching flags.  The default "nn" is plain row-major.
 
 --impl reference times the CPU oracle (fp64, all host cores) on bounded row
 samples of the same workload: the comparison arm.  N > 1 runs independent
@@ -56,11 +60,15 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def workload_config(w, epi):
+LAYOUT_TEXT = {"nn": "row-major A [M,K] and B [K,N]", "nt": "row-major A [M,K], B stored transposed [N,K]",
+               "tn": "A stored transposed [K,M], row-major B [K,N]", "tt": "A stored [K,M] and B stored [N,K]"}
+
+
+def workload_config(w, epi, layout="nn"):
     return {
-        "workload": f"{w.name}: M={w.M} N={w.N} K={w.K} epilogue={epi}, fp16 row-major A,B "
+        "workload": f"{w.name}: M={w.M} N={w.N} K={w.K} epilogue={epi}, fp16 {LAYOUT_TEXT[layout]} "
                     f"~{w.ab_dist}*{w.ab_scale}, bias ~{w.bias_dist}, seed {w.seed}",
-        "M": w.M, "N": w.N, "K": w.K, "epilogue": epi, "seed": w.seed,
+        "M": w.M, "N": w.N, "K": w.K, "epilogue": epi, "seed": w.seed, "layout": layout,
         "accumulate": "f32", "flops_per_step": w.flops(), "alg_bytes_per_step": w.alg_bytes(),
         "l2": ("inputs larger than L2 (no flush)" if w.alg_bytes() > L2_BYTES
                else "L2 flushed between steps (256 MiB write)"),
@@ -249,7 +257,7 @@ def run_reference(args, w, epi):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(w, epi),
+        "data": "synthetic", "config": workload_config(w, epi, args.layout),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -275,8 +283,13 @@ def run_ours(args, w, epi):
     A, B, bias = wr.make()
     log(f"[rank {rank}] inputs generated in {time.perf_counter() - t_gen:.1f}s")
     b_np = bias if epi != "none" else None
-    tA = torch.from_numpy(A).to(dev)
-    tB = torch.from_numpy(B).to(dev)
+    ta, tbt = args.layout[0] == "t", args.layout[1] == "t"
+    # the operands as stored in HBM (the same logical matrices)
+    A_st = np.ascontiguousarray(A.T) if ta else A
+    B_st = np.ascontiguousarray(B.T) if tbt else B
+    lda, ldb, flags = A_st.shape[1], B_st.shape[1], (1 if ta else 0) | (2 if tbt else 0)
+    tA = torch.from_numpy(A_st).to(dev)
+    tB = torch.from_numpy(B_st).to(dev)
     tb = torch.from_numpy(b_np).to(dev) if b_np is not None else None
     C = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
     stream = torch.cuda.Stream(device=dev)
@@ -286,7 +299,8 @@ def run_ours(args, w, epi):
         flush = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
     plan = g.gemm_f16_plan(w.M, w.N, w.K, epi, num_sms=props.multi_processor_count,
                            a_addr=tA.data_ptr(), b_addr=tB.data_ptr(), c_addr=C.data_ptr(),
-                           bias_addr=tb.data_ptr() if tb is not None else 0)
+                           bias_addr=tb.data_ptr() if tb is not None else 0, lda=lda, ldb=ldb,
+                           trans_a=ta, trans_b=tbt)
     launches_per_step = 1 + plan["pack_a"] + plan["pack_b"]
 
     def flush_l2():
@@ -294,8 +308,8 @@ def run_ours(args, w, epi):
             flush.fill_(1.0)
 
     def step():
-        st = g.gemm_f16_ptr(tA.data_ptr(), tB.data_ptr(), tb.data_ptr() if tb is not None else 0,
-                            C.data_ptr(), w.M, w.N, w.K, epi, sh)
+        st = g.gemm_f16_ex_ptr(tA.data_ptr(), lda, tB.data_ptr(), ldb, tb.data_ptr() if tb is not None else 0,
+                               C.data_ptr(), w.N, w.M, w.N, w.K, epi, flags, sh)
         if st != 0:
             raise g.GemmError(st)
 
@@ -344,11 +358,11 @@ def run_ours(args, w, epi):
     avg_launch_ms = statistics.mean(per_launch_ms)
     achieved = flops / (avg_launch_ms * 1e-3) / 1e12
     peak, peak_src, _ = read_peaks()
-    traffic = committed_traffic(w.name)
+    traffic = committed_traffic(w.name if args.layout == "nn" else f"{w.name}:{args.layout}")
 
     # ---- end to end: pinned host buffers through the C ABI, copies inside the timed region
-    hA = torch.from_numpy(A).pin_memory()
-    hB = torch.from_numpy(B).pin_memory()
+    hA = torch.from_numpy(A_st).pin_memory()
+    hB = torch.from_numpy(B_st).pin_memory()
     hb = torch.from_numpy(b_np).pin_memory() if b_np is not None else None
     hC = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
     h2d = hA.numel() * 2 + hB.numel() * 2 + (hb.numel() * 2 if hb is not None else 0)
@@ -393,7 +407,8 @@ def run_ours(args, w, epi):
             "warmup": max(3, args.warmup), "ms_per_step": elapsed_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic",
-            "config": {**workload_config(w, epi), "parallelism": f"replicas{world}" if world > 1 else "single"},
+            "config": {**workload_config(w, epi, args.layout),
+                       "parallelism": f"replicas{world}" if world > 1 else "single"},
             "pct_of_peak": 100.0 * achieved / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic,
@@ -423,6 +438,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--epilogue", default=None)
+    ap.add_argument("--layout", default="nn", choices=sorted(LAYOUT_TEXT))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()

@@ -22,9 +22,11 @@ EPILOGUES = {"none": GEMM_EPI_NONE, "bias": GEMM_EPI_BIAS, "bias_relu": GEMM_EPI
 GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED_DEVICE, GEMM_ERR_MISALIGNED = 0, 1, 2, 3
 GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT, GEMM_ERR_NO_MEMORY, GEMM_ERR_SCRATCH_LIMIT = 4, 5, 6, 7
 
-EXPORTS = ("gemm_f16", "gemm_f16_status_string", "gemm_f16_last_cuda_error", "gemm_f16_debug_status",
-           "gemm_f16_release_workspace", "gemm_f16_plan", "gemm_f16_selftest_timeout", "gemm_f16_noalloc",
-           "gemm_f16_force_config")
+GEMM_F16_TRANS_A, GEMM_F16_TRANS_B = 1, 2
+
+EXPORTS = ("gemm_f16", "gemm_f16_ex", "gemm_f16_status_string", "gemm_f16_last_cuda_error",
+           "gemm_f16_debug_status", "gemm_f16_release_workspace", "gemm_f16_plan", "gemm_f16_plan_ex",
+           "gemm_f16_selftest_timeout", "gemm_f16_noalloc", "gemm_f16_force_config")
 CONFIGS = {"auto": 0, "pair256x256": 1, "128x256": 2, "128x128": 3, "128x64": 4, "swap": 5, "pair_whole": 6}
 
 if not os.path.exists(LIB_PATH):
@@ -35,6 +37,8 @@ lib = ctypes.CDLL(LIB_PATH)
 _vp, _i64, _int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 lib.gemm_f16.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
 lib.gemm_f16.restype = _int
+lib.gemm_f16_ex.argtypes = [_vp, _i64, _vp, _i64, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, _vp]
+lib.gemm_f16_ex.restype = _int
 lib.gemm_f16_status_string.argtypes = [_int]
 lib.gemm_f16_status_string.restype = ctypes.c_char_p
 lib.gemm_f16_last_cuda_error.restype = _int
@@ -43,6 +47,9 @@ lib.gemm_f16_debug_status.restype = _int
 lib.gemm_f16_release_workspace.restype = _int
 lib.gemm_f16_plan.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, ctypes.POINTER(ctypes.c_int64)]
 lib.gemm_f16_plan.restype = _int
+lib.gemm_f16_plan_ex.argtypes = [_vp, _i64, _vp, _i64, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, _int,
+                                 ctypes.POINTER(ctypes.c_int64)]
+lib.gemm_f16_plan_ex.restype = _int
 lib.gemm_f16_selftest_timeout.argtypes = [_vp, ctypes.c_uint32]
 lib.gemm_f16_selftest_timeout.restype = _int
 lib.gemm_f16_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
@@ -82,13 +89,44 @@ def gemm_f16_ptr(a_ptr: int, b_ptr: int, bias_ptr: int, c_ptr: int, M: int, N: i
                         int(M), int(N), int(K), _epi(epilogue), stream or None)
 
 
+def gemm_f16_ex_ptr(a_ptr: int, lda: int, b_ptr: int, ldb: int, bias_ptr: int, c_ptr: int, ldc: int,
+                    M: int, N: int, K: int, epilogue=GEMM_EPI_NONE, flags: int = 0, stream: int = 0) -> int:
+    """Raw call of gemm_f16_ex (pitches in elements, GEMM_F16_TRANS_* flags); returns the status code."""
+    return lib.gemm_f16_ex(a_ptr or None, int(lda), b_ptr or None, int(ldb), bias_ptr or None, c_ptr or None,
+                           int(ldc), int(M), int(N), int(K), _epi(epilogue), int(flags), stream or None)
+
+
+def _operand_layout(t, name):
+    """(stored transposed, row pitch) of a 2-D view whose rows are contiguous
+    (strides (ld, 1)) or whose columns are (strides (1, ld): the transpose of a
+    row-major matrix, e.g. W.t() of a Linear weight W).  Size-1 dimensions
+    take any stride."""
+    rows, cols = t.shape
+    s0, s1 = t.stride()
+    if cols <= 1 or s1 == 1:
+        if rows <= 1:
+            return False, max(cols, 1)
+        if s0 >= max(cols, 1):
+            return False, s0
+    if rows <= 1 or s0 == 1:
+        if cols <= 1:
+            return True, max(rows, 1)
+        if s1 >= max(rows, 1):
+            return True, s1
+    raise ValueError(f"{name} (shape {tuple(t.shape)}, strides {t.stride()}) needs contiguous rows or "
+                     "contiguous columns with non-overlapping lines")
+
+
 def gemm_f16(A, B, bias, C, epilogue="none", stream=None):
     """C = epilogue(A @ B + bias) into the preallocated fp16 CUDA tensor C.
 
     A [M,K], B [K,N], C [M,N] and bias [N] (or None for "none") are
-    contiguous torch.float16 CUDA tensors on the current device.  Enqueued on
-    `stream` (default: torch's current stream); raises GemmError on a nonzero
-    status.
+    torch.float16 CUDA tensors on the current device.  A and B may be row
+    views with any pitch or transposed views (A = X.t(), B = W.t() for a
+    weight W [N,K]); they are passed to gemm_f16_ex as pitches and layout
+    flags, never copied here.  C needs contiguous rows (any pitch), bias is
+    contiguous.  Enqueued on `stream` (default: torch's current stream);
+    raises GemmError on a nonzero status.
     """
     import torch
     M, K = A.shape
@@ -96,24 +134,38 @@ def gemm_f16(A, B, bias, C, epilogue="none", stream=None):
     if K2 != K or tuple(C.shape) != (M, N):
         raise ValueError(f"shape mismatch: A {tuple(A.shape)}, B {tuple(B.shape)}, C {tuple(C.shape)}")
     for name, t in (("A", A), ("B", B), ("C", C)) + ((("bias", bias),) if bias is not None else ()):
-        if t.dtype != torch.float16 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous float16 CUDA tensor")
-    if bias is not None and tuple(bias.shape) != (N,):
-        raise ValueError(f"bias must have shape ({N},)")
-    st = lib.gemm_f16(A.data_ptr() or None, B.data_ptr() or None,
-                      bias.data_ptr() if bias is not None else None, C.data_ptr() or None,
-                      M, N, K, _epi(epilogue), _stream_handle(stream))
+        if t.dtype != torch.float16 or not t.is_cuda:
+            raise ValueError(f"{name} must be a float16 CUDA tensor")
+    if bias is not None and (tuple(bias.shape) != (N,) or not bias.is_contiguous()):
+        raise ValueError(f"bias must be a contiguous tensor of shape ({N},)")
+    ta, lda = _operand_layout(A, "A")
+    tb, ldb = _operand_layout(B, "B")
+    tc, ldc = _operand_layout(C, "C")
+    if tc and M > 1 and N > 1:
+        raise ValueError("C needs contiguous rows")
+    if tc:
+        ldc = N
+    flags = (GEMM_F16_TRANS_A if ta else 0) | (GEMM_F16_TRANS_B if tb else 0)
+    st = lib.gemm_f16_ex(A.data_ptr() or None, lda, B.data_ptr() or None, ldb,
+                         bias.data_ptr() if bias is not None else None, C.data_ptr() or None, ldc,
+                         M, N, K, _epi(epilogue), flags, _stream_handle(stream))
     if st != GEMM_OK:
         raise GemmError(st)
     return C
 
 
 def gemm_f16_plan(M, N, K, epilogue="none", num_sms=152, a_addr=256, b_addr=256, c_addr=256,
-                  bias_addr=256):
-    """Host-only: the plan gemm_f16 would pick (dict), without touching a device."""
+                  bias_addr=256, lda=None, ldb=None, ldc=None, trans_a=False, trans_b=False):
+    """Host-only: the plan gemm_f16 / gemm_f16_ex would pick (dict), without
+    touching a device.  Pitches default to the dense ones of the layout."""
     out = (ctypes.c_int64 * 11)()
-    st = lib.gemm_f16_plan(a_addr or None, b_addr or None, bias_addr or None, c_addr or None,
-                           int(M), int(N), int(K), _epi(epilogue), int(num_sms), out)
+    lda = lda if lda is not None else (M if trans_a else K)
+    ldb = ldb if ldb is not None else (K if trans_b else N)
+    ldc = ldc if ldc is not None else N
+    flags = (GEMM_F16_TRANS_A if trans_a else 0) | (GEMM_F16_TRANS_B if trans_b else 0)
+    st = lib.gemm_f16_plan_ex(a_addr or None, int(lda), b_addr or None, int(ldb), bias_addr or None,
+                              c_addr or None, int(ldc), int(M), int(N), int(K), _epi(epilogue), flags,
+                              int(num_sms), out)
     if st != GEMM_OK:
         raise GemmError(st, "gemm_f16_plan")
     keys = ("path", "tile_m", "tile_n", "stages", "ctas", "pack_a", "pack_b", "vec_store", "splits", "scratch",

@@ -97,25 +97,54 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
-int check_args(const void* A, const void* B, const void* bias, const void* C, int64_t M, int64_t N, int64_t K,
-               int epilogue) {
+// The operands of one call as stored: A is M x K with row pitch lda, or, with
+// trans_a, K x M (A^T row-major, pitch lda); B is K x N with pitch ldb, or,
+// with trans_b, N x K; C is M x N with pitch ldc.  Pitches in elements.
+struct Operands {
+    const void* A = nullptr;
+    const void* B = nullptr;
+    void* C = nullptr;
+    int64_t lda = 0, ldb = 0, ldc = 0;
+    bool ta = false, tb = false;
+    // stored rows x contiguous extent of each operand
+    int64_t a_rows(int64_t M, int64_t K) const { return ta ? K : M; }
+    int64_t a_cols(int64_t M, int64_t K) const { return ta ? M : K; }
+    int64_t b_rows(int64_t N, int64_t K) const { return tb ? N : K; }
+    int64_t b_cols(int64_t N, int64_t K) const { return tb ? K : N; }
+};
+
+Operands dense_operands(const void* A, const void* B, void* C, int64_t N, int64_t K) {
+    Operands op;
+    op.A = A;
+    op.B = B;
+    op.C = C;
+    op.lda = K;
+    op.ldb = N;
+    op.ldc = N;
+    return op;
+}
+
+int check_args(const Operands& op, const void* bias, int64_t M, int64_t N, int64_t K, int epilogue) {
+    constexpr int64_t kLim = int64_t(1) << 31;
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
-    if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return GEMM_ERR_INVALID_ARG;
+    if (M >= kLim || N >= kLim || K >= kLim) return GEMM_ERR_INVALID_ARG;
     if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_BIAS_GELU_TANH) return GEMM_ERR_INVALID_ARG;
+    if (op.lda >= kLim || op.ldb >= kLim || op.ldc >= kLim) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM_OK;
-    if (C == nullptr) return GEMM_ERR_INVALID_ARG;
-    if (K > 0 && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_ARG;
+    if (op.C == nullptr || op.ldc < N) return GEMM_ERR_INVALID_ARG;
+    if (K > 0 && (op.A == nullptr || op.B == nullptr)) return GEMM_ERR_INVALID_ARG;
+    if (K > 0 && (op.lda < op.a_cols(M, K) || op.ldb < op.b_cols(N, K))) return GEMM_ERR_INVALID_ARG;
     if (epilogue != GEMM_EPI_NONE && bias == nullptr) return GEMM_ERR_INVALID_ARG;
-    if (!aligned(C, 2) || (K > 0 && (!aligned(A, 2) || !aligned(B, 2))) ||
+    if (!aligned(op.C, 2) || (K > 0 && (!aligned(op.A, 2) || !aligned(op.B, 2))) ||
         (epilogue != GEMM_EPI_NONE && !aligned(bias, 2)))
         return GEMM_ERR_MISALIGNED;
     // every tile index of the smallest tile shape must fit an int
-    if (((M + 127) / 128) * ((N + 63) / 64) >= (int64_t(1) << 31)) return GEMM_ERR_INVALID_ARG;
+    if (((M + 127) / 128) * ((N + 63) / 64) >= kLim) return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
 }
 
-Plan make_plan(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K, int num_sms,
-               int pair_clusters, int force, bool allow_split = true) {
+Plan make_plan(const Operands& op, int64_t M, int64_t N, int64_t K, int num_sms, int pair_clusters, int force,
+               bool allow_split = true) {
     Plan pl;
     if (M == 0 || N == 0) return pl;
     if (K == 0) {
@@ -124,13 +153,15 @@ Plan make_plan(const void* A, const void* B, const void* C, int64_t M, int64_t N
         return pl;
     }
     pl.path = 2;
-    pl.pack_a = !(aligned(A, 16) && K % 8 == 0);
-    pl.pack_b = !(aligned(B, 16) && N % 8 == 0);
-    pl.lda_packed = pl.pack_a ? round_up(K, 8) : K;
-    pl.ldb_packed = pl.pack_b ? round_up(N, 8) : N;
-    pl.a_scratch = pl.pack_a ? align256(static_cast<size_t>(M * pl.lda_packed * 2)) : 0;
-    pl.b_scratch = pl.pack_b ? align256(static_cast<size_t>(K * pl.ldb_packed * 2)) : 0;
-    pl.vec_store = aligned(C, 16) && N % 8 == 0;
+    // TMA wants a 16-byte aligned base and a pitch of a multiple of 16 bytes;
+    // otherwise the operand is first copied, in its own layout, to scratch
+    pl.pack_a = !(aligned(op.A, 16) && op.lda % 8 == 0);
+    pl.pack_b = !(aligned(op.B, 16) && op.ldb % 8 == 0);
+    pl.lda_packed = pl.pack_a ? round_up(op.a_cols(M, K), 8) : op.lda;
+    pl.ldb_packed = pl.pack_b ? round_up(op.b_cols(N, K), 8) : op.ldb;
+    pl.a_scratch = pl.pack_a ? align256(static_cast<size_t>(op.a_rows(M, K) * pl.lda_packed * 2)) : 0;
+    pl.b_scratch = pl.pack_b ? align256(static_cast<size_t>(op.b_rows(N, K) * pl.ldb_packed * 2)) : 0;
+    pl.vec_store = aligned(op.C, 16) && op.ldc % 8 == 0;
     const int64_t tiles_m = (M + 127) / 128;
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     int cfg = force;
@@ -170,7 +201,8 @@ Plan make_plan(const void* A, const void* B, const void* C, int64_t M, int64_t N
         }
         case CFG_SWAP:
             pl.path = 3;
-            pl.tile_m = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+            // A stored K x M is one MN-major box of 64 rows (a 128-byte swizzle row)
+            pl.tile_m = (M <= 16 && !op.ta) ? 16 : ((M <= 32 && !op.ta) ? 32 : 64);
             pl.tile_n = 128;
             pl.stages = pl.tile_m == 16 ? kStagesSwap16 : (pl.tile_m == 32 ? kStagesSwap32 : kStagesSwap64);
             break;
@@ -368,18 +400,19 @@ int launch_tc_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParam
 // Everything after scratch is settled: repack (into `scratch`, which holds
 // pl.a_scratch + pl.b_scratch bytes when a repack is planned), tensor maps,
 // and the tensor-core kernel, all on stream `s`.
-int enqueue_plan(const Plan& pl, const void* A, const void* B, const __half* biasp, void* C, int64_t M, int64_t N,
-                 int64_t K, int epilogue, uint8_t* scratch, cudaStream_t s) {
+int enqueue_plan(const Plan& pl, const Operands& op, const __half* biasp, int64_t M, int64_t N, int64_t K,
+                 int epilogue, uint8_t* scratch, cudaStream_t s) {
     int st = GEMM_OK;
-    const void* a_src = A;
-    const void* b_src = B;
+    const void* a_src = op.A;
+    const void* b_src = op.B;
     if (pl.pack_a) {
-        st = launch_repack(reinterpret_cast<uint16_t*>(scratch), A, M, K, K, pl.lda_packed, s);
+        st = launch_repack(reinterpret_cast<uint16_t*>(scratch), op.A, op.a_rows(M, K), op.a_cols(M, K), op.lda,
+                           pl.lda_packed, s);
         a_src = scratch;
     }
     if (st == GEMM_OK && pl.pack_b) {
         uint16_t* bdst = reinterpret_cast<uint16_t*>(scratch + pl.a_scratch);
-        st = launch_repack(bdst, B, K, N, N, pl.ldb_packed, s);
+        st = launch_repack(bdst, op.B, op.b_rows(N, K), op.b_cols(N, K), op.ldb, pl.ldb_packed, s);
         b_src = bdst;
     }
     float* partials = nullptr;
@@ -391,17 +424,26 @@ int enqueue_plan(const Plan& pl, const void* A, const void* B, const __half* bia
         if (e != cudaSuccess) st = cuda_fail(e);
     }
     CUtensorMap ta, tb;
-    // A boxes are 64 K x 128 rows, or 64 K x MT rows for the swap-AB kernel
-    if (st == GEMM_OK) st = encode_2d(&ta, a_src, K, M, pl.lda_packed, kBK, pl.path == 3 ? pl.tile_m : kBM);
-    if (st == GEMM_OK) st = encode_2d(&tb, b_src, N, K, pl.ldb_packed, 64, kBK);
+    // A boxes: 64 K x 128 rows (64 K x MT rows for the swap-AB kernel), or,
+    // for A stored K x M, 64 rows x 64 K; B boxes: 64 x 64 in either layout
+    if (st == GEMM_OK) {
+        st = op.ta ? encode_2d(&ta, a_src, M, K, pl.lda_packed, 64, kBK)
+                   : encode_2d(&ta, a_src, K, M, pl.lda_packed, kBK, pl.path == 3 ? pl.tile_m : kBM);
+    }
+    if (st == GEMM_OK) {
+        st = op.tb ? encode_2d(&tb, b_src, K, N, pl.ldb_packed, kBK, 64)
+                   : encode_2d(&tb, b_src, N, K, pl.ldb_packed, 64, kBK);
+    }
     if (st != GEMM_OK) return st;
     GemmParams prm;
-    prm.C = static_cast<__half*>(C);
+    prm.C = static_cast<__half*>(op.C);
     prm.bias = biasp;
     prm.M = static_cast<int>(M);
     prm.N = static_cast<int>(N);
     prm.K = static_cast<int>(K);
-    prm.ldc = static_cast<int>(N);
+    prm.ldc = static_cast<int>(op.ldc);
+    prm.trans_a = op.ta ? 1 : 0;
+    prm.trans_b = op.tb ? 1 : 0;
     prm.epi = epilogue;
     prm.vec_store = pl.vec_store ? 1 : 0;
     prm.bias_vec = (biasp != nullptr && aligned(biasp, 16)) ? 1 : 0;
@@ -424,9 +466,9 @@ int enqueue_plan(const Plan& pl, const void* A, const void* B, const __half* bia
     }
 }
 
-int enqueue_bias_only(const Plan& pl, const __half* biasp, void* C, int64_t M, int64_t N, int epilogue,
+int enqueue_bias_only(const Plan& pl, const __half* biasp, void* C, int64_t ldc, int64_t M, int64_t N, int epilogue,
                       cudaStream_t s) {
-    gemm_f16_bias_only_kernel<<<pl.ctas, 256, 0, s>>>(static_cast<__half*>(C), biasp, M, N, N, epilogue);
+    gemm_f16_bias_only_kernel<<<pl.ctas, 256, 0, s>>>(static_cast<__half*>(C), biasp, M, N, ldc, epilogue);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
@@ -483,12 +525,23 @@ int gemm_f16_force_config(int config) {
     return g_force_config.exchange(config);
 }
 
-int gemm_f16_plan(const void* A, const void* B, const void* bias, const void* C, int64_t M, int64_t N, int64_t K,
-                  int epilogue, int num_sms, int64_t plan[11]) {
+int gemm_f16_plan_ex(const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias, const void* C,
+                     int64_t ldc, int64_t M, int64_t N, int64_t K, int epilogue, int flags, int num_sms,
+                     int64_t plan[11]) {
     if (plan == nullptr || num_sms <= 0) return GEMM_ERR_INVALID_ARG;
-    const int st = check_args(A, B, bias, C, M, N, K, epilogue);
+    if (flags & ~(GEMM_F16_TRANS_A | GEMM_F16_TRANS_B)) return GEMM_ERR_INVALID_ARG;
+    Operands op;
+    op.A = A;
+    op.B = B;
+    op.C = const_cast<void*>(C);
+    op.lda = lda;
+    op.ldb = ldb;
+    op.ldc = ldc;
+    op.ta = (flags & GEMM_F16_TRANS_A) != 0;
+    op.tb = (flags & GEMM_F16_TRANS_B) != 0;
+    const int st = check_args(op, bias, M, N, K, epilogue);
     if (st != GEMM_OK) return st;
-    const Plan pl = make_plan(A, B, C, M, N, K, num_sms, num_sms / 2, g_force_config.load());
+    const Plan pl = make_plan(op, M, N, K, num_sms, num_sms / 2, g_force_config.load());
     plan[0] = pl.path;
     plan[1] = pl.tile_m;
     plan[2] = pl.tile_n;
@@ -503,9 +556,24 @@ int gemm_f16_plan(const void* A, const void* B, const void* bias, const void* C,
     return GEMM_OK;
 }
 
-int gemm_f16(const void* A, const void* B, const void* bias, void* C, int64_t M, int64_t N, int64_t K, int epilogue,
-             void* cuda_stream) {
-    int st = check_args(A, B, bias, C, M, N, K, epilogue);
+int gemm_f16_plan(const void* A, const void* B, const void* bias, const void* C, int64_t M, int64_t N, int64_t K,
+                  int epilogue, int num_sms, int64_t plan[11]) {
+    return gemm_f16_plan_ex(A, K, B, N, bias, C, N, M, N, K, epilogue, 0, num_sms, plan);
+}
+
+int gemm_f16_ex(const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias, void* C, int64_t ldc,
+                int64_t M, int64_t N, int64_t K, int epilogue, int flags, void* cuda_stream) {
+    if (flags & ~(GEMM_F16_TRANS_A | GEMM_F16_TRANS_B)) return GEMM_ERR_INVALID_ARG;
+    Operands op;
+    op.A = A;
+    op.B = B;
+    op.C = C;
+    op.lda = lda;
+    op.ldb = ldb;
+    op.ldc = ldc;
+    op.ta = (flags & GEMM_F16_TRANS_A) != 0;
+    op.tb = (flags & GEMM_F16_TRANS_B) != 0;
+    int st = check_args(op, bias, M, N, K, epilogue);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
     int dev = 0;
@@ -515,9 +583,9 @@ int gemm_f16(const void* A, const void* B, const void* bias, void* C, int64_t M,
     if (st != GEMM_OK) return st;
     const DeviceState& ds = g_dev[dev];
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-    const Plan pl = make_plan(A, B, C, M, N, K, ds.num_sms, ds.pair_clusters, g_force_config.load());
+    const Plan pl = make_plan(op, M, N, K, ds.num_sms, ds.pair_clusters, g_force_config.load());
     const __half* biasp = epilogue == GEMM_EPI_NONE ? nullptr : static_cast<const __half*>(bias);
-    if (pl.path == 1) return enqueue_bias_only(pl, biasp, C, M, N, epilogue, s);
+    if (pl.path == 1) return enqueue_bias_only(pl, biasp, C, ldc, M, N, epilogue, s);
 
     void* scratch = nullptr;
     const size_t scratch_bytes = pl.scratch_bytes();
@@ -531,7 +599,7 @@ int gemm_f16(const void* A, const void* B, const void* bias, void* C, int64_t M,
             return GEMM_ERR_NO_MEMORY;
         }
     }
-    st = enqueue_plan(pl, A, B, biasp, C, M, N, K, epilogue, static_cast<uint8_t*>(scratch), s);
+    st = enqueue_plan(pl, op, biasp, M, N, K, epilogue, static_cast<uint8_t*>(scratch), s);
     if (scratch != nullptr) {
         e = cudaFreeAsync(scratch, s);   // stream-ordered: freed after the GEMM has read it
         if (e != cudaSuccess && st == GEMM_OK) st = cuda_fail(e);
@@ -539,9 +607,15 @@ int gemm_f16(const void* A, const void* B, const void* bias, void* C, int64_t M,
     return st;
 }
 
+int gemm_f16(const void* A, const void* B, const void* bias, void* C, int64_t M, int64_t N, int64_t K, int epilogue,
+             void* cuda_stream) {
+    return gemm_f16_ex(A, K, B, N, bias, C, N, M, N, K, epilogue, 0, cuda_stream);
+}
+
 int gemm_f16_noalloc(const void* A, const void* B, const void* bias, void* C, int64_t M, int64_t N, int64_t K,
                      int epilogue, void* cuda_stream) {
-    int st = check_args(A, B, bias, C, M, N, K, epilogue);
+    const Operands op = dense_operands(A, B, C, N, K);
+    int st = check_args(op, bias, M, N, K, epilogue);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
     int dev = 0;
@@ -551,17 +625,17 @@ int gemm_f16_noalloc(const void* A, const void* B, const void* bias, void* C, in
     if (st != GEMM_OK) return st;
     const DeviceState& ds = g_dev[dev];
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-    Plan pl = make_plan(A, B, C, M, N, K, ds.num_sms, ds.pair_clusters, g_force_config.load());
+    Plan pl = make_plan(op, M, N, K, ds.num_sms, ds.pair_clusters, g_force_config.load());
     const __half* biasp = epilogue == GEMM_EPI_NONE ? nullptr : static_cast<const __half*>(bias);
-    if (pl.path == 1) return enqueue_bias_only(pl, biasp, C, M, N, epilogue, s);
+    if (pl.path == 1) return enqueue_bias_only(pl, biasp, C, N, M, N, epilogue, s);
     // Same scratch layout as gemm_f16, inside the fixed buffer.  The repacks
     // need no zeroed memory (the tensor maps stop at the true extents); the
     // split-K counters are zeroed by a stream-ordered memset in enqueue_plan.
     // Without room for split-K partials the plan runs unsplit.
     if (pl.scratch_bytes() > kNoAllocScratchBytes)
-        pl = make_plan(A, B, C, M, N, K, ds.num_sms, ds.pair_clusters, g_force_config.load(), false);
+        pl = make_plan(op, M, N, K, ds.num_sms, ds.pair_clusters, g_force_config.load(), false);
     if (pl.scratch_bytes() > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
-    return enqueue_plan(pl, A, B, biasp, C, M, N, K, epilogue, ds.noalloc_scratch, s);
+    return enqueue_plan(pl, op, biasp, M, N, K, epilogue, ds.noalloc_scratch, s);
 }
 
 int gemm_f16_debug_status(void* cuda_stream, uint32_t* detail) {

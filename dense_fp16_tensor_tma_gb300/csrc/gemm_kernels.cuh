@@ -146,7 +146,30 @@ struct GemmParams {
     int splits;
     float* partials;          // [tile][split][MT][128] fp32 partial sums
     unsigned int* counters;   // [tile][4]: parts finished per 32-column slice (zero before the launch)
+    // operand layouts: trans_a = A stored K x M (M contiguous, MN-major);
+    // trans_b = B stored N x K (K contiguous, K-major)
+    int trans_a;
+    int trans_b;
 };
+
+// One 64 (M or N) x 64 (K) box of an operand tile.  The tensor map of a
+// K-major operand has K as its inner coordinate, that of an MN-major one M
+// (or N).  Either way the box is 8 KiB, and boxes placed 8 KiB apart extend
+// the tile along M (or N): for K-major that continues the run of 8-row
+// swizzle atoms, for MN-major it is the next 64-element atom column (LBO).
+__device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* tm, uint32_t bar, bool k_major,
+                                             int mn, int k) {
+    if (k_major) tma_load_2d(dst, tm, bar, k, mn);
+    else tma_load_2d(dst, tm, bar, mn, k);
+}
+
+// Shared-memory descriptor of the 16-deep K step `k` of an operand tile at
+// `base`.  K-major: 128-byte rows, 8-row atoms 1 KiB apart (SBO), the step
+// 32 bytes into the swizzled row.  MN-major: 64-element atom columns 8 KiB
+// apart (LBO), 8-deep K groups 1 KiB apart (SBO), the step 16 rows = 2 KiB.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int k, bool mn_major) {
+    return mn_major ? smem_desc_sw128(base + k * 2048, kBBoxBytes, 1024) : smem_desc_sw128(base + k * 32, 0, 1024);
+}
 
 // Stage the bias of columns n0 .. n0 + ncol - 1 (zero past N) as packed fp16
 // pairs in this warp's shared memory: done before the accumulator wait, so
@@ -265,8 +288,8 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                    const GemmParams p) {
     using SP = SmemPlan<BN, STAGES>;
     constexpr int kBoxesB = BN / 64;
-    constexpr uint32_t kIdesc = idesc_f16_f32(kBM, BN, /*b_mn_major=*/true);
     constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators, power of two >= 32
+    const bool ta = p.trans_a != 0, tb = p.trans_b != 0;
 
     extern __shared__ uint8_t smem_raw[];
     // 1 KiB alignment of the shared-window address (128-byte swizzle atoms).
@@ -332,15 +355,25 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 // B boxes entirely right of N are skipped: the stale smem they
                 // leave only feeds accumulator columns >= N, which are never stored.
                 const int live_boxes = min(kBoxesB, (p.N - tc.n0 + 63) / 64);
-                const uint32_t bytes = kATileBytes + static_cast<uint32_t>(live_boxes) * kBBoxBytes;
+                // A: one 128-row K-major box, or (A stored K x M) two 64-row
+                // boxes, the second skipped when it starts past M
+                const int a_boxes = ta ? (tc.m0 + 64 < p.M ? 2 : 1) : 1;
+                const uint32_t bytes = (ta ? static_cast<uint32_t>(a_boxes) * kBBoxBytes : kATileBytes) +
+                                       static_cast<uint32_t>(live_boxes) * kBBoxBytes;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, status,
                                            ROLE_PRODUCER, BAR_EMPTY)) { ok = false; break; }
                     mbar_arrive_expect_tx(full_bar(stage), bytes);
-                    tma_load_2d(sA + stage * kATileBytes, &tmA, full_bar(stage), kb * kBK, tc.m0);
+                    if (ta) {
+                        for (int c = 0; c < a_boxes; ++c)
+                            tma_load_box(sA + stage * kATileBytes + c * kBBoxBytes, &tmA, full_bar(stage), false,
+                                         tc.m0 + 64 * c, kb * kBK);
+                    } else {
+                        tma_load_2d(sA + stage * kATileBytes, &tmA, full_bar(stage), kb * kBK, tc.m0);
+                    }
                     for (int c = 0; c < live_boxes; ++c)
-                        tma_load_2d(sB + stage * SP::kBTileBytes + c * kBBoxBytes, &tmB, full_bar(stage),
-                                    tc.n0 + 64 * c, kb * kBK);
+                        tma_load_box(sB + stage * SP::kBTileBytes + c * kBBoxBytes, &tmB, full_bar(stage), tb,
+                                     tc.n0 + 64 * c, kb * kBK);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -357,6 +390,7 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32(kBM, BN, /*b_mn_major=*/!tb, /*a_mn_major=*/ta);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -375,13 +409,10 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     const uint32_t b0 = sB + stage * SP::kBTileBytes;
 #pragma unroll
                     for (int k = 0; k < kBK / kUMMA_K; ++k) {
-                        // A: K-major, 128-byte rows, 8-row atoms 1 KiB apart; a K step
-                        //    of 16 fp16 = 32 bytes inside the swizzled row.
-                        // B: N-major, 64-column boxes 8 KiB apart (LBO), 8-row K
-                        //    groups 1 KiB apart (SBO); a K step of 16 rows = 2 KiB.
-                        const uint64_t adesc = smem_desc_sw128(a0 + k * 32, 0, 1024);
-                        const uint64_t bdesc = smem_desc_sw128(b0 + k * 2048, kBBoxBytes, 1024);
-                        tc_mma_f16(d_tmem, adesc, bdesc, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                        // A K-major unless stored K x M; B MN-major unless stored N x K
+                        const uint64_t adesc = operand_desc(a0, k, ta);
+                        const uint64_t bdesc = operand_desc(b0, k, !tb);
+                        tc_mma_f16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
                     }
                     tc_commit(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }

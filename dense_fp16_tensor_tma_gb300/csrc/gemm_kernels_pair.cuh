@@ -29,6 +29,13 @@ namespace gemm_f16_dev {
 
 constexpr uint32_t kBHalfSubBytes = 128 * kBK * 2;   // this CTA's 128 columns of a 64-deep K sub-block: 16 KiB
 
+// tma_load_box for the pair: the bytes complete on the leader CTA's barrier.
+__device__ __forceinline__ void tma_load_box_pair(uint32_t dst, const CUtensorMap* tm, uint32_t bar_leader,
+                                                  bool k_major, int mn, int k) {
+    if (k_major) tma_load_2d_pair(dst, tm, bar_leader, k, mn);
+    else tma_load_2d_pair(dst, tm, bar_leader, mn, k);
+}
+
 template <int STAGES, int KSUB>
 struct SmemPlanPair {
     static constexpr uint32_t kAStage = KSUB * kATileBytes;        // KSUB A boxes
@@ -97,9 +104,8 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     constexpr int kStageK = KSUB * kBK;      // K per pipeline stage
     constexpr int PM = 256;                  // pair tile rows = MMA M
     constexpr int BN = 256;                  // pair tile columns = MMA N
-    constexpr uint32_t kIdesc = idesc_f16_f32(PM, BN, /*b_mn_major=*/true);
-    constexpr uint32_t kIdescHalf = idesc_f16_f32(PM, BN / 2, /*b_mn_major=*/true);   // 256 x 128 units
     constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators of 256 fp32 columns
+    const bool ta = p.trans_a != 0, tb = p.trans_b != 0;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -158,11 +164,17 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     auto units = [&]() { return PairUnitIter(cid, nclusters, p.dp_tiles, num_tiles, p.tail_split); };
     unsigned int* status = &g_status;
 
-    // Boxes each CTA loads for a tile: its A box unless all 128 rows are past
-    // M, and those of its two 64-column B boxes that start before N.  The
-    // skipped ones would only feed accumulator rows / columns that are never
-    // stored.
-    auto a_live = [&](int m0, int r) { return (m0 + 128 * r) < p.M ? 1 : 0; };
+    // Boxes each CTA loads for a tile: its A rows unless all are past M (one
+    // 128-row K-major box, or, with A stored K x M, those of its two 64-row
+    // boxes that start before M), and those of its two 64-column B boxes that
+    // start before N.  The skipped ones would only feed accumulator rows /
+    // columns that are never stored.
+    auto a_boxes = [&](int m0, int r) {
+        return ta ? max(0, min(2, (p.M - (m0 + 128 * r) + 63) / 64)) : ((m0 + 128 * r) < p.M ? 1 : 0);
+    };
+    auto a_bytes = [&](int m0, int r) {
+        return static_cast<uint32_t>(a_boxes(m0, r)) * (ta ? kBBoxBytes : kATileBytes);
+    };
     auto b_live = [&](int n0, int r) { return max(0, min(2, (p.N - (n0 + 128 * r) + 63) / 64)); };
 
     if (warp == 0) {
@@ -176,7 +188,7 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             PairUnit un;
             while (ok && it.next(un)) {
                 const TileCoord tc = tile_coord_bm(un.tile, tiles_m, tiles_n, p.group_m, PM, BN);
-                const int my_a = a_live(tc.m0, rank);
+                const int my_a = a_boxes(tc.m0, rank);
                 // a whole tile: CTA r loads columns n0 + 128r (two boxes); a half
                 // tile h: CTA r loads the one box at n0 + 128h + 64r
                 const int bcol = un.half < 0 ? tc.n0 + 128 * static_cast<int>(rank) : tc.n0 + 128 * un.half + 64 * static_cast<int>(rank);
@@ -186,9 +198,8 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int my_b = live(rank);
                 // every sub-block's boxes are issued, also those starting past K
                 // (they arrive as zeros), so each stage carries the same bytes
-                const uint32_t pair_bytes = KSUB * (
-                    static_cast<uint32_t>(a_live(tc.m0, 0) + a_live(tc.m0, 1)) * kATileBytes +
-                    static_cast<uint32_t>(live(0) + live(1)) * kBBoxBytes);
+                const uint32_t pair_bytes = KSUB * (a_bytes(tc.m0, 0) + a_bytes(tc.m0, 1) +
+                                                    static_cast<uint32_t>(live(0) + live(1)) * kBBoxBytes);
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_cluster_bounded(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, status,
                                                    ROLE_PRODUCER, BAR_EMPTY)) { ok = false; break; }
@@ -196,12 +207,17 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (leader) mbar_arrive_expect_tx(full_bar(stage), pair_bytes);
                     for (int ks = 0; ks < KSUB; ++ks) {
                         const int k0 = kb * kStageK + ks * kBK;
-                        if (my_a)
-                            tma_load_2d_pair(sA + stage * SP::kAStage + ks * kATileBytes, &tmA, full_leader, k0,
-                                             tc.m0 + 128 * rank);
+                        const uint32_t a_dst = sA + stage * SP::kAStage + ks * kATileBytes;
+                        const int arow = tc.m0 + 128 * static_cast<int>(rank);
+                        if (ta) {
+                            for (int c = 0; c < my_a; ++c)
+                                tma_load_box_pair(a_dst + c * kBBoxBytes, &tmA, full_leader, false, arow + 64 * c, k0);
+                        } else if (my_a) {
+                            tma_load_2d_pair(a_dst, &tmA, full_leader, k0, arow);
+                        }
                         for (int c = 0; c < my_b; ++c)
-                            tma_load_2d_pair(sB + stage * SP::kBStage + ks * kBHalfSubBytes + c * kBBoxBytes, &tmB,
-                                             full_leader, bcol + 64 * c, k0);
+                            tma_load_box_pair(sB + stage * SP::kBStage + ks * kBHalfSubBytes + c * kBBoxBytes, &tmB,
+                                              full_leader, tb, bcol + 64 * c, k0);
                     }
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -222,6 +238,8 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (CTA 0 only)
         if (leader && lane == 0) {
+            const uint32_t idesc_whole = idesc_f16_f32(PM, BN, /*b_mn_major=*/!tb, /*a_mn_major=*/ta);
+            const uint32_t idesc_half = idesc_f16_f32(PM, BN / 2, !tb, ta);   // 256 x 128 units
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -234,7 +252,7 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                                                ROLE_MMA, BAR_ACC_EMPTY)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                const uint32_t idesc = un.half < 0 ? kIdesc : kIdescHalf;
+                const uint32_t idesc = un.half < 0 ? idesc_whole : idesc_half;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_cluster_bounded(full_bar(stage), phase, p.timeout_ns, abort_flag, status,
                                                    ROLE_MMA, BAR_FULL)) { ok = false; break; }
@@ -246,9 +264,9 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
                         for (int k = 0; k < kBK / kUMMA_K; ++k) {
                             // same layouts as the single-SM kernel; B here is this
-                            // CTA's 128 columns (two 64-column boxes, LBO 8 KiB)
-                            const uint64_t adesc = smem_desc_sw128(a0 + k * 32, 0, 1024);
-                            const uint64_t bdesc = smem_desc_sw128(b0 + k * 2048, kBBoxBytes, 1024);
+                            // CTA's 128 columns (two 64-column boxes)
+                            const uint64_t adesc = operand_desc(a0, k, ta);
+                            const uint64_t bdesc = operand_desc(b0, k, !tb);
                             tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | ks | k) != 0 ? 1u : 0u);
                         }
                     }

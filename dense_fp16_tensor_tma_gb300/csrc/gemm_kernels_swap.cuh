@@ -12,9 +12,10 @@
 //
 //   * tile = 128 columns of C (MMA M, one TMEM lane each) x MT rows of C
 //     (MMA N = 16, 32 or 64);
-//   * MMA "A" operand = B^T: the same N-contiguous 64 x 64 boxes as the
-//     regular kernel's B (MN-major, LBO 8 KiB, SBO 1 KiB);
-//   * MMA "B" operand = A^T: an MT x 64 box of A rows (K-major, SBO 1 KiB);
+//   * MMA "A" operand = B^T: the same two 64 x 64 boxes as the regular
+//     kernel's B (MN-major; K-major when B is stored N x K);
+//   * MMA "B" operand = A^T: an MT x 64 box of A rows (K-major; when A is
+//     stored K x M, MT = 64 and the box is MN-major);
 //   * stage = 16 KiB of B + MT x 128 B of A, 9 to 12 stages deep;
 //   * epilogue: thread = one output column n (its TMEM lane), registers = MT
 //     rows; bias[n] is one value per thread; every store of a warp covers 32
@@ -54,7 +55,8 @@ gemm_f16_swap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                      const GemmParams p) {
     using SP = SmemPlanSwap<MT, STAGES>;
     constexpr int TN = 128;                                      // columns of C per tile
-    constexpr uint32_t kIdesc = idesc_f16_f32(TN, MT, /*b_mn_major=*/false, /*a_mn_major=*/true);
+    // A stored K x M takes MT = 64 (the host plans it so): one MN-major box
+    const bool ta = p.trans_a != 0, tb = p.trans_b != 0;
     constexpr uint32_t kTmemCols = 2 * MT < 32 ? 32 : 2 * MT;    // two accumulators
 
     extern __shared__ uint8_t smem_raw[];
@@ -133,8 +135,9 @@ gemm_f16_swap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     const uint32_t st = base_s + stage * SP::kStage;
                     mbar_arrive_expect_tx(full_bar(stage), bytes);
                     for (int c = 0; c < live_b; ++c)
-                        tma_load_2d(st + c * kBBoxBytes, &tmB, full_bar(stage), n0 + 64 * c, kb * kBK);
-                    tma_load_2d(st + SP::kBtBytes, &tmA, full_bar(stage), kb * kBK, m0);
+                        tma_load_box(st + c * kBBoxBytes, &tmB, full_bar(stage), tb, n0 + 64 * c, kb * kBK);
+                    if (ta) tma_load_2d(st + SP::kBtBytes, &tmA, full_bar(stage), m0, kb * kBK);
+                    else tma_load_2d(st + SP::kBtBytes, &tmA, full_bar(stage), kb * kBK, m0);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -149,6 +152,8 @@ gemm_f16_swap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            // MMA A = B^T (MN-major unless B is stored N x K), MMA B = A^T (K-major unless A is stored K x M)
+            const uint32_t idesc = idesc_f16_f32(TN, MT, /*b_mn_major=*/ta, /*a_mn_major=*/!tb);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -167,10 +172,9 @@ gemm_f16_swap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     const uint32_t st = base_s + stage * SP::kStage;
 #pragma unroll
                     for (int k = 0; k < kBK / kUMMA_K; ++k) {
-                        // B^T: N-major boxes, K step of 16 rows = 2 KiB; A^T: K-major rows, K step 32 B
-                        const uint64_t adesc = smem_desc_sw128(st + k * 2048, kBBoxBytes, 1024);
-                        const uint64_t bdesc = smem_desc_sw128(st + SP::kBtBytes + k * 32, 0, 1024);
-                        tc_mma_f16(d_tmem, adesc, bdesc, kIdesc, (kb != kb0 || k != 0) ? 1u : 0u);
+                        const uint64_t adesc = operand_desc(st, k, !tb);
+                        const uint64_t bdesc = operand_desc(st + SP::kBtBytes, k, ta);
+                        tc_mma_f16(d_tmem, adesc, bdesc, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
                     }
                     tc_commit(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }

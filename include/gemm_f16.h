@@ -17,16 +17,18 @@
  * 0.5 x (1 + erf(x / sqrt 2)); its tanh approximation and the sigmoid (the
  * checklist's other "GEMM + fusion" activation) are also offered.
  *
- * Layout: all matrices are dense row-major (lda = K, ldb = N, ldc = N),
- * element type IEEE binary16 passed as raw pointers.  bias is a length-N
- * vector broadcast over the rows of C.
+ * Layout: gemm_f16 takes dense row-major matrices (lda = K, ldb = N,
+ * ldc = N); gemm_f16_ex takes any row pitches and either operand stored
+ * transposed.  Element type IEEE binary16 passed as raw pointers.  bias is a
+ * length-N vector broadcast over the rows of C.
  *
  * Pointers: A, B, bias and C are DEVICE pointers on the current CUDA device.
  * The caller owns them; the library never frees or retains them.  C must not
  * overlap A, B or bias.  Every pointer must be at least 2-byte aligned.
  * Operands whose base is not 16-byte aligned, or whose row pitch in bytes is
- * not a multiple of 16 (K % 8 != 0 for A, N % 8 != 0 for B), are repacked
- * into a library-owned, stream-ordered scratch buffer before the GEMM.
+ * not a multiple of 16 (e.g. K % 8 != 0 for a dense A, N % 8 != 0 for a
+ * dense B), are repacked, in their own layout, into a library-owned,
+ * stream-ordered scratch buffer before the GEMM.
  *
  * Streams: every call is asynchronous on `cuda_stream` (a cudaStream_t, or
  * NULL for the legacy default stream) and returns once the work is enqueued.
@@ -82,6 +84,38 @@ typedef enum {
 int gemm_f16(const void* A, const void* B, const void* bias, void* C,
              int64_t M, int64_t N, int64_t K, int epilogue, void* cuda_stream);
 
+/* Operand layout flags of gemm_f16_ex (bitwise or). */
+typedef enum {
+    GEMM_F16_TRANS_A = 1,  /* A is stored transposed: K x M, M contiguous */
+    GEMM_F16_TRANS_B = 2   /* B is stored transposed: N x K, K contiguous */
+} gemm_f16_flags_t;
+
+/*
+ * gemm_f16_ex -- gemm_f16 with row pitches and transposed operands: the
+ * transpose_A / transpose_B options of the tile GEMM primitive in
+ * "writing-tilelang-kernels", Key API Patterns (T.gemm), applied to the
+ * operands in global memory.  Computes the same C[M,N] = epilogue(A.B + bias)
+ * where, with pitches in elements,
+ *
+ *   A[i,k] = A_ptr[i*lda + k]   (lda >= K)   or, with GEMM_F16_TRANS_A,
+ *            A_ptr[k*lda + i]   (lda >= M)
+ *   B[k,j] = B_ptr[k*ldb + j]   (ldb >= N)   or, with GEMM_F16_TRANS_B,
+ *            B_ptr[j*ldb + k]   (ldb >= K)   (a Linear layer's weight W[N,K]: C = A.W^T)
+ *   C[i,j] = C_ptr[i*ldc + j]   (ldc >= N; elements between rows untouched)
+ *
+ * The tensor cores read both layouts directly (K-major or MN-major shared-
+ * memory operands); only a base not 16-byte aligned or a pitch not a multiple
+ * of 8 elements costs a repack, as in gemm_f16.  Pitches are < 2^31; the
+ * pitch checks apply only to operands that are read (K > 0, M, N > 0).
+ * Unknown flag bits, a pitch below its minimum, or the gemm_f16 argument
+ * errors return GEMM_ERR_INVALID_ARG (or GEMM_ERR_MISALIGNED) before any
+ * CUDA call.  Otherwise as gemm_f16; gemm_f16(A, B, bias, C, M, N, K, e, s)
+ * is gemm_f16_ex(A, K, B, N, bias, C, N, M, N, K, e, 0, s).
+ */
+int gemm_f16_ex(const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias, void* C,
+                int64_t ldc, int64_t M, int64_t N, int64_t K, int epilogue, int flags,
+                void* cuda_stream);
+
 /* Static, human-readable name of a status code. */
 const char* gemm_f16_status_string(int status);
 
@@ -118,6 +152,11 @@ int gemm_f16_release_workspace(void);
 int gemm_f16_plan(const void* A, const void* B, const void* bias, const void* C,
                   int64_t M, int64_t N, int64_t K, int epilogue, int num_sms,
                   int64_t plan[11]);
+
+/* gemm_f16_plan for the arguments of gemm_f16_ex (same plan[] entries). */
+int gemm_f16_plan_ex(const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias,
+                     const void* C, int64_t ldc, int64_t M, int64_t N, int64_t K, int epilogue,
+                     int flags, int num_sms, int64_t plan[11]);
 
 /*
  * Diagnostic (no counterpart on the pages): pins the kernel configuration

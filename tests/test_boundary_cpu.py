@@ -148,3 +148,84 @@ def test_plan_short_a_uses_swap_ab(g):
     assert (p["splits"], p["ctas"], p["scratch"]) == (1, 128, 0)
     assert g.gemm_f16_plan(33, 1000, 64, "none", num_sms=152)["tile_m"] == 64
     assert g.gemm_f16_plan(65, 1000, 64, "none", num_sms=152)["path"] == 2
+
+
+# ---------------------------------------------------------------- gemm_f16_ex: pitches and transposed operands
+
+TA, TB = 1, 2
+
+
+# Only calls that fail before any CUDA call: the fake addresses are never
+# handed to a device.
+@pytest.mark.parametrize("args", [
+    # (lda, ldb, ldc, M, N, K, flags)
+    (7, 8, 8, 8, 8, 8, 0),             # lda < K
+    (8, 7, 8, 8, 8, 8, 0),             # ldb < N
+    (8, 8, 7, 8, 8, 8, 0),             # ldc < N
+    (8, 8, 8, 16, 8, 8, TA),           # A stored K x M: lda < M
+    (8, 31, 64, 8, 64, 32, TB),        # B stored N x K: ldb < K
+    (64, 64, 64, 64, 64, 64, 4),       # unknown flag bit
+    (64, 64, 64, 64, 64, 64, -1),
+    (1 << 31, 64, 64, 64, 64, 64, 0),  # pitch too large
+    (64, 64, -1, 64, 64, 64, 0),
+])
+def test_ex_argument_errors_need_no_device(g, args):
+    lda, ldb, ldc, M, N, K, flags = args
+    assert g.gemm_f16_ex_ptr(GOOD, lda, GOOD, ldb, GOOD, GOOD, ldc, M, N, K, "bias", flags, 0) == 1
+
+
+def test_ex_empty_problems_are_no_ops(g):
+    assert g.gemm_f16_ex_ptr(0, 0, 0, 0, 0, 0, 0, 0, 8, 8, "none", TA | TB, 0) == 0
+    assert g.gemm_f16_ex_ptr(0, 0, 0, 0, 0, 0, 0, 8, 0, 8, "none", 0, 0) == 0
+    # with K == 0 neither operand is read, so their pitches are not checked
+    assert g.gemm_f16_plan(8, 8, 0, "bias", lda=0, ldb=0, trans_a=True)["path"] == 1
+
+
+def test_ex_dense_call_is_gemm_f16(g):
+    for M, N, K in ((8192, 8192, 8192), (3001, 5003, 1000), (16, 8192, 8192), (64, 64, 60)):
+        assert g.gemm_f16_plan(M, N, K, "bias") == g.gemm_f16_plan(M, N, K, "bias", lda=K, ldb=N, ldc=N)
+
+
+def test_plan_transposed_operands_are_read_in_place(g):
+    # both layouts of both operands go to the tensor cores without a repack
+    for ta in (False, True):
+        for tb in (False, True):
+            p = g.gemm_f16_plan(8192, 8192, 8192, "bias_gelu_erf", trans_a=ta, trans_b=tb)
+            assert (p["path"], p["tile_m"], p["pack_a"], p["pack_b"], p["ctas"]) == (2, 256, 0, 0, 152)
+
+
+def test_plan_pitches_decide_repack_and_store_width(g):
+    # a pitch that is not a multiple of 8 elements repacks that operand only
+    p = g.gemm_f16_plan(300, 520, 200, "bias", lda=203, ldb=208, trans_b=True)    # B stored 520 x 200
+    assert (p["pack_a"], p["pack_b"], p["vec_store"]) == (1, 0, 1)
+    p = g.gemm_f16_plan(300, 520, 200, "bias", lda=304, ldb=525, trans_a=True)    # A stored 200 x 300
+    assert (p["pack_a"], p["pack_b"]) == (0, 1)
+    assert p["scratch"] == ((200 * 520 * 2 + 255) // 256) * 256   # B rows re-pitched to the dense 520
+    assert g.gemm_f16_plan(300, 520, 200, "bias", ldc=527)["vec_store"] == 0
+    assert g.gemm_f16_plan(300, 520, 200, "bias", ldc=528)["vec_store"] == 1
+    # the dense ragged workload's N = 5003 needs the repack; a padded pitch does not
+    assert g.gemm_f16_plan(3001, 5003, 1000, "bias_relu", ldb=5008)["pack_b"] == 0
+
+
+def test_plan_short_transposed_a_takes_64_row_swap_tiles(g):
+    p = g.gemm_f16_plan(16, 8192, 8192, "none", trans_a=True)
+    assert (p["path"], p["tile_m"], p["pack_a"], p["splits"]) == (3, 64, 0, 2)
+    p = g.gemm_f16_plan(16, 8192, 8192, "none", trans_b=True)
+    assert (p["path"], p["tile_m"], p["pack_b"]) == (3, 16, 0)
+
+
+def test_binding_layout_detection():
+    torch = pytest.importorskip("torch")
+    import dense_fp16_tensor_tma_gb300 as mod
+    lay = mod._operand_layout
+    X = torch.zeros(6, 10, dtype=torch.float16)
+    assert lay(X, "X") == (False, 10)
+    assert lay(X.t(), "X") == (True, 10)
+    assert lay(X[:, :7], "X") == (False, 10)
+    assert lay(X[:, :7].t(), "X") == (True, 10)
+    assert lay(X[:1], "X") == (False, 10)
+    assert lay(torch.zeros(10, 1, dtype=torch.float16).t(), "X") == (False, 10)   # 1 x 10, any row stride
+    with pytest.raises(ValueError):
+        lay(X[:, ::2], "X")                   # neither rows nor columns contiguous
+    with pytest.raises(ValueError):
+        lay(torch.zeros(10, dtype=torch.float16).expand(4, 10), "X")   # rows overlap (stride 0)
