@@ -26,7 +26,7 @@ GEMM_F16_TRANS_A, GEMM_F16_TRANS_B = 1, 2
 
 EXPORTS = ("gemm_f16", "gemm_f16_ex", "gemm_f16_status_string", "gemm_f16_last_cuda_error",
            "gemm_f16_debug_status", "gemm_f16_release_workspace", "gemm_f16_plan", "gemm_f16_plan_ex",
-           "gemm_f16_selftest_timeout", "gemm_f16_noalloc", "gemm_f16_force_config")
+           "gemm_f16_selftest_timeout", "gemm_f16_noalloc", "gemm_f16_force_config", "gemm_f16_set_pdl")
 CONFIGS = {"auto": 0, "pair256x256": 1, "128x256": 2, "128x128": 3, "128x64": 4, "swap": 5, "pair_whole": 6}
 
 if not os.path.exists(LIB_PATH):
@@ -56,6 +56,8 @@ lib.gemm_f16_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp
 lib.gemm_f16_noalloc.restype = _int
 lib.gemm_f16_force_config.argtypes = [_int]
 lib.gemm_f16_force_config.restype = _int
+lib.gemm_f16_set_pdl.argtypes = [_int]
+lib.gemm_f16_set_pdl.restype = _int
 
 
 class GemmError(RuntimeError):
@@ -192,6 +194,12 @@ def gemm_f16_force_config(config) -> int:
     if prev < 0:
         raise ValueError(f"unknown configuration {config!r}")
     return prev
+
+
+def gemm_f16_set_pdl(enable: bool) -> bool:
+    """Programmatic dependent launch of the library's kernels on/off
+    (process-wide); returns the previous setting."""
+    return bool(lib.gemm_f16_set_pdl(1 if enable else 0))
 
 
 def gemm_f16_selftest_timeout(timeout_us: int = 1000, stream=None) -> int:

@@ -72,6 +72,21 @@ DeviceState g_dev[kMaxDevices];
 EncodeTiledFn g_encode = nullptr;
 uint64_t g_timeout_ns = 2000000000ull;   // 2 s per bounded wait
 std::atomic<int> g_force_config{CFG_AUTO};
+// Programmatic dependent launch on every kernel of the library (GEMM_F16_PDL=0
+// in the environment, or gemm_f16_set_pdl(0), turns it off).
+std::atomic<int> g_pdl{-1};   // -1: not yet read from the environment
+
+bool pdl_enabled() {
+    int v = g_pdl.load(std::memory_order_relaxed);
+    if (v < 0) {
+        const char* env = std::getenv("GEMM_F16_PDL");
+        v = (env != nullptr && env[0] == '0') ? 0 : 1;
+        int expected = -1;
+        g_pdl.compare_exchange_strong(expected, v);
+        v = g_pdl.load(std::memory_order_relaxed);
+    }
+    return v != 0;
+}
 
 int cuda_fail(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
@@ -242,6 +257,34 @@ cudaLaunchConfig_t launch_config(int ctas, uint32_t smem, cudaStream_t s) {
     return cfg;
 }
 
+// Launch attributes of a kernel of this library: a cluster of `cluster` CTAs
+// (if > 1) and programmatic stream serialization (if enabled): the kernel may
+// start while the previous one in the stream finishes; every kernel here
+// calls grid_dependency_wait() before touching global memory.
+struct LaunchAttrs {
+    cudaLaunchAttribute a[2];
+    unsigned n = 0;
+    LaunchAttrs(int cluster, bool pdl) {
+        std::memset(a, 0, sizeof(a));
+        if (cluster > 1) {
+            a[n].id = cudaLaunchAttributeClusterDimension;
+            a[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+            a[n].val.clusterDim.y = 1;
+            a[n].val.clusterDim.z = 1;
+            ++n;
+        }
+        if (pdl) {
+            a[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            a[n].val.programmaticStreamSerializationAllowed = 1;
+            ++n;
+        }
+    }
+    void apply(cudaLaunchConfig_t& cfg) {
+        cfg.attrs = n ? a : nullptr;
+        cfg.numAttrs = n;
+    }
+};
+
 // One-time per-device checks and kernel attributes (allocates nothing).
 // Called with g_mu held.
 int init_common_locked(int dev, DeviceState& st) {
@@ -361,17 +404,22 @@ int encode_2d(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int
 
 int launch_repack(uint16_t* dst, const void* src, int64_t rows, int64_t cols, int64_t ld_src, int64_t ld_dst,
                   cudaStream_t s) {
-    dim3 block(256);   // 8 elements per thread: 2048 per block along a row
-    dim3 grid(static_cast<unsigned>((cols + 2047) / 2048), static_cast<unsigned>(std::min<int64_t>(rows, 65535)));
-    gemm_f16_repack_kernel<<<grid, block, 0, s>>>(dst, static_cast<const uint16_t*>(src), rows, cols, ld_src,
-                                                  ld_dst);
-    cudaError_t e = cudaGetLastError();
+    // 256 threads, 8 elements per thread: 2048 per block along a row
+    cudaLaunchConfig_t cfg = launch_config(1, 0, s);
+    cfg.gridDim = dim3(static_cast<unsigned>((cols + 2047) / 2048), static_cast<unsigned>(std::min<int64_t>(rows, 65535)));
+    cfg.blockDim = dim3(256);
+    LaunchAttrs la(1, pdl_enabled());
+    la.apply(cfg);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_repack_kernel, dst, static_cast<const uint16_t*>(src), rows,
+                                       cols, ld_src, ld_dst);
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
 
 template <int BN, int STAGES>
 int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& prm, int ctas, cudaStream_t s) {
     cudaLaunchConfig_t cfg = launch_config(ctas, SmemPlan<BN, STAGES>::kDynamicBytes, s);
+    LaunchAttrs la(1, pdl_enabled());
+    la.apply(cfg);
     cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_tc_kernel<BN, STAGES>, ta, tb, prm);
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
@@ -380,19 +428,16 @@ template <int MT, int STAGES>
 int launch_swap(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& prm, int ctas, cudaStream_t s) {
     cudaLaunchConfig_t cfg = launch_config(ctas, SmemPlanSwap<MT, STAGES>::kDynamicBytes, s);
     cfg.blockDim = dim3(kSwapThreads);
+    LaunchAttrs la(1, pdl_enabled());
+    la.apply(cfg);
     cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_swap_kernel<MT, STAGES>, ta, tb, prm);
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
 
 int launch_tc_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& prm, int ctas, cudaStream_t s) {
     cudaLaunchConfig_t cfg = launch_config(ctas, SmemPlanPair<kStagesPair, kKSubPair>::kDynamicBytes, s);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    LaunchAttrs la(2, pdl_enabled());
+    la.apply(cfg);
     cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_kernel<kStagesPair, kKSubPair>, ta, tb, prm);
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
@@ -468,8 +513,12 @@ int enqueue_plan(const Plan& pl, const Operands& op, const __half* biasp, int64_
 
 int enqueue_bias_only(const Plan& pl, const __half* biasp, void* C, int64_t ldc, int64_t M, int64_t N, int epilogue,
                       cudaStream_t s) {
-    gemm_f16_bias_only_kernel<<<pl.ctas, 256, 0, s>>>(static_cast<__half*>(C), biasp, M, N, ldc, epilogue);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = launch_config(pl.ctas, 0, s);
+    cfg.blockDim = dim3(256);
+    LaunchAttrs la(1, pdl_enabled());
+    la.apply(cfg);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_bias_only_kernel, static_cast<__half*>(C), biasp, M, N, ldc,
+                                       epilogue);
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
 
@@ -519,6 +568,12 @@ const char* gemm_f16_status_string(int status) {
 }
 
 int gemm_f16_last_cuda_error(void) { return t_last_cuda_error; }
+
+int gemm_f16_set_pdl(int enable) {
+    const int prev = pdl_enabled() ? 1 : 0;
+    g_pdl.store(enable ? 1 : 0);
+    return prev;
+}
 
 int gemm_f16_force_config(int config) {
     if (config < CFG_AUTO || config > CFG_PAIR_256_WHOLE) return -1;

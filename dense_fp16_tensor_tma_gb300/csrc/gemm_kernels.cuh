@@ -336,6 +336,9 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // set-up above overlaps the previous kernel; global memory only from here
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     const int tiles_m = (p.M + kBM - 1) / kBM;
     const int tiles_n = (p.N + BN - 1) / BN;
@@ -460,6 +463,8 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
 // K == 0: C = epilogue(bias) (zeros for NONE).
 __global__ void gemm_f16_bias_only_kernel(__half* C, const __half* bias, int64_t M, int64_t N, int64_t ldc, int epi) {
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int64_t total = M * N;
     for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
          e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -478,6 +483,8 @@ __global__ void gemm_f16_bias_only_kernel(__half* C, const __half* bias, int64_t
 // grid.y strides over rows.
 __global__ void gemm_f16_repack_kernel(uint16_t* __restrict__ dst, const uint16_t* __restrict__ src,
                                        int64_t rows, int64_t cols, int64_t ld_src, int64_t ld_dst) {
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int64_t c = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
     if (c >= cols) return;
     for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {

@@ -154,6 +154,9 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     cluster_sync_all();     // both CTAs' barriers exist before any cross-CTA arrive or complete_tx
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // set-up above overlaps the previous kernel; global memory only from here
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     const int tiles_m = (p.M + PM - 1) / PM;
     const int tiles_n = (p.N + BN - 1) / BN;

@@ -100,6 +100,9 @@ gemm_f16_swap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // set-up above overlaps the previous kernel; global memory only from here
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     const int tiles_m = (p.M + MT - 1) / MT;
     const int tiles_n = (p.N + TN - 1) / TN;

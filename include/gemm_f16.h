@@ -171,6 +171,20 @@ int gemm_f16_plan_ex(const void* A, int64_t lda, const void* B, int64_t ldb, con
 int gemm_f16_force_config(int config);
 
 /*
+ * Programmatic dependent launch (on by default; the environment variable
+ * GEMM_F16_PDL=0 turns it off at start-up).  Every kernel of this library is
+ * launched with programmatic stream serialization: it may begin while the
+ * previous kernel in the stream is still finishing, runs its set-up (barrier
+ * initialisation, tensor-memory allocation, descriptor prefetch) meanwhile,
+ * and waits for that kernel's completion and memory before its first access
+ * to global memory.  Results are the same either way; back-to-back small
+ * calls (and their CUDA graphs) lose part of the launch latency.  No
+ * counterpart on the pages.  Returns the previous setting (0/1).
+ * Process-wide; set it while no other host thread is calling.
+ */
+int gemm_f16_set_pdl(int enable);
+
+/*
  * Diagnostic for the bounded-wait machinery (no counterpart on the pages):
  * launches one CTA that waits on an mbarrier nothing ever arrives on, with a
  * limit of `timeout_us` microseconds, and returns what gemm_f16_debug_status
