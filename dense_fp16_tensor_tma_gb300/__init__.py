@@ -77,9 +77,12 @@ def _epi(epilogue) -> int:
     return EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
 
 
-def _stream_handle(stream):
+def _stream_handle(stream, device_index=None):
     if stream is None:
         import torch
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:   # the current stream's handle without building a Stream object
+            return raw(torch.cuda.current_device() if device_index is None else device_index)
         return torch.cuda.current_stream().cuda_stream
     return getattr(stream, "cuda_stream", stream)
 
@@ -150,7 +153,7 @@ def gemm_f16(A, B, bias, C, epilogue="none", stream=None):
     flags = (GEMM_F16_TRANS_A if ta else 0) | (GEMM_F16_TRANS_B if tb else 0)
     st = lib.gemm_f16_ex(A.data_ptr() or None, lda, B.data_ptr() or None, ldb,
                          bias.data_ptr() if bias is not None else None, C.data_ptr() or None, ldc,
-                         M, N, K, _epi(epilogue), flags, _stream_handle(stream))
+                         M, N, K, _epi(epilogue), flags, _stream_handle(stream, C.get_device()))
     if st != GEMM_OK:
         raise GemmError(st)
     return C

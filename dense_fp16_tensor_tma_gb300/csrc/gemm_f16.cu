@@ -383,11 +383,35 @@ int ensure_pool(int dev) {
     return GEMM_OK;
 }
 
+// Encoded tensor maps of recent calls.  A map is a pure function of its
+// arguments (address, extents, pitch, box; the rest is fixed), so a hit is
+// exactly the map a new encoding would give; repeated calls on the same
+// buffers (a layer's weights, a serving loop) skip the encoder.
+struct TensorMapCache {
+    static constexpr int kWays = 16;
+    struct Entry {
+        const void* ptr = nullptr;
+        int64_t inner = 0, outer = 0, ld = 0;
+        int box_inner = 0, box_outer = 0;
+        CUtensorMap map;
+    };
+    Entry e[kWays];
+    int next = 0;
+};
+thread_local TensorMapCache t_maps;
+
 // 2-D fp16 tensor map: `inner` contiguous elements per row, `outer` rows,
 // row pitch `ld` elements, box `box_inner` x `box_outer`, 128-byte swizzle,
 // zero fill outside the tensor.
 int encode_2d(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int64_t ld, int box_inner,
               int box_outer) {
+    for (const TensorMapCache::Entry& c : t_maps.e) {
+        if (c.ptr == ptr && ptr != nullptr && c.inner == inner && c.outer == outer && c.ld == ld &&
+            c.box_inner == box_inner && c.box_outer == box_outer) {
+            *m = c.map;
+            return GEMM_OK;
+        }
+    }
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
@@ -399,6 +423,15 @@ int encode_2d(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int
         t_last_cuda_error = static_cast<int>(r);
         return GEMM_ERR_CUDA;
     }
+    TensorMapCache::Entry& c = t_maps.e[t_maps.next];
+    t_maps.next = (t_maps.next + 1) % TensorMapCache::kWays;
+    c.ptr = ptr;
+    c.inner = inner;
+    c.outer = outer;
+    c.ld = ld;
+    c.box_inner = box_inner;
+    c.box_outer = box_outer;
+    c.map = *m;
     return GEMM_OK;
 }
 

@@ -195,3 +195,23 @@ def test_side_stream_pdl_does_not_cross_streams(pdl_restore, torch_dev, oracle_m
         g.gemm_f16(c1, t["W2"], t["b2"], c2, "bias")
     torch.cuda.synchronize()
     assert np.array_equal(c2.cpu().numpy(), ref[1])
+
+
+def test_one_buffer_many_shapes_same_address(g, torch_dev, oracle_mod):
+    # the same base addresses with other extents and pitches: every call must
+    # see its own operand shape (encoded tensor maps are reused only on an
+    # exact match of address, extents, pitch and box)
+    torch, dev = torch_dev
+    rng = np.random.default_rng(31)
+    bufA = torch.zeros(1 << 20, dtype=torch.float16, device=dev)
+    bufB = torch.zeros(1 << 20, dtype=torch.float16, device=dev)
+    for M, N, K, lda, ldb in [(256, 256, 256, 256, 256), (256, 128, 512, 512, 128), (128, 256, 256, 512, 256),
+                              (256, 256, 256, 264, 256), (256, 256, 256, 256, 256), (64, 1024, 128, 128, 1024)]:
+        A, B = tern(rng, (M, K)), tern(rng, (K, N))
+        Av = bufA[:M * lda].view(M, lda)[:, :K]
+        Bv = bufB[:K * ldb].view(K, ldb)[:, :N]
+        Av.copy_(torch.from_numpy(A).to(dev))
+        Bv.copy_(torch.from_numpy(B).to(dev))
+        C = torch.empty((M, N), dtype=torch.float16, device=dev)
+        g.gemm_f16(Av, Bv, None, C, "none")
+        assert np.array_equal(C.cpu().numpy(), oracle_mod.gemm(A, B, None, "none")), (M, N, K, lda, ldb)
