@@ -26,7 +26,8 @@ GEMM_F16_TRANS_A, GEMM_F16_TRANS_B = 1, 2
 
 EXPORTS = ("gemm_f16", "gemm_f16_ex", "gemm_f16_status_string", "gemm_f16_last_cuda_error",
            "gemm_f16_debug_status", "gemm_f16_release_workspace", "gemm_f16_plan", "gemm_f16_plan_ex",
-           "gemm_f16_selftest_timeout", "gemm_f16_noalloc", "gemm_f16_force_config", "gemm_f16_set_pdl")
+           "gemm_f16_selftest_timeout", "gemm_f16_noalloc", "gemm_f16_force_config", "gemm_f16_set_pdl",
+           "gemm_f16_grouped")
 CONFIGS = {"auto": 0, "pair256x256": 1, "128x256": 2, "128x128": 3, "128x64": 4, "swap": 5, "pair_whole": 6}
 
 if not os.path.exists(LIB_PATH):
@@ -35,6 +36,14 @@ if not os.path.exists(LIB_PATH):
 
 lib = ctypes.CDLL(LIB_PATH)
 _vp, _i64, _int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+
+
+class GemmProblem(ctypes.Structure):
+    """gemm_f16_problem_t of include/gemm_f16.h."""
+    _fields_ = [("A", _vp), ("lda", _i64), ("B", _vp), ("ldb", _i64), ("bias", _vp), ("C", _vp), ("ldc", _i64),
+                ("M", _i64), ("N", _i64), ("K", _i64)]
+
+
 lib.gemm_f16.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
 lib.gemm_f16.restype = _int
 lib.gemm_f16_ex.argtypes = [_vp, _i64, _vp, _i64, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, _vp]
@@ -56,6 +65,8 @@ lib.gemm_f16_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp
 lib.gemm_f16_noalloc.restype = _int
 lib.gemm_f16_force_config.argtypes = [_int]
 lib.gemm_f16_force_config.restype = _int
+lib.gemm_f16_grouped.argtypes = [ctypes.POINTER(GemmProblem), _int, _int, _int, _vp]
+lib.gemm_f16_grouped.restype = _int
 lib.gemm_f16_set_pdl.argtypes = [_int]
 lib.gemm_f16_set_pdl.restype = _int
 
@@ -104,10 +115,12 @@ def gemm_f16_ex_ptr(a_ptr: int, lda: int, b_ptr: int, ldb: int, bias_ptr: int, c
 def _operand_layout(t, name):
     """(stored transposed, row pitch) of a 2-D view whose rows are contiguous
     (strides (ld, 1)) or whose columns are (strides (1, ld): the transpose of a
-    row-major matrix, e.g. W.t() of a Linear weight W).  Size-1 dimensions
-    take any stride."""
+    row-major matrix, e.g. W.t() of a Linear weight W).  Size-1 dimensions,
+    and empty tensors, take any stride."""
     rows, cols = t.shape
     s0, s1 = t.stride()
+    if rows == 0 or cols == 0:
+        return False, max(cols, 1)   # nothing is read or written: any strides
     if cols <= 1 or s1 == 1:
         if rows <= 1:
             return False, max(cols, 1)
@@ -157,6 +170,55 @@ def gemm_f16(A, B, bias, C, epilogue="none", stream=None):
     if st != GEMM_OK:
         raise GemmError(st)
     return C
+
+
+def gemm_f16_grouped_ptr(problems, epilogue=GEMM_EPI_NONE, flags: int = 0, stream: int = 0) -> int:
+    """Raw call of gemm_f16_grouped: `problems` is a sequence of tuples
+    (A, lda, B, ldb, bias, C, ldc, M, N, K) of integers (device addresses,
+    pitches and sizes).  Returns the status code."""
+    arr = (GemmProblem * max(1, len(problems)))()
+    for i, q in enumerate(problems):
+        arr[i] = GemmProblem(*[(int(x) or None) if k in (0, 2, 4, 5) else int(x) for k, x in enumerate(q)])
+    return lib.gemm_f16_grouped(arr, len(problems), _epi(epilogue), int(flags), stream or None)
+
+
+def gemm_f16_grouped(problems, epilogue="none", stream=None):
+    """C_g = epilogue(A_g @ B_g + bias_g) for every (A_g, B_g, bias_g, C_g) in
+    `problems`, in one grouped launch per operand layout present (the layouts
+    are read from each view as in gemm_f16; bias_g may be None for "none").
+    Raises GemmError on a nonzero status."""
+    import torch
+    by_flags = {}
+    dev = None
+    for idx, (A, B, bias, C) in enumerate(problems):
+        M, K = A.shape
+        K2, N = B.shape
+        if K2 != K or tuple(C.shape) != (M, N):
+            raise ValueError(f"problem {idx}: shape mismatch A {tuple(A.shape)}, B {tuple(B.shape)}, "
+                             f"C {tuple(C.shape)}")
+        for name, t in (("A", A), ("B", B), ("C", C)) + ((("bias", bias),) if bias is not None else ()):
+            if t.dtype != torch.float16 or not t.is_cuda:
+                raise ValueError(f"problem {idx}: {name} must be a float16 CUDA tensor")
+        if bias is not None and (tuple(bias.shape) != (N,) or not bias.is_contiguous()):
+            raise ValueError(f"problem {idx}: bias must be a contiguous tensor of shape ({N},)")
+        ta, lda = _operand_layout(A, "A")
+        tb, ldb = _operand_layout(B, "B")
+        tc, ldc = _operand_layout(C, "C")
+        if tc and M > 1 and N > 1:
+            raise ValueError(f"problem {idx}: C needs contiguous rows")
+        if tc:
+            ldc = N
+        flags = (GEMM_F16_TRANS_A if ta else 0) | (GEMM_F16_TRANS_B if tb else 0)
+        by_flags.setdefault(flags, []).append((A.data_ptr(), lda, B.data_ptr(), ldb,
+                                               bias.data_ptr() if bias is not None else 0, C.data_ptr(), ldc,
+                                               M, N, K))
+        dev = C.get_device()
+    handle = _stream_handle(stream, dev)
+    for flags, probs in by_flags.items():
+        st = gemm_f16_grouped_ptr(probs, epilogue, flags, handle)
+        if st != GEMM_OK:
+            raise GemmError(st, "gemm_f16_grouped")
+    return [C for _, _, _, C in problems]
 
 
 def gemm_f16_plan(M, N, K, epilogue="none", num_sms=152, a_addr=256, b_addr=256, c_addr=256,

@@ -12,6 +12,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "gemm_f16.h"
 #include "gemm_kernels.cuh"
@@ -310,6 +311,10 @@ int init_common_locked(int dev, DeviceState& st) {
     e = cudaFuncSetAttribute(gemm_f16_tc2_kernel<kStagesPair, kKSubPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SmemPlanPair<kStagesPair, kKSubPair>::kDynamicBytes);
     if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_f16_tc2_grouped_kernel<kStagesPair, kKSubPair>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SmemPlanPair<kStagesPair, kKSubPair>::kDynamicBytes);
+    if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gemm_f16_tc_kernel<256, kStages256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SmemPlan<256, kStages256>::kDynamicBytes);
     if (e == cudaSuccess)
@@ -475,6 +480,27 @@ int launch_tc_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParam
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
 
+// Kernel parameters of one problem (split-K and tail fields left empty).
+GemmParams kernel_params(const Operands& op, const __half* biasp, int64_t M, int64_t N, int64_t K, int epilogue) {
+    GemmParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    prm.C = static_cast<__half*>(op.C);
+    prm.bias = biasp;
+    prm.M = static_cast<int>(M);
+    prm.N = static_cast<int>(N);
+    prm.K = static_cast<int>(K);
+    prm.ldc = static_cast<int>(op.ldc);
+    prm.trans_a = op.ta ? 1 : 0;
+    prm.trans_b = op.tb ? 1 : 0;
+    prm.epi = epilogue;
+    prm.vec_store = (aligned(op.C, 16) && op.ldc % 8 == 0) ? 1 : 0;
+    prm.bias_vec = (biasp != nullptr && aligned(biasp, 16)) ? 1 : 0;
+    prm.group_m = kGroupM;
+    prm.timeout_ns = g_timeout_ns;
+    prm.splits = 1;
+    return prm;
+}
+
 // Everything after scratch is settled: repack (into `scratch`, which holds
 // pl.a_scratch + pl.b_scratch bytes when a repack is planned), tensor maps,
 // and the tensor-core kernel, all on stream `s`.
@@ -513,20 +539,7 @@ int enqueue_plan(const Plan& pl, const Operands& op, const __half* biasp, int64_
                    : encode_2d(&tb, b_src, N, K, pl.ldb_packed, 64, kBK);
     }
     if (st != GEMM_OK) return st;
-    GemmParams prm;
-    prm.C = static_cast<__half*>(op.C);
-    prm.bias = biasp;
-    prm.M = static_cast<int>(M);
-    prm.N = static_cast<int>(N);
-    prm.K = static_cast<int>(K);
-    prm.ldc = static_cast<int>(op.ldc);
-    prm.trans_a = op.ta ? 1 : 0;
-    prm.trans_b = op.tb ? 1 : 0;
-    prm.epi = epilogue;
-    prm.vec_store = pl.vec_store ? 1 : 0;
-    prm.bias_vec = (biasp != nullptr && aligned(biasp, 16)) ? 1 : 0;
-    prm.group_m = kGroupM;
-    prm.timeout_ns = g_timeout_ns;
+    GemmParams prm = kernel_params(op, biasp, M, N, K, epilogue);
     prm.dp_tiles = pl.dp_tiles;
     prm.tail_split = pl.tail_split;
     prm.splits = pl.splits;
@@ -554,6 +567,32 @@ int enqueue_bias_only(const Plan& pl, const __half* biasp, void* C, int64_t ldc,
                                        epilogue);
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
+
+// ---------------------------------------------------------------- grouped GEMM
+Operands problem_operands(const gemm_f16_problem_t& q, int flags) {
+    Operands op;
+    op.A = q.A;
+    op.B = q.B;
+    op.C = q.C;
+    op.lda = q.lda;
+    op.ldb = q.ldb;
+    op.ldc = q.ldc;
+    op.ta = (flags & GEMM_F16_TRANS_A) != 0;
+    op.tb = (flags & GEMM_F16_TRANS_B) != 0;
+    return op;
+}
+
+int launch_grouped(const GroupedParams& gp, int ctas, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = launch_config(ctas, SmemPlanPair<kStagesPair, kKSubPair>::kDynamicBytes, s);
+    LaunchAttrs la(2, pdl_enabled());
+    la.apply(cfg);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_grouped_kernel<kStagesPair, kKSubPair>, gp);
+    return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+}
+
+// Kernel parameter of one grouped launch, filled per launch (the launch call
+// copies it).
+thread_local GroupedParams t_grouped;
 
 // ---------------------------------------------------------------- no-alloc variant
 // Fixed repack buffer for gemm_f16_noalloc, part of the module image: every
@@ -724,6 +763,118 @@ int gemm_f16_noalloc(const void* A, const void* B, const void* bias, void* C, in
         pl = make_plan(op, M, N, K, ds.num_sms, ds.pair_clusters, g_force_config.load(), false);
     if (pl.scratch_bytes() > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
     return enqueue_plan(pl, op, biasp, M, N, K, epilogue, ds.noalloc_scratch, s);
+}
+
+int gemm_f16_grouped(const gemm_f16_problem_t* problems, int count, int epilogue, int flags, void* cuda_stream) {
+    if (count < 0 || (count > 0 && problems == nullptr)) return GEMM_ERR_INVALID_ARG;
+    if (flags & ~(GEMM_F16_TRANS_A | GEMM_F16_TRANS_B)) return GEMM_ERR_INVALID_ARG;
+    for (int i = 0; i < count; ++i) {
+        const gemm_f16_problem_t& q = problems[i];
+        const int st = check_args(problem_operands(q, flags), q.bias, q.M, q.N, q.K, epilogue);
+        if (st != GEMM_OK) return st;
+    }
+    bool any = false;
+    for (int i = 0; i < count; ++i) any = any || (problems[i].M > 0 && problems[i].N > 0);
+    if (!any) return GEMM_OK;   // nothing to compute: no CUDA call
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int st = init_device(dev);
+    if (st != GEMM_OK) return st;
+    const DeviceState& ds = g_dev[dev];
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+
+    // Repack scratch for every operand a tensor map cannot describe, in one
+    // stream-ordered allocation: [problem 0 A][problem 0 B][problem 1 A] ...
+    struct Prep {
+        Operands op;
+        Plan pl;          // repack decisions and pitches (tile fields unused)
+        size_t off = 0;   // this problem's scratch offset
+    };
+    Prep* prep = new (std::nothrow) Prep[count > 0 ? count : 1];
+    if (prep == nullptr) return GEMM_ERR_NO_MEMORY;
+    size_t scratch_bytes = 0;
+    for (int i = 0; i < count; ++i) {
+        const gemm_f16_problem_t& q = problems[i];
+        prep[i].op = problem_operands(q, flags);
+        prep[i].pl = make_plan(prep[i].op, q.M, q.N, q.K, ds.num_sms, ds.pair_clusters, CFG_PAIR_256_WHOLE, false);
+        prep[i].off = scratch_bytes;
+        scratch_bytes += prep[i].pl.a_scratch + prep[i].pl.b_scratch;
+    }
+    uint8_t* scratch = nullptr;
+    if (scratch_bytes > 0) {
+        st = ensure_pool(dev);
+        if (st == GEMM_OK) {
+            void* ptr = nullptr;
+            e = cudaMallocFromPoolAsync(&ptr, scratch_bytes, ds.pool, s);
+            if (e != cudaSuccess) {
+                t_last_cuda_error = static_cast<int>(e);
+                cudaGetLastError();
+                st = GEMM_ERR_NO_MEMORY;
+            }
+            scratch = static_cast<uint8_t*>(ptr);
+        }
+    }
+    GroupedParams& gp = t_grouped;
+    gp.count = 0;
+    gp.tile_start[0] = 0;
+    auto flush = [&]() -> int {
+        if (gp.count == 0) return GEMM_OK;
+        const int tiles = gp.tile_start[gp.count];
+        const int ctas = 2 * std::min(tiles, std::max(1, ds.pair_clusters));
+        const int r = launch_grouped(gp, ctas, s);
+        gp.count = 0;
+        return r;
+    };
+    for (int i = 0; st == GEMM_OK && i < count; ++i) {
+        const gemm_f16_problem_t& q = problems[i];
+        const Prep& pr = prep[i];
+        if (q.M == 0 || q.N == 0) continue;
+        const __half* biasp = epilogue == GEMM_EPI_NONE ? nullptr : static_cast<const __half*>(q.bias);
+        if (q.K == 0) {
+            Plan bl;
+            bl.path = 1;
+            bl.ctas = static_cast<int>(std::min<int64_t>((q.M * q.N + 255) / 256, int64_t(ds.num_sms) * 8));
+            st = enqueue_bias_only(bl, biasp, q.C, q.ldc, q.M, q.N, epilogue, s);
+            continue;
+        }
+        const int64_t tiles = ((q.M + 255) / 256) * ((q.N + 255) / 256);   // < 2^28 by check_args
+        if (int64_t(gp.tile_start[gp.count]) + tiles >= (int64_t(1) << 31)) {
+            st = flush();   // keep every tile index of a launch an int
+            if (st != GEMM_OK) break;
+        }
+        const void* a_src = q.A;
+        const void* b_src = q.B;
+        if (pr.pl.pack_a) {
+            uint16_t* dst = reinterpret_cast<uint16_t*>(scratch + pr.off);
+            st = launch_repack(dst, q.A, pr.op.a_rows(q.M, q.K), pr.op.a_cols(q.M, q.K), q.lda, pr.pl.lda_packed, s);
+            a_src = dst;
+        }
+        if (st == GEMM_OK && pr.pl.pack_b) {
+            uint16_t* dst = reinterpret_cast<uint16_t*>(scratch + pr.off + pr.pl.a_scratch);
+            st = launch_repack(dst, q.B, pr.op.b_rows(q.N, q.K), pr.op.b_cols(q.N, q.K), q.ldb, pr.pl.ldb_packed, s);
+            b_src = dst;
+        }
+        if (st != GEMM_OK) break;
+        const int j = gp.count;
+        st = pr.op.ta ? encode_2d(&gp.tmA[j], a_src, q.M, q.K, pr.pl.lda_packed, 64, kBK)
+                      : encode_2d(&gp.tmA[j], a_src, q.K, q.M, pr.pl.lda_packed, kBK, kBM);
+        if (st == GEMM_OK)
+            st = pr.op.tb ? encode_2d(&gp.tmB[j], b_src, q.K, q.N, pr.pl.ldb_packed, kBK, 64)
+                          : encode_2d(&gp.tmB[j], b_src, q.N, q.K, pr.pl.ldb_packed, 64, kBK);
+        if (st != GEMM_OK) break;
+        gp.prob[j] = kernel_params(pr.op, biasp, q.M, q.N, q.K, epilogue);
+        gp.tile_start[j + 1] = gp.tile_start[j] + static_cast<int>(tiles);
+        gp.count = j + 1;
+        if (gp.count == kMaxGroupProblems) st = flush();
+    }
+    if (st == GEMM_OK) st = flush();
+    if (scratch != nullptr) {
+        e = cudaFreeAsync(scratch, s);   // stream-ordered: after every launch above has read it
+        if (e != cudaSuccess && st == GEMM_OK) st = cuda_fail(e);
+    }
+    delete[] prep;
+    return st;
 }
 
 int gemm_f16_debug_status(void* cuda_stream, uint32_t* detail) {

@@ -116,6 +116,40 @@ int gemm_f16_ex(const void* A, int64_t lda, const void* B, int64_t ldb, const vo
                 int64_t ldc, int64_t M, int64_t N, int64_t K, int epilogue, int flags,
                 void* cuda_stream);
 
+/*
+ * One problem of a grouped call: the arguments of gemm_f16_ex (pitches in
+ * elements; the layout flags are the call's).
+ */
+typedef struct gemm_f16_problem {
+    const void* A;
+    int64_t lda;
+    const void* B;
+    int64_t ldb;
+    const void* bias;   /* required unless the epilogue is GEMM_EPI_NONE */
+    void* C;
+    int64_t ldc;
+    int64_t M, N, K;
+} gemm_f16_problem_t;
+
+/*
+ * gemm_f16_grouped -- many independent GEMMs in one persistent launch (the
+ * "grouped GEMM" of the tilelang documentation's advanced examples):
+ *
+ *   C_g = epilogue(A_g . B_g + bias_g)   for g = 0 .. count-1,
+ *
+ * each problem with its own sizes, pointers and pitches, all with the same
+ * epilogue and operand-layout flags (see gemm_f16_ex).  `problems` is a HOST
+ * array, read during the call only.  Every problem is checked first; any
+ * argument error returns before anything is enqueued.  Problems with M or N
+ * of 0 are skipped; K == 0 problems get C_g = epilogue(bias_g).  The tiles of
+ * all problems (256 x 256, CTA pairs) are scheduled together, up to 64
+ * problems per launch (more take further launches on the same stream).
+ * Problems must not write each other's C or read another problem's C.
+ * No counterpart beyond the name on the pages; the numerics are gemm_f16's.
+ */
+int gemm_f16_grouped(const gemm_f16_problem_t* problems, int count, int epilogue, int flags,
+                     void* cuda_stream);
+
 /* Static, human-readable name of a status code. */
 const char* gemm_f16_status_string(int status);
 

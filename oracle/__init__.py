@@ -160,3 +160,19 @@ def gemm_elems(A, B, bias, epilogue, ii, jj, threads: int = 0, want_f64: bool = 
         raise ValueError("oracle_gemm_elems: bad arguments")
     out = out.view(np.float16)
     return (out, f64) if want_f64 else out
+
+
+def gemm_grouped(problems, epilogue, threads: int = 0):
+    """Grouped GEMM ("grouped GEMM" in the tilelang documentation's advanced
+    examples: many independent GEMMs in one launch).  By definition each
+    problem's C_g = epilogue(A_g . B_g + bias_g) on its own, so this is `gemm`
+    applied to every (A_g, B_g, bias_g) of `problems` in turn; an empty
+    problem (M or N of 0) gives an empty C_g."""
+    out = []
+    for A, B, bias in problems:
+        M, N = np.shape(A)[0], np.shape(B)[1]
+        if M == 0 or N == 0:
+            out.append(np.zeros((M, N), np.float16))
+        else:
+            out.append(gemm(A, B, bias if _epi(epilogue) != 0 else None, epilogue, threads))
+    return out

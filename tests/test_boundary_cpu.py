@@ -225,7 +225,25 @@ def test_binding_layout_detection():
     assert lay(X[:, :7].t(), "X") == (True, 10)
     assert lay(X[:1], "X") == (False, 10)
     assert lay(torch.zeros(10, 1, dtype=torch.float16).t(), "X") == (False, 10)   # 1 x 10, any row stride
+    assert lay(torch.zeros(0, 64, dtype=torch.float16).expand(0, 64), "X") == (False, 64)   # empty: any strides
     with pytest.raises(ValueError):
         lay(X[:, ::2], "X")                   # neither rows nor columns contiguous
     with pytest.raises(ValueError):
         lay(torch.zeros(10, dtype=torch.float16).expand(4, 10), "X")   # rows overlap (stride 0)
+
+
+# ---------------------------------------------------------------- gemm_f16_grouped
+
+def test_grouped_argument_errors_need_no_device(g):
+    ok = (GOOD, 64, GOOD, 64, GOOD, GOOD, 64, 64, 64, 64)
+    assert g.gemm_f16_grouped_ptr([], "bias", 0, 0) == 0                  # nothing to do
+    assert g.gemm_f16_grouped_ptr([ok], "bias", 4, 0) == 1                # unknown flag
+    assert g.gemm_f16_grouped_ptr([ok], 9, 0, 0) == 1                     # unknown epilogue
+    bad_pitch = (GOOD, 63, GOOD, 64, GOOD, GOOD, 64, 64, 64, 64)           # lda < K
+    assert g.gemm_f16_grouped_ptr([ok, ok, bad_pitch], "bias", 0, 0) == 1
+    no_bias = (GOOD, 64, GOOD, 64, 0, GOOD, 64, 64, 64, 64)
+    assert g.gemm_f16_grouped_ptr([ok, no_bias], "bias", 0, 0) == 1
+    odd_c = (GOOD, 64, GOOD, 64, GOOD, GOOD + 1, 64, 64, 64, 64)
+    assert g.gemm_f16_grouped_ptr([odd_c], "bias", 0, 0) == 3
+    assert g.lib.gemm_f16_grouped(None, 2, 0, 0, None) == 1              # null array, count > 0
+    assert g.lib.gemm_f16_grouped(None, -1, 0, 0, None) == 1

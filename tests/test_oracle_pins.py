@@ -325,6 +325,48 @@ def test_bad_arguments_rejected(oracle_mod):
         oracle_mod.gemm_rows(A, B, None, "none", [5])   # row out of range
 
 
+# ---------------------------------------------------------------- grouped GEMM
+
+def _block_diag(blocks, rows_cols):
+    R = sum(r for r, _ in rows_cols)
+    C = sum(c for _, c in rows_cols)
+    out = np.zeros((R, C), np.float16)
+    r0 = c0 = 0
+    for b, (r, c) in zip(blocks, rows_cols):
+        out[r0:r0 + r, c0:c0 + c] = b
+        r0, c0 = r0 + r, c0 + c
+    return out
+
+
+@pytest.mark.parametrize("epi", ["none", "bias_relu", "bias_gelu_erf"])
+def test_grouped_is_the_block_diagonal_product(oracle_mod, epi):
+    # stacking the problems block-diagonally turns them into ONE GEMM whose
+    # diagonal blocks are the problems' products and whose off-diagonal
+    # blocks are epilogue(0 + bias): an independent construction of what a
+    # grouped call must return (a mixed-up operand or bias fails it)
+    rng = np.random.default_rng(40)
+    shapes = [(5, 7, 3), (1, 9, 12), (8, 2, 5), (4, 6, 1)]
+    probs = [(_rand16(rng, (M, K)), _rand16(rng, (K, N)), _rand16(rng, N)) for M, N, K in shapes]
+    got = oracle_mod.gemm_grouped(probs, epi)
+    Abig = _block_diag([a for a, _, _ in probs], [(M, K) for M, N, K in shapes])
+    Bbig = _block_diag([b for _, b, _ in probs], [(K, N) for M, N, K in shapes])
+    bias_big = np.concatenate([c for _, _, c in probs])
+    big = oracle_mod.gemm(Abig, Bbig, bias_big if epi != "none" else None, epi)
+    r0 = c0 = 0
+    for (M, N, K), g in zip(shapes, got):
+        assert np.array_equal(g.view(np.uint16), big[r0:r0 + M, c0:c0 + N].view(np.uint16))
+        r0, c0 = r0 + M, c0 + N
+
+
+def test_grouped_empty_and_k_zero_problems(oracle_mod):
+    rng = np.random.default_rng(41)
+    bias = _rand16(rng, 4)
+    out = oracle_mod.gemm_grouped([(np.zeros((0, 3), np.float16), np.zeros((3, 4), np.float16), bias),
+                                   (np.zeros((2, 0), np.float16), np.zeros((0, 4), np.float16), bias)], "bias_relu")
+    assert out[0].shape == (0, 4)
+    assert np.array_equal(out[1].view(np.uint16), np.broadcast_to(np.maximum(bias, 0), (2, 4)).view(np.uint16))
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def test_planted_transpose_is_caught(oracle_mod):
