@@ -96,6 +96,239 @@ struct PairUnitIter {
     }
 };
 
+template <int STAGES, int KSUB>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const GemmParams p) {
+    using SP = SmemPlanPair<STAGES, KSUB>;
+    constexpr int kStageK = KSUB * kBK;      // K per pipeline stage
+    constexpr int PM = 256;                  // pair tile rows = MMA M
+    constexpr int BN = 256;                  // pair tile columns = MMA N
+    constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators of 256 fp32 columns
+    const bool ta = p.trans_a != 0, tb = p.trans_b != 0;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;   // identical in both CTAs of the pair
+    uint8_t* base = smem_raw + (base_s - raw_s);
+
+    const uint32_t sA = base_s + SP::kA;
+    const uint32_t sB = base_s + SP::kB;
+    const uint32_t bars = base_s + SP::kBars;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
+    auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bars + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + SP::kTmemSlot);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + SP::kAbort);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);      // CTA 0's producer arrives; both CTAs' bytes complete it
+            mbar_init(empty_bar(s), 1);     // one multicast MMA commit
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);      // one multicast MMA commit
+            mbar_init(acce_bar(b), 2 * kEpiWarps);   // epilogue warps of both CTAs (used on CTA 0)
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish_pair();
+        tc_fence_before();
+    }
+    __syncthreads();
+    cluster_sync_all();     // both CTAs' barriers exist before any cross-CTA arrive or complete_tx
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    // set-up above overlaps the previous kernel; global memory only from here
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    const int tiles_m = (p.M + PM - 1) / PM;
+    const int tiles_n = (p.N + BN - 1) / BN;
+    const int num_tiles = tiles_m * tiles_n;
+    const int kblocks = (p.K + kStageK - 1) / kStageK;   // pipeline stages per tile
+    const int cid = blockIdx.x >> 1;
+    const int nclusters = gridDim.x >> 1;
+    auto units = [&]() { return PairUnitIter(cid, nclusters, p.dp_tiles, num_tiles, p.tail_split); };
+    unsigned int* status = &g_status;
+
+    // Boxes each CTA loads for a tile: its A rows unless all are past M (one
+    // 128-row K-major box, or, with A stored K x M, those of its two 64-row
+    // boxes that start before M), and those of its two 64-column B boxes that
+    // start before N.  The skipped ones would only feed accumulator rows /
+    // columns that are never stored.
+    auto a_boxes = [&](int m0, int r) {
+        return ta ? max(0, min(2, (p.M - (m0 + 128 * r) + 63) / 64)) : ((m0 + 128 * r) < p.M ? 1 : 0);
+    };
+    auto a_bytes = [&](int m0, int r) {
+        return static_cast<uint32_t>(a_boxes(m0, r)) * (ta ? kBBoxBytes : kATileBytes);
+    };
+    auto b_live = [&](int n0, int r) { return max(0, min(2, (p.N - (n0 + 128 * r) + 63) / 64)); };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            PairUnitIter it = units();
+            PairUnit un;
+            while (ok && it.next(un)) {
+                const TileCoord tc = tile_coord_bm(un.tile, tiles_m, tiles_n, p.group_m, PM, BN);
+                const int my_a = a_boxes(tc.m0, rank);
+                // a whole tile: CTA r loads columns n0 + 128r (two boxes); a half
+                // tile h: CTA r loads the one box at n0 + 128h + 64r
+                const int bcol = un.half < 0 ? tc.n0 + 128 * static_cast<int>(rank) : tc.n0 + 128 * un.half + 64 * static_cast<int>(rank);
+                auto live = [&](int r) {
+                    return un.half < 0 ? b_live(tc.n0, r) : (tc.n0 + 128 * un.half + 64 * r < p.N ? 1 : 0);
+                };
+                const int my_b = live(rank);
+                // every sub-block's boxes are issued, also those starting past K
+                // (they arrive as zeros), so each stage carries the same bytes
+                const uint32_t pair_bytes = KSUB * (a_bytes(tc.m0, 0) + a_bytes(tc.m0, 1) +
+                                                    static_cast<uint32_t>(live(0) + live(1)) * kBBoxBytes);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_cluster_bounded(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, status,
+                                                   ROLE_PRODUCER, BAR_EMPTY)) { ok = false; break; }
+                    const uint32_t full_leader = mapa_shared(full_bar(stage), 0);
+                    if (leader) mbar_arrive_expect_tx(full_bar(stage), pair_bytes);
+                    for (int ks = 0; ks < KSUB; ++ks) {
+                        const int k0 = kb * kStageK + ks * kBK;
+                        const uint32_t a_dst = sA + stage * SP::kAStage + ks * kATileBytes;
+                        const int arow = tc.m0 + 128 * static_cast<int>(rank);
+                        if (ta) {
+                            for (int c = 0; c < my_a; ++c)
+                                tma_load_box_pair(a_dst + c * kBBoxBytes, &tmA, full_leader, false, arow + 64 * c, k0);
+                        } else if (my_a) {
+                            tma_load_2d_pair(a_dst, &tmA, full_leader, k0, arow);
+                        }
+                        for (int c = 0; c < my_b; ++c)
+                            tma_load_box_pair(sB + stage * SP::kBStage + ks * kBHalfSubBytes + c * kBBoxBytes, &tmB,
+                                              full_leader, tb, bcol + 64 * c, k0);
+                    }
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // CTA 0's full barriers count both CTAs' bytes: draining them there
+            // covers every load of the pair still in flight.
+            if (leader) {
+                const int pending = min(issued, STAGES);
+                for (int i = 0; i < pending; ++i) {
+                    if (--stage < 0) { stage = STAGES - 1; phase ^= 1u; }
+                    mbar_wait_cluster_bounded(full_bar(stage), phase, p.timeout_ns, nullptr, status, ROLE_DRAIN,
+                                              BAR_FULL);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (CTA 0 only)
+        if (leader && lane == 0) {
+            const uint32_t idesc_whole = idesc_f16_f32(PM, BN, /*b_mn_major=*/!tb, /*a_mn_major=*/ta);
+            const uint32_t idesc_half = idesc_f16_f32(PM, BN / 2, !tb, ta);   // 256 x 128 units
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            PairUnitIter it = units();
+            PairUnit un;
+            while (ok && it.next(un)) {
+                if (!mbar_wait_cluster_bounded(acce_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag, status,
+                                               ROLE_MMA, BAR_ACC_EMPTY)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                const uint32_t idesc = un.half < 0 ? idesc_whole : idesc_half;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_cluster_bounded(full_bar(stage), phase, p.timeout_ns, abort_flag, status,
+                                                   ROLE_MMA, BAR_FULL)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < KSUB; ++ks) {
+                        const uint32_t a0 = sA + stage * SP::kAStage + ks * kATileBytes;
+                        const uint32_t b0 = sB + stage * SP::kBStage + ks * kBHalfSubBytes;
+#pragma unroll
+                        for (int k = 0; k < kBK / kUMMA_K; ++k) {
+                            // same layouts as the single-SM kernel; B here is this
+                            // CTA's 128 columns (two 64-column boxes)
+                            const uint64_t adesc = operand_desc(a0, k, ta);
+                            const uint64_t bdesc = operand_desc(b0, k, !tb);
+                            tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | ks | k) != 0 ? 1u : 0u);
+                        }
+                    }
+                    tc_commit_pair_mc(empty_bar(stage), 0x3);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit_pair_mc(accf_bar(acc), 0x3);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            tc_commit_pair_mc(drain_bar, 0x1);
+            mbar_wait_bounded(drain_bar, 0, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_DRAIN);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
+        const uint32_t acce_leader1 = mapa_shared(acce_bar(1), 0);
+        PairUnitIter it = units();
+        PairUnit un;
+        while (it.next(un)) {
+            const TileCoord tc = tile_coord_bm(un.tile, tiles_m, tiles_n, p.group_m, PM, BN);
+            const int half = (warp - 2) >> 2;   // which half of the unit's columns this warp takes
+            const int ucols = un.half < 0 ? BN : BN / 2;                       // the unit's width
+            const int un0 = un.half < 0 ? tc.n0 : tc.n0 + (BN / 2) * un.half;  // its first column
+            uint32_t* stage = reinterpret_cast<uint32_t*>(base + SP::kStage + (warp - 2) * kStageWarpBytes);
+            if (p.epi != EPI_NONE) stage_bias(p, stage + kStageBlockWords, un0 + half * (ucols / 2), ucols / 2);
+            const bool ready = mbar_wait_cluster_bounded(accf_bar(acc), acc_phase, p.timeout_ns, abort_flag, status,
+                                                         ROLE_EPILOGUE, BAR_ACC_FULL);
+            if (!__all_sync(0xffffffffu, ready)) break;
+            tc_fence_after();
+            const uint32_t t_base = tmem_base + static_cast<uint32_t>(acc * BN + half * (ucols / 2)) +
+                                    (static_cast<uint32_t>(32 * q) << 16);
+            const int row0 = tc.m0 + 128 * static_cast<int>(rank) + 32 * q;
+            if (un.half < 0)
+                epilogue_rows<BN / 2>(p, t_base, row0, un0 + half * (BN / 2), stage);
+            else
+                epilogue_rows<BN / 4>(p, t_base, row0, un0 + half * (BN / 4), stage);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc == 0 ? acce_leader0 : acce_leader1);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    __syncthreads();
+    cluster_sync_all();     // the peer no longer touches this CTA's shared or tensor memory
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+
+// ---------------------------------------------------------------- grouped launch
+
 // A unit of a CTA pair's work as a work source hands it out.
 struct PairJob {
     const CUtensorMap* tmA;
@@ -103,32 +336,6 @@ struct PairJob {
     int prob;     // which problem (its GemmParams)
     int m0, n0;   // the tile's first row and column
     int half;     // -1: the whole 256 x 256 tile; 0 / 1: its 256 x 128 column half
-};
-
-// Work source of one problem: PairUnitIter over its tiles in grouped raster
-// order (whole tiles, then the half-tile units of a partial last wave).
-struct SinglePairSource {
-    const CUtensorMap* tmA;
-    const CUtensorMap* tmB;
-    const GemmParams* p;
-    int tiles_m, tiles_n;
-    PairUnitIter it;
-    __device__ SinglePairSource(const CUtensorMap* a, const CUtensorMap* b, const GemmParams* p_, int cid, int G)
-        : tmA(a), tmB(b), p(p_), tiles_m((p_->M + 255) / 256), tiles_n((p_->N + 255) / 256),
-          it(cid, G, p_->dp_tiles, ((p_->M + 255) / 256) * ((p_->N + 255) / 256), p_->tail_split) {}
-    __device__ bool next(PairJob& j) {
-        PairUnit u;
-        if (!it.next(u)) return false;
-        const TileCoord tc = tile_coord_bm(u.tile, tiles_m, tiles_n, p->group_m, 256, 256);
-        j.tmA = tmA;
-        j.tmB = tmB;
-        j.prob = 0;
-        j.m0 = tc.m0;
-        j.n0 = tc.n0;
-        j.half = u.half;
-        return true;
-    }
-    __device__ const GemmParams& params(int) const { return *p; }
 };
 
 // Independent problems of one grouped launch (at most kMaxGroupProblems, all
@@ -168,10 +375,14 @@ struct GroupedPairSource {
     __device__ const GemmParams& params(int g) const { return gp->prob[g]; }
 };
 
-// The CTA-pair GEMM over the units of a work source.  `cp` holds the
-// settings every unit shares (epilogue kind, operand layouts, wait limit).
+// The CTA-pair GEMM over the units of a work source (the grouped launch).
+// `cp` holds the settings every unit shares (epilogue kind, operand
+// layouts, wait limit).  Same roles, barriers and layouts as
+// gemm_f16_tc2_kernel above, with each unit's operands and parameters taken
+// from the source.  The single-problem kernel keeps its own body: routing it
+// through this template measured 1-3 % slower on the large squares.
 template <int STAGES, int KSUB, class Src>
-__device__ __forceinline__ void pair_gemm(const Src& src, const GemmParams& cp) {
+__device__ __forceinline__ void pair_gemm(const Src& src, const GemmParams cp) {
 
     using SP = SmemPlanPair<STAGES, KSUB>;
     constexpr int kStageK = KSUB * kBK;      // K per pipeline stage
@@ -261,7 +472,7 @@ __device__ __forceinline__ void pair_gemm(const Src& src, const GemmParams& cp) 
             Src it = src;
             PairJob un;
             while (ok && it.next(un)) {
-                const GemmParams& pp = it.params(un.prob);
+                const GemmParams pp = it.params(un.prob);   // by value: kept in registers
                 const TileCoord tc{un.m0, un.n0};
                 const int kblocks = kblocks_of(pp);
                 const int my_a = a_boxes(pp.M, tc.m0, rank);
@@ -368,7 +579,7 @@ __device__ __forceinline__ void pair_gemm(const Src& src, const GemmParams& cp) 
         Src it = src;
         PairJob un;
         while (it.next(un)) {
-            const GemmParams& pp = it.params(un.prob);
+            const GemmParams pp = it.params(un.prob);   // by value: kept in registers
             const TileCoord tc{un.m0, un.n0};
             const int half = (warp - 2) >> 2;   // which half of the unit's columns this warp takes
             const int ucols = un.half < 0 ? BN : BN / 2;                       // the unit's width
@@ -401,14 +612,6 @@ __device__ __forceinline__ void pair_gemm(const Src& src, const GemmParams& cp) 
     }
 }
 
-
-template <int STAGES, int KSUB>
-__global__ void __launch_bounds__(kThreads, 1)
-gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ GemmParams p) {
-    const SinglePairSource src(&tmA, &tmB, &p, static_cast<int>(blockIdx.x >> 1), static_cast<int>(gridDim.x >> 1));
-    pair_gemm<STAGES, KSUB>(src, p);
-}
 
 // Grouped GEMM: C_g = epilogue(A_g . B_g + bias_g) for every problem g of
 // `gp` in one persistent launch.
