@@ -13,6 +13,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <type_traits>
 
 #include "gemm_f16.h"
 #include "gemm_kernels.cuh"
@@ -87,6 +88,19 @@ bool pdl_enabled() {
         v = g_pdl.load(std::memory_order_relaxed);
     }
     return v != 0;
+}
+
+// Calls f(std::integral_constant<int, E>) for every epilogue kind E in
+// order; stops at and returns the first error.
+template <class F>
+cudaError_t for_each_epilogue(F f) {
+    cudaError_t e = f(std::integral_constant<int, GEMM_EPI_NONE>());
+    if (e == cudaSuccess) e = f(std::integral_constant<int, GEMM_EPI_BIAS>());
+    if (e == cudaSuccess) e = f(std::integral_constant<int, GEMM_EPI_BIAS_RELU>());
+    if (e == cudaSuccess) e = f(std::integral_constant<int, GEMM_EPI_BIAS_GELU_ERF>());
+    if (e == cudaSuccess) e = f(std::integral_constant<int, GEMM_EPI_BIAS_SIGMOID>());
+    if (e == cudaSuccess) e = f(std::integral_constant<int, GEMM_EPI_BIAS_GELU_TANH>());
+    return e;
 }
 
 int cuda_fail(cudaError_t e) {
@@ -308,12 +322,16 @@ int init_common_locked(int dev, DeviceState& st) {
             return cuda_fail(e != cudaSuccess ? e : cudaErrorSymbolNotFound);
         g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    e = cudaFuncSetAttribute(gemm_f16_tc2_kernel<kStagesPair, kKSubPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SmemPlanPair<kStagesPair, kKSubPair>::kDynamicBytes);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemm_f16_tc2_grouped_kernel<kStagesPair, kKSubPair>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SmemPlanPair<kStagesPair, kKSubPair>::kDynamicBytes);
+    e = for_each_epilogue([](auto epi) {
+        constexpr int E = decltype(epi)::value;
+        constexpr uint32_t smem = SmemPlanPair<kStagesPair, kKSubPair>::kDynamicBytes;
+        cudaError_t r = cudaFuncSetAttribute(gemm_f16_tc2_kernel<kStagesPair, kKSubPair, E>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(gemm_f16_tc2_grouped_kernel<kStagesPair, kKSubPair, E>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        return r;
+    });
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gemm_f16_tc_kernel<256, kStages256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SmemPlan<256, kStages256>::kDynamicBytes);
@@ -344,7 +362,8 @@ int init_common_locked(int dev, DeviceState& st) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(gemm_f16_tc2_kernel<kStagesPair, kKSubPair>),
+        if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(
+                                               gemm_f16_tc2_kernel<kStagesPair, kKSubPair, GEMM_EPI_BIAS_GELU_ERF>),
                                            &cfg) != cudaSuccess || n <= 0) {
             cudaGetLastError();
             n = sms / 2;
@@ -476,7 +495,24 @@ int launch_tc_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParam
     cudaLaunchConfig_t cfg = launch_config(ctas, SmemPlanPair<kStagesPair, kKSubPair>::kDynamicBytes, s);
     LaunchAttrs la(2, pdl_enabled());
     la.apply(cfg);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_kernel<kStagesPair, kKSubPair>, ta, tb, prm);
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (prm.epi) {
+        case GEMM_EPI_NONE: e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_kernel<kStagesPair, kKSubPair, 0>, ta, tb, prm); break;
+        case GEMM_EPI_BIAS: e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_kernel<kStagesPair, kKSubPair, 1>, ta, tb, prm); break;
+        case GEMM_EPI_BIAS_RELU:
+            e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_kernel<kStagesPair, kKSubPair, 2>, ta, tb, prm);
+            break;
+        case GEMM_EPI_BIAS_GELU_ERF:
+            e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_kernel<kStagesPair, kKSubPair, 3>, ta, tb, prm);
+            break;
+        case GEMM_EPI_BIAS_SIGMOID:
+            e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_kernel<kStagesPair, kKSubPair, 4>, ta, tb, prm);
+            break;
+        case GEMM_EPI_BIAS_GELU_TANH:
+            e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_kernel<kStagesPair, kKSubPair, 5>, ta, tb, prm);
+            break;
+        default: break;
+    }
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
 
@@ -586,7 +622,24 @@ int launch_grouped(const GroupedParams& gp, int ctas, cudaStream_t s) {
     cudaLaunchConfig_t cfg = launch_config(ctas, SmemPlanPair<kStagesPair, kKSubPair>::kDynamicBytes, s);
     LaunchAttrs la(2, pdl_enabled());
     la.apply(cfg);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_grouped_kernel<kStagesPair, kKSubPair>, gp);
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (gp.prob[0].epi) {
+        case GEMM_EPI_NONE: e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_grouped_kernel<kStagesPair, kKSubPair, 0>, gp); break;
+        case GEMM_EPI_BIAS: e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_grouped_kernel<kStagesPair, kKSubPair, 1>, gp); break;
+        case GEMM_EPI_BIAS_RELU:
+            e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_grouped_kernel<kStagesPair, kKSubPair, 2>, gp);
+            break;
+        case GEMM_EPI_BIAS_GELU_ERF:
+            e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_grouped_kernel<kStagesPair, kKSubPair, 3>, gp);
+            break;
+        case GEMM_EPI_BIAS_SIGMOID:
+            e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_grouped_kernel<kStagesPair, kKSubPair, 4>, gp);
+            break;
+        case GEMM_EPI_BIAS_GELU_TANH:
+            e = cudaLaunchKernelEx(&cfg, gemm_f16_tc2_grouped_kernel<kStagesPair, kKSubPair, 5>, gp);
+            break;
+        default: break;
+    }
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
 

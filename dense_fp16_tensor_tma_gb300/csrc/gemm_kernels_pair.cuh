@@ -96,7 +96,9 @@ struct PairUnitIter {
     }
 };
 
-template <int STAGES, int KSUB>
+// EPI: the epilogue kind (p.epi), fixed at compile time so that the
+// epilogue warps run one activation with no dispatch.
+template <int STAGES, int KSUB, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams p) {
@@ -243,6 +245,7 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (leader && lane == 0) {
             const uint32_t idesc_whole = idesc_f16_f32(PM, BN, /*b_mn_major=*/!tb, /*a_mn_major=*/ta);
             const uint32_t idesc_half = idesc_f16_f32(PM, BN / 2, !tb, ta);   // 256 x 128 units
+            const uint64_t a_step = desc_step(ta), b_step = desc_step(!tb);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -262,16 +265,14 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < KSUB; ++ks) {
-                        const uint32_t a0 = sA + stage * SP::kAStage + ks * kATileBytes;
-                        const uint32_t b0 = sB + stage * SP::kBStage + ks * kBHalfSubBytes;
+                        // same layouts as the single-SM kernel; B here is this
+                        // CTA's 128 columns (two 64-column boxes)
+                        const uint64_t a_desc = desc_base(sA + stage * SP::kAStage + ks * kATileBytes, ta);
+                        const uint64_t b_desc = desc_base(sB + stage * SP::kBStage + ks * kBHalfSubBytes, !tb);
 #pragma unroll
-                        for (int k = 0; k < kBK / kUMMA_K; ++k) {
-                            // same layouts as the single-SM kernel; B here is this
-                            // CTA's 128 columns (two 64-column boxes)
-                            const uint64_t adesc = operand_desc(a0, k, ta);
-                            const uint64_t bdesc = operand_desc(b0, k, !tb);
-                            tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | ks | k) != 0 ? 1u : 0u);
-                        }
+                        for (int k = 0; k < kBK / kUMMA_K; ++k)
+                            tc_mma_f16_pair(d_tmem, a_desc + k * a_step, b_desc + k * b_step, idesc,
+                                            (kb | ks | k) != 0 ? 1u : 0u);
                     }
                     tc_commit_pair_mc(empty_bar(stage), 0x3);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -299,7 +300,7 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int ucols = un.half < 0 ? BN : BN / 2;                       // the unit's width
             const int un0 = un.half < 0 ? tc.n0 : tc.n0 + (BN / 2) * un.half;  // its first column
             uint32_t* stage = reinterpret_cast<uint32_t*>(base + SP::kStage + (warp - 2) * kStageWarpBytes);
-            if (p.epi != EPI_NONE) stage_bias(p, stage + kStageBlockWords, un0 + half * (ucols / 2), ucols / 2);
+            if (EPI != EPI_NONE) stage_bias(p, stage + kStageBlockWords, un0 + half * (ucols / 2), ucols / 2);
             const bool ready = mbar_wait_cluster_bounded(accf_bar(acc), acc_phase, p.timeout_ns, abort_flag, status,
                                                          ROLE_EPILOGUE, BAR_ACC_FULL);
             if (!__all_sync(0xffffffffu, ready)) break;
@@ -308,9 +309,9 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                                     (static_cast<uint32_t>(32 * q) << 16);
             const int row0 = tc.m0 + 128 * static_cast<int>(rank) + 32 * q;
             if (un.half < 0)
-                epilogue_rows<BN / 2>(p, t_base, row0, un0 + half * (BN / 2), stage);
+                epilogue_rows_act<BN / 2, EPI, EPI != EPI_NONE>(p, t_base, row0, un0 + half * (BN / 2), stage);
             else
-                epilogue_rows<BN / 4>(p, t_base, row0, un0 + half * (BN / 4), stage);
+                epilogue_rows_act<BN / 4, EPI, EPI != EPI_NONE>(p, t_base, row0, un0 + half * (BN / 4), stage);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acc == 0 ? acce_leader0 : acce_leader1);
@@ -381,7 +382,7 @@ struct GroupedPairSource {
 // gemm_f16_tc2_kernel above, with each unit's operands and parameters taken
 // from the source.  The single-problem kernel keeps its own body: routing it
 // through this template measured 1-3 % slower on the large squares.
-template <int STAGES, int KSUB, class Src>
+template <int STAGES, int KSUB, int EPI, class Src>
 __device__ __forceinline__ void pair_gemm(const Src& src, const GemmParams cp) {
 
     using SP = SmemPlanPair<STAGES, KSUB>;
@@ -527,6 +528,7 @@ __device__ __forceinline__ void pair_gemm(const Src& src, const GemmParams cp) {
         if (leader && lane == 0) {
             const uint32_t idesc_whole = idesc_f16_f32(PM, BN, /*b_mn_major=*/!tb, /*a_mn_major=*/ta);
             const uint32_t idesc_half = idesc_f16_f32(PM, BN / 2, !tb, ta);   // 256 x 128 units
+            const uint64_t a_step = desc_step(ta), b_step = desc_step(!tb);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -547,16 +549,14 @@ __device__ __forceinline__ void pair_gemm(const Src& src, const GemmParams cp) {
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < KSUB; ++ks) {
-                        const uint32_t a0 = sA + stage * SP::kAStage + ks * kATileBytes;
-                        const uint32_t b0 = sB + stage * SP::kBStage + ks * kBHalfSubBytes;
+                        // same layouts as the single-SM kernel; B here is this
+                        // CTA's 128 columns (two 64-column boxes)
+                        const uint64_t a_desc = desc_base(sA + stage * SP::kAStage + ks * kATileBytes, ta);
+                        const uint64_t b_desc = desc_base(sB + stage * SP::kBStage + ks * kBHalfSubBytes, !tb);
 #pragma unroll
-                        for (int k = 0; k < kBK / kUMMA_K; ++k) {
-                            // same layouts as the single-SM kernel; B here is this
-                            // CTA's 128 columns (two 64-column boxes)
-                            const uint64_t adesc = operand_desc(a0, k, ta);
-                            const uint64_t bdesc = operand_desc(b0, k, !tb);
-                            tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | ks | k) != 0 ? 1u : 0u);
-                        }
+                        for (int k = 0; k < kBK / kUMMA_K; ++k)
+                            tc_mma_f16_pair(d_tmem, a_desc + k * a_step, b_desc + k * b_step, idesc,
+                                            (kb | ks | k) != 0 ? 1u : 0u);
                     }
                     tc_commit_pair_mc(empty_bar(stage), 0x3);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -585,7 +585,7 @@ __device__ __forceinline__ void pair_gemm(const Src& src, const GemmParams cp) {
             const int ucols = un.half < 0 ? BN : BN / 2;                       // the unit's width
             const int un0 = un.half < 0 ? tc.n0 : tc.n0 + (BN / 2) * un.half;  // its first column
             uint32_t* stage = reinterpret_cast<uint32_t*>(base + SP::kStage + (warp - 2) * kStageWarpBytes);
-            if (pp.epi != EPI_NONE) stage_bias(pp, stage + kStageBlockWords, un0 + half * (ucols / 2), ucols / 2);
+            if (EPI != EPI_NONE) stage_bias(pp, stage + kStageBlockWords, un0 + half * (ucols / 2), ucols / 2);
             const bool ready = mbar_wait_cluster_bounded(accf_bar(acc), acc_phase, cp.timeout_ns, abort_flag, status,
                                                          ROLE_EPILOGUE, BAR_ACC_FULL);
             if (!__all_sync(0xffffffffu, ready)) break;
@@ -594,9 +594,9 @@ __device__ __forceinline__ void pair_gemm(const Src& src, const GemmParams cp) {
                                     (static_cast<uint32_t>(32 * q) << 16);
             const int row0 = tc.m0 + 128 * static_cast<int>(rank) + 32 * q;
             if (un.half < 0)
-                epilogue_rows<BN / 2>(pp, t_base, row0, un0 + half * (BN / 2), stage);
+                epilogue_rows_act<BN / 2, EPI, EPI != EPI_NONE>(pp, t_base, row0, un0 + half * (BN / 2), stage);
             else
-                epilogue_rows<BN / 4>(pp, t_base, row0, un0 + half * (BN / 4), stage);
+                epilogue_rows_act<BN / 4, EPI, EPI != EPI_NONE>(pp, t_base, row0, un0 + half * (BN / 4), stage);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acc == 0 ? acce_leader0 : acce_leader1);
@@ -615,11 +615,11 @@ __device__ __forceinline__ void pair_gemm(const Src& src, const GemmParams cp) {
 
 // Grouped GEMM: C_g = epilogue(A_g . B_g + bias_g) for every problem g of
 // `gp` in one persistent launch.
-template <int STAGES, int KSUB>
+template <int STAGES, int KSUB, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_f16_tc2_grouped_kernel(const __grid_constant__ GroupedParams gp) {
     const GroupedPairSource src(&gp, static_cast<int>(blockIdx.x >> 1), static_cast<int>(gridDim.x >> 1));
-    pair_gemm<STAGES, KSUB>(src, gp.prob[0]);
+    pair_gemm<STAGES, KSUB, EPI>(src, gp.prob[0]);
 }
 
 }  // namespace gemm_f16_dev

@@ -49,6 +49,18 @@ struct SmemPlanSwap {
     static_assert(kStage % 1024 == 0, "swizzle atoms need 1 KiB alignment");
 };
 
+// Column n of rows m0 .. m0 + MT - 1 of C (one thread): activation ACT of
+// v[i] + b, rounded to fp16; rows past M and columns past N are not stored.
+template <int ACT, int MT>
+__device__ __forceinline__ void swap_store(const GemmParams& p, const float (&v)[MT], float b, int m0, int n,
+                                           bool col_ok) {
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+        const int m = m0 + i;
+        if (col_ok && m < p.M) p.C[static_cast<int64_t>(m) * p.ldc + n] = __float2half_rn(act<ACT>(v[i] + b));
+    }
+}
+
 template <int MT, int STAGES>
 __global__ void __launch_bounds__(kSwapThreads, 1)
 gemm_f16_swap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -157,6 +169,7 @@ gemm_f16_swap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         if (lane == 0) {
             // MMA A = B^T (MN-major unless B is stored N x K), MMA B = A^T (K-major unless A is stored K x M)
             const uint32_t idesc = idesc_f16_f32(TN, MT, /*b_mn_major=*/ta, /*a_mn_major=*/!tb);
+            const uint64_t a_step = desc_step(!tb), b_step = desc_step(ta);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -173,12 +186,12 @@ gemm_f16_swap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                                            ROLE_MMA, BAR_FULL)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t st = base_s + stage * SP::kStage;
+                    const uint64_t a_desc = desc_base(st, !tb);
+                    const uint64_t b_desc = desc_base(st + SP::kBtBytes, ta);
 #pragma unroll
-                    for (int k = 0; k < kBK / kUMMA_K; ++k) {
-                        const uint64_t adesc = operand_desc(st, k, !tb);
-                        const uint64_t bdesc = operand_desc(st + SP::kBtBytes, k, ta);
-                        tc_mma_f16(d_tmem, adesc, bdesc, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
-                    }
+                    for (int k = 0; k < kBK / kUMMA_K; ++k)
+                        tc_mma_f16(d_tmem, a_desc + k * a_step, b_desc + k * b_step, idesc,
+                                   (kb != kb0 || k != 0) ? 1u : 0u);
                     tc_commit(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -250,11 +263,12 @@ gemm_f16_swap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             }
             if (finish) {
                 const float b = (p.epi != EPI_NONE && col_ok) ? __half2float(p.bias[n]) : 0.0f;
-#pragma unroll
-                for (int i = 0; i < MT; ++i) {
-                    const int m = m0 + i;
-                    if (col_ok && m < p.M)
-                        p.C[static_cast<int64_t>(m) * p.ldc + n] = __float2half_rn(apply_act(v[i] + b, p.epi));
+                switch (p.epi) {   // once per tile, not per element
+                    case EPI_BIAS_RELU: swap_store<EPI_BIAS_RELU, MT>(p, v, b, m0, n, col_ok); break;
+                    case EPI_BIAS_GELU_ERF: swap_store<EPI_BIAS_GELU_ERF, MT>(p, v, b, m0, n, col_ok); break;
+                    case EPI_BIAS_SIGMOID: swap_store<EPI_BIAS_SIGMOID, MT>(p, v, b, m0, n, col_ok); break;
+                    case EPI_BIAS_GELU_TANH: swap_store<EPI_BIAS_GELU_TANH, MT>(p, v, b, m0, n, col_ok); break;
+                    default: swap_store<EPI_NONE, MT>(p, v, b, m0, n, col_ok); break;
                 }
             }
         }
