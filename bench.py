@@ -40,6 +40,7 @@ UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "fused8192"
 L2_BYTES = 129 * 10 ** 6
 FALLBACK_TENSOR_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
 FP16_PER_BF16 = 1.0          # nominal dense fp16 rate / dense bf16 rate
 KERNEL_SOURCES = ("dense_fp16_tensor_tma_gb300/csrc/gemm_kernels.cuh",
                   "dense_fp16_tensor_tma_gb300/csrc/gemm_kernels_pair.cuh",
@@ -87,13 +88,32 @@ def kernel_name(plan):
 
 
 def read_peaks():
+    """(fp16 tensor TFLOP/s, HBM GB/s, source): the measured burst figures, else the fallbacks."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             pk = json.load(f)
-        return float(pk["bf16_tflops"]) * FP16_PER_BF16, "measured", pk
+        return float(pk["bf16_tflops"]) * FP16_PER_BF16, float(pk["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
-        return FALLBACK_TENSOR_TFLOPS, "fallback", None
+        return FALLBACK_TENSOR_TFLOPS, FALLBACK_HBM_GBS, "fallback"
+
+
+def roofline(w, avg_launch_ms, traffic, plan):
+    """Roofline of the dominant kernel: tensor-bound when the workload's
+    arithmetic intensity (algorithmic FLOPs per algorithmic byte) is above the
+    ridge point of the two peaks, else HBM-bound."""
+    tensor_peak, hbm_peak, src = read_peaks()
+    intensity = w.flops() / w.alg_bytes()
+    ridge = tensor_peak * 1e12 / (hbm_peak * 1e9)
+    if intensity >= ridge:
+        achieved, peak, unit, bound = w.flops() / (avg_launch_ms * 1e-3) / 1e12, tensor_peak, "TFLOP/s", "tensor"
+        peak_src = f"{src} (bf16 burst x fp16/bf16 ratio {FP16_PER_BF16})"
+    else:
+        achieved, peak, unit, bound = w.alg_bytes() / (avg_launch_ms * 1e-3) / 1e9, hbm_peak, "GB/s", "hbm"
+        peak_src = f"{src} (copy bandwidth)"
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "traffic": traffic, "peak_source": peak_src, "intensity_flop_per_byte": intensity,
+            "ridge_flop_per_byte": ridge, "kernel": kernel_name(plan), "avg_launch_ms": avg_launch_ms}
 
 
 def committed_traffic(workload_name):
@@ -356,9 +376,9 @@ def run_ours(args, w, epi):
     flops = w.flops()
     value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
     avg_launch_ms = statistics.mean(per_launch_ms)
-    achieved = flops / (avg_launch_ms * 1e-3) / 1e12
-    peak, peak_src, _ = read_peaks()
     traffic = committed_traffic(w.name if args.layout == "nn" else f"{w.name}:{args.layout}")
+    roof = roofline(w, avg_launch_ms, traffic, plan)
+    tensor_peak = read_peaks()[0]
 
     # ---- end to end: pinned host buffers through the C ABI, copies inside the timed region
     hA = torch.from_numpy(A_st).pin_memory()
@@ -409,11 +429,8 @@ def run_ours(args, w, epi):
             "data": "synthetic",
             "config": {**workload_config(w, epi, args.layout),
                        "parallelism": f"replicas{world}" if world > 1 else "single"},
-            "pct_of_peak": 100.0 * achieved / peak,
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{peak_src} (bf16 burst x fp16/bf16 ratio {FP16_PER_BF16})",
-                         "kernel": kernel_name(plan), "avg_launch_ms": avg_launch_ms},
+            "pct_of_peak": 100.0 * (flops / (avg_launch_ms * 1e-3) / 1e12) / tensor_peak,
+            "roofline": roof,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms / e2e_steps},
             "gpu_launches": launches_per_step * args.steps,
