@@ -1,4 +1,6 @@
-"""CPU oracle for C = epilogue(A.B + bias) in fp64, rounded once to fp16.
+"""CPU oracle, in fp64 rounded once to fp16, for C = epilogue(A.B + bias)
+(gemm_oracle.cpp) and for attention O = softmax(scale Q K^T) V
+(attn_oracle.cpp).
 
 TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the bench's CPU
 baseline leg are the only callers.  The product library never imports this
@@ -30,19 +32,19 @@ EPILOGUES = {"none": EPI_NONE, "bias": EPI_BIAS, "bias_relu": EPI_BIAS_RELU,
              "bias_gelu_tanh": EPI_BIAS_GELU_TANH}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "gemm_oracle.cpp")
+_SRCS = [os.path.join(_HERE, "gemm_oracle.cpp"), os.path.join(_HERE, "attn_oracle.cpp")]
 _LIB = os.path.join(_HERE, "_build", "liboracle.so")
 _lib = None
 
 
 def build(force: bool = False) -> str:
     """Compile the oracle with g++ (portable flags: runs on x86-64 and aarch64)."""
-    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+    if not force and os.path.exists(_LIB) and all(os.path.getmtime(_LIB) >= os.path.getmtime(f) for f in _SRCS):
         return _LIB
     os.makedirs(os.path.dirname(_LIB), exist_ok=True)
     tmp = _LIB + f".tmp{os.getpid()}"
     subprocess.check_call(["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread",
-                           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp])
+                           "-fno-fast-math", "-ffp-contract=off", *_SRCS, "-o", tmp])
     os.replace(tmp, _LIB)
     return _LIB
 
@@ -71,6 +73,9 @@ def _load():
                                       i64p, i64p, i64, u16p, f64p, ctypes.c_int]
     lib.oracle_gemm_elems.restype = ctypes.c_int
     lib.oracle_default_threads.restype = ctypes.c_int
+    lib.oracle_attn_rows.argtypes = [u16p, u16p, u16p, i64, i64, i64, i64, ctypes.c_int, ctypes.c_double,
+                                     i64p, i64, u16p, f64p, ctypes.c_int]
+    lib.oracle_attn_rows.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -176,3 +181,33 @@ def gemm_grouped(problems, epilogue, threads: int = 0):
         else:
             out.append(gemm(A, B, bias if _epi(epilogue) != 0 else None, epilogue, threads))
     return out
+
+
+def attention_rows(Q, K, V, causal, scale, rows, threads: int = 0, want_f64: bool = False):
+    """Rows of O = softmax(scale Q K^T) V (attn_oracle.cpp) for (B, H, S, D)
+    fp16 Q, K, V: `rows` index the flattened (B * H * S) query rows; returns
+    an fp16 array [len(rows), D] (and the values before rounding)."""
+    Q, K, V = _bits(Q), _bits(K), _bits(V)
+    B, H, S, D = Q.shape
+    assert K.shape == Q.shape and V.shape == Q.shape
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((rows.size, D), np.uint16)
+    f64 = np.empty((rows.size, D), np.float64) if want_f64 else None
+    rc = _load().oracle_attn_rows(_p(Q, ctypes.c_uint16), _p(K, ctypes.c_uint16), _p(V, ctypes.c_uint16),
+                                  B, H, S, D, 1 if causal else 0, float(scale), _p(rows, ctypes.c_int64), rows.size,
+                                  _p(out, ctypes.c_uint16), _p(f64, ctypes.c_double), threads)
+    if rc != 0:
+        raise ValueError("oracle_attn_rows: bad arguments")
+    out = out.view(np.float16)
+    return (out, f64) if want_f64 else out
+
+
+def attention(Q, K, V, causal, scale=None, threads: int = 0, want_f64: bool = False):
+    """The whole of O (fp16, shape of Q).  scale defaults to 1/sqrt(D), the
+    default of the scaled-dot-product attention the pages validate against."""
+    B, H, S, D = np.shape(Q)
+    scale = 1.0 / np.sqrt(D) if scale is None else scale
+    r = attention_rows(Q, K, V, causal, scale, np.arange(B * H * S), threads, want_f64)
+    if want_f64:
+        return r[0].reshape(B, H, S, D), r[1].reshape(B, H, S, D)
+    return r.reshape(B, H, S, D)

@@ -367,6 +367,116 @@ def test_grouped_empty_and_k_zero_problems(oracle_mod):
     assert np.array_equal(out[1].view(np.uint16), np.broadcast_to(np.maximum(bias, 0), (2, 4)).view(np.uint16))
 
 
+# ---------------------------------------------------------------- attention
+
+def _qkv(rng, B, H, S, D, scale=1.0):
+    return tuple((rng.standard_normal((B, H, S, D)) * scale).astype(np.float16) for _ in range(3))
+
+
+def test_attention_single_key_is_v(oracle_mod):
+    # one admissible key: its weight is exp(0)/exp(0) = 1 exactly
+    rng = np.random.default_rng(70)
+    Q, K, V = _qkv(rng, 2, 3, 1, 16)
+    assert np.array_equal(oracle_mod.attention(Q, K, V, False).view(np.uint16), V.view(np.uint16))
+    Q, K, V = _qkv(rng, 1, 2, 9, 16)
+    O = oracle_mod.attention(Q, K, V, True)             # causal: query 0 sees key 0 only
+    assert np.array_equal(O[:, :, 0].view(np.uint16), V[:, :, 0].view(np.uint16))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_equal_scores_average_v(oracle_mod, causal):
+    # Q = 0: every score is 0, the weights 1/n, O the mean of the admissible V rows
+    rng = np.random.default_rng(71)
+    B, H, S, D = 1, 2, 11, 8
+    _, K, V = _qkv(rng, B, H, S, D)
+    Q = np.zeros_like(V)
+    _, f64 = oracle_mod.attention(Q, K, V, causal, want_f64=True)
+    v = V.astype(np.float64)
+    ref = np.cumsum(v, axis=2) / np.arange(1, S + 1)[None, None, :, None] if causal else \
+        np.broadcast_to(v.mean(axis=2, keepdims=True), v.shape)
+    assert np.allclose(f64, ref, rtol=1e-13, atol=1e-15)
+
+
+def test_attention_constant_v_is_returned(oracle_mod):
+    rng = np.random.default_rng(72)
+    Q, K, _ = _qkv(rng, 2, 2, 13, 32, 2.0)
+    c = rng.standard_normal(32).astype(np.float16)
+    V = np.broadcast_to(c, Q.shape).astype(np.float16)
+    for causal in (False, True):
+        O = oracle_mod.attention(Q, K, V, causal)
+        assert np.array_equal(O.view(np.uint16), V.view(np.uint16))
+
+
+def test_attention_one_hot_keys_closed_form(oracle_mod):
+    # K rows = unit vectors e_j, Q row i = alpha e_{pi(i)}, scale 1: query i
+    # scores alpha on key pi(i) and 0 elsewhere, so
+    # O[i] = (e^alpha V[pi(i)] + sum_{j != pi(i)} V[j]) / (e^alpha + S - 1)
+    rng = np.random.default_rng(73)
+    S, D, alpha = 6, 8, 3.0
+    K = np.zeros((1, 1, S, D), np.float16)
+    K[0, 0, np.arange(S), np.arange(S)] = 1.0
+    perm = rng.permutation(S)
+    Q = np.zeros((1, 1, S, D), np.float16)
+    Q[0, 0, np.arange(S), perm] = alpha
+    V = rng.standard_normal((1, 1, S, D)).astype(np.float16)
+    _, f64 = oracle_mod.attention(Q, K, V, False, scale=1.0, want_f64=True)
+    v = V[0, 0].astype(np.float64)
+    e = math.exp(alpha)
+    for i in range(S):
+        ref = (e * v[perm[i]] + (v.sum(axis=0) - v[perm[i]])) / (e + S - 1)
+        assert np.allclose(f64[0, 0, i], ref, rtol=1e-13, atol=1e-15)
+
+
+def test_attention_brute_force_tiny(oracle_mod):
+    # plain Python: exp of the raw scores (no max subtraction), then the ratio
+    rng = np.random.default_rng(74)
+    for B, H, S, D, causal in [(1, 1, 3, 4, False), (2, 1, 5, 3, True), (1, 2, 4, 8, False), (1, 1, 7, 2, True)]:
+        Q, K, V = _qkv(rng, B, H, S, D, 0.5)
+        scale = 0.7
+        _, f64 = oracle_mod.attention(Q, K, V, causal, scale=scale, want_f64=True)
+        q, k, v = (x.astype(np.float64).tolist() for x in (Q, K, V))
+        for b in range(B):
+            for h in range(H):
+                for i in range(S):
+                    keys = range(i + 1) if causal else range(S)
+                    w = [math.exp(scale * sum(q[b][h][i][d] * k[b][h][j][d] for d in range(D))) for j in keys]
+                    tot = sum(w)
+                    for d in range(D):
+                        ref = sum(w[n] * v[b][h][j][d] for n, j in enumerate(keys)) / tot
+                        assert abs(f64[b, h, i, d] - ref) <= 1e-13 * max(1.0, abs(ref))
+
+
+def test_attention_causal_row_is_the_prefix_problem(oracle_mod):
+    # causal query i sees exactly the non-causal problem over the first i + 1 rows
+    rng = np.random.default_rng(75)
+    Q, K, V = _qkv(rng, 1, 2, 10, 16)
+    Oc = oracle_mod.attention(Q, K, V, True)
+    for i in (0, 3, 9):
+        On = oracle_mod.attention(Q[:, :, :i + 1], K[:, :, :i + 1], V[:, :, :i + 1], False)
+        assert np.array_equal(Oc[:, :, i].view(np.uint16), On[:, :, i].view(np.uint16))
+
+
+def test_attention_key_permutation_and_scale_invariances(oracle_mod):
+    rng = np.random.default_rng(76)
+    Q, K, V = _qkv(rng, 1, 2, 12, 16)
+    _, f0 = oracle_mod.attention(Q, K, V, False, want_f64=True)
+    perm = rng.permutation(12)
+    _, f1 = oracle_mod.attention(Q, K[:, :, perm], V[:, :, perm], False, want_f64=True)
+    assert np.allclose(f0, f1, rtol=1e-13, atol=1e-15)       # keys and values moved together
+    Q2 = (Q.astype(np.float32) * 2).astype(np.float16)        # exact doubling
+    a = oracle_mod.attention(Q, K, V, True, scale=0.5)
+    b = oracle_mod.attention(Q2, K, V, True, scale=0.25)
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+def test_attention_planted_missing_mask_is_caught(oracle_mod):
+    # without the causal mask, query 0 averages over every key and is no longer V[0]
+    rng = np.random.default_rng(77)
+    Q, K, V = _qkv(rng, 1, 1, 8, 16)
+    O = oracle_mod.attention(Q, K, V, False)
+    assert not np.array_equal(O[:, :, 0].view(np.uint16), V[:, :, 0].view(np.uint16))
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def test_planted_transpose_is_caught(oracle_mod):
