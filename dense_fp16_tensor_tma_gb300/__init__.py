@@ -27,7 +27,7 @@ GEMM_F16_TRANS_A, GEMM_F16_TRANS_B = 1, 2
 EXPORTS = ("gemm_f16", "gemm_f16_ex", "gemm_f16_status_string", "gemm_f16_last_cuda_error",
            "gemm_f16_debug_status", "gemm_f16_release_workspace", "gemm_f16_plan", "gemm_f16_plan_ex",
            "gemm_f16_selftest_timeout", "gemm_f16_noalloc", "gemm_f16_force_config", "gemm_f16_set_pdl",
-           "gemm_f16_grouped")
+           "gemm_f16_grouped", "attn_f16_fwd", "attn_f16_debug_status", "attn_f16_last_cuda_error")
 CONFIGS = {"auto": 0, "pair256x256": 1, "128x256": 2, "128x128": 3, "128x64": 4, "swap": 5, "pair_whole": 6}
 
 if not os.path.exists(LIB_PATH):
@@ -67,6 +67,11 @@ lib.gemm_f16_force_config.argtypes = [_int]
 lib.gemm_f16_force_config.restype = _int
 lib.gemm_f16_grouped.argtypes = [ctypes.POINTER(GemmProblem), _int, _int, _int, _vp]
 lib.gemm_f16_grouped.restype = _int
+lib.attn_f16_fwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, ctypes.c_float, _vp]
+lib.attn_f16_fwd.restype = _int
+lib.attn_f16_debug_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
+lib.attn_f16_debug_status.restype = _int
+lib.attn_f16_last_cuda_error.restype = _int
 lib.gemm_f16_set_pdl.argtypes = [_int]
 lib.gemm_f16_set_pdl.restype = _int
 
@@ -76,7 +81,8 @@ class GemmError(RuntimeError):
         self.status = status
         msg = gemm_f16_status_string(status)
         if status == GEMM_ERR_CUDA:
-            msg += f" (cudaError {lib.gemm_f16_last_cuda_error()})"
+            err = lib.attn_f16_last_cuda_error() if where.startswith("attn") else lib.gemm_f16_last_cuda_error()
+            msg += f" (cudaError {err})"
         super().__init__(f"{where}: {msg}")
 
 
@@ -284,3 +290,46 @@ def gemm_f16_noalloc_ptr(a_ptr: int, b_ptr: int, bias_ptr: int, c_ptr: int, M: i
     """
     return lib.gemm_f16_noalloc(a_ptr or None, b_ptr or None, bias_ptr or None, c_ptr or None,
                                 int(M), int(N), int(K), _epi(epilogue), stream or None)
+
+
+# ---------------------------------------------------------------- attention forward
+
+def attn_f16_fwd_ptr(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, B: int, H: int, S: int, D: int,
+                     causal: bool = False, scale: float = 0.0, stream: int = 0) -> int:
+    """Raw call of attn_f16_fwd (device addresses as integers); returns the status code."""
+    return lib.attn_f16_fwd(q_ptr or None, k_ptr or None, v_ptr or None, o_ptr or None, int(B), int(H), int(S),
+                            int(D), 1 if causal else 0, float(scale), stream or None)
+
+
+def attn_f16_fwd(Q, K, V, O, causal=False, scale=None, stream=None):
+    """O = softmax(scale * Q @ K^T) @ V per (batch, head), into the preallocated
+    O.  Q, K, V, O: contiguous torch.float16 CUDA tensors of shape (B, H, S, D),
+    D 64 or 128.  scale defaults to 1/sqrt(D).  Raises GemmError on a nonzero
+    status."""
+    import torch
+    shape = tuple(Q.shape)
+    if len(shape) != 4 or tuple(K.shape) != shape or tuple(V.shape) != shape or tuple(O.shape) != shape:
+        raise ValueError(f"Q, K, V, O must share one (B, H, S, D) shape: {shape}, {tuple(K.shape)}, "
+                         f"{tuple(V.shape)}, {tuple(O.shape)}")
+    for name, t in (("Q", Q), ("K", K), ("V", V), ("O", O)):
+        if t.dtype != torch.float16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float16 CUDA tensor")
+    B, H, S, D = shape
+    st = lib.attn_f16_fwd(Q.data_ptr() or None, K.data_ptr() or None, V.data_ptr() or None, O.data_ptr() or None,
+                          B, H, S, D, 1 if causal else 0, 0.0 if scale is None else float(scale),
+                          _stream_handle(stream, O.get_device()))
+    if st != GEMM_OK:
+        raise GemmError(st, "attn_f16_fwd")
+    return O
+
+
+def attn_f16_debug_status(stream=None):
+    """Synchronise the stream; (status, raw status word) of the attention kernels."""
+    word = ctypes.c_uint32(0)
+    st = lib.attn_f16_debug_status(_stream_handle(stream), ctypes.byref(word))
+    return st, word.value
+
+
+def attention_flops(B, H, S, D, causal):
+    """The pages' FLOP model of attention forward: 4 B H S^2 D, halved when causal."""
+    return 4.0 * B * H * S * S * D * (0.5 if causal else 1.0)

@@ -1,0 +1,174 @@
+// C-ABI boundary of the attention forward (declared in include/attn_f16.h):
+// argument checks, device check, 3-D TMA tensor maps over (D, S, B*H), and
+// the launch of attn_f16_fwd_kernel on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "attn_f16.h"
+#include "attn_kernels.cuh"
+
+namespace {
+
+using namespace attn_dev;
+
+thread_local int t_last_cuda_error = 0;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr int kMaxDevices = 64;
+struct AttnDevice {
+    bool ready = false;
+    int status = GEMM_OK;
+};
+std::mutex g_mu;
+AttnDevice g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+uint64_t g_timeout_ns = 2000000000ull;
+bool g_pdl = true;   // programmatic dependent launch unless GEMM_F16_PDL=0
+
+int cuda_fail(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return GEMM_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int init_device(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    AttnDevice& st = g_dev[dev];
+    if (st.ready) return st.status;
+    int major = 0, minor = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (major != 10 || minor != 3) {
+        st.ready = true;
+        st.status = GEMM_ERR_UNSUPPORTED_DEVICE;
+        return st.status;
+    }
+    if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return cuda_fail(e != cudaSuccess ? e : cudaErrorSymbolNotFound);
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    e = cudaFuncSetAttribute(attn_f16_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AttnSmem<64>::kDynamicBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attn_f16_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 AttnSmem<128>::kDynamicBytes);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (const char* env = std::getenv("GEMM_F16_TIMEOUT_MS")) {
+        const long ms = std::strtol(env, nullptr, 10);
+        if (ms > 0) g_timeout_ns = static_cast<uint64_t>(ms) * 1000000ull;
+    }
+    if (const char* env = std::getenv("GEMM_F16_PDL")) g_pdl = env[0] != '0';
+    st.ready = true;
+    st.status = GEMM_OK;
+    return GEMM_OK;
+}
+
+// (D, S, B*H) fp16 tensor with box 64 x 128 x 1, 128-byte swizzle, zeros
+// outside the tensor (rows past S of a head never come from the next head).
+int encode_3d(CUtensorMap* m, const void* ptr, int64_t D, int64_t S, int64_t BH) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S * D) * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kQRows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = static_cast<int>(r);
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+template <int D>
+cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const AttnParams& prm, int ctas,
+                   cudaStream_t s) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = AttnSmem<D>::kDynamicBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    std::memset(attr, 0, sizeof(attr));
+    if (g_pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, attn_f16_fwd_kernel<D>, q, k, v, prm);
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_f16_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B, int64_t H, int64_t S, int64_t D,
+                 int causal, float scale, void* cuda_stream) {
+    if (B < 0 || H < 0 || S < 0) return GEMM_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return GEMM_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return GEMM_ERR_INVALID_ARG;
+    if (S >= (int64_t(1) << 31) || B >= (int64_t(1) << 31) || H >= (int64_t(1) << 31)) return GEMM_ERR_INVALID_ARG;
+    if (B * H >= (int64_t(1) << 31)) return GEMM_ERR_INVALID_ARG;
+    if (B == 0 || H == 0 || S == 0) return GEMM_OK;
+    const int64_t nq = (S + kQRows - 1) / kQRows;
+    if (B * H * nq >= (int64_t(1) << 31)) return GEMM_ERR_INVALID_ARG;
+    if (!Q || !K || !V || !O) return GEMM_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return GEMM_ERR_MISALIGNED;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int st = init_device(dev);
+    if (st != GEMM_OK) return st;
+    CUtensorMap tq, tk, tv;
+    st = encode_3d(&tq, Q, D, S, B * H);
+    if (st == GEMM_OK) st = encode_3d(&tk, K, D, S, B * H);
+    if (st == GEMM_OK) st = encode_3d(&tv, V, D, S, B * H);
+    if (st != GEMM_OK) return st;
+    AttnParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    prm.O = static_cast<__half*>(O);
+    prm.S = static_cast<int>(S);
+    prm.BH = static_cast<int>(B * H);
+    prm.nq = static_cast<int>(nq);
+    prm.causal = causal ? 1 : 0;
+    const double sc = scale == 0.0f ? 1.0 / std::sqrt(static_cast<double>(D)) : static_cast<double>(scale);
+    prm.scale_log2 = static_cast<float>(sc * 1.4426950408889634);
+    prm.timeout_ns = g_timeout_ns;
+    const int ctas = static_cast<int>(B * H * nq);
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    e = D == 64 ? launch<64>(tq, tk, tv, prm, ctas, s) : launch<128>(tq, tk, tv, prm, ctas, s);
+    return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+}
+
+int attn_f16_last_cuda_error(void) { return t_last_cuda_error; }
+
+int attn_f16_debug_status(void* cuda_stream, uint32_t* detail) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned int word = 0, zero = 0;
+    e = cudaMemcpyFromSymbol(&word, g_attn_status, sizeof(word));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (detail) *detail = word;
+    return word != 0 ? GEMM_ERR_TIMEOUT : GEMM_OK;
+}
+
+}  // extern "C"

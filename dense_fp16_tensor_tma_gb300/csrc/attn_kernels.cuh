@@ -1,0 +1,414 @@
+// Attention forward for sm_103a:  O = softmax(scale * Q K^T) V  per (batch, head).
+//
+// The method: "writing-tilelang-kernels", Flash Attention Forward (Q, K, V, O
+// as (B, H, S, D) fp16 tensors; one program per block of query rows) and its
+// pattern table's "Online Softmax" row (running max, exp, rescaling);
+// "TileLang: Write, Autotune, and Ship Fused Tensor-Core Kernels from
+// Python", FlashAttention: the FLOP model (softmax computed online, the S x S
+// score matrix never written to memory; causal and non-causal).
+//
+// GB300 design (one CTA per 128 query rows of one head):
+//   * warp 0: TMA producer.  Q once (D/64 boxes of 64 x 128), then K and V
+//     blocks of 128 keys through two 2-slot rings; 3-D tensor maps
+//     (D, S, B*H), so rows past S arrive as zeros and never come from the
+//     next head;
+//   * warp 1: allocates tensor memory and issues tcgen05.mma from one thread:
+//     S_j = Q K_j^T (M = 128, N = 128, K = D; both operands K-major) into one
+//     of two TMEM score buffers, and O += P_j V_j (M = 128, N = D, K = 128;
+//     P K-major from shared memory, V MN-major) into the TMEM output;
+//     S_{j+1} is computed while the softmax of block j runs;
+//   * warps 2..5: softmax, one query row per thread (its TMEM lane): pass 1
+//     reads the row of S_j for the block maximum, pass 2 reads it again,
+//     forms p = 2^(s * scale * log2 e - m) in fp32, sums it and writes it as
+//     fp16 into a shared-memory P tile in the 128-byte-swizzled K-major layout
+//     the tensor core reads.  The running maximum m is raised only when a
+//     block's maximum exceeds it by more than 8 (in log2 units); O and the
+//     running sum l are then rescaled in place (TMEM load, multiply, store).
+//     Between raises p stays below 2^8, which fp16 and the fp32 sums hold
+//     exactly enough, and the final O / l is the same ratio;
+//   * after the last block: O / l rounded to fp16, 16-byte stores of each
+//     thread's row.
+// Every wait is bounded (as in the GEMM kernels): on a timeout the role
+// records itself in the status word, raises a shared abort flag, drains what
+// it issued and leaves; tensor memory is always freed.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace attn_dev {
+
+using namespace gemm_f16_dev;
+
+__device__ unsigned int g_attn_status;   // bounded-wait status word of the attention kernels
+
+constexpr int kQRows = 128;              // query rows per CTA = MMA M = TMEM lanes
+constexpr int kKeys = 128;               // keys per block = N of S = K of P V
+constexpr int kAttnThreads = 192;        // producer, MMA, 4 softmax warps
+constexpr uint32_t kBox = 64 * 128 * 2;  // one 64 (D or keys) x 128 (rows) fp16 box: 16 KiB
+constexpr uint32_t kTmemCols = 512;      // two 128-column score buffers + O (<= 128 columns)
+constexpr uint32_t kOCol = 256;          // first TMEM column of O
+constexpr float kRaise = 8.0f;           // raise the running max only past 2^8 growth
+
+enum : uint32_t { ROLE_SOFTMAX = 6, BAR_Q = 7, BAR_K = 8, BAR_V = 9, BAR_S = 10, BAR_P = 11, BAR_PV = 12 };
+
+struct AttnParams {
+    __half* O;
+    int S;              // sequence length (queries = keys)
+    int BH;             // batch * heads
+    int nq;             // query tiles per head
+    int causal;
+    float scale_log2;   // softmax scale * log2(e)
+    uint64_t timeout_ns;
+};
+
+template <int D>
+struct AttnSmem {
+    static constexpr uint32_t kQ = 0;                        // D/64 boxes
+    static constexpr uint32_t kK = kQ + (D / 64) * kBox;     // 2 slots x D/64 boxes
+    static constexpr uint32_t kV = kK + 2 * (D / 64) * kBox; // 2 slots x D/64 boxes
+    static constexpr uint32_t kP = kV + 2 * (D / 64) * kBox; // 2 boxes (keys 0-63, 64-127)
+    static constexpr uint32_t kBars = kP + 2 * kBox;
+    // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full, pv_done, drain
+    static constexpr uint32_t kNumBars = 14;
+    static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
+    static constexpr uint32_t kAbort = kTmemSlot + 4;
+    static constexpr uint32_t kEnd = kAbort + 4;
+    // The CTA allocates all 512 tensor-memory columns, so a second CTA on the
+    // same SM would only wait in its allocation: ask for enough shared memory
+    // (> half of the SM's 228 KiB) that one CTA fits per SM.
+    static constexpr uint32_t kOnePerSm = 120 * 1024;
+    static constexpr uint32_t kDynamicBytes = kEnd + 1024 > kOnePerSm ? kEnd + 1024 : kOnePerSm;
+};
+
+// 3-D tiled load (D, S, B*H) global -> shared, completing `bar`.  c0 (the D
+// offset) is 0 or 64: a multiple of 8 elements (16 bytes).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                                            int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns from registers to tensor memory.
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+          "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+          "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Generic-proxy shared-memory writes made visible to the tensor core (async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    static_assert(D == 64 || D == 128, "head dimension 64 or 128");
+    using SM = AttnSmem<D>;
+    constexpr int kDB = D / 64;                     // 64-wide boxes per row of Q, K, V
+    constexpr uint32_t kTileBytes = kDB * kBox;     // one Q, K or V tile
+    // S = Q K^T: M 128, N 128, both K-major.  O += P V: M 128, N D, V MN-major.
+    constexpr uint32_t kIdescS = idesc_f16_f32(kQRows, kKeys, /*b_mn_major=*/false);
+    constexpr uint32_t kIdescO = idesc_f16_f32(kQRows, D, /*b_mn_major=*/true);
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t* base = smem_raw + (base_s - raw_s);
+    const uint32_t sQ = base_s + SM::kQ, sK = base_s + SM::kK, sV = base_s + SM::kV, sP = base_s + SM::kP;
+    const uint32_t bars = base_s + SM::kBars;
+    const uint32_t q_full = bars;
+    auto k_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto k_empty = [&](int s) { return bars + 8u * (3 + s); };
+    auto v_full = [&](int s) { return bars + 8u * (5 + s); };
+    auto v_empty = [&](int s) { return bars + 8u * (7 + s); };
+    auto s_full = [&](int b) { return bars + 8u * (9 + b); };
+    const uint32_t p_full = bars + 8u * 11, pv_done = bars + 8u * 12, drain_bar = bars + 8u * 13;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + SM::kTmemSlot);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + SM::kAbort);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // heaviest query tiles first (causal: later tiles see more keys)
+    const int qt = p.nq - 1 - static_cast<int>(blockIdx.x) / p.BH;
+    const int bh = static_cast<int>(blockIdx.x) % p.BH;
+    const int q0 = qt * kQRows;
+    const int kblocks_all = (p.S + kKeys - 1) / kKeys;
+    const int nblk = p.causal ? min(kblocks_all, qt + 1) : kblocks_all;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(k_full(s), 1);
+            mbar_init(k_empty(s), 1);
+            mbar_init(v_full(s), 1);
+            mbar_init(v_empty(s), 1);
+            mbar_init(s_full(s), 1);
+        }
+        mbar_init(p_full, 4);      // the four softmax warps
+        mbar_init(pv_done, 1);
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    grid_dependency_wait();      // set-up above overlaps the previous kernel
+    grid_launch_dependents();
+    unsigned int* status = &g_attn_status;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            bool ok = true;
+            mbar_arrive_expect_tx(q_full, kTileBytes);
+            for (int c = 0; c < kDB; ++c) tma_load_3d(sQ + c * kBox, &tmQ, q_full, 64 * c, q0, bh);
+            int k_issued = 0, v_issued = 0;
+            for (int j = 0; ok && j < nblk; ++j) {
+                const int s = j & 1;
+                const uint32_t ph = static_cast<uint32_t>((j >> 1) & 1);
+                if (!mbar_wait_bounded(k_empty(s), ph ^ 1u, p.timeout_ns, abort_flag, status, ROLE_PRODUCER,
+                                       BAR_K)) { ok = false; break; }
+                mbar_arrive_expect_tx(k_full(s), kTileBytes);
+                for (int c = 0; c < kDB; ++c)
+                    tma_load_3d(sK + (s * kDB + c) * kBox, &tmK, k_full(s), 64 * c, j * kKeys, bh);
+                ++k_issued;
+                if (!mbar_wait_bounded(v_empty(s), ph ^ 1u, p.timeout_ns, abort_flag, status, ROLE_PRODUCER,
+                                       BAR_V)) { ok = false; break; }
+                mbar_arrive_expect_tx(v_full(s), kTileBytes);
+                for (int c = 0; c < kDB; ++c)
+                    tma_load_3d(sV + (s * kDB + c) * kBox, &tmV, v_full(s), 64 * c, j * kKeys, bh);
+                ++v_issued;
+            }
+            // every issued load lands before the CTA can exit (the last one or
+            // two of each ring; earlier ones were waited for by the MMA thread)
+            mbar_wait_bounded(q_full, 0, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_Q);
+            for (int j = max(0, k_issued - 2); j < k_issued; ++j)
+                mbar_wait_bounded(k_full(j & 1), (j >> 1) & 1, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_K);
+            for (int j = max(0, v_issued - 2); j < v_issued; ++j)
+                mbar_wait_bounded(v_full(j & 1), (j >> 1) & 1, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_V);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = mbar_wait_bounded(q_full, 0, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_Q);
+            tc_fence_after();
+            auto issue_s = [&](int j) -> bool {   // S_j = Q K_j^T into score buffer j & 1
+                const int s = j & 1;
+                if (!mbar_wait_bounded(k_full(s), (j >> 1) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_K))
+                    return false;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(s * kKeys);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    // K-major: box k / 4, 32 bytes per 16-deep step inside the swizzled row
+                    const uint64_t a = smem_desc_sw128(sQ + (k >> 2) * kBox + (k & 3) * 32, 0, 1024);
+                    const uint64_t b = smem_desc_sw128(sK + (s * kDB + (k >> 2)) * kBox + (k & 3) * 32, 0, 1024);
+                    tc_mma_f16(d_tmem, a, b, kIdescS, k != 0 ? 1u : 0u);
+                }
+                tc_commit(k_empty(s));       // K_j no longer needed: the next K may load
+                tc_commit(s_full(s));
+                return true;
+            };
+            if (ok && nblk > 0) ok = issue_s(0);
+            if (ok && nblk > 1) ok = issue_s(1);
+            for (int j = 0; ok && j < nblk; ++j) {
+                // P_j written (and O rescaled) by the softmax warps
+                if (!mbar_wait_bounded(p_full, j & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_P)) {
+                    ok = false;
+                    break;
+                }
+                const int s = j & 1;
+                if (!mbar_wait_bounded(v_full(s), (j >> 1) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_V)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t o_tmem = tmem_base + kOCol;
+#pragma unroll
+                for (int k = 0; k < kKeys / 16; ++k) {
+                    // P: K-major, keys 0-63 in box 0, 64-127 in box 1; V: MN-major,
+                    // 64-column boxes 16 KiB apart (LBO), 16 key rows = 2 KiB per step
+                    const uint64_t a = smem_desc_sw128(sP + (k >> 2) * kBox + (k & 3) * 32, 0, 1024);
+                    const uint64_t b = smem_desc_sw128(sV + s * kDB * kBox + k * 2048, kBox, 1024);
+                    tc_mma_f16(o_tmem, a, b, kIdescO, (j | k) != 0 ? 1u : 0u);
+                }
+                tc_commit(v_empty(s));
+                tc_commit(pv_done);
+                if (j + 2 < nblk) ok = issue_s(j + 2);   // score buffer s was read before P_j was written
+            }
+            tc_commit(drain_bar);
+            mbar_wait_bounded(drain_bar, 0, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_DRAIN);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax + output
+        const int quarter = warp & 3;                // TMEM lanes 32 * quarter ..
+        const int r = 32 * quarter + lane;           // this thread's row of the tile
+        const int q = q0 + r;                        // its query index
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
+        float m = -INFINITY, l = 0.0f;
+        bool ok = true;
+        for (int j = 0; j < nblk; ++j) {
+            const int k0 = j * kKeys;
+            const int s = j & 1;
+            const uint32_t s_tmem = lane_base + static_cast<uint32_t>(s * kKeys);
+            ok = mbar_wait_bounded(s_full(s), (j >> 1) & 1, p.timeout_ns, abort_flag, status, ROLE_SOFTMAX, BAR_S);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            // keys past S, and (causal) keys after this query, do not count
+            const bool masked_block = (k0 + kKeys > p.S) || (p.causal && j == nblk - 1);
+            const int key_lim = p.causal ? min(p.S, q + 1) - k0 : p.S - k0;   // valid keys: col < key_lim
+            // pass 1: the block maximum of this row
+            float bmax = -INFINITY;
+#pragma unroll 1
+            for (int c = 0; c < kKeys / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(s_tmem + 32u * c, v);
+                tmem_wait_ld(v);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    const float x = __uint_as_float(v[t]);
+                    const bool valid = !masked_block || (32 * c + t < key_lim);
+                    bmax = valid ? fmaxf(bmax, x) : bmax;
+                }
+            }
+            const float bmax2 = bmax * p.scale_log2;   // -inf if no valid key in this block
+            float m_new = m;
+            bool raise = false;
+            if (bmax2 > m + kRaise || m == -INFINITY) {
+                m_new = fmaxf(m, bmax2);
+                raise = m != -INFINITY && m_new != m;
+            }
+            // P and O are still read by the previous block's P V product
+            if (j > 0) {
+                ok = mbar_wait_bounded(pv_done, (j - 1) & 1, p.timeout_ns, abort_flag, status, ROLE_SOFTMAX, BAR_PV);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, raise)) {
+                const float alpha = raise ? fast_exp2(m - m_new) : 1.0f;
+                l *= alpha;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(lane_base + kOCol + 32u * c, v);
+                    tmem_wait_ld(v);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
+                    tmem_st_32x32b_x32(lane_base + kOCol + 32u * c, v);
+                }
+                tmem_wait_st();
+            }
+            m = m_new;
+            // pass 2: p = 2^(x * scale_log2 - m) as fp16 into the swizzled P tile
+            const float mm = (m == -INFINITY) ? 0.0f : m;
+#pragma unroll 1
+            for (int c = 0; c < kKeys / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(s_tmem + 32u * c, v);
+                tmem_wait_ld(v);
+                uint32_t h[16];
+                float rs = 0.0f;
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const bool v0 = !masked_block || (32 * c + 2 * t < key_lim);
+                    const bool v1 = !masked_block || (32 * c + 2 * t + 1 < key_lim);
+                    const float e0 = v0 ? fast_exp2(fmaf(__uint_as_float(v[2 * t]), p.scale_log2, -mm)) : 0.0f;
+                    const float e1 = v1 ? fast_exp2(fmaf(__uint_as_float(v[2 * t + 1]), p.scale_log2, -mm)) : 0.0f;
+                    const __half2 hv = __floats2half2_rn(e0, e1);
+                    // the sum takes the fp16 values the tensor core multiplies
+                    const float2 back = __half22float2(hv);
+                    rs += back.x + back.y;
+                    h[t] = *reinterpret_cast<const uint32_t*>(&hv);
+                }
+                l += rs;
+                // keys 32c .. 32c+31 = box c / 2, 16-byte chunks 4 (c % 2) .. 4 (c % 2) + 3,
+                // chunk position XOR (row % 8): the 128-byte swizzle
+                const uint32_t row_base = sP + (c >> 1) * kBox + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t chunk = static_cast<uint32_t>((4 * (c & 1) + u) ^ (r & 7));
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                                 ::"r"(row_base + chunk * 16u), "r"(h[4 * u]), "r"(h[4 * u + 1]),
+                                   "r"(h[4 * u + 2]), "r"(h[4 * u + 3])
+                                 : "memory");
+                }
+            }
+            fence_proxy_async_smem();    // P visible to the tensor core
+            tc_fence_before();           // and the O rescale, if any
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        // output: O / l after the last P V product
+        if (ok && nblk > 0) {
+            ok = mbar_wait_bounded(pv_done, (nblk - 1) & 1, p.timeout_ns, abort_flag, status, ROLE_SOFTMAX, BAR_PV);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok && nblk > 0) {
+            tc_fence_after();
+            const float inv = 1.0f / l;
+            __half* orow = p.O + (static_cast<int64_t>(bh) * p.S + q) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(lane_base + kOCol + 32u * c, v);
+                tmem_wait_ld(v);
+                uint32_t h[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const __half2 hv = __floats2half2_rn(__uint_as_float(v[2 * t]) * inv,
+                                                         __uint_as_float(v[2 * t + 1]) * inv);
+                    h[t] = *reinterpret_cast<const uint32_t*>(&hv);
+                }
+                if (q < p.S) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) dst[u] = make_uint4(h[4 * u], h[4 * u + 1], h[4 * u + 2], h[4 * u + 3]);
+                }
+            }
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace attn_dev

@@ -23,7 +23,7 @@ def _declared_functions():
         if fn.endswith(".h"):
             text = open(os.path.join(ROOT, "include", fn)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-            names |= set(re.findall(r"\b(gemm_f16\w*)\s*\(", text))
+            names |= set(re.findall(r"\b((?:gemm|attn)_f16\w*)\s*\(", text))
     return names
 
 
@@ -247,3 +247,33 @@ def test_grouped_argument_errors_need_no_device(g):
     assert g.gemm_f16_grouped_ptr([odd_c], "bias", 0, 0) == 3
     assert g.lib.gemm_f16_grouped(None, 2, 0, 0, None) == 1              # null array, count > 0
     assert g.lib.gemm_f16_grouped(None, -1, 0, 0, None) == 1
+
+
+# ---------------------------------------------------------------- attention forward
+
+@pytest.mark.parametrize("args, expect", [
+    # (B, H, S, D, scale)
+    ((1, 1, 128, 96, 0.0), 1),        # D must be 64 or 128
+    ((1, 1, 128, 32, 0.0), 1),
+    ((-1, 1, 128, 64, 0.0), 1),
+    ((1, 1, -5, 64, 0.0), 1),
+    ((1, 1, 128, 64, float("nan")), 1),
+    ((1, 1, 128, 64, float("inf")), 1),
+    ((1 << 16, 1 << 15, 128, 64, 0.0), 1),   # B * H >= 2^31
+    ((0, 4, 128, 64, 0.0), 0),        # empty: no-op
+    ((2, 2, 0, 128, 0.0), 0),
+])
+def test_attention_argument_errors_need_no_device(g, args, expect):
+    B, H, S, D, scale = args
+    assert g.attn_f16_fwd_ptr(GOOD, GOOD, GOOD, GOOD, B, H, S, D, False, scale, 0) == expect
+
+
+def test_attention_pointer_checks_need_no_device(g):
+    assert g.attn_f16_fwd_ptr(0, GOOD, GOOD, GOOD, 1, 1, 128, 64) == 1             # null Q
+    assert g.attn_f16_fwd_ptr(GOOD, GOOD, GOOD, GOOD + 2, 1, 1, 128, 64) == 3      # O not 16-byte aligned
+    assert g.attn_f16_fwd_ptr(GOOD + 8, GOOD, GOOD, GOOD, 1, 1, 128, 128) == 3
+
+
+def test_attention_flop_model(g):
+    assert g.attention_flops(4, 32, 4096, 128, False) == 4 * 4 * 32 * 4096 ** 2 * 128
+    assert g.attention_flops(4, 32, 4096, 128, True) == 2 * 4 * 32 * 4096 ** 2 * 128

@@ -1,0 +1,169 @@
+"""GPU parity of the attention forward (attn_f16_fwd) against the fp64 oracle.
+
+Bar: the oracle.compare tolerance (relative Frobenius error <= 1e-3, per
+element |err| <= 1e-2 (1 + |ref|)); bit-exact where the method is exact (one
+admissible key, constant V).  Inputs: workloads.ATTN_WORKLOADS (seeded) and
+seeded numpy draws for the special cases.
+"""
+import numpy as np
+import pytest
+
+import workloads
+from oracle.compare import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch_dev():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch, torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def g(torch_dev):
+    import dense_fp16_tensor_tma_gb300 as mod
+    return mod
+
+
+def run_attn(g, torch_dev, Q, K, V, causal, scale=None):
+    torch, dev = torch_dev
+    tq, tk, tv = (torch.from_numpy(np.ascontiguousarray(x)).to(dev) for x in (Q, K, V))
+    O = torch.full(Q.shape, float("nan"), dtype=torch.float16, device=dev)
+    g.attn_f16_fwd(tq, tk, tv, O, causal, scale)
+    st, word = g.attn_f16_debug_status()
+    assert st == 0, f"device status {st} word {word:#x}"
+    return O.cpu().numpy()
+
+
+def qkv(rng, shape, scale=1.0):
+    return tuple((rng.standard_normal(shape) * scale).astype(np.float16) for _ in range(3))
+
+
+def check(got, ref, what):
+    res = parity(got.reshape(-1, got.shape[-1]), ref.reshape(-1, ref.shape[-1]))
+    assert res["ok"], f"{what}: {res}"
+    return res
+
+
+# ---------------------------------------------------------------- the workloads
+
+@pytest.mark.parametrize("name", ["attn_small", "attn_small_causal", "attn_ragged_causal"])
+def test_attention_workloads_full(g, torch_dev, oracle_mod, name):
+    w = workloads.ATTN_WORKLOADS[name]
+    Q, K, V = w.make()
+    got = run_attn(g, torch_dev, Q, K, V, w.causal)
+    check(got, oracle_mod.attention(Q, K, V, w.causal), name)
+
+
+@pytest.mark.parametrize("name", ["attn_prefill", "attn_prefill_causal"])
+def test_attention_prefill_sampled_rows(g, torch_dev, oracle_mod, name):
+    w = workloads.ATTN_WORKLOADS[name]
+    Q, K, V = w.make()
+    got = run_attn(g, torch_dev, Q, K, V, w.causal)
+    rows = w.sample_rows(384)
+    ref = oracle_mod.attention_rows(Q, K, V, w.causal, 1.0 / np.sqrt(w.D), rows)
+    check(got.reshape(-1, w.D)[rows], ref, name)
+
+
+# ---------------------------------------------------------------- shapes
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("S", [1, 7, 127, 128, 129, 300, 513])
+def test_attention_shape_sweep(g, torch_dev, oracle_mod, D, causal, S):
+    rng = np.random.default_rng(S * 3 + D + causal)
+    Q, K, V = qkv(rng, (2, 3, S, D))
+    got = run_attn(g, torch_dev, Q, K, V, causal)
+    check(got, oracle_mod.attention(Q, K, V, causal), f"S={S} D={D} causal={causal}")
+
+
+# ---------------------------------------------------------------- exact special cases
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_attention_single_key_is_exactly_v(g, torch_dev, D):
+    # one key: p = 2^0 = 1 exactly, the sum is 1, O = V
+    rng = np.random.default_rng(80 + D)
+    Q, K, V = qkv(rng, (3, 2, 1, D))
+    got = run_attn(g, torch_dev, Q, K, V, False)
+    assert np.array_equal(got.view(np.uint16), V.view(np.uint16))
+    # causal: query 0 of every head sees key 0 only
+    Q, K, V = qkv(rng, (1, 2, 300, D))
+    got = run_attn(g, torch_dev, Q, K, V, True)
+    assert np.array_equal(got[:, :, 0].view(np.uint16), V[:, :, 0].view(np.uint16))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_constant_v_is_exact(g, torch_dev, causal):
+    # sum_j p_j c / sum_j p_j = c up to a few fp32 ulps: rounds back to c
+    rng = np.random.default_rng(81)
+    Q, K, _ = qkv(rng, (2, 2, 700, 128), 2.0)
+    c = rng.standard_normal(128).astype(np.float16)
+    V = np.broadcast_to(c, Q.shape).astype(np.float16)
+    got = run_attn(g, torch_dev, Q, K, V, causal)
+    assert np.array_equal(got.view(np.uint16), V.view(np.uint16))
+
+
+def test_attention_equal_scores_average(g, torch_dev, oracle_mod):
+    rng = np.random.default_rng(82)
+    _, K, V = qkv(rng, (1, 2, 500, 64))
+    Q = np.zeros_like(K)
+    for causal in (False, True):
+        check(run_attn(g, torch_dev, Q, K, V, causal), oracle_mod.attention(Q, K, V, causal), f"Q=0 {causal}")
+
+
+# ---------------------------------------------------------------- the online maximum
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_attention_running_max_raised_every_block(g, torch_dev, oracle_mod, D):
+    # scores rise along the keys for even query rows and fall for odd ones:
+    # the even rows raise their running maximum (and rescale O) in every
+    # block, the odd rows never do, within the same warps
+    rng = np.random.default_rng(83)
+    S = 640
+    sign = np.where(np.arange(S) % 2 == 0, 1.0, -1.0)
+    Q = np.broadcast_to((sign[:, None] * np.ones(D))[None, None], (1, 2, S, D)).astype(np.float16)
+    ramp = (np.arange(S) * 0.1)[:, None] * np.ones(D)
+    K = np.broadcast_to(ramp[None, None], (1, 2, S, D)).astype(np.float16)
+    V = rng.standard_normal((1, 2, S, D)).astype(np.float16)
+    scale = 1.0 / D   # scores +-0.1 j: 12.8 (18 in log2 units) more per block of 128 keys
+    for causal in (False, True):
+        got = run_attn(g, torch_dev, Q, K, V, causal, scale)
+        check(got, oracle_mod.attention(Q, K, V, causal, scale=scale), f"ramp causal={causal}")
+
+
+@pytest.mark.parametrize("scale", [0.05, -0.1, 0.3])
+def test_attention_explicit_scale(g, torch_dev, oracle_mod, scale):
+    rng = np.random.default_rng(84)
+    Q, K, V = qkv(rng, (2, 2, 384, 64))
+    got = run_attn(g, torch_dev, Q, K, V, True, scale)
+    check(got, oracle_mod.attention(Q, K, V, True, scale=scale), f"scale {scale}")
+
+
+def test_attention_deterministic_and_pdl_chain(g, torch_dev, oracle_mod):
+    # attention then a GEMM that reads its output, back to back on one stream,
+    # twice: bit-identical results, and the GEMM sees the finished O
+    torch, dev = torch_dev
+    rng = np.random.default_rng(85)
+    B, H, S, D = 1, 4, 512, 64
+    Q, K, V = qkv(rng, (B, H, S, D))
+    W = (rng.standard_normal((D, 96)) * 0.1).astype(np.float16)
+    tq, tk, tv, tw = (torch.from_numpy(x).to(dev) for x in (Q, K, V, W))
+    outs = []
+    for _ in range(2):
+        O = torch.empty((B, H, S, D), dtype=torch.float16, device=dev)
+        C = torch.empty((B * H * S, 96), dtype=torch.float16, device=dev)
+        g.attn_f16_fwd(tq, tk, tv, O, True)
+        g.gemm_f16(O.view(B * H * S, D), tw, None, C, "none")
+        torch.cuda.synchronize()
+        outs.append((O.cpu().numpy(), C.cpu().numpy()))
+    assert np.array_equal(outs[0][0].view(np.uint16), outs[1][0].view(np.uint16))
+    assert np.array_equal(outs[0][1].view(np.uint16), outs[1][1].view(np.uint16))
+    O_ref = oracle_mod.attention(Q, K, V, True)
+    check(outs[0][0], O_ref, "attention")
+    # the composition, all on the oracle's side
+    res = parity(outs[0][1], oracle_mod.gemm(O_ref.reshape(B * H * S, D), W, None, "none"))
+    assert res["ok"], res
+    assert g.attn_f16_debug_status()[0] == 0 and g.gemm_f16_debug_status()[0] == 0

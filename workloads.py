@@ -21,7 +21,9 @@ Generator (counter based, so any element can be drawn independently):
   rounded to fp16 (round to nearest even, numpy's conversion).
 
 The five workloads are the fused-GEMM configurations: shapes, distributions
-and seeds as listed in ``WORKLOADS``.
+and seeds as listed in ``WORKLOADS``.  ``ATTN_WORKLOADS`` are the attention
+forward configurations: Q, K, V drawn from streams t = 4, 5, 6 of their seed,
+N(0,1) rounded to fp16; query rows to check drawn from stream 7.
 """
 from __future__ import annotations
 
@@ -37,6 +39,7 @@ _C2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 22
 
 T_A, T_B, T_BIAS, T_SAMPLES = 0, 1, 2, 3
+T_Q, T_K, T_V, T_ROWS = 4, 5, 6, 7
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -150,3 +153,46 @@ WORKLOADS = {
 
 # the 8192^3 check: 4096 seeded elements plus full rows 0 and M-1
 SAMPLED_ELEMS = 4096
+
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    """Attention forward O = softmax(Q K^T / sqrt(D)) V on (B, H, S, D) fp16
+    tensors; Q, K, V ~ N(0, 1).  The pages give the operation and its FLOP
+    model but no sizes: the shapes are those of a long-context prefill (S 4096,
+    head dimension 128) and small and ragged cases for full checks."""
+    name: str
+    B: int
+    H: int
+    S: int
+    D: int
+    causal: bool
+    seed: int
+    check: str            # "full" or "sampled"
+
+    def flops(self) -> float:
+        return 4.0 * self.B * self.H * self.S * self.S * self.D * (0.5 if self.causal else 1.0)
+
+    def alg_bytes(self) -> float:
+        return 4.0 * 2.0 * self.B * self.H * self.S * self.D   # Q, K, V read once, O written once
+
+    def make(self):
+        shape = (self.B, self.H, self.S, self.D)
+        return tuple(fp16_tensor(shape, "normal", 1.0, self.seed, t) for t in (T_Q, T_K, T_V))
+
+    def sample_rows(self, count: int) -> np.ndarray:
+        """`count` seeded flattened query rows (b * H + h) * S + i, plus the
+        first and last row of the first and last head."""
+        total = self.B * self.H * self.S
+        x = raw_draws(self.seed, T_ROWS, 0, count)
+        extra = [0, self.S - 1, total - self.S, total - 1]
+        return np.unique(np.concatenate([(x % np.uint64(total)).astype(np.int64), np.array(extra, np.int64)]))
+
+
+ATTN_WORKLOADS = {
+    "attn_small": AttnWorkload("attn_small", 1, 2, 256, 64, False, 10, "full"),
+    "attn_small_causal": AttnWorkload("attn_small_causal", 1, 2, 256, 128, True, 11, "full"),
+    "attn_ragged_causal": AttnWorkload("attn_ragged_causal", 2, 3, 1000, 128, True, 12, "full"),
+    "attn_prefill": AttnWorkload("attn_prefill", 4, 32, 4096, 128, False, 13, "sampled"),
+    "attn_prefill_causal": AttnWorkload("attn_prefill_causal", 4, 32, 4096, 128, True, 14, "sampled"),
+}
