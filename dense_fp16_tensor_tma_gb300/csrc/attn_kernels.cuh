@@ -17,11 +17,13 @@
 //     of two TMEM score buffers, and O += P_j V_j (M = 128, N = D, K = 128;
 //     P K-major from shared memory, V MN-major) into the TMEM output;
 //     S_{j+1} is computed while the softmax of block j runs;
-//   * warps 2..5: softmax, one query row per thread (its TMEM lane): pass 1
+//   * warps 2..9: softmax, one query row per thread pair (its TMEM lane; the
+//     two warps of a lane quarter each take 64 keys of a block): pass 1
 //     reads the row of S_j for the block maximum, pass 2 reads it again,
 //     forms p = 2^(s * scale * log2 e - m) in fp32, sums it and writes it as
-//     fp16 into a shared-memory P tile in the 128-byte-swizzled K-major layout
-//     the tensor core reads.  The running maximum m is raised only when a
+//     fp16 into one of two shared-memory P tiles (128-byte-swizzled K-major,
+//     as the tensor core reads it), so the softmax of block j + 1 never waits
+//     for the P V product of block j.  The running maximum m is raised only when a
 //     block's maximum exceeds it by more than 8 (in log2 units); O and the
 //     running sum l are then rescaled in place (TMEM load, multiply, store).
 //     Between raises p stays below 2^8, which fp16 and the fp32 sums hold
@@ -46,13 +48,15 @@ __device__ unsigned int g_attn_status;   // bounded-wait status word of the atte
 
 constexpr int kQRows = 128;              // query rows per CTA = MMA M = TMEM lanes
 constexpr int kKeys = 128;               // keys per block = N of S = K of P V
-constexpr int kAttnThreads = 192;        // producer, MMA, 4 softmax warps
+constexpr int kAttnThreads = 320;        // producer, MMA, 8 softmax warps (two per TMEM lane quarter)
+constexpr uint32_t kMaxDynSmem = 232448;  // 227 KiB: the most dynamic shared memory a CTA may have
 constexpr uint32_t kBox = 64 * 128 * 2;  // one 64 (D or keys) x 128 (rows) fp16 box: 16 KiB
 constexpr uint32_t kTmemCols = 512;      // two 128-column score buffers + O (<= 128 columns)
 constexpr uint32_t kOCol = 256;          // first TMEM column of O
 constexpr float kRaise = 8.0f;           // raise the running max only past 2^8 growth
 
-enum : uint32_t { ROLE_SOFTMAX = 6, BAR_Q = 7, BAR_K = 8, BAR_V = 9, BAR_S = 10, BAR_P = 11, BAR_PV = 12 };
+enum : uint32_t { ROLE_SOFTMAX = 6, BAR_Q = 7, BAR_K = 8, BAR_V = 9, BAR_S = 10, BAR_P = 11, BAR_PV = 12,
+                  BAR_X = 13, BAR_ALIGN = 14 };
 
 struct AttnParams {
     __half* O;
@@ -69,18 +73,27 @@ struct AttnSmem {
     static constexpr uint32_t kQ = 0;                        // D/64 boxes
     static constexpr uint32_t kK = kQ + (D / 64) * kBox;     // 2 slots x D/64 boxes
     static constexpr uint32_t kV = kK + 2 * (D / 64) * kBox; // 2 slots x D/64 boxes
-    static constexpr uint32_t kP = kV + 2 * (D / 64) * kBox; // 2 boxes (keys 0-63, 64-127)
-    static constexpr uint32_t kBars = kP + 2 * kBox;
-    // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full, pv_done, drain
-    static constexpr uint32_t kNumBars = 14;
+    static constexpr uint32_t kP = kV + 2 * (D / 64) * kBox; // 2 buffers x 2 boxes (keys 0-63, 64-127)
+    static constexpr uint32_t kX = kP + 4 * kBox;             // row-maximum exchange [2 parity][2 half][128]
+    static constexpr uint32_t kBars = kX + 2 * 2 * 128 * 4;
+    // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full, pv_done[2], drain,
+    // xch[4 quarters][2 parity]
+    static constexpr uint32_t kNumBars = 15 + 8;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kEnd = kAbort + 4;
+    // 1 KiB of slack aligns the base to the 128-byte swizzle's 1 KiB atoms
+    // when it fits; otherwise (D = 128) the kernel checks that the base is
+    // already aligned (the dynamic window starts after the 1 KiB the system
+    // reserves) and reports BAR_ALIGN instead of running if it is not.
+    static constexpr bool kSlack = kEnd + 1024 <= kMaxDynSmem;
     // The CTA allocates all 512 tensor-memory columns, so a second CTA on the
     // same SM would only wait in its allocation: ask for enough shared memory
     // (> half of the SM's 228 KiB) that one CTA fits per SM.
     static constexpr uint32_t kOnePerSm = 120 * 1024;
-    static constexpr uint32_t kDynamicBytes = kEnd + 1024 > kOnePerSm ? kEnd + 1024 : kOnePerSm;
+    static constexpr uint32_t kNeed = kEnd + (kSlack ? 1024 : 0);
+    static constexpr uint32_t kDynamicBytes = kNeed > kOnePerSm ? kNeed : kOnePerSm;
+    static_assert(kDynamicBytes <= kMaxDynSmem, "shared memory plan too large");
 };
 
 // 3-D tiled load (D, S, B*H) global -> shared, completing `bar`.  c0 (the D
@@ -113,6 +126,15 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// acc + the two fp16 halves of w, each widened exactly to fp32 (the
+// mixed-precision add of sm_100 and later: no separate conversion)
+__device__ __forceinline__ float add_f16x2_to_f32(float acc, uint32_t w) {
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "add.f32.f16 %0, lo, %0;\n\tadd.f32.f16 %0, hi, %0;\n\t}"
+        : "+f"(acc) : "r"(w));
+    return acc;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -133,6 +155,10 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
+    if (!SM::kSlack && (raw_s & 1023u) != 0) {   // uniform over the CTA: nothing started yet
+        if (threadIdx.x == 0) atomicCAS(&g_attn_status, 0u, 0x80000000u | (ROLE_SOFTMAX << 8) | BAR_ALIGN);
+        return;
+    }
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
     uint8_t* base = smem_raw + (base_s - raw_s);
     const uint32_t sQ = base_s + SM::kQ, sK = base_s + SM::kK, sV = base_s + SM::kV, sP = base_s + SM::kP;
@@ -143,7 +169,10 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     auto v_full = [&](int s) { return bars + 8u * (5 + s); };
     auto v_empty = [&](int s) { return bars + 8u * (7 + s); };
     auto s_full = [&](int b) { return bars + 8u * (9 + b); };
-    const uint32_t p_full = bars + 8u * 11, pv_done = bars + 8u * 12, drain_bar = bars + 8u * 13;
+    const uint32_t p_full = bars + 8u * 11, drain_bar = bars + 8u * 14;
+    auto pv_done = [&](int b) { return bars + 8u * (12 + b); };   // P V of blocks b, b + 2, ... completed
+    auto xch_bar = [&](int quarter, int b) { return bars + 8u * (15 + 2 * quarter + b); };
+    auto p_buf = [&](int b) { return sP + static_cast<uint32_t>(b) * 2u * kBox; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + SM::kTmemSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + SM::kAbort);
 
@@ -166,8 +195,10 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             mbar_init(v_empty(s), 1);
             mbar_init(s_full(s), 1);
         }
-        mbar_init(p_full, 4);      // the four softmax warps
-        mbar_init(pv_done, 1);
+        mbar_init(p_full, 8);      // the eight softmax warps
+        mbar_init(pv_done(0), 1);
+        mbar_init(pv_done(1), 1);
+        for (int i = 0; i < 8; ++i) mbar_init(bars + 8u * (15 + i), 64);   // both warps of a lane quarter
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -262,12 +293,12 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 for (int k = 0; k < kKeys / 16; ++k) {
                     // P: K-major, keys 0-63 in box 0, 64-127 in box 1; V: MN-major,
                     // 64-column boxes 16 KiB apart (LBO), 16 key rows = 2 KiB per step
-                    const uint64_t a = smem_desc_sw128(sP + (k >> 2) * kBox + (k & 3) * 32, 0, 1024);
+                    const uint64_t a = smem_desc_sw128(p_buf(s) + (k >> 2) * kBox + (k & 3) * 32, 0, 1024);
                     const uint64_t b = smem_desc_sw128(sV + s * kDB * kBox + k * 2048, kBox, 1024);
                     tc_mma_f16(o_tmem, a, b, kIdescO, (j | k) != 0 ? 1u : 0u);
                 }
                 tc_commit(v_empty(s));
-                tc_commit(pv_done);
+                tc_commit(pv_done(s));
                 if (j + 2 < nblk) ok = issue_s(j + 2);   // score buffer s was read before P_j was written
             }
             tc_commit(drain_bar);
@@ -276,92 +307,130 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + output
+        // Two warps per TMEM lane quarter: warp half h takes keys 64h .. 64h + 63
+        // of every block (it writes P box h) and O columns h D/2 .. (h + 1) D/2.
+        // The pair combines its row maxima (and, at the end, its row sums)
+        // through shared memory, double-buffered by block parity, behind a
+        // 64-thread mbarrier with a bounded wait.
         const int quarter = warp & 3;                // TMEM lanes 32 * quarter ..
+        const int half = (warp - 2) >> 2;
         const int r = 32 * quarter + lane;           // this thread's row of the tile
         const int q = q0 + r;                        // its query index
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
+        volatile float* xch = reinterpret_cast<volatile float*>(base + SM::kX);
+        auto exchange = [&](int use, int parity_slot, float mine, float& theirs) -> bool {
+            // use: how many times this (quarter, slot) barrier was used before
+            xch[(parity_slot * 2 + half) * 128 + r] = mine;
+            mbar_arrive(xch_bar(quarter, parity_slot));
+            const bool got = mbar_wait_bounded(xch_bar(quarter, parity_slot), use & 1, p.timeout_ns, abort_flag,
+                                               status, ROLE_SOFTMAX, BAR_X);
+            theirs = xch[(parity_slot * 2 + (1 - half)) * 128 + r];
+            return got;
+        };
+        constexpr int kOCols = D / 2;                // this warp's O columns
+        const uint32_t o_cols = lane_base + kOCol + static_cast<uint32_t>(half * kOCols);
         float m = -INFINITY, l = 0.0f;
         bool ok = true;
         for (int j = 0; j < nblk; ++j) {
             const int k0 = j * kKeys;
             const int s = j & 1;
-            const uint32_t s_tmem = lane_base + static_cast<uint32_t>(s * kKeys);
+            const uint32_t s_tmem = lane_base + static_cast<uint32_t>(s * kKeys + 64 * half);
             ok = mbar_wait_bounded(s_full(s), (j >> 1) & 1, p.timeout_ns, abort_flag, status, ROLE_SOFTMAX, BAR_S);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             // keys past S, and (causal) keys after this query, do not count
             const bool masked_block = (k0 + kKeys > p.S) || (p.causal && j == nblk - 1);
-            const int key_lim = p.causal ? min(p.S, q + 1) - k0 : p.S - k0;   // valid keys: col < key_lim
-            // pass 1: the block maximum of this row
-            float bmax = -INFINITY;
-#pragma unroll 1
-            for (int c = 0; c < kKeys / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(s_tmem + 32u * c, v);
-                tmem_wait_ld(v);
+            const int key_lim = (p.causal ? min(p.S, q + 1) - k0 : p.S - k0) - 64 * half;   // valid: col < key_lim
+            // this warp's 64 scores of the row: two loads in flight, one wait, kept
+            // in registers for both passes (each wait call ties one chunk's registers)
+            uint32_t v[64];
+            tmem_ld_32x32b_x32(s_tmem, *reinterpret_cast<uint32_t(*)[32]>(v));
+            tmem_ld_32x32b_x32(s_tmem + 32u, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+            tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(v));
+            tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(v + 32));
+            // The largest scaled score comes from the largest raw score when the
+            // scale is positive and from the smallest when it is negative.  Keys
+            // that do not count get the raw score that loses that comparison
+            // (-inf, or +inf for a negative scale): their scaled score is -inf
+            // and their weight 2^-inf = 0.
+            const bool pos = p.scale_log2 >= 0.0f;
+            if (masked_block) {
+                const uint32_t lose = __float_as_uint(pos ? -INFINITY : INFINITY);
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    const float x = __uint_as_float(v[t]);
-                    const bool valid = !masked_block || (32 * c + t < key_lim);
-                    bmax = valid ? fmaxf(bmax, x) : bmax;
-                }
+                for (int t = 0; t < 64; ++t)
+                    if (t >= key_lim) v[t] = lose;
             }
-            const float bmax2 = bmax * p.scale_log2;   // -inf if no valid key in this block
+            // pass 1: the row's largest scaled score over this warp's 64 keys, then the pair's
+            float bm[4];   // four independent chains
+            if (pos) {
+                bm[0] = bm[1] = bm[2] = bm[3] = -INFINITY;
+#pragma unroll
+                for (int t = 0; t < 64; ++t) bm[t & 3] = fmaxf(bm[t & 3], __uint_as_float(v[t]));
+            } else {
+                bm[0] = bm[1] = bm[2] = bm[3] = INFINITY;
+#pragma unroll
+                for (int t = 0; t < 64; ++t) bm[t & 3] = fminf(bm[t & 3], __uint_as_float(v[t]));
+            }
+            float bmax = pos ? fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3]))
+                             : fminf(fminf(bm[0], bm[1]), fminf(bm[2], bm[3]));
+            bmax *= p.scale_log2;   // the largest scaled score (log2 units); -inf if no key counts
+            float other = -INFINITY;
+            ok = exchange(j >> 1, s, bmax, other);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            const float bmax2 = fmaxf(bmax, other);
             float m_new = m;
             bool raise = false;
             if (bmax2 > m + kRaise || m == -INFINITY) {
                 m_new = fmaxf(m, bmax2);
                 raise = m != -INFINITY && m_new != m;
             }
-            // P and O are still read by the previous block's P V product
-            if (j > 0) {
-                ok = mbar_wait_bounded(pv_done, (j - 1) & 1, p.timeout_ns, abort_flag, status, ROLE_SOFTMAX, BAR_PV);
+            // P buffer j & 1 was last read by P V of block j - 2, which completed
+            // before S_j (the tensor core finishes its MMAs in issue order).  O is
+            // rescaled only after P V of block j - 1 has finished; that barrier
+            // is then at most one phase behind, so its parity names the phase.
+            if (__any_sync(0xffffffffu, raise)) {
+                ok = mbar_wait_bounded(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, p.timeout_ns, abort_flag, status,
+                                       ROLE_SOFTMAX, BAR_PV);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
-            }
-            if (__any_sync(0xffffffffu, raise)) {
                 const float alpha = raise ? fast_exp2(m - m_new) : 1.0f;
                 l *= alpha;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < kOCols / 32; ++c) {
                     uint32_t v[32];
-                    tmem_ld_32x32b_x32(lane_base + kOCol + 32u * c, v);
+                    tmem_ld_32x32b_x32(o_cols + 32u * c, v);
                     tmem_wait_ld(v);
 #pragma unroll
                     for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
-                    tmem_st_32x32b_x32(lane_base + kOCol + 32u * c, v);
+                    tmem_st_32x32b_x32(o_cols + 32u * c, v);
                 }
                 tmem_wait_st();
             }
             m = m_new;
-            // pass 2: p = 2^(x * scale_log2 - m) as fp16 into the swizzled P tile
+            // pass 2: p = 2^(x * scale_log2 - m) as fp16 into box `half` of P buffer s
             const float mm = (m == -INFINITY) ? 0.0f : m;
-#pragma unroll 1
-            for (int c = 0; c < kKeys / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(s_tmem + 32u * c, v);
-                tmem_wait_ld(v);
+            const uint32_t row_base = p_buf(s) + static_cast<uint32_t>(half) * kBox + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
                 uint32_t h[16];
-                float rs = 0.0f;
+                float rs0 = 0.0f, rs1 = 0.0f;
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
-                    const bool v0 = !masked_block || (32 * c + 2 * t < key_lim);
-                    const bool v1 = !masked_block || (32 * c + 2 * t + 1 < key_lim);
-                    const float e0 = v0 ? fast_exp2(fmaf(__uint_as_float(v[2 * t]), p.scale_log2, -mm)) : 0.0f;
-                    const float e1 = v1 ? fast_exp2(fmaf(__uint_as_float(v[2 * t + 1]), p.scale_log2, -mm)) : 0.0f;
+                    // masked keys hold -inf: 2^-inf = 0
+                    const float e0 = fast_exp2(fmaf(__uint_as_float(v[32 * c + 2 * t]), p.scale_log2, -mm));
+                    const float e1 = fast_exp2(fmaf(__uint_as_float(v[32 * c + 2 * t + 1]), p.scale_log2, -mm));
                     const __half2 hv = __floats2half2_rn(e0, e1);
-                    // the sum takes the fp16 values the tensor core multiplies
-                    const float2 back = __half22float2(hv);
-                    rs += back.x + back.y;
                     h[t] = *reinterpret_cast<const uint32_t*>(&hv);
+                    // the sum takes the fp16 values the tensor core multiplies
+                    if (t & 1) rs1 = add_f16x2_to_f32(rs1, h[t]);
+                    else rs0 = add_f16x2_to_f32(rs0, h[t]);
                 }
-                l += rs;
-                // keys 32c .. 32c+31 = box c / 2, 16-byte chunks 4 (c % 2) .. 4 (c % 2) + 3,
-                // chunk position XOR (row % 8): the 128-byte swizzle
-                const uint32_t row_base = sP + (c >> 1) * kBox + static_cast<uint32_t>(r) * 128u;
+                l += rs0 + rs1;
+                // keys 32c .. 32c+31 of the box: 16-byte chunks 4c .. 4c + 3, chunk
+                // position XOR (row % 8): the 128-byte swizzle
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const uint32_t chunk = static_cast<uint32_t>((4 * (c & 1) + u) ^ (r & 7));
+                    const uint32_t chunk = static_cast<uint32_t>((4 * c + u) ^ (r & 7));
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                                  ::"r"(row_base + chunk * 16u), "r"(h[4 * u]), "r"(h[4 * u + 1]),
                                    "r"(h[4 * u + 2]), "r"(h[4 * u + 3])
@@ -374,18 +443,25 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             if (lane == 0) mbar_arrive(p_full);
         }
         // output: O / l after the last P V product
-        if (ok && nblk > 0) {
-            ok = mbar_wait_bounded(pv_done, (nblk - 1) & 1, p.timeout_ns, abort_flag, status, ROLE_SOFTMAX, BAR_PV);
+        if (ok && nblk > 0) {   // the last P V (its commit also covers every earlier MMA)
+            const int jl = nblk - 1;
+            ok = mbar_wait_bounded(pv_done(jl & 1), (jl >> 1) & 1, p.timeout_ns, abort_flag, status, ROLE_SOFTMAX,
+                                   BAR_PV);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        float l_other = 0.0f;
+        if (ok && nblk > 0) {   // the row sum: both halves of the keys
+            ok = exchange(nblk >> 1, nblk & 1, l, l_other);
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok && nblk > 0) {
             tc_fence_after();
-            const float inv = 1.0f / l;
-            __half* orow = p.O + (static_cast<int64_t>(bh) * p.S + q) * D;
+            const float inv = 1.0f / (l + l_other);
+            __half* orow = p.O + (static_cast<int64_t>(bh) * p.S + q) * D + half * kOCols;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < kOCols / 32; ++c) {
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(lane_base + kOCol + 32u * c, v);
+                tmem_ld_32x32b_x32(o_cols + 32u * c, v);
                 tmem_wait_ld(v);
                 uint32_t h[16];
 #pragma unroll

@@ -134,7 +134,7 @@ def test_attention_running_max_raised_every_block(g, torch_dev, oracle_mod, D):
         check(got, oracle_mod.attention(Q, K, V, causal, scale=scale), f"ramp causal={causal}")
 
 
-@pytest.mark.parametrize("scale", [0.05, -0.1, 0.3])
+@pytest.mark.parametrize("scale", [0.05, -0.1, 0.3, -1.0])
 def test_attention_explicit_scale(g, torch_dev, oracle_mod, scale):
     rng = np.random.default_rng(84)
     Q, K, V = qkv(rng, (2, 2, 384, 64))
