@@ -15,12 +15,17 @@ gemm_f16_ex with the matching flags.  The default "nn" is plain row-major.
 --impl reference times the CPU oracle (fp64, all host cores) on bounded row
 samples of the same workload: the comparison arm.  N > 1 runs independent
 replicas, one per GPU (weak scaling; no collective on the data path).
+
+The attention workloads (--workload attn_*) time attn_f16_fwd the same way:
+one step = one attention forward over (B, H, S, D) inputs resident in HBM,
+throughput by the FLOP model 4 B H S^2 D (halved when causal).
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -447,13 +452,220 @@ def run_ours(args, w, epi):
     return 0
 
 
+# ------------------------------------------------------------------ attention forward
+
+ATTN_METRIC = "TFLOP/s of fused fp16 attention forward (FLOP model 4 B H S^2 D, halved when causal)"
+
+
+def attn_config(w):
+    return {
+        "workload": f"{w.name}: B={w.B} H={w.H} S={w.S} D={w.D} causal={int(w.causal)}, fp16 Q,K,V ~normal, "
+                    f"scale 1/sqrt(D), seed {w.seed}",
+        "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": w.causal, "seed": w.seed,
+        "flops_per_step": w.flops(), "alg_bytes_per_step": w.alg_bytes(),
+        "flop_model": "4 B H S^2 D, x0.5 causal",
+        "l2": ("inputs larger than L2 (no flush)" if w.alg_bytes() > L2_BYTES
+               else "L2 flushed between steps (256 MiB write)"),
+    }
+
+
+def attn_oracle_timing(w, Q, K, V, target_s):
+    """Time the oracle on a bounded sample of query rows; (TFLOP/s by the FLOP model, s, rows, threads)."""
+    import oracle
+    threads = oracle.default_threads()
+    scale = 1.0 / math.sqrt(w.D)
+    probe = w.sample_rows(max(threads, 16))
+    t0 = time.perf_counter()
+    oracle.attention_rows(Q, K, V, w.causal, scale, probe)
+    per_row = max(time.perf_counter() - t0, 1e-6) / probe.size
+    total = w.B * w.H * w.S
+    n = int(min(total, max(threads, target_s / per_row)))
+    rows = w.sample_rows(n)
+    t0 = time.perf_counter()
+    oracle.attention_rows(Q, K, V, w.causal, scale, rows)
+    dt = time.perf_counter() - t0
+    # model FLOPs of the sampled rows: the workload's FLOPs x the share of rows
+    return w.flops() * rows.size / total / dt / 1e12, dt, rows.size, threads
+
+
+def run_attention_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    Q, K, V = w.make()
+    budget_s = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    tfl, _, rows, threads = attn_oracle_timing(w, Q, K, V, budget_s)
+    total = w.B * w.H * w.S
+    sample_rows = w.sample_rows(rows)
+    scale = 1.0 / math.sqrt(w.D)
+    for _ in range(args.warmup):
+        oracle.attention_rows(Q, K, V, w.causal, scale, sample_rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention_rows(Q, K, V, w.causal, scale, sample_rows)
+    dt = time.perf_counter() - t0
+    value = w.flops() * sample_rows.size / total * args.steps / dt / 1e12
+    sample = (f"{sample_rows.size} of {total} query rows per step (every admissible key, full D), "
+              f"fp64 C++ oracle")
+    line = {
+        "impl": "reference", "metric": ATTN_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": attn_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_attention(args, w):
+    import torch
+    world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import dense_fp16_tensor_tma_gb300 as g
+
+    wr = w if world == 1 else workloads.AttnWorkload(**{**w.__dict__, "seed": w.seed + 1000 * rank})
+    t_gen = time.perf_counter()
+    Q, K, V = wr.make()
+    log(f"[rank {rank}] inputs generated in {time.perf_counter() - t_gen:.1f}s")
+    tq, tk, tv = (torch.from_numpy(x).to(dev) for x in (Q, K, V))
+    O = torch.empty_like(tq)
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    flush = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device=dev) if w.alg_bytes() <= L2_BYTES else None
+
+    def step():
+        st = g.attn_f16_fwd_ptr(tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), O.data_ptr(), w.B, w.H, w.S, w.D,
+                                w.causal, 0.0, sh)
+        if st != 0:
+            raise g.GemmError(st, "attn_f16_fwd")
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            if flush is not None:
+                flush.fill_(1.0)
+            step()
+    stream.synchronize()
+    st, word = g.attn_f16_debug_status(stream)
+    if st != 0:
+        raise SystemExit(f"device status {st} ({word:#x}) after warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    dist_barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(1.0)       # outside the events
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    dist_barrier(world)
+    clock_lines = sampler.stop()
+    per_launch_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    elapsed_ms = starts[0].elapsed_time(ends[-1]) if flush is None else sum(per_launch_ms)
+    elapsed_ms = dist_max(world, elapsed_ms)
+    st, word = g.attn_f16_debug_status(stream)
+    if st != 0:
+        raise SystemExit(f"device status {st} ({word:#x}) after timed steps")
+    flops = w.flops()
+    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    avg_launch_ms = statistics.mean(per_launch_ms)
+    tensor_peak, _, src = read_peaks()
+    achieved = flops / (avg_launch_ms * 1e-3) / 1e12
+    traffic = committed_traffic(w.name)
+    roof = {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
+            "frac": achieved / tensor_peak, "traffic": traffic,
+            "peak_source": f"{src} (bf16 burst x fp16/bf16 ratio {FP16_PER_BF16})",
+            "kernel": f"attn_f16_fwd_kernel<{w.D}>", "avg_launch_ms": avg_launch_ms}
+
+    # ---- end to end: pinned host Q, K, V in and O out through the C ABI every step
+    hq, hk, hv = (torch.from_numpy(x).pin_memory() for x in (Q, K, V))
+    ho = torch.empty(tuple(O.shape), dtype=torch.float16).pin_memory()
+    h2d = 3 * hq.numel() * 2
+    d2h = ho.numel() * 2
+
+    def e2e_step():
+        tq.copy_(hq, non_blocking=True)
+        tk.copy_(hk, non_blocking=True)
+        tv.copy_(hv, non_blocking=True)
+        step()
+        ho.copy_(O, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 50))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+    stream.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_barrier(world)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = dist_max(world, ev0.elapsed_time(ev1))
+    dist_barrier(world)
+    e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tfl, secs, rows, threads = attn_oracle_timing(w, Q, K, V, args.cpu_seconds)
+        cpu = {"value": tfl, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{rows} of {w.B * w.H * w.S} query rows (every admissible key, full D), fp64 C++ oracle, "
+                         f"{secs:.1f}s"}
+    if rank == 0:
+        clocks = ClockSampler.summarize(ClockSampler.parse(clock_lines), t_wall0, t_wall1)
+        line = {
+            "metric": ATTN_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": elapsed_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic",
+            "config": {**attn_config(w), "parallelism": f"replicas{world}" if world > 1 else "single"},
+            "roofline": roof,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms / e2e_steps},
+            "gpu_launches": args.steps,
+            "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                       "reasons": clocks["reasons"], "samples": clocks["samples"],
+                       "window": clocks["window"], "window_s": round(t_wall1 - t_wall0, 3)},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.ATTN_WORKLOADS))
     ap.add_argument("--epilogue", default=None)
     ap.add_argument("--layout", default="nn", choices=sorted(LAYOUT_TEXT))
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -461,6 +673,9 @@ def main():
     args = ap.parse_args()
     if args.steps < 1:
         raise SystemExit("--steps must be >= 1")
+    if args.workload in workloads.ATTN_WORKLOADS:
+        w = workloads.ATTN_WORKLOADS[args.workload]
+        return run_attention_reference(args, w) if args.impl == "reference" else run_attention(args, w)
     w = workloads.WORKLOADS[args.workload]
     epi = args.epilogue or w.epilogues[-1]
     if args.impl == "reference":

@@ -179,9 +179,13 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // heaviest query tiles first (causal: later tiles see more keys)
-    const int qt = p.nq - 1 - static_cast<int>(blockIdx.x) / p.BH;
-    const int bh = static_cast<int>(blockIdx.x) % p.BH;
+    // Consecutive CTAs take the query tiles of one head, so the CTAs in flight
+    // share a few heads' K and V in L2 (ordering by tile across heads made
+    // every query tile read its head's K and V from HBM again: 7.4 GB per
+    // launch at B 4, H 32, S 4096, D 128).  Within a head the heaviest tiles
+    // (causal: the last ones) start first.
+    const int bh = static_cast<int>(blockIdx.x) / p.nq;
+    const int qt = p.nq - 1 - static_cast<int>(blockIdx.x) % p.nq;
     const int q0 = qt * kQRows;
     const int kblocks_all = (p.S + kKeys - 1) / kKeys;
     const int nblk = p.causal ? min(kblocks_all, qt + 1) : kblocks_all;
