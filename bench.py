@@ -58,9 +58,14 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
-def kernel_source_hash() -> str:
+ATTN_SOURCES = ("dense_fp16_tensor_tma_gb300/csrc/attn_kernels.cuh",
+                "dense_fp16_tensor_tma_gb300/csrc/attn_f16.cu",
+                "dense_fp16_tensor_tma_gb300/csrc/ptx.cuh")
+
+
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -121,7 +126,7 @@ def roofline(w, avg_launch_ms, traffic, plan):
             "ridge_flop_per_byte": ridge, "kernel": kernel_name(plan), "avg_launch_ms": avg_launch_ms}
 
 
-def committed_traffic(workload_name):
+def committed_traffic(workload_name, sources=KERNEL_SOURCES):
     """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
@@ -129,7 +134,7 @@ def committed_traffic(workload_name):
             rec = json.load(f).get(workload_name)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("kernel_source_hash") != kernel_source_hash():
+    if not rec or rec.get("kernel_source_hash") != kernel_source_hash(sources):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -591,7 +596,7 @@ def run_attention(args, w):
     avg_launch_ms = statistics.mean(per_launch_ms)
     tensor_peak, _, src = read_peaks()
     achieved = flops / (avg_launch_ms * 1e-3) / 1e12
-    traffic = committed_traffic(w.name)
+    traffic = committed_traffic(w.name, ATTN_SOURCES)
     roof = {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
             "frac": achieved / tensor_peak, "traffic": traffic,
             "peak_source": f"{src} (bf16 burst x fp16/bf16 ratio {FP16_PER_BF16})",
