@@ -8,8 +8,8 @@
 // score matrix never written to memory; causal and non-causal).
 //
 // GB300 design (one CTA per 128 query rows of one head):
-//   * warp 0: TMA producer.  Q once (D/64 boxes of 64 x 128), then K and V
-//     blocks of 128 keys through two 2-slot rings; 3-D tensor maps
+//   * warp 0: TMA producers (lane 0: Q once, then K; lane 1: V), blocks of
+//     128 keys through two 2-slot rings; 3-D tensor maps
 //     (D, S, B*H), so rows past S arrive as zeros and never come from the
 //     next head;
 //   * warp 1: allocates tensor memory and issues tcgen05.mma from one thread:
@@ -135,6 +135,29 @@ __device__ __forceinline__ float add_f16x2_to_f32(float acc, uint32_t w) {
     return acc;
 }
 
+// Three-input maximum / minimum (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float m;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+    return m;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+    float m;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+    return m;
+}
+// (a.x * b + c, a.y * b + c) as one paired fp32 FMA (sm_100 and later).
+__device__ __forceinline__ float2 fma2_bc(float ax, float ay, float b, float c) {
+    uint64_t x, y, z, d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(ax), "f"(ay));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(y) : "f"(b));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(z) : "f"(c));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(x), "l"(y), "l"(z));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+    return r;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -226,34 +249,38 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
+        // lane 0 streams Q and K, lane 1 streams V: a K load never waits behind
+        // a V slot (V_j frees only after P V of block j - 2, K_j after S_{j-2})
+        if (lane < 2) {
+            const bool is_k = lane == 0;
             bool ok = true;
-            mbar_arrive_expect_tx(q_full, kTileBytes);
-            for (int c = 0; c < kDB; ++c) tma_load_3d(sQ + c * kBox, &tmQ, q_full, 64 * c, q0, bh);
-            int k_issued = 0, v_issued = 0;
+            if (is_k) {
+                mbar_arrive_expect_tx(q_full, kTileBytes);
+                for (int c = 0; c < kDB; ++c) tma_load_3d(sQ + c * kBox, &tmQ, q_full, 64 * c, q0, bh);
+            }
+            const CUtensorMap* tm = is_k ? &tmK : &tmV;
+            const uint32_t ring = is_k ? sK : sV;
+            const uint32_t which = is_k ? BAR_K : BAR_V;
+            int issued = 0;
             for (int j = 0; ok && j < nblk; ++j) {
                 const int s = j & 1;
                 const uint32_t ph = static_cast<uint32_t>((j >> 1) & 1);
-                if (!mbar_wait_bounded(k_empty(s), ph ^ 1u, p.timeout_ns, abort_flag, status, ROLE_PRODUCER,
-                                       BAR_K)) { ok = false; break; }
-                mbar_arrive_expect_tx(k_full(s), kTileBytes);
-                for (int c = 0; c < kDB; ++c)
-                    tma_load_3d(sK + (s * kDB + c) * kBox, &tmK, k_full(s), 64 * c, j * kKeys, bh);
-                ++k_issued;
-                if (!mbar_wait_bounded(v_empty(s), ph ^ 1u, p.timeout_ns, abort_flag, status, ROLE_PRODUCER,
-                                       BAR_V)) { ok = false; break; }
-                mbar_arrive_expect_tx(v_full(s), kTileBytes);
-                for (int c = 0; c < kDB; ++c)
-                    tma_load_3d(sV + (s * kDB + c) * kBox, &tmV, v_full(s), 64 * c, j * kKeys, bh);
-                ++v_issued;
+                const uint32_t empty = is_k ? k_empty(s) : v_empty(s);
+                const uint32_t full = is_k ? k_full(s) : v_full(s);
+                if (!mbar_wait_bounded(empty, ph ^ 1u, p.timeout_ns, abort_flag, status, ROLE_PRODUCER, which)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(full, kTileBytes);
+                for (int c = 0; c < kDB; ++c) tma_load_3d(ring + (s * kDB + c) * kBox, tm, full, 64 * c, j * kKeys, bh);
+                ++issued;
             }
-            // every issued load lands before the CTA can exit (the last one or
-            // two of each ring; earlier ones were waited for by the MMA thread)
-            mbar_wait_bounded(q_full, 0, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_Q);
-            for (int j = max(0, k_issued - 2); j < k_issued; ++j)
-                mbar_wait_bounded(k_full(j & 1), (j >> 1) & 1, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_K);
-            for (int j = max(0, v_issued - 2); j < v_issued; ++j)
-                mbar_wait_bounded(v_full(j & 1), (j >> 1) & 1, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_V);
+            // every issued load lands before the CTA can exit (the last one or two
+            // of each ring; earlier ones were waited for by the MMA thread)
+            if (is_k) mbar_wait_bounded(q_full, 0, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_Q);
+            for (int j = max(0, issued - 2); j < issued; ++j)
+                mbar_wait_bounded(is_k ? k_full(j & 1) : v_full(j & 1), (j >> 1) & 1, p.timeout_ns, nullptr, status,
+                                  ROLE_DRAIN, which);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -365,15 +392,17 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     if (t >= key_lim) v[t] = lose;
             }
             // pass 1: the row's largest scaled score over this warp's 64 keys, then the pair's
-            float bm[4];   // four independent chains
+            float bm[4];   // four independent chains, two new values per three-input step
             if (pos) {
                 bm[0] = bm[1] = bm[2] = bm[3] = -INFINITY;
 #pragma unroll
-                for (int t = 0; t < 64; ++t) bm[t & 3] = fmaxf(bm[t & 3], __uint_as_float(v[t]));
+                for (int t = 0; t < 64; t += 2)
+                    bm[(t >> 1) & 3] = max3f(bm[(t >> 1) & 3], __uint_as_float(v[t]), __uint_as_float(v[t + 1]));
             } else {
                 bm[0] = bm[1] = bm[2] = bm[3] = INFINITY;
 #pragma unroll
-                for (int t = 0; t < 64; ++t) bm[t & 3] = fminf(bm[t & 3], __uint_as_float(v[t]));
+                for (int t = 0; t < 64; t += 2)
+                    bm[(t >> 1) & 3] = min3f(bm[(t >> 1) & 3], __uint_as_float(v[t]), __uint_as_float(v[t + 1]));
             }
             float bmax = pos ? fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3]))
                              : fminf(fminf(bm[0], bm[1]), fminf(bm[2], bm[3]));
@@ -421,8 +450,10 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     // masked keys hold -inf: 2^-inf = 0
-                    const float e0 = fast_exp2(fmaf(__uint_as_float(v[32 * c + 2 * t]), p.scale_log2, -mm));
-                    const float e1 = fast_exp2(fmaf(__uint_as_float(v[32 * c + 2 * t + 1]), p.scale_log2, -mm));
+                    const float2 xs = fma2_bc(__uint_as_float(v[32 * c + 2 * t]), __uint_as_float(v[32 * c + 2 * t + 1]),
+                                              p.scale_log2, -mm);
+                    const float e0 = fast_exp2(xs.x);
+                    const float e1 = fast_exp2(xs.y);
                     const __half2 hv = __floats2half2_rn(e0, e1);
                     h[t] = *reinterpret_cast<const uint32_t*>(&hv);
                     // the sum takes the fp16 values the tensor core multiplies
