@@ -76,9 +76,9 @@ struct AttnSmem {
     static constexpr uint32_t kP = kV + 2 * (D / 64) * kBox; // 2 buffers x 2 boxes (keys 0-63, 64-127)
     static constexpr uint32_t kX = kP + 4 * kBox;             // row-maximum exchange [2 parity][2 half][128]
     static constexpr uint32_t kBars = kX + 2 * 2 * 128 * 4;
-    // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full, pv_done[2], drain,
+    // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2], drain,
     // xch[4 quarters][2 parity]
-    static constexpr uint32_t kNumBars = 15 + 8;
+    static constexpr uint32_t kNumBars = 16 + 8;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kEnd = kAbort + 4;
@@ -192,9 +192,14 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     auto v_full = [&](int s) { return bars + 8u * (5 + s); };
     auto v_empty = [&](int s) { return bars + 8u * (7 + s); };
     auto s_full = [&](int b) { return bars + 8u * (9 + b); };
-    const uint32_t p_full = bars + 8u * 11, drain_bar = bars + 8u * 14;
-    auto pv_done = [&](int b) { return bars + 8u * (12 + b); };   // P V of blocks b, b + 2, ... completed
-    auto xch_bar = [&](int quarter, int b) { return bars + 8u * (15 + 2 * quarter + b); };
+    // P_j written (and O rescaled) for blocks b, b + 2, ...: one barrier per P
+    // buffer, so the softmax of block j + 1 cannot complete a phase before the
+    // MMA thread has seen the one of block j (its next arrival on the same
+    // barrier, block j + 2, needs S_{j+2}, issued only after that)
+    auto p_full = [&](int b) { return bars + 8u * (11 + b); };
+    auto pv_done = [&](int b) { return bars + 8u * (13 + b); };   // P V of blocks b, b + 2, ... completed
+    const uint32_t drain_bar = bars + 8u * 15;
+    auto xch_bar = [&](int quarter, int b) { return bars + 8u * (16 + 2 * quarter + b); };
     auto p_buf = [&](int b) { return sP + static_cast<uint32_t>(b) * 2u * kBox; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + SM::kTmemSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + SM::kAbort);
@@ -222,10 +227,11 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             mbar_init(v_empty(s), 1);
             mbar_init(s_full(s), 1);
         }
-        mbar_init(p_full, 8);      // the eight softmax warps
-        mbar_init(pv_done(0), 1);
-        mbar_init(pv_done(1), 1);
-        for (int i = 0; i < 8; ++i) mbar_init(bars + 8u * (15 + i), 64);   // both warps of a lane quarter
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(p_full(b), 8);   // the eight softmax warps
+            mbar_init(pv_done(b), 1);
+        }
+        for (int i = 0; i < 8; ++i) mbar_init(bars + 8u * (16 + i), 64);   // both warps of a lane quarter
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -309,7 +315,8 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             if (ok && nblk > 1) ok = issue_s(1);
             for (int j = 0; ok && j < nblk; ++j) {
                 // P_j written (and O rescaled) by the softmax warps
-                if (!mbar_wait_bounded(p_full, j & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_P)) {
+                if (!mbar_wait_bounded(p_full(j & 1), (j >> 1) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA,
+                                       BAR_P)) {
                     ok = false;
                     break;
                 }
@@ -475,7 +482,7 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             fence_proxy_async_smem();    // P visible to the tensor core
             tc_fence_before();           // and the O rescale, if any
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(p_full(s));
         }
         // output: O / l after the last P V product
         if (ok && nblk > 0) {   // the last P V (its commit also covers every earlier MMA)
