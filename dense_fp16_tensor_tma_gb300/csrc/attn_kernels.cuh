@@ -15,15 +15,19 @@
 //   * warp 1: allocates tensor memory and issues tcgen05.mma from one thread:
 //     S_j = Q K_j^T (M = 128, N = 128, K = D; both operands K-major) into one
 //     of two TMEM score buffers, and O += P_j V_j (M = 128, N = D, K = 128;
-//     P K-major from shared memory, V MN-major) into the TMEM output;
+//     P read by the tensor core straight from tensor memory, V MN-major from
+//     shared memory) into the TMEM output;
 //     S_{j+1} is computed while the softmax of block j runs;
 //   * warps 2..9: softmax, one query row per thread pair (its TMEM lane; the
 //     two warps of a lane quarter each take 64 keys of a block): pass 1
 //     reads the row of S_j for the block maximum, pass 2 reads it again,
 //     forms p = 2^(s * scale * log2 e - m) in fp32, sums it and writes it as
-//     fp16 into one of two shared-memory P tiles (128-byte-swizzled K-major,
-//     as the tensor core reads it), so the softmax of block j + 1 never waits
-//     for the P V product of block j.  The running maximum m is raised only when a
+//     fp16 pairs into one of two tensor-memory P buffers (one row per lane,
+//     the layout the MMA reads its A operand in), so the softmax of block
+//     j + 1 never waits for the P V product of block j (keeping P in tensor
+//     memory instead of shared memory measured 3 % faster and frees 64 KiB of
+//     shared memory; spending that on a third K and V ring slot did not pay).
+//     The running maximum m is raised only when a
 //     block's maximum exceeds it by more than 8 (in log2 units); O and the
 //     running sum l are then rescaled in place (TMEM load, multiply, store).
 //     Between raises p stays below 2^8, which fp16 and the fp32 sums hold
@@ -51,8 +55,9 @@ constexpr int kKeys = 128;               // keys per block = N of S = K of P V
 constexpr int kAttnThreads = 320;        // producer, MMA, 8 softmax warps (two per TMEM lane quarter)
 constexpr uint32_t kMaxDynSmem = 232448;  // 227 KiB: the most dynamic shared memory a CTA may have
 constexpr uint32_t kBox = 64 * 128 * 2;  // one 64 (D or keys) x 128 (rows) fp16 box: 16 KiB
-constexpr uint32_t kTmemCols = 512;      // two 128-column score buffers + O (<= 128 columns)
+constexpr uint32_t kTmemCols = 512;      // two 128-column score buffers, O (<= 128 columns), two P buffers
 constexpr uint32_t kOCol = 256;          // first TMEM column of O
+constexpr uint32_t kPCol = 384;          // two 64-column P buffers (fp16 pairs), columns 384 .. 511
 constexpr float kRaise = 8.0f;           // raise the running max only past 2^8 growth
 
 enum : uint32_t { ROLE_SOFTMAX = 6, BAR_Q = 7, BAR_K = 8, BAR_V = 9, BAR_S = 10, BAR_P = 11, BAR_PV = 12,
@@ -73,8 +78,7 @@ struct AttnSmem {
     static constexpr uint32_t kQ = 0;                        // D/64 boxes
     static constexpr uint32_t kK = kQ + (D / 64) * kBox;     // 2 slots x D/64 boxes
     static constexpr uint32_t kV = kK + 2 * (D / 64) * kBox; // 2 slots x D/64 boxes
-    static constexpr uint32_t kP = kV + 2 * (D / 64) * kBox; // 2 buffers x 2 boxes (keys 0-63, 64-127)
-    static constexpr uint32_t kX = kP + 4 * kBox;             // row-maximum exchange [2 parity][2 half][128]
+    static constexpr uint32_t kX = kV + 2 * (D / 64) * kBox; // row-maximum exchange [2 parity][2 half][128]
     static constexpr uint32_t kBars = kX + 2 * 2 * 128 * 4;
     // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2], drain,
     // xch[4 quarters][2 parity]
@@ -119,12 +123,26 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
           "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
 }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// Generic-proxy shared-memory writes made visible to the tensor core (async proxy).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem desc]: A (M x 16, fp16) held in tensor memory,
+// one row per lane, two fp16 per 32-bit column.
+__device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // acc + the two fp16 halves of w, each widened exactly to fp32 (the
 // mixed-precision add of sm_100 and later: no separate conversion)
@@ -184,7 +202,7 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     }
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
     uint8_t* base = smem_raw + (base_s - raw_s);
-    const uint32_t sQ = base_s + SM::kQ, sK = base_s + SM::kK, sV = base_s + SM::kV, sP = base_s + SM::kP;
+    const uint32_t sQ = base_s + SM::kQ, sK = base_s + SM::kK, sV = base_s + SM::kV;
     const uint32_t bars = base_s + SM::kBars;
     const uint32_t q_full = bars;
     auto k_full = [&](int s) { return bars + 8u * (1 + s); };
@@ -200,7 +218,6 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     auto pv_done = [&](int b) { return bars + 8u * (13 + b); };   // P V of blocks b, b + 2, ... completed
     const uint32_t drain_bar = bars + 8u * 15;
     auto xch_bar = [&](int quarter, int b) { return bars + 8u * (16 + 2 * quarter + b); };
-    auto p_buf = [&](int b) { return sP + static_cast<uint32_t>(b) * 2u * kBox; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + SM::kTmemSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + SM::kAbort);
 
@@ -329,11 +346,11 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 const uint32_t o_tmem = tmem_base + kOCol;
 #pragma unroll
                 for (int k = 0; k < kKeys / 16; ++k) {
-                    // P: K-major, keys 0-63 in box 0, 64-127 in box 1; V: MN-major,
-                    // 64-column boxes 16 KiB apart (LBO), 16 key rows = 2 KiB per step
-                    const uint64_t a = smem_desc_sw128(p_buf(s) + (k >> 2) * kBox + (k & 3) * 32, 0, 1024);
+                    // P from tensor memory (16 keys = 8 columns of fp16 pairs per step);
+                    // V: MN-major, 64-column boxes 16 KiB apart (LBO), 16 key rows = 2 KiB per step
+                    const uint32_t a = tmem_base + kPCol + static_cast<uint32_t>(s * 64 + k * 8);
                     const uint64_t b = smem_desc_sw128(sV + s * kDB * kBox + k * 2048, kBox, 1024);
-                    tc_mma_f16(o_tmem, a, b, kIdescO, (j | k) != 0 ? 1u : 0u);
+                    tc_mma_f16_ta(o_tmem, a, b, kIdescO, (j | k) != 0 ? 1u : 0u);
                 }
                 tc_commit(v_empty(s));
                 tc_commit(pv_done(s));
@@ -449,7 +466,6 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             m = m_new;
             // pass 2: p = 2^(x * scale_log2 - m) as fp16 into box `half` of P buffer s
             const float mm = (m == -INFINITY) ? 0.0f : m;
-            const uint32_t row_base = p_buf(s) + static_cast<uint32_t>(half) * kBox + static_cast<uint32_t>(r) * 128u;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t h[16];
@@ -468,19 +484,11 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     else rs0 = add_f16x2_to_f32(rs0, h[t]);
                 }
                 l += rs0 + rs1;
-                // keys 32c .. 32c+31 of the box: 16-byte chunks 4c .. 4c + 3, chunk
-                // position XOR (row % 8): the 128-byte swizzle
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t chunk = static_cast<uint32_t>((4 * c + u) ^ (r & 7));
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                                 ::"r"(row_base + chunk * 16u), "r"(h[4 * u]), "r"(h[4 * u + 1]),
-                                   "r"(h[4 * u + 2]), "r"(h[4 * u + 3])
-                                 : "memory");
-                }
+                // keys 64 half + 32c .. + 31: P buffer s columns 32 half + 16c .. + 15
+                tmem_st_32x32b_x16(lane_base + kPCol + static_cast<uint32_t>(s * 64 + 32 * half + 16 * c), h);
             }
-            fence_proxy_async_smem();    // P visible to the tensor core
-            tc_fence_before();           // and the O rescale, if any
+            tmem_wait_st();
+            tc_fence_before();           // P and the O rescale, if any, before the signal
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(s));
         }
