@@ -80,9 +80,8 @@ struct AttnSmem {
     static constexpr uint32_t kV = kK + 2 * (D / 64) * kBox; // 2 slots x D/64 boxes
     static constexpr uint32_t kX = kV + 2 * (D / 64) * kBox; // row-maximum exchange [2 parity][2 half][128]
     static constexpr uint32_t kBars = kX + 2 * 2 * 128 * 4;
-    // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2], drain,
-    // xch[4 quarters][2 parity]
-    static constexpr uint32_t kNumBars = 16 + 8;
+    // q_full, k_full[2], v_full[2], s_full[2], p_full[2], pv_done[2], drain, xch[4 quarters][2 parity]
+    static constexpr uint32_t kNumBars = 12 + 8;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kEnd = kAbort + 4;
@@ -206,18 +205,18 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const uint32_t bars = base_s + SM::kBars;
     const uint32_t q_full = bars;
     auto k_full = [&](int s) { return bars + 8u * (1 + s); };
-    auto k_empty = [&](int s) { return bars + 8u * (3 + s); };
-    auto v_full = [&](int s) { return bars + 8u * (5 + s); };
-    auto v_empty = [&](int s) { return bars + 8u * (7 + s); };
-    auto s_full = [&](int b) { return bars + 8u * (9 + b); };
+    auto v_full = [&](int s) { return bars + 8u * (3 + s); };
+    // S_j completed (block j in score buffer j & 1; K slot j & 1 free again)
+    auto s_full = [&](int b) { return bars + 8u * (5 + b); };
     // P_j written (and O rescaled) for blocks b, b + 2, ...: one barrier per P
     // buffer, so the softmax of block j + 1 cannot complete a phase before the
     // MMA thread has seen the one of block j (its next arrival on the same
     // barrier, block j + 2, needs S_{j+2}, issued only after that)
-    auto p_full = [&](int b) { return bars + 8u * (11 + b); };
-    auto pv_done = [&](int b) { return bars + 8u * (13 + b); };   // P V of blocks b, b + 2, ... completed
-    const uint32_t drain_bar = bars + 8u * 15;
-    auto xch_bar = [&](int quarter, int b) { return bars + 8u * (16 + 2 * quarter + b); };
+    auto p_full = [&](int b) { return bars + 8u * (7 + b); };
+    // P V of blocks b, b + 2, ... completed (V slot b free again)
+    auto pv_done = [&](int b) { return bars + 8u * (9 + b); };
+    const uint32_t drain_bar = bars + 8u * 11;
+    auto xch_bar = [&](int quarter, int b) { return bars + 8u * (12 + 2 * quarter + b); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + SM::kTmemSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + SM::kAbort);
 
@@ -239,16 +238,15 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         mbar_init(q_full, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(k_full(s), 1);
-            mbar_init(k_empty(s), 1);
             mbar_init(v_full(s), 1);
-            mbar_init(v_empty(s), 1);
             mbar_init(s_full(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(p_full(b), 8);   // the eight softmax warps
             mbar_init(pv_done(b), 1);
         }
-        for (int i = 0; i < 8; ++i) mbar_init(bars + 8u * (16 + i), 64);   // both warps of a lane quarter
+        for (int q = 0; q < 4; ++q)
+            for (int b = 0; b < 2; ++b) mbar_init(xch_bar(q, b), 64);   // both warps of a lane quarter
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -288,7 +286,10 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             for (int j = 0; ok && j < nblk; ++j) {
                 const int s = j & 1;
                 const uint32_t ph = static_cast<uint32_t>((j >> 1) & 1);
-                const uint32_t empty = is_k ? k_empty(s) : v_empty(s);
+                // slot s is free once S (for K) or P V (for V) of block j - 2 completed:
+                // the barriers the softmax waits on serve the producer as well
+                // (one commit fewer per group of MMAs)
+                const uint32_t empty = is_k ? s_full(s) : pv_done(s);
                 const uint32_t full = is_k ? k_full(s) : v_full(s);
                 if (!mbar_wait_bounded(empty, ph ^ 1u, p.timeout_ns, abort_flag, status, ROLE_PRODUCER, which)) {
                     ok = false;
@@ -311,21 +312,29 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         if (lane == 0) {
             bool ok = mbar_wait_bounded(q_full, 0, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_Q);
             tc_fence_after();
+            // One thread keeps the tensor pipe fed only if the work between two
+            // MMAs (64 cycles each at N = 128) stays short: the descriptors are
+            // built once, and each MMA adds a constant to the start-address
+            // field (in 16-byte units; every shared address is below 2^18, so
+            // the 14-bit field never carries).
+            const uint64_t q_desc = smem_desc_sw128(sQ, 0, 1024);
+            const uint64_t k_desc = smem_desc_sw128(sK, 0, 1024);
+            const uint64_t v_desc = smem_desc_sw128(sV, kBox, 1024);   // MN-major: 64-column boxes kBox apart
+            constexpr uint32_t kSlotUnits = kTileBytes >> 4;           // one ring slot, in 16-byte units
             auto issue_s = [&](int j) -> bool {   // S_j = Q K_j^T into score buffer j & 1
                 const int s = j & 1;
                 if (!mbar_wait_bounded(k_full(s), (j >> 1) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_K))
                     return false;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(s * kKeys);
+                const uint64_t kd = k_desc + static_cast<uint64_t>(s * kSlotUnits);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     // K-major: box k / 4, 32 bytes per 16-deep step inside the swizzled row
-                    const uint64_t a = smem_desc_sw128(sQ + (k >> 2) * kBox + (k & 3) * 32, 0, 1024);
-                    const uint64_t b = smem_desc_sw128(sK + (s * kDB + (k >> 2)) * kBox + (k & 3) * 32, 0, 1024);
-                    tc_mma_f16(d_tmem, a, b, kIdescS, k != 0 ? 1u : 0u);
+                    const uint64_t off = static_cast<uint64_t>(((k >> 2) * kBox + (k & 3) * 32) >> 4);
+                    tc_mma_f16(d_tmem, q_desc + off, kd + off, kIdescS, k != 0 ? 1u : 0u);
                 }
-                tc_commit(k_empty(s));       // K_j no longer needed: the next K may load
-                tc_commit(s_full(s));
+                tc_commit(s_full(s));        // also frees K slot s
                 return true;
             };
             if (ok && nblk > 0) ok = issue_s(0);
@@ -344,16 +353,16 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
                 tc_fence_after();
                 const uint32_t o_tmem = tmem_base + kOCol;
+                const uint32_t pa = tmem_base + kPCol + static_cast<uint32_t>(s * 64);
+                const uint64_t vd = v_desc + static_cast<uint64_t>(s * kSlotUnits);
 #pragma unroll
                 for (int k = 0; k < kKeys / 16; ++k) {
                     // P from tensor memory (16 keys = 8 columns of fp16 pairs per step);
-                    // V: MN-major, 64-column boxes 16 KiB apart (LBO), 16 key rows = 2 KiB per step
-                    const uint32_t a = tmem_base + kPCol + static_cast<uint32_t>(s * 64 + k * 8);
-                    const uint64_t b = smem_desc_sw128(sV + s * kDB * kBox + k * 2048, kBox, 1024);
-                    tc_mma_f16_ta(o_tmem, a, b, kIdescO, (j | k) != 0 ? 1u : 0u);
+                    // V: MN-major, 16 key rows = 2 KiB per step
+                    tc_mma_f16_ta(o_tmem, pa + static_cast<uint32_t>(k * 8), vd + static_cast<uint64_t>(k * 2048 >> 4),
+                                  kIdescO, (j | k) != 0 ? 1u : 0u);
                 }
-                tc_commit(v_empty(s));
-                tc_commit(pv_done(s));
+                tc_commit(pv_done(s));       // also frees V slot s
                 if (j + 2 < nblk) ok = issue_s(j + 2);   // score buffer s was read before P_j was written
             }
             tc_commit(drain_bar);
