@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -27,6 +28,7 @@ constexpr int kMaxDevices = 64;
 struct AttnDevice {
     bool ready = false;
     int status = GEMM_OK;
+    int sms = 0;          // streaming multiprocessors: one persistent CTA each
 };
 std::mutex g_mu;
 AttnDevice g_dev[kMaxDevices];
@@ -55,6 +57,8 @@ int init_device(int dev) {
         st.status = GEMM_ERR_UNSUPPORTED_DEVICE;
         return st.status;
     }
+    e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
     if (g_encode == nullptr) {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -152,7 +156,14 @@ int attn_f16_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B
     const double sc = scale == 0.0f ? 1.0 / std::sqrt(static_cast<double>(D)) : static_cast<double>(scale);
     prm.scale_log2 = static_cast<float>(sc * 1.4426950408889634);
     prm.timeout_ns = g_timeout_ns;
-    const int ctas = static_cast<int>(B * H * nq);
+    // Work units: query tiles, or, causal with at least two tiles per SM, pairs
+    // of a head's tiles nq - 1 - k and k (equal cost per unit; with fewer tiles
+    // pairing would only halve the parallelism).
+    const int sms = g_dev[dev].sms;
+    prm.pair = causal && B * H * nq >= 2 * static_cast<int64_t>(sms) ? 1 : 0;
+    const int64_t units = prm.pair ? B * H * ((nq + 1) / 2) : B * H * nq;
+    prm.units = static_cast<int>(units);
+    const int ctas = static_cast<int>(std::min<int64_t>(units, sms));
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     e = D == 64 ? launch<64>(tq, tk, tv, prm, ctas, s) : launch<128>(tq, tk, tv, prm, ctas, s);
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);

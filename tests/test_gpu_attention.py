@@ -68,6 +68,27 @@ def test_attention_prefill_sampled_rows(g, torch_dev, oracle_mod, name):
     check(got.reshape(-1, w.D)[rows], ref, name)
 
 
+# ---------------------------------------------------------------- many tiles per CTA
+# More query tiles than SMs, so every CTA walks several tiles: causal tiles are
+# then paired (nq - 1 - k with k); an odd tile count (S 1300: 11 tiles) leaves
+# the middle tile alone; ragged S makes every head's last tile partial.
+
+@pytest.mark.parametrize("B,H,S,D,causal", [(4, 32, 1300, 128, True), (4, 32, 1300, 64, True),
+                                            (8, 16, 1000, 128, False), (8, 24, 700, 64, True)])
+def test_attention_many_tiles_per_cta_sampled_rows(g, torch_dev, oracle_mod, B, H, S, D, causal):
+    rng = np.random.default_rng(S + D + 7 * causal)
+    Q, K, V = qkv(rng, (B, H, S, D))
+    got = run_attn(g, torch_dev, Q, K, V, causal)
+    total = B * H * S
+    # rows of the first, a middle and the last head, each head's first and last
+    # query tile, and a seeded sample
+    heads = [0, (B * H) // 2, B * H - 1]
+    rows = [h * S + i for h in heads for i in (0, 1, 127, 128, S - 129, S - 128, S - 2, S - 1)]
+    rows = np.unique(np.concatenate([np.array(rows, np.int64), rng.integers(0, total, 256)]))
+    ref = oracle_mod.attention_rows(Q, K, V, causal, 1.0 / np.sqrt(D), rows)
+    check(got.reshape(-1, D)[rows], ref, f"B{B} H{H} S{S} D{D} causal={causal}")
+
+
 # ---------------------------------------------------------------- shapes
 
 @pytest.mark.parametrize("D", [64, 128])
