@@ -145,6 +145,7 @@ struct GemmParams {
     int ldc;
     int epi;
     int vec_store;       // C base 16-byte aligned and ldc % 8 == 0
+    int mn3d_a, mn3d_b;  // MN-major operand map is 3-D (64, K, MN / 64): two 64-wide boxes per load
     int bias_vec;        // bias base 16-byte aligned (8-wide bias loads)
     int group_m;
     uint64_t timeout_ns;

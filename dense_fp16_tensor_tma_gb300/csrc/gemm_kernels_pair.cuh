@@ -178,7 +178,9 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         return ta ? max(0, min(2, (p.M - (m0 + 128 * r) + 63) / 64)) : ((m0 + 128 * r) < p.M ? 1 : 0);
     };
     auto a_bytes = [&](int m0, int r) {
-        return static_cast<uint32_t>(a_boxes(m0, r)) * (ta ? kBBoxBytes : kATileBytes);
+        const int n = a_boxes(m0, r);
+        if (ta && p.mn3d_a) return n > 0 ? 2u * kBBoxBytes : 0u;   // one load of both boxes
+        return static_cast<uint32_t>(n) * (ta ? kBBoxBytes : kATileBytes);
     };
     auto b_live = [&](int n0, int r) { return max(0, min(2, (p.N - (n0 + 128 * r) + 63) / 64)); };
 
@@ -201,10 +203,13 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     return un.half < 0 ? b_live(tc.n0, r) : (tc.n0 + 128 * un.half + 64 * r < p.N ? 1 : 0);
                 };
                 const int my_b = live(rank);
+                const bool b3 = !tb && p.mn3d_b;   // both of a CTA's B boxes in one load
+                auto b_bytes = [&](int r) {
+                    return b3 ? (live(r) > 0 ? 2u * kBBoxBytes : 0u) : static_cast<uint32_t>(live(r)) * kBBoxBytes;
+                };
                 // every sub-block's boxes are issued, also those starting past K
                 // (they arrive as zeros), so each stage carries the same bytes
-                const uint32_t pair_bytes = KSUB * (a_bytes(tc.m0, 0) + a_bytes(tc.m0, 1) +
-                                                    static_cast<uint32_t>(live(0) + live(1)) * kBBoxBytes);
+                const uint32_t pair_bytes = KSUB * (a_bytes(tc.m0, 0) + a_bytes(tc.m0, 1) + b_bytes(0) + b_bytes(1));
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_cluster_bounded(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, status,
                                                    ROLE_PRODUCER, BAR_EMPTY)) { ok = false; break; }
@@ -214,15 +219,23 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         const int k0 = kb * kStageK + ks * kBK;
                         const uint32_t a_dst = sA + stage * SP::kAStage + ks * kATileBytes;
                         const int arow = tc.m0 + 128 * static_cast<int>(rank);
-                        if (ta) {
+                        if (ta && p.mn3d_a) {
+                            if (my_a) tma_load_3d_pair(a_dst, &tmA, full_leader, 0, k0, arow >> 6);
+                        } else if (ta) {
                             for (int c = 0; c < my_a; ++c)
                                 tma_load_box_pair(a_dst + c * kBBoxBytes, &tmA, full_leader, false, arow + 64 * c, k0);
                         } else if (my_a) {
                             tma_load_2d_pair(a_dst, &tmA, full_leader, k0, arow);
                         }
-                        for (int c = 0; c < my_b; ++c)
-                            tma_load_box_pair(sB + stage * SP::kBStage + ks * kBHalfSubBytes + c * kBBoxBytes, &tmB,
-                                              full_leader, tb, bcol + 64 * c, k0);
+                        if (b3) {
+                            if (my_b)
+                                tma_load_3d_pair(sB + stage * SP::kBStage + ks * kBHalfSubBytes, &tmB, full_leader, 0, k0,
+                                                 bcol >> 6);
+                        } else {
+                            for (int c = 0; c < my_b; ++c)
+                                tma_load_box_pair(sB + stage * SP::kBStage + ks * kBHalfSubBytes + c * kBBoxBytes, &tmB,
+                                                  full_leader, tb, bcol + 64 * c, k0);
+                        }
                     }
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -484,10 +497,17 @@ __device__ __forceinline__ void pair_gemm(const Src& src, const GemmParams cp) {
                     return un.half < 0 ? b_live(pp.N, tc.n0, r) : (tc.n0 + 128 * un.half + 64 * r < pp.N ? 1 : 0);
                 };
                 const int my_b = live(rank);
+                const bool a3 = ta && pp.mn3d_a;   // both of a CTA's MN-major boxes in one load
+                const bool b3 = !tb && pp.mn3d_b;
+                auto a_load_bytes = [&](int r) {
+                    return a3 ? (a_boxes(pp.M, tc.m0, r) > 0 ? 2u * kBBoxBytes : 0u) : a_bytes(pp.M, tc.m0, r);
+                };
+                auto b_load_bytes = [&](int r) {
+                    return b3 ? (live(r) > 0 ? 2u * kBBoxBytes : 0u) : static_cast<uint32_t>(live(r)) * kBBoxBytes;
+                };
                 // every sub-block's boxes are issued, also those starting past K
                 // (they arrive as zeros), so each stage carries the same bytes
-                const uint32_t pair_bytes = KSUB * (a_bytes(pp.M, tc.m0, 0) + a_bytes(pp.M, tc.m0, 1) +
-                                                    static_cast<uint32_t>(live(0) + live(1)) * kBBoxBytes);
+                const uint32_t pair_bytes = KSUB * (a_load_bytes(0) + a_load_bytes(1) + b_load_bytes(0) + b_load_bytes(1));
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_cluster_bounded(empty_bar(stage), phase ^ 1u, cp.timeout_ns, abort_flag, status,
                                                    ROLE_PRODUCER, BAR_EMPTY)) { ok = false; break; }
@@ -497,15 +517,23 @@ __device__ __forceinline__ void pair_gemm(const Src& src, const GemmParams cp) {
                         const int k0 = kb * kStageK + ks * kBK;
                         const uint32_t a_dst = sA + stage * SP::kAStage + ks * kATileBytes;
                         const int arow = tc.m0 + 128 * static_cast<int>(rank);
-                        if (ta) {
+                        if (a3) {
+                            if (my_a) tma_load_3d_pair(a_dst, un.tmA, full_leader, 0, k0, arow >> 6);
+                        } else if (ta) {
                             for (int c = 0; c < my_a; ++c)
                                 tma_load_box_pair(a_dst + c * kBBoxBytes, un.tmA, full_leader, false, arow + 64 * c, k0);
                         } else if (my_a) {
                             tma_load_2d_pair(a_dst, un.tmA, full_leader, k0, arow);
                         }
-                        for (int c = 0; c < my_b; ++c)
-                            tma_load_box_pair(sB + stage * SP::kBStage + ks * kBHalfSubBytes + c * kBBoxBytes, un.tmB,
-                                              full_leader, tb, bcol + 64 * c, k0);
+                        if (b3) {
+                            if (my_b)
+                                tma_load_3d_pair(sB + stage * SP::kBStage + ks * kBHalfSubBytes, un.tmB, full_leader, 0,
+                                                 k0, bcol >> 6);
+                        } else {
+                            for (int c = 0; c < my_b; ++c)
+                                tma_load_box_pair(sB + stage * SP::kBStage + ks * kBHalfSubBytes + c * kBBoxBytes,
+                                                  un.tmB, full_leader, tb, bcol + 64 * c, k0);
+                        }
                     }
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
