@@ -235,6 +235,60 @@ def dist_max(world, x: float) -> float:
 
 # ------------------------------------------------------------------ CPU oracle timing
 
+E2E_MODE = ("pipelined: step i's host-to-device copies overlap step i-1's computation and step i-2's "
+            "device-to-host copy (two device buffer sets, three streams); serial_*: copy in, compute, copy out "
+            "one after another on one stream")
+
+
+def pipelined_e2e(torch, dev, world, nsteps, comp_stream, copy_in, compute, copy_out):
+    """End-to-end steps the way a serving loop runs them: step i's inputs are
+    copied from pinned host memory into one of two device buffer sets on a
+    copy-in stream while step i - 1 computes on `comp_stream` and step i - 2's
+    result is copied out on a copy-out stream.  A set's inputs are overwritten
+    only after the step that read them has computed, and its result only after
+    it has been copied out.  Every step's copies lie inside the timed region
+    (first copy-in to last copy-out).  copy_in(b), compute(b), copy_out(b) enqueue
+    on the current stream for buffer set b.  Returns milliseconds (max over ranks)."""
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+
+    def run(n):
+        ev_in, ev_comp, ev_out = [], [], []
+        for i in range(n):
+            b = i & 1
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_comp[i - 2])
+                copy_in(b)
+                ev_in.append(torch.cuda.Event())
+                ev_in[-1].record(s_in)
+            with torch.cuda.stream(comp_stream):
+                comp_stream.wait_event(ev_in[i])
+                if i >= 2:
+                    comp_stream.wait_event(ev_out[i - 2])
+                compute(b)
+                ev_comp.append(torch.cuda.Event())
+                ev_comp[-1].record(comp_stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[i])
+                copy_out(b)
+                ev_out.append(torch.cuda.Event())
+                ev_out[-1].record(s_out)
+
+    run(3)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_barrier(world)
+    torch.cuda.synchronize(dev)
+    ev0.record(s_in)
+    run(nsteps)
+    ev1.record(s_out)                  # the last copy-out depends on every earlier operation
+    torch.cuda.synchronize(dev)
+    ms = dist_max(world, ev0.elapsed_time(ev1))
+    dist_barrier(world)
+    return ms
+
+
 def oracle_rows_timing(w, epi, A, B, bias, target_s):
     """Time the oracle on a bounded sample of full rows; returns (tflops, seconds, rows, threads)."""
     import oracle
@@ -420,9 +474,35 @@ def run_ours(args, w, epi):
             e2e_step()
         ev1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = dist_max(world, ev0.elapsed_time(ev1))
+    serial_ms = dist_max(world, ev0.elapsed_time(ev1))
     dist_barrier(world)
+    serial_value = world * flops * e2e_steps / (serial_ms * 1e-3) / 1e12
+    # the same steps pipelined over two device buffer sets (copies overlap computation)
+    sets_A, sets_B = [tA, torch.empty_like(tA)], [tB, torch.empty_like(tB)]
+    sets_b = [tb, torch.empty_like(tb)] if tb is not None else [None, None]
+    sets_C, host_C = [C, torch.empty_like(C)], [hC, torch.empty_like(hC).pin_memory()]
+
+    def copy_in(b):
+        sets_A[b].copy_(hA, non_blocking=True)
+        sets_B[b].copy_(hB, non_blocking=True)
+        if hb is not None:
+            sets_b[b].copy_(hb, non_blocking=True)
+
+    def compute(b):
+        st = g.gemm_f16_ex_ptr(sets_A[b].data_ptr(), lda, sets_B[b].data_ptr(), ldb,
+                               sets_b[b].data_ptr() if sets_b[b] is not None else 0, sets_C[b].data_ptr(), w.N,
+                               w.M, w.N, w.K, epi, flags, torch.cuda.current_stream().cuda_stream)
+        if st != 0:
+            raise g.GemmError(st)
+
+    def copy_out(b):
+        host_C[b].copy_(sets_C[b], non_blocking=True)
+
+    e2e_ms = pipelined_e2e(torch, dev, world, e2e_steps, stream, copy_in, compute, copy_out)
     e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    st, word = g.gemm_f16_debug_status(stream)
+    if st != 0:
+        raise SystemExit(f"device status {st} ({word:#x}) after the end-to-end steps")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -442,7 +522,8 @@ def run_ours(args, w, epi):
             "pct_of_peak": 100.0 * (flops / (avg_launch_ms * 1e-3) / 1e12) / tensor_peak,
             "roofline": roof,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms / e2e_steps},
+                    "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
+                    "mode": E2E_MODE, "serial_value": serial_value, "serial_ms_per_step": serial_ms / e2e_steps},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                        "reasons": clocks["reasons"], "samples": clocks["samples"],
@@ -629,9 +710,32 @@ def run_attention(args, w):
             e2e_step()
         ev1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = dist_max(world, ev0.elapsed_time(ev1))
+    serial_ms = dist_max(world, ev0.elapsed_time(ev1))
     dist_barrier(world)
+    serial_value = world * flops * e2e_steps / (serial_ms * 1e-3) / 1e12
+    # the same steps pipelined over two device buffer sets (copies overlap computation)
+    sets = [(tq, tk, tv, O), tuple(torch.empty_like(x) for x in (tq, tk, tv, O))]
+    host_O = [ho, torch.empty_like(ho).pin_memory()]
+
+    def copy_in(b):
+        for d, h in zip(sets[b][:3], (hq, hk, hv)):
+            d.copy_(h, non_blocking=True)
+
+    def compute(b):
+        q_, k_, v_, o_ = sets[b]
+        st = g.attn_f16_fwd_ptr(q_.data_ptr(), k_.data_ptr(), v_.data_ptr(), o_.data_ptr(), w.B, w.H, w.S, w.D,
+                                w.causal, 0.0, torch.cuda.current_stream().cuda_stream)
+        if st != 0:
+            raise g.GemmError(st, "attn_f16_fwd")
+
+    def copy_out(b):
+        host_O[b].copy_(sets[b][3], non_blocking=True)
+
+    e2e_ms = pipelined_e2e(torch, dev, world, e2e_steps, stream, copy_in, compute, copy_out)
     e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    st, word = g.attn_f16_debug_status(stream)
+    if st != 0:
+        raise SystemExit(f"device status {st} ({word:#x}) after the end-to-end steps")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -649,7 +753,8 @@ def run_attention(args, w):
             "config": {**attn_config(w), "parallelism": f"replicas{world}" if world > 1 else "single"},
             "roofline": roof,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms / e2e_steps},
+                    "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
+                    "mode": E2E_MODE, "serial_value": serial_value, "serial_ms_per_step": serial_ms / e2e_steps},
             "gpu_launches": args.steps,
             "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                        "reasons": clocks["reasons"], "samples": clocks["samples"],
