@@ -98,6 +98,26 @@ def test_layout_integer_exact(forced, torch_dev, oracle_mod, cfg, layout, M, N, 
     assert np.array_equal(got, ref), f"{cfg} {layout}: max diff {np.abs(got.astype(float) - ref).max()}"
 
 
+# ---------------------------------------------------------------- 3-D operand maps
+# MN-major operands (B stored K x N, A stored K x M) whose MN extent and pitch are
+# multiples of 64 load both 64-wide boxes of a CTA's slice with one 3-D tensor-map
+# load: an odd number of 64-wide groups leaves the last slice's second box past
+# the end (read as zeros); a pitch of MN + 64 keeps the 3-D path with rows longer
+# than MN; a pitch of MN + 8 falls back to 2-D boxes.  Small shapes run as CTA-pair
+# half tiles, larger ones as whole tiles.
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("M,N,K,pad", [(192, 320, 128, 0), (320, 192, 200, 0), (448, 576, 264, 64),
+                                       (576, 448, 128, 8), (2304, 2624, 192, 0)])
+def test_mn3d_maps_integer_exact(forced, torch_dev, oracle_mod, layout, M, N, K, pad):
+    forced.gemm_f16_force_config("pair256x256")
+    rng = np.random.default_rng(M + N + K + pad)
+    A, B, bias = ints(rng, (M, K)), ints(rng, (K, N)), ints(rng, N, -8, 9)
+    got = run_layout(forced, torch_dev, A, B, bias, "bias", layout, pad, pad)
+    ref = oracle_mod.gemm(A, B, bias, "bias")
+    assert np.array_equal(got, ref), f"{layout} {M}x{N}x{K} pad {pad}: max diff {np.abs(got.astype(float) - ref).max()}"
+
+
 # ---------------------------------------------------------------- row pitches
 
 @pytest.mark.parametrize("layout", LAYOUTS)
