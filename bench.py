@@ -233,7 +233,7 @@ def dist_max(world, x: float) -> float:
     return float(t.item())
 
 
-# ------------------------------------------------------------------ CPU oracle timing
+# ------------------------------------------------------------------ end-to-end steps
 
 E2E_MODE = ("pipelined: step i's host-to-device copies overlap step i-1's computation and step i-2's "
             "device-to-host copy (two device buffer sets, three streams); serial_*: copy in, compute, copy out "
@@ -288,6 +288,8 @@ def pipelined_e2e(torch, dev, world, nsteps, comp_stream, copy_in, compute, copy
     dist_barrier(world)
     return ms
 
+
+# ------------------------------------------------------------------ CPU oracle timing
 
 def oracle_rows_timing(w, epi, A, B, bias, target_s):
     """Time the oracle on a bounded sample of full rows; returns (tflops, seconds, rows, threads)."""
