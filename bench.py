@@ -139,6 +139,16 @@ def committed_traffic(workload_name, sources=KERNEL_SOURCES):
     return rec.get("dram_bytes_per_launch")
 
 
+def launch_stats(per_launch_ms):
+    """Median, min, p90 and mean of the per-launch CUDA-event times (ms): the
+    median-of-reps timing of "TileLang: Write, Autotune, and Ship Fused
+    Tensor-Core Kernels from Python", Practical defaults, with its spread."""
+    xs = sorted(per_launch_ms)
+    p90 = xs[min(len(xs) - 1, int(math.ceil(0.9 * len(xs))) - 1)]
+    return {"median": statistics.median(xs), "min": xs[0], "p90": p90, "mean": statistics.mean(xs),
+            "n": len(xs)}
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -146,7 +156,7 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_uuid=None, interval_ms=100):
+    def __init__(self, gpu_uuid=None, interval_ms=20):
         self.proc = None
         self.lines = []
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -189,7 +199,7 @@ class ClockSampler:
         return out
 
     @staticmethod
-    def summarize(samples, t0=None, t1=None, pad_s=0.25):
+    def summarize(samples, t0=None, t1=None, pad_s=0.03):
         """Median SM clock and throttle reasons of the samples inside [t0-pad, t1+pad];
         when the window holds none (a short run), the samples of the whole run."""
         window = "timed"
@@ -522,6 +532,7 @@ def run_ours(args, w, epi):
             "config": {**workload_config(w, epi, args.layout),
                        "parallelism": f"replicas{world}" if world > 1 else "single"},
             "pct_of_peak": 100.0 * (flops / (avg_launch_ms * 1e-3) / 1e12) / tensor_peak,
+            "launch_ms": launch_stats(per_launch_ms),
             "roofline": roof,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
@@ -753,6 +764,7 @@ def run_attention(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic",
             "config": {**attn_config(w), "parallelism": f"replicas{world}" if world > 1 else "single"},
+            "launch_ms": launch_stats(per_launch_ms),
             "roofline": roof,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,

@@ -22,12 +22,14 @@ EPILOGUES = {"none": GEMM_EPI_NONE, "bias": GEMM_EPI_BIAS, "bias_relu": GEMM_EPI
 GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED_DEVICE, GEMM_ERR_MISALIGNED = 0, 1, 2, 3
 GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT, GEMM_ERR_NO_MEMORY, GEMM_ERR_SCRATCH_LIMIT = 4, 5, 6, 7
 
-GEMM_F16_TRANS_A, GEMM_F16_TRANS_B = 1, 2
+GEMM_F16_TRANS_A, GEMM_F16_TRANS_B, GEMM_F16_PLAN_NOALLOC = 1, 2, 4
 
 EXPORTS = ("gemm_f16", "gemm_f16_ex", "gemm_f16_status_string", "gemm_f16_last_cuda_error",
            "gemm_f16_debug_status", "gemm_f16_release_workspace", "gemm_f16_plan", "gemm_f16_plan_ex",
            "gemm_f16_selftest_timeout", "gemm_f16_noalloc", "gemm_f16_force_config", "gemm_f16_set_pdl",
-           "gemm_f16_grouped", "attn_f16_fwd", "attn_f16_debug_status", "attn_f16_last_cuda_error")
+           "gemm_f16_grouped", "attn_f16_fwd", "attn_f16_debug_status", "attn_f16_last_cuda_error",
+           "gemm_f16_debug_inject", "attn_f16_debug_inject")
+GEMM_F16_FAULT_NONE, GEMM_F16_FAULT_SKIP_LOADS, GEMM_F16_FAULT_ENCODE = 0, 1, 2
 CONFIGS = {"auto": 0, "pair256x256": 1, "128x256": 2, "128x128": 3, "128x64": 4, "swap": 5, "pair_whole": 6}
 
 if not os.path.exists(LIB_PATH):
@@ -74,6 +76,10 @@ lib.attn_f16_debug_status.restype = _int
 lib.attn_f16_last_cuda_error.restype = _int
 lib.gemm_f16_set_pdl.argtypes = [_int]
 lib.gemm_f16_set_pdl.restype = _int
+lib.gemm_f16_debug_inject.argtypes = [_int, ctypes.c_uint32]
+lib.gemm_f16_debug_inject.restype = _int
+lib.attn_f16_debug_inject.argtypes = [_int, ctypes.c_uint32]
+lib.attn_f16_debug_inject.restype = _int
 
 
 class GemmError(RuntimeError):
@@ -228,14 +234,16 @@ def gemm_f16_grouped(problems, epilogue="none", stream=None):
 
 
 def gemm_f16_plan(M, N, K, epilogue="none", num_sms=152, a_addr=256, b_addr=256, c_addr=256,
-                  bias_addr=256, lda=None, ldb=None, ldc=None, trans_a=False, trans_b=False):
+                  bias_addr=256, lda=None, ldb=None, ldc=None, trans_a=False, trans_b=False, noalloc=False):
     """Host-only: the plan gemm_f16 / gemm_f16_ex would pick (dict), without
-    touching a device.  Pitches default to the dense ones of the layout."""
+    touching a device; with noalloc=True the plan of gemm_f16_noalloc.
+    Pitches default to the dense ones of the layout."""
     out = (ctypes.c_int64 * 11)()
     lda = lda if lda is not None else (M if trans_a else K)
     ldb = ldb if ldb is not None else (K if trans_b else N)
     ldc = ldc if ldc is not None else N
-    flags = (GEMM_F16_TRANS_A if trans_a else 0) | (GEMM_F16_TRANS_B if trans_b else 0)
+    flags = ((GEMM_F16_TRANS_A if trans_a else 0) | (GEMM_F16_TRANS_B if trans_b else 0) |
+             (GEMM_F16_PLAN_NOALLOC if noalloc else 0))
     st = lib.gemm_f16_plan_ex(a_addr or None, int(lda), b_addr or None, int(ldb), bias_addr or None,
                               c_addr or None, int(ldc), int(M), int(N), int(K), _epi(epilogue), flags,
                               int(num_sms), out)
@@ -271,6 +279,17 @@ def gemm_f16_set_pdl(enable: bool) -> bool:
     """Programmatic dependent launch of the library's kernels on/off
     (process-wide); returns the previous setting."""
     return bool(lib.gemm_f16_set_pdl(1 if enable else 0))
+
+
+def gemm_f16_debug_inject(fault: int, wait_us: int = 0) -> int:
+    """Test hook: arm one fault (GEMM_F16_FAULT_*) for the next GEMM call that
+    reaches it; returns the status code."""
+    return lib.gemm_f16_debug_inject(int(fault), int(wait_us))
+
+
+def attn_f16_debug_inject(fault: int, wait_us: int = 0) -> int:
+    """Test hook: arm one fault (GEMM_F16_FAULT_*) for the next attention call."""
+    return lib.attn_f16_debug_inject(int(fault), int(wait_us))
 
 
 def gemm_f16_selftest_timeout(timeout_us: int = 1000, stream=None) -> int:

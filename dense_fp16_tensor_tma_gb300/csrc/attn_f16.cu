@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -33,8 +34,19 @@ struct AttnDevice {
 std::mutex g_mu;
 AttnDevice g_dev[kMaxDevices];
 EncodeTiledFn g_encode = nullptr;
-uint64_t g_timeout_ns = 2000000000ull;
-bool g_pdl = true;   // programmatic dependent launch unless GEMM_F16_PDL=0
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};   // set once at set-up, read by every caller
+std::atomic<bool> g_pdl{true};   // programmatic dependent launch unless GEMM_F16_PDL=0
+
+// Fault injection for the tests of the error paths (attn_f16_debug_inject):
+// one-shot and process-wide, like the GEMM library's.
+std::atomic<int> g_fault{GEMM_F16_FAULT_NONE};
+std::atomic<uint64_t> g_fault_wait_ns{0};
+
+bool take_fault(int kind) {
+    if (g_fault.load(std::memory_order_relaxed) != kind) return false;
+    int expected = kind;
+    return g_fault.compare_exchange_strong(expected, GEMM_F16_FAULT_NONE);
+}
 
 int cuda_fail(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
@@ -75,9 +87,9 @@ int init_device(int dev) {
     if (e != cudaSuccess) return cuda_fail(e);
     if (const char* env = std::getenv("GEMM_F16_TIMEOUT_MS")) {
         const long ms = std::strtol(env, nullptr, 10);
-        if (ms > 0) g_timeout_ns = static_cast<uint64_t>(ms) * 1000000ull;
+        if (ms > 0) g_timeout_ns.store(static_cast<uint64_t>(ms) * 1000000ull, std::memory_order_relaxed);
     }
-    if (const char* env = std::getenv("GEMM_F16_PDL")) g_pdl = env[0] != '0';
+    if (const char* env = std::getenv("GEMM_F16_PDL")) g_pdl.store(env[0] != '0', std::memory_order_relaxed);
     st.ready = true;
     st.status = GEMM_OK;
     return GEMM_OK;
@@ -86,6 +98,10 @@ int init_device(int dev) {
 // (D, S, B*H) fp16 tensor with box 64 x 128 x 1, 128-byte swizzle, zeros
 // outside the tensor (rows past S of a head never come from the next head).
 int encode_3d(CUtensorMap* m, const void* ptr, int64_t D, int64_t S, int64_t BH) {
+    if (take_fault(GEMM_F16_FAULT_ENCODE)) {   // injected: what the encoder returns for an invalid map
+        t_last_cuda_error = static_cast<int>(CUDA_ERROR_INVALID_VALUE);
+        return GEMM_ERR_CUDA;
+    }
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(BH)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S * D) * 2};
     cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kQRows), 1};
@@ -111,7 +127,7 @@ cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     std::memset(attr, 0, sizeof(attr));
-    if (g_pdl) {
+    if (g_pdl.load(std::memory_order_relaxed)) {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
@@ -155,7 +171,12 @@ int attn_f16_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B
     prm.causal = causal ? 1 : 0;
     const double sc = scale == 0.0f ? 1.0 / std::sqrt(static_cast<double>(D)) : static_cast<double>(scale);
     prm.scale_log2 = static_cast<float>(sc * 1.4426950408889634);
-    prm.timeout_ns = g_timeout_ns;
+    prm.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+    prm.fault_skip_block = -1;
+    if (take_fault(GEMM_F16_FAULT_SKIP_LOADS)) {
+        prm.fault_skip_block = 1;
+        prm.timeout_ns = g_fault_wait_ns.load(std::memory_order_relaxed);
+    }
     // Work units: query tiles, or, causal with at least two tiles per SM, pairs
     // of a head's tiles nq - 1 - k and k (equal cost per unit; with fewer tiles
     // pairing would only halve the parallelism).
@@ -170,6 +191,14 @@ int attn_f16_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B
 }
 
 int attn_f16_last_cuda_error(void) { return t_last_cuda_error; }
+
+int attn_f16_debug_inject(int fault, uint32_t wait_us) {
+    if (fault < GEMM_F16_FAULT_NONE || fault > GEMM_F16_FAULT_ENCODE) return GEMM_ERR_INVALID_ARG;
+    if (fault == GEMM_F16_FAULT_SKIP_LOADS && wait_us == 0) return GEMM_ERR_INVALID_ARG;
+    g_fault_wait_ns.store(static_cast<uint64_t>(wait_us) * 1000ull, std::memory_order_relaxed);
+    g_fault.store(fault);
+    return GEMM_OK;
+}
 
 int attn_f16_debug_status(void* cuda_stream, uint32_t* detail) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));

@@ -76,6 +76,11 @@ struct AttnParams {
     int pair;           // causal, with at least two tiles per SM: a unit is a pair of tiles
     float scale_log2;   // softmax scale * log2(e)
     uint64_t timeout_ns;
+    // Fault injection for the tests of the bounded waits (-1 in every normal
+    // call): the K producer never loads key block `fault_skip_block` of the
+    // CTA's block sequence, so the MMA thread's wait for it runs out and the
+    // abort path runs with no copy in flight for that block.
+    int fault_skip_block;
 };
 
 template <int D>
@@ -341,6 +346,7 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                             ok = false;
                             break;
                         }
+                        if (is_k && gb == p.fault_skip_block) continue;   // injected fault: never loaded
                         const uint32_t full = is_k ? k_full(s) : v_full(s);
                         mbar_arrive_expect_tx(full, kTileBytes);
                         for (int c = 0; c < kDB; ++c)

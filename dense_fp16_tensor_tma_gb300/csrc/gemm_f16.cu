@@ -72,7 +72,9 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 EncodeTiledFn g_encode = nullptr;
-uint64_t g_timeout_ns = 2000000000ull;   // 2 s per bounded wait
+// 2 s per bounded wait; written once at set-up (under g_mu), read by every
+// calling thread when it fills kernel parameters
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_force_config{CFG_AUTO};
 // Programmatic dependent launch on every kernel of the library (GEMM_F16_PDL=0
 // in the environment, or gemm_f16_set_pdl(0), turns it off).
@@ -88,6 +90,20 @@ bool pdl_enabled() {
         v = g_pdl.load(std::memory_order_relaxed);
     }
     return v != 0;
+}
+
+// Fault injection for the tests of the error paths (gemm_f16_debug_inject):
+// one-shot and process-wide.  GEMM_F16_FAULT_SKIP_LOADS: the next launch of a
+// single-CTA tensor-core kernel (128-row tiles or swap-AB) never loads the
+// second K block of each CTA's first tile and waits at most g_fault_wait_ns;
+// GEMM_F16_FAULT_ENCODE: the next tensor-map encoding fails.
+std::atomic<int> g_fault{GEMM_F16_FAULT_NONE};
+std::atomic<uint64_t> g_fault_wait_ns{0};
+
+bool take_fault(int kind) {
+    if (g_fault.load(std::memory_order_relaxed) != kind) return false;   // the usual case: one load
+    int expected = kind;
+    return g_fault.compare_exchange_strong(expected, GEMM_F16_FAULT_NONE);
 }
 
 // Calls f(std::integral_constant<int, E>) for every epilogue kind E in
@@ -372,7 +388,7 @@ int init_common_locked(int dev, DeviceState& st) {
     }
     if (const char* env = std::getenv("GEMM_F16_TIMEOUT_MS")) {
         const long ms = std::strtol(env, nullptr, 10);
-        if (ms > 0) g_timeout_ns = static_cast<uint64_t>(ms) * 1000000ull;
+        if (ms > 0) g_timeout_ns.store(static_cast<uint64_t>(ms) * 1000000ull, std::memory_order_relaxed);
     }
     st.num_sms = sms;
     st.ready = true;
@@ -435,7 +451,14 @@ thread_local TensorMapCache t_maps;
 // coordinates past K or past MN / 64 read as zeros without touching memory.
 bool mn3d_ok(bool mn_major, int64_t mn, int64_t ld) { return mn_major && mn % 64 == 0 && ld % 64 == 0; }
 
+// An injected encoding failure (what the driver returns for an invalid map).
+int injected_encode_failure() {
+    t_last_cuda_error = static_cast<int>(CUDA_ERROR_INVALID_VALUE);
+    return GEMM_ERR_CUDA;
+}
+
 int encode_mn3d(CUtensorMap* m, const void* ptr, int64_t mn, int64_t k, int64_t ld) {
+    if (take_fault(GEMM_F16_FAULT_ENCODE)) return injected_encode_failure();
     cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(mn / 64)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, 128};
     cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBK), 2};
@@ -455,6 +478,7 @@ int encode_mn3d(CUtensorMap* m, const void* ptr, int64_t mn, int64_t k, int64_t 
 // zero fill outside the tensor.
 int encode_2d(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int64_t ld, int box_inner,
               int box_outer) {
+    if (take_fault(GEMM_F16_FAULT_ENCODE)) return injected_encode_failure();
     for (const TensorMapCache::Entry& c : t_maps.e) {
         if (c.ptr == ptr && ptr != nullptr && c.inner == inner && c.outer == outer && c.ld == ld &&
             c.box_inner == box_inner && c.box_outer == box_outer) {
@@ -558,29 +582,41 @@ GemmParams kernel_params(const Operands& op, const __half* biasp, int64_t M, int
     prm.vec_store = (aligned(op.C, 16) && op.ldc % 8 == 0) ? 1 : 0;
     prm.bias_vec = (biasp != nullptr && aligned(biasp, 16)) ? 1 : 0;
     prm.group_m = kGroupM;
-    prm.timeout_ns = g_timeout_ns;
+    prm.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
     prm.splits = 1;
+    prm.fault_skip_kb = -1;
     return prm;
 }
 
-// Everything after scratch is settled: repack (into `scratch`, which holds
-// pl.a_scratch + pl.b_scratch bytes when a repack is planned), tensor maps,
-// and the tensor-core kernel, all on stream `s`.
+// Everything after scratch is settled, all on stream `s`: the tensor maps
+// (encoded first, so that an encoding failure enqueues nothing), the repacks
+// (into `scratch`, which holds pl.a_scratch + pl.b_scratch bytes when a
+// repack is planned), the split-K counters' reset, and the tensor-core kernel.
 int enqueue_plan(const Plan& pl, const Operands& op, const __half* biasp, int64_t M, int64_t N, int64_t K,
                  int epilogue, uint8_t* scratch, cudaStream_t s) {
-    int st = GEMM_OK;
-    const void* a_src = op.A;
-    const void* b_src = op.B;
-    if (pl.pack_a) {
+    const void* a_src = pl.pack_a ? static_cast<const void*>(scratch) : op.A;
+    uint16_t* bdst = pl.pack_b ? reinterpret_cast<uint16_t*>(scratch + pl.a_scratch) : nullptr;
+    const void* b_src = pl.pack_b ? static_cast<const void*>(bdst) : op.B;
+    CUtensorMap ta, tb;
+    // A boxes: 64 K x 128 rows (64 K x MT rows for the swap-AB kernel), or,
+    // for A stored K x M, 64 rows x 64 K; B boxes: 64 x 64 in either layout
+    const bool pair = pl.cfg == CFG_PAIR_256;
+    const bool a3 = pair && mn3d_ok(op.ta, M, pl.lda_packed);
+    const bool b3 = pair && mn3d_ok(!op.tb, N, pl.ldb_packed);
+    int st = a3 ? encode_mn3d(&ta, a_src, M, K, pl.lda_packed)
+             : op.ta ? encode_2d(&ta, a_src, M, K, pl.lda_packed, 64, kBK)
+                     : encode_2d(&ta, a_src, K, M, pl.lda_packed, kBK, pl.path == 3 ? pl.tile_m : kBM);
+    if (st == GEMM_OK) {
+        st = b3 ? encode_mn3d(&tb, b_src, N, K, pl.ldb_packed)
+             : op.tb ? encode_2d(&tb, b_src, K, N, pl.ldb_packed, kBK, 64)
+                     : encode_2d(&tb, b_src, N, K, pl.ldb_packed, 64, kBK);
+    }
+    if (st != GEMM_OK) return st;
+    if (pl.pack_a)
         st = launch_repack(reinterpret_cast<uint16_t*>(scratch), op.A, op.a_rows(M, K), op.a_cols(M, K), op.lda,
                            pl.lda_packed, s);
-        a_src = scratch;
-    }
-    if (st == GEMM_OK && pl.pack_b) {
-        uint16_t* bdst = reinterpret_cast<uint16_t*>(scratch + pl.a_scratch);
+    if (st == GEMM_OK && pl.pack_b)
         st = launch_repack(bdst, op.B, op.b_rows(N, K), op.b_cols(N, K), op.ldb, pl.ldb_packed, s);
-        b_src = bdst;
-    }
     float* partials = nullptr;
     unsigned int* counters = nullptr;
     if (st == GEMM_OK && pl.splits > 1) {
@@ -588,22 +624,6 @@ int enqueue_plan(const Plan& pl, const Operands& op, const __half* biasp, int64_
         counters = reinterpret_cast<unsigned int*>(scratch + pl.a_scratch + pl.b_scratch + pl.p_scratch);
         const cudaError_t e = cudaMemsetAsync(counters, 0, pl.c_scratch, s);   // every slice starts at zero parts
         if (e != cudaSuccess) st = cuda_fail(e);
-    }
-    CUtensorMap ta, tb;
-    // A boxes: 64 K x 128 rows (64 K x MT rows for the swap-AB kernel), or,
-    // for A stored K x M, 64 rows x 64 K; B boxes: 64 x 64 in either layout
-    const bool pair = pl.cfg == CFG_PAIR_256;
-    const bool a3 = pair && mn3d_ok(op.ta, M, pl.lda_packed);
-    const bool b3 = pair && mn3d_ok(!op.tb, N, pl.ldb_packed);
-    if (st == GEMM_OK) {
-        st = a3 ? encode_mn3d(&ta, a_src, M, K, pl.lda_packed)
-             : op.ta ? encode_2d(&ta, a_src, M, K, pl.lda_packed, 64, kBK)
-                     : encode_2d(&ta, a_src, K, M, pl.lda_packed, kBK, pl.path == 3 ? pl.tile_m : kBM);
-    }
-    if (st == GEMM_OK) {
-        st = b3 ? encode_mn3d(&tb, b_src, N, K, pl.ldb_packed)
-             : op.tb ? encode_2d(&tb, b_src, K, N, pl.ldb_packed, kBK, 64)
-                     : encode_2d(&tb, b_src, N, K, pl.ldb_packed, 64, kBK);
     }
     if (st != GEMM_OK) return st;
     GemmParams prm = kernel_params(op, biasp, M, N, K, epilogue);
@@ -614,6 +634,10 @@ int enqueue_plan(const Plan& pl, const Operands& op, const __half* biasp, int64_
     prm.splits = pl.splits;
     prm.partials = partials;
     prm.counters = counters;
+    if (!pair && take_fault(GEMM_F16_FAULT_SKIP_LOADS)) {
+        prm.fault_skip_kb = 1;
+        prm.timeout_ns = g_fault_wait_ns.load(std::memory_order_relaxed);
+    }
     switch (pl.cfg) {
         case CFG_PAIR_256: return launch_tc_pair(ta, tb, prm, pl.ctas, s);
         case CFG_SWAP:
@@ -706,6 +730,17 @@ int init_device_noalloc(int dev) {
     return GEMM_OK;
 }
 
+// The plan gemm_f16_noalloc runs: gemm_f16's, inside the fixed buffer.
+// Without room for the split-K partials the problem runs unsplit; if even
+// the repacks alone do not fit, *fits is false.
+Plan make_noalloc_plan(const Operands& op, int64_t M, int64_t N, int64_t K, int num_sms, int pair_clusters,
+                       int force, bool* fits) {
+    Plan pl = make_plan(op, M, N, K, num_sms, pair_clusters, force);
+    if (pl.scratch_bytes() > kNoAllocScratchBytes) pl = make_plan(op, M, N, K, num_sms, pair_clusters, force, false);
+    *fits = pl.scratch_bytes() <= kNoAllocScratchBytes;
+    return pl;
+}
+
 }  // namespace
 
 extern "C" {
@@ -742,7 +777,7 @@ int gemm_f16_plan_ex(const void* A, int64_t lda, const void* B, int64_t ldb, con
                      int64_t ldc, int64_t M, int64_t N, int64_t K, int epilogue, int flags, int num_sms,
                      int64_t plan[11]) {
     if (plan == nullptr || num_sms <= 0) return GEMM_ERR_INVALID_ARG;
-    if (flags & ~(GEMM_F16_TRANS_A | GEMM_F16_TRANS_B)) return GEMM_ERR_INVALID_ARG;
+    if (flags & ~(GEMM_F16_TRANS_A | GEMM_F16_TRANS_B | GEMM_F16_PLAN_NOALLOC)) return GEMM_ERR_INVALID_ARG;
     Operands op;
     op.A = A;
     op.B = B;
@@ -754,7 +789,14 @@ int gemm_f16_plan_ex(const void* A, int64_t lda, const void* B, int64_t ldb, con
     op.tb = (flags & GEMM_F16_TRANS_B) != 0;
     const int st = check_args(op, bias, M, N, K, epilogue);
     if (st != GEMM_OK) return st;
-    const Plan pl = make_plan(op, M, N, K, num_sms, num_sms / 2, g_force_config.load());
+    Plan pl;
+    if (flags & GEMM_F16_PLAN_NOALLOC) {
+        bool fits = true;
+        pl = make_noalloc_plan(op, M, N, K, num_sms, num_sms / 2, g_force_config.load(), &fits);
+        if (!fits) return GEMM_ERR_SCRATCH_LIMIT;
+    } else {
+        pl = make_plan(op, M, N, K, num_sms, num_sms / 2, g_force_config.load());
+    }
     plan[0] = pl.path;
     plan[1] = pl.tile_m;
     plan[2] = pl.tile_n;
@@ -830,24 +872,24 @@ int gemm_f16_noalloc(const void* A, const void* B, const void* bias, void* C, in
     const Operands op = dense_operands(A, B, C, N, K);
     int st = check_args(op, bias, M, N, K, epilogue);
     if (st != GEMM_OK) return st;
-    if (M == 0 || N == 0) return GEMM_OK;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
+    // the set-up (and with it the fixed buffer's reservation) also runs for an
+    // empty problem, so that a caller can take it at start-up
     st = init_device_noalloc(dev);
     if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
     const DeviceState& ds = g_dev[dev];
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-    Plan pl = make_plan(op, M, N, K, ds.num_sms, ds.pair_clusters, g_force_config.load());
-    const __half* biasp = epilogue == GEMM_EPI_NONE ? nullptr : static_cast<const __half*>(bias);
-    if (pl.path == 1) return enqueue_bias_only(pl, biasp, C, N, M, N, epilogue, s);
     // Same scratch layout as gemm_f16, inside the fixed buffer.  The repacks
     // need no zeroed memory (the tensor maps stop at the true extents); the
     // split-K counters are zeroed by a stream-ordered memset in enqueue_plan.
-    // Without room for split-K partials the plan runs unsplit.
-    if (pl.scratch_bytes() > kNoAllocScratchBytes)
-        pl = make_plan(op, M, N, K, ds.num_sms, ds.pair_clusters, g_force_config.load(), false);
-    if (pl.scratch_bytes() > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
+    bool fits = true;
+    const Plan pl = make_noalloc_plan(op, M, N, K, ds.num_sms, ds.pair_clusters, g_force_config.load(), &fits);
+    const __half* biasp = epilogue == GEMM_EPI_NONE ? nullptr : static_cast<const __half*>(bias);
+    if (pl.path == 1) return enqueue_bias_only(pl, biasp, C, N, M, N, epilogue, s);
+    if (!fits) return GEMM_ERR_SCRATCH_LIMIT;
     return enqueue_plan(pl, op, biasp, M, N, K, epilogue, ds.noalloc_scratch, s);
 }
 
@@ -990,6 +1032,14 @@ int gemm_f16_release_workspace(void) {
         e = cudaMemPoolTrimTo(g_dev[dev].pool, 0);
         if (e != cudaSuccess) return cuda_fail(e);
     }
+    return GEMM_OK;
+}
+
+int gemm_f16_debug_inject(int fault, uint32_t wait_us) {
+    if (fault < GEMM_F16_FAULT_NONE || fault > GEMM_F16_FAULT_ENCODE) return GEMM_ERR_INVALID_ARG;
+    if (fault == GEMM_F16_FAULT_SKIP_LOADS && wait_us == 0) return GEMM_ERR_INVALID_ARG;
+    g_fault_wait_ns.store(static_cast<uint64_t>(wait_us) * 1000ull, std::memory_order_relaxed);
+    g_fault.store(fault);
     return GEMM_OK;
 }
 

@@ -80,28 +80,31 @@ __device__ __forceinline__ TileCoord tile_coord(int t, int tiles_m, int tiles_n,
     return c;
 }
 
-// erf(z) for z >= 0 by Abramowitz & Stegun, Handbook of Mathematical
-// Functions, eq. 7.1.26: erf(z) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5)
-// exp(-z^2), t = 1 / (1 + p z), with |error| <= 1.5e-7 over z >= 0.  In fp32
-// with the approximate reciprocal and exponential the total error stays a few
-// 1e-7, below the spacing of fp16 results; it costs about half the
+// erfc(z) for z >= 0 by Abramowitz & Stegun, Handbook of Mathematical
+// Functions, eq. 7.1.26: erfc(z) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5)
+// exp(-z^2), t = 1 / (1 + p z), with |error| <= 1.5e-7 over z >= 0 (absolute;
+// relative to erfc itself it stays below 8e-4 for z <= 3.1, where GELU's
+// negative tail leaves the fp16 normal range).  It costs about half the
 // instructions of erff, which matters because the epilogue shares the SM's
 // issue slots with the MMA and load warps.
-__device__ __forceinline__ float erf_as_7_1_26(float z) {
+__device__ __forceinline__ float erfc_as_7_1_26(float z) {
     const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));
     float q = fmaf(1.061405429f, t, -1.453152027f);
     q = fmaf(q, t, 1.421413741f);
     q = fmaf(q, t, -0.284496736f);
     q = fmaf(q, t, 0.254829592f);
     q *= t;
-    return 1.0f - q * __expf(-z * z);
+    return q * __expf(-z * z);
 }
 
-// GELU(x) = x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)), erf odd: sign moved outside.
+// GELU(x) = x Phi(x) = 0.5 x (1 + erf(x / sqrt 2)).  With z = |x| / sqrt 2 and
+// c = erfc(z): 1 + erf = 2 - c for x >= 0 and 1 - erf(z) = c for x < 0.  The
+// negative tail is thus the product 0.5 x c, with no cancellation: it keeps
+// the relative accuracy of c down to the fp16 subnormals.
 __device__ __forceinline__ float gelu_erf(float x) {
-    const float e = erf_as_7_1_26(fabsf(x) * 0.70710678118654752440f);
+    const float c = erfc_as_7_1_26(fabsf(x) * 0.70710678118654752440f);
     const float hx = 0.5f * x;
-    return fmaf(hx, copysignf(e, x), hx);
+    return hx * (x < 0.0f ? c : 2.0f - c);
 }
 
 // 1 / (1 + e^-x): e^-x overflows to +inf for x < -88, giving 0.
@@ -110,11 +113,12 @@ __device__ __forceinline__ float sigmoid_f(float x) {
 }
 
 // GELU, tanh form: 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3),
-// with 1 + tanh(u) = 2 - 2 / (1 + e^(2u)) (absolute error ~1e-7; exact
-// saturation: e^(2u) = inf gives 2, e^(2u) = 0 gives 0).
+// with 1 + tanh(u) = 2 / (1 + e^(-2u)): a quotient, never a difference, so
+// the negative tail keeps its relative accuracy (e^(-2u) = 0 gives 2,
+// e^(-2u) = inf gives 0).
 __device__ __forceinline__ float gelu_tanh_f(float x) {
     const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
-    const float one_plus_t = 2.0f - __fdividef(2.0f, 1.0f + __expf(2.0f * u));
+    const float one_plus_t = __fdividef(2.0f, 1.0f + __expf(-2.0f * u));
     return 0.5f * x * one_plus_t;
 }
 
@@ -161,6 +165,11 @@ struct GemmParams {
     // trans_b = B stored N x K (K contiguous, K-major)
     int trans_a;
     int trans_b;
+    // Fault injection for the tests of the bounded waits (single-CTA kernels
+    // only; -1 in every normal call): the producer never issues the loads of
+    // K block `fault_skip_kb` of its first tile, so the MMA thread's wait for
+    // that stage runs out and the abort path runs with no copy in flight.
+    int fault_skip_kb;
 };
 
 // One 64 (M or N) x 64 (K) box of an operand tile.  The tensor map of a
@@ -400,6 +409,7 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
+            int skip_kb = p.fault_skip_kb;   // -1 except in fault-injection tests
             for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
                 const TileCoord tc = tile_coord(t, tiles_m, tiles_n, p.group_m, BN);
                 // B boxes entirely right of N are skipped: the stale smem they
@@ -413,6 +423,11 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, status,
                                            ROLE_PRODUCER, BAR_EMPTY)) { ok = false; break; }
+                    if (kb == skip_kb) {   // injected fault: this stage's loads never come
+                        ++issued;
+                        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                        continue;
+                    }
                     mbar_arrive_expect_tx(full_bar(stage), bytes);
                     if (ta) {
                         for (int c = 0; c < a_boxes; ++c)
@@ -427,6 +442,7 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
+                skip_kb = -1;
             }
             // Let the last (up to STAGES) loads land before the CTA can exit:
             // earlier ones were consumed, which the empty-barrier waits proved.

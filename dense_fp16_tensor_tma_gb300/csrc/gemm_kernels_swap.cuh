@@ -137,6 +137,7 @@ gemm_f16_swap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
+            int skip_kb = p.fault_skip_kb;   // -1 except in fault-injection tests
             for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
                 const int t = u / S;
                 const int m0 = tile_m0(t), n0 = tile_n0(t);
@@ -147,6 +148,11 @@ gemm_f16_swap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 for (int kb = kb_begin(u); kb < kb_end(u); ++kb) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, status,
                                            ROLE_PRODUCER, BAR_EMPTY)) { ok = false; break; }
+                    if (kb - kb_begin(u) == skip_kb) {   // injected fault: this stage's loads never come
+                        ++issued;
+                        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                        continue;
+                    }
                     const uint32_t st = base_s + stage * SP::kStage;
                     mbar_arrive_expect_tx(full_bar(stage), bytes);
                     for (int c = 0; c < live_b; ++c)
@@ -156,6 +162,7 @@ gemm_f16_swap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
+                skip_kb = -1;
             }
             const int pending = min(issued, STAGES);
             for (int i = 0; i < pending; ++i) {

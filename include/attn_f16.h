@@ -64,6 +64,26 @@ int attn_f16_last_cuda_error(void);
  */
 int attn_f16_debug_status(void* cuda_stream, uint32_t* detail);
 
+/*
+ * Test hook for the attention forward's error paths (no counterpart on the
+ * pages; not for production use), like gemm_f16_debug_inject and with the
+ * same gemm_f16_fault_t values, armed separately for this entry point:
+ *
+ *   GEMM_F16_FAULT_SKIP_LOADS: the next attn_f16_fwd launch never loads the
+ *     second key block of each CTA's block sequence (S must exceed 128), and
+ *     its bounded waits give up after `wait_us` microseconds (> 0): the MMA
+ *     thread's wait for that block runs out, every role leaves, the rest is
+ *     drained and tensor memory freed; attn_f16_debug_status then reports
+ *     GEMM_ERR_TIMEOUT and the context stays usable.  O is left partly
+ *     written.
+ *   GEMM_F16_FAULT_ENCODE: the next tensor-map encoding fails: that
+ *     attn_f16_fwd call returns GEMM_ERR_CUDA and enqueues nothing.
+ *
+ * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for an unknown fault or a zero
+ * wait with GEMM_F16_FAULT_SKIP_LOADS.
+ */
+int attn_f16_debug_inject(int fault, uint32_t wait_us);
+
 #ifdef __cplusplus
 }
 #endif

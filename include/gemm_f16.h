@@ -86,8 +86,9 @@ int gemm_f16(const void* A, const void* B, const void* bias, void* C,
 
 /* Operand layout flags of gemm_f16_ex (bitwise or). */
 typedef enum {
-    GEMM_F16_TRANS_A = 1,  /* A is stored transposed: K x M, M contiguous */
-    GEMM_F16_TRANS_B = 2   /* B is stored transposed: N x K, K contiguous */
+    GEMM_F16_TRANS_A = 1,     /* A is stored transposed: K x M, M contiguous */
+    GEMM_F16_TRANS_B = 2,     /* B is stored transposed: N x K, K contiguous */
+    GEMM_F16_PLAN_NOALLOC = 4 /* gemm_f16_plan_ex only: the plan of gemm_f16_noalloc */
 } gemm_f16_flags_t;
 
 /*
@@ -187,7 +188,11 @@ int gemm_f16_plan(const void* A, const void* B, const void* bias, const void* C,
                   int64_t M, int64_t N, int64_t K, int epilogue, int num_sms,
                   int64_t plan[11]);
 
-/* gemm_f16_plan for the arguments of gemm_f16_ex (same plan[] entries). */
+/* gemm_f16_plan for the arguments of gemm_f16_ex (same plan[] entries).
+ * With GEMM_F16_PLAN_NOALLOC in `flags`: the plan gemm_f16_noalloc takes
+ * (all of its scratch inside the fixed buffer, split-K dropped when the
+ * partial sums do not fit beside the repacks), or GEMM_ERR_SCRATCH_LIMIT
+ * when the repacks alone exceed the buffer. */
 int gemm_f16_plan_ex(const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias,
                      const void* C, int64_t ldc, int64_t M, int64_t N, int64_t K, int epilogue,
                      int flags, int num_sms, int64_t plan[11]);
@@ -217,6 +222,40 @@ int gemm_f16_force_config(int config);
  * Process-wide; set it while no other host thread is calling.
  */
 int gemm_f16_set_pdl(int enable);
+
+/* Faults gemm_f16_debug_inject can arm. */
+typedef enum {
+    GEMM_F16_FAULT_NONE = 0,
+    GEMM_F16_FAULT_SKIP_LOADS = 1,  /* next single-CTA tensor-core launch skips one stage's loads */
+    GEMM_F16_FAULT_ENCODE = 2       /* next TMA tensor-map encoding fails */
+} gemm_f16_fault_t;
+
+/*
+ * Test hook for the library's error paths (no counterpart on the pages; not
+ * for production use).  Arms one fault, process-wide, consumed by the first
+ * call that reaches it; GEMM_F16_FAULT_NONE disarms.
+ *
+ *   GEMM_F16_FAULT_SKIP_LOADS: the next launch of a single-CTA tensor-core
+ *     kernel (128-row tiles or swap-AB; CTA-pair launches neither use nor
+ *     consume it) never issues the loads of the second K block of each CTA's
+ *     first tile, and every bounded wait of that launch gives up after
+ *     `wait_us` microseconds (> 0).  The MMA thread's wait for that stage
+ *     runs out; the kernel records the timeout in the status word, every role
+ *     leaves, in-flight loads and MMAs are drained and tensor memory is freed.
+ *     Nothing is ever in flight for the skipped stage.  C is left partly
+ *     written; gemm_f16_debug_status then reports GEMM_ERR_TIMEOUT, and the
+ *     context stays usable.  The problem must have at least two K blocks
+ *     (K > 64), or nothing is skipped.
+ *   GEMM_F16_FAULT_ENCODE: the next tensor-map encoding fails as the driver's
+ *     encoder would for an invalid map: that call returns GEMM_ERR_CUDA
+ *     (gemm_f16_last_cuda_error = CUDA_ERROR_INVALID_VALUE).  gemm_f16,
+ *     gemm_f16_ex and gemm_f16_noalloc encode their maps before enqueueing
+ *     any work, so such a call enqueues no kernel.
+ *
+ * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for an unknown fault or a zero
+ * wait with GEMM_F16_FAULT_SKIP_LOADS.
+ */
+int gemm_f16_debug_inject(int fault, uint32_t wait_us);
 
 /*
  * Diagnostic for the bounded-wait machinery (no counterpart on the pages):
@@ -256,7 +295,13 @@ int gemm_f16_selftest_timeout(void* cuda_stream, uint32_t timeout_us);
  *     (the problem runs unsplit) when they do not.
  *   - Set-up: the first call on each device (with that device current) looks
  *     up the buffer's device address and sets kernel attributes; make that
- *     first call before any stream capture.
+ *     first call before any stream capture.  The buffer is reserved when the
+ *     library's device code is loaded onto the device; with CUDA's lazy
+ *     module loading (the default) that happens during this set-up, so on a
+ *     device whose memory another allocator has already claimed the first
+ *     call can fail with GEMM_ERR_CUDA.  A call with M == 0 or N == 0 (valid
+ *     arguments, nothing to compute) runs the set-up and enqueues nothing:
+ *     make one at start-up to take the buffer before the device fills up.
  *   - Sharing: every call on a device uses the same buffer, which keeps the
  *     previous call's contents (nothing in it needs to start at zero).  Calls
  *     whose GPU work overlaps (e.g. on two streams without ordering between

@@ -200,3 +200,13 @@ def test_pipelined_e2e_orders_copies_and_kernels():
             # compute i writes set b's result only after copy-out i - 2 read it
             assert event_of(comp, "compute", i - 2) in waits_before(s_in, position(s_in, "in", i))
             assert event_of(s_out, "out", i - 2) in waits_before(comp, position(comp, "compute", i))
+
+
+def test_launch_stats_median_min_p90():
+    import bench
+    xs = [float(v) for v in range(1, 21)]          # 1 .. 20 ms
+    st = bench.launch_stats(list(reversed(xs)))
+    assert st["min"] == 1.0 and st["median"] == 10.5 and st["p90"] == 18.0 and st["n"] == 20
+    assert st["mean"] == sum(xs) / 20
+    one = bench.launch_stats([0.5])
+    assert one["min"] == one["median"] == one["p90"] == one["mean"] == 0.5

@@ -277,3 +277,12 @@ def test_attention_pointer_checks_need_no_device(g):
 def test_attention_flop_model(g):
     assert g.attention_flops(4, 32, 4096, 128, False) == 4 * 4 * 32 * 4096 ** 2 * 128
     assert g.attention_flops(4, 32, 4096, 128, True) == 2 * 4 * 32 * 4096 ** 2 * 128
+
+
+def test_fault_injection_arguments_need_no_device(g):
+    for inject in (g.gemm_f16_debug_inject, g.attn_f16_debug_inject):
+        assert inject(3) == g.GEMM_ERR_INVALID_ARG
+        assert inject(-1) == g.GEMM_ERR_INVALID_ARG
+        assert inject(g.GEMM_F16_FAULT_SKIP_LOADS, 0) == g.GEMM_ERR_INVALID_ARG   # needs a wait limit
+        assert inject(g.GEMM_F16_FAULT_SKIP_LOADS, 2000) == g.GEMM_OK
+        assert inject(g.GEMM_F16_FAULT_NONE) == g.GEMM_OK                         # disarmed again

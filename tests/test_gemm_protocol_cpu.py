@@ -184,3 +184,169 @@ def test_gemm_protocol_model_catches_planted_defects(defect):
     with pytest.raises(AssertionError):
         for seed in range(40):
             run_pair(units, 3, seed, defect=defect)
+
+
+# ---------------------------------------------------------------- a stage's loads never arrive
+
+def run_pair_lost_load(units, stages, seed, lost_cta, lost_pos, epi_warps=2, defect=None):
+    """The protocol of run_pair with its abort paths: one CTA's producer never
+    issues the loads of position `lost_pos` (the leader then posts no expected
+    bytes for it either), so that stage's `full` phase never completes.  Every
+    wait is bounded: a wait may run out only when nothing else can move (a
+    load or a tensor-core operation still in flight always lands first), and
+    then sets its CTA's abort flag (the final drains have no abort flag and
+    only give up); a wait in a CTA whose flag is up may give up at any time.
+    Each role then takes the kernel's exit path.  Checked: every role ends,
+    no load is in flight and the tensor pipe is empty when the CTAs exit (the
+    shared memory the loads write and the tensor memory the MMAs write are
+    released only then), no barrier over-arrives, and a timeout was reported.
+    `defect` = "no_mma_drain" plants a mistake: the MMA thread leaves without
+    waiting for its drain commit."""
+    rnd = random.Random(seed)
+    full = [Barrier(f"full{s}", 1) for s in range(stages)]
+    empty = [[Barrier(f"empty{s}@cta{c}", 1) for s in range(stages)] for c in range(2)]
+    acc_full = [[Barrier(f"acc_full{b}@cta{c}", 1) for b in range(2)] for c in range(2)]
+    acc_empty = [Barrier(f"acc_empty{b}", 2 * epi_warps) for b in range(2)]
+    drain = Barrier("drain", 1)
+    tma, pipe = [], []
+    abort = [False, False]
+    status = []
+
+    def wait(bar, index, who, cta, honours_abort=True):
+        return (bar, index & 1, who, index, cta, honours_abort)
+
+    def producer(cta):
+        stage = issued = 0
+        count = [0] * stages
+        ok = True
+        pos = 0
+        for kblocks in units:
+            for _ in range(kblocks):
+                ok = yield wait(empty[cta][stage], count[stage] - 1, f"producer {cta}", cta)
+                if not ok:
+                    break
+                if not (cta == lost_cta and pos == lost_pos):
+                    if cta == 0:
+                        full[stage].arrive(tx=2)
+                    tma.append(full[stage])
+                count[stage] += 1
+                issued += 1
+                pos += 1
+                stage = (stage + 1) % stages
+            if not ok:
+                break
+        if cta == 0:
+            for _ in range(min(issued, stages)):
+                stage = (stage - 1) % stages
+                yield wait(full[stage], count[stage] - 1, "producer drain", cta, honours_abort=False)
+
+    def mma():
+        stage = acc = 0
+        count = [0] * stages
+        acc_count = [0, 0]
+        ok = True
+        for kblocks in units:
+            ok = yield wait(acc_empty[acc], acc_count[acc] - 1, "mma acc_empty", 0)
+            if not ok:
+                break
+            for _ in range(kblocks):
+                ok = yield wait(full[stage], count[stage], "mma full", 0)
+                if not ok:
+                    break
+                count[stage] += 1
+                pipe.append(("mma", None))
+                pipe.append(("commit", [empty[0][stage], empty[1][stage]]))
+                stage = (stage + 1) % stages
+            if not ok:
+                break
+            pipe.append(("commit", [acc_full[0][acc], acc_full[1][acc]]))
+            acc_count[acc] += 1
+            acc ^= 1
+        pipe.append(("commit", [drain]))
+        if defect != "no_mma_drain":
+            yield wait(drain, 0, "mma drain", 0, honours_abort=False)
+
+    def epilogue(cta):
+        acc = 0
+        acc_count = [0, 0]
+        for _ in units:
+            ok = yield wait(acc_full[cta][acc], acc_count[acc], f"epilogue {cta}", cta)
+            if not ok:
+                break
+            acc_empty[acc].arrive()
+            acc_count[acc] += 1
+            acc ^= 1
+
+    roles = [producer(0), producer(1), mma()] + [epilogue(c) for c in (0, 1) for _ in range(epi_warps)]
+    current = [None] * len(roles)
+    live = [True] * len(roles)
+
+    def resume(i, value):
+        try:
+            current[i] = roles[i].send(value) if current[i] is not None else next(roles[i])
+        except StopIteration:
+            live[i], current[i] = False, None
+
+    for _ in range(2_000_000):
+        if not any(live):                               # the CTAs exit here
+            break
+        ready, stuck = [], []
+        for i in range(len(roles)):
+            if not live[i]:
+                continue
+            if current[i] is None:
+                ready.append(("role", i))
+                continue
+            bar, parity, who, index, cta, honours = current[i]
+            assert bar.n <= index + 1, f"{who}: {bar.name} is {bar.n - index - 1} phase(s) past the awaited one"
+            if bar.passes(parity):
+                assert bar.n == index + 1, f"{who}: {bar.name} passes {index + 1 - bar.n} phase(s) early"
+                ready.append(("role", i))
+            else:
+                stuck.append(i)
+                if honours and abort[cta]:
+                    ready.append(("give_up", i))
+        if tma:
+            ready.append(("tma", None))
+        if pipe:
+            ready.append(("pipe", None))
+        if not ready:
+            i = rnd.choice(stuck)                       # nothing can move: one wait runs out
+            bar, parity, who, index, cta, honours = current[i]
+            status.append(who)
+            if honours:
+                abort[cta] = True
+            resume(i, False)
+            continue
+        kind, i = rnd.choice(ready)
+        if kind == "tma":
+            tma.pop(rnd.randrange(len(tma))).complete_tx(1)
+        elif kind == "pipe":
+            op, bars = pipe.pop(0)
+            if op == "commit":
+                for bar in bars:
+                    bar.arrive()
+        elif kind == "give_up":
+            resume(i, False)
+        else:
+            resume(i, True)
+    else:
+        raise AssertionError("no progress bound reached")
+    assert not any(live), "a role never ended"
+    assert not tma, "a load still in flight when the CTAs exit"
+    assert not pipe, "tensor-core work still in flight when tensor memory is freed"
+    assert status, "the lost load went unnoticed"
+
+
+@pytest.mark.parametrize("stages", [2, 3])
+@pytest.mark.parametrize("lost_cta", [0, 1])
+@pytest.mark.parametrize("units,lost_pos", [([1], 0), ([4], 1), ([3, 3, 2], 4), ([2] * 6, 9), ([5, 5], 9)])
+def test_gemm_pair_lost_load_ends_cleanly(stages, lost_cta, units, lost_pos):
+    for seed in range(12):
+        run_pair_lost_load(units, stages, seed, lost_cta, lost_pos)
+
+
+def test_lost_load_model_catches_a_missing_drain():
+    with pytest.raises(AssertionError, match="tensor-core work still in flight"):
+        for seed in range(40):
+            run_pair_lost_load([2] * 6, 3, seed, 1, 9, defect="no_mma_drain")
