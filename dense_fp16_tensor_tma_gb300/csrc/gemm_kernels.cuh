@@ -152,6 +152,8 @@ struct GemmParams {
     int mn3d_a, mn3d_b;  // MN-major operand map is 3-D (64, K, MN / 64): two 64-wide boxes per load
     int bias_vec;        // bias base 16-byte aligned (8-wide bias loads)
     int group_m;
+    int group_n;         // CTA-pair tile order: blocks of group_n tile-columns (0: whole width)
+    int snake;           // CTA-pair tile order: odd bands of group_m tile-rows walk from the right
     uint64_t timeout_ns;
     // CTA-pair kernel: tiles [0, dp_tiles) whole; with tail_split the rest are
     // computed as two 256 x 128 halves each (a partial last wave costs half a tile)
@@ -538,26 +540,70 @@ __global__ void gemm_f16_bias_only_kernel(__half* C, const __half* bias, int64_t
 // Row repack: dst[r, 0:cols] = src[r, 0:cols] with a 16-byte-multiple pitch,
 // so the tensor map can describe the copy (columns >= cols are left as is;
 // the tensor map's extent stops at `cols`, so TMA never reads them).  Each
-// thread gathers 8 consecutive source elements (the source rows are only
-// 2-byte aligned) and writes them with one 16-byte store (ld_dst % 8 == 0 and
-// dst is 256-byte aligned).  grid.x covers a row in 2048-element pieces,
-// grid.y strides over rows.
+// thread writes 16-byte pieces, elements c .. c+7 of `group` rows (ld_dst
+// % 8 == 0 and dst is 256-byte aligned).  A source piece is only 2-byte
+// aligned: it lies within the aligned 16-byte chunk holding its first element
+// and, unless it starts on a chunk boundary, the next chunk; each of these
+// holds at least one element of the piece, so neither load reaches outside
+// the memory pages the source occupies.  The piece is cut out of the two
+// chunks by a funnel shift (odd element offset) and a word offset picked by
+// selects.  All of a thread's loads are issued before its first store, so
+// each thread keeps up to 2 x kRepackRows loads in flight (large copies use
+// groups of kRepackRows rows; small ones, where blocks are scarce, single
+// rows).  A row's last piece, if shorter than 8 elements, is copied element
+// by element.  grid.x covers a row in 2048-element pieces, grid.y strides
+// over groups of rows.
+constexpr int kRepackRows = 4;
+
+__device__ __forceinline__ uint4 repack_cut(const uint4 v0, const uint4 v1, uint32_t off) {
+    const uint32_t x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    const uint32_t sh = (off & 2u) ? 16u : 0u;   // an odd element offset
+    const uint32_t wo = off >> 2;                  // whole words to skip: 0 .. 3
+    uint32_t z[7];
+#pragma unroll
+    for (int i = 0; i < 7; ++i) z[i] = __funnelshift_r(x[i], x[i + 1], sh);
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = (wo & 1u) ? z[j + 1] : z[j];
+        const uint32_t hi = (wo & 1u) ? z[j + 3] : z[j + 2];
+        w[j] = (wo & 2u) ? hi : lo;
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 __global__ void gemm_f16_repack_kernel(uint16_t* __restrict__ dst, const uint16_t* __restrict__ src,
-                                       int64_t rows, int64_t cols, int64_t ld_src, int64_t ld_dst) {
+                                       int64_t rows, int64_t cols, int64_t ld_src, int64_t ld_dst, int group) {
     grid_dependency_wait();
     grid_launch_dependents();
     const int64_t c = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
     if (c >= cols) return;
-    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
-        const uint16_t* s = src + r * ld_src + c;
-        uint16_t* d = dst + r * ld_dst + c;
-        if (c + 8 <= cols) {
-            uint32_t w[4];
+    const bool whole = c + 8 <= cols;
+    for (int64_t r0 = static_cast<int64_t>(blockIdx.y) * group; r0 < rows;
+         r0 += static_cast<int64_t>(gridDim.y) * group) {
+        const int64_t r_end = min(rows, r0 + group);
+        if (whole) {
+            uint4 v0[kRepackRows], v1[kRepackRows];
+            uint32_t off[kRepackRows];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) w[j] = static_cast<uint32_t>(s[2 * j]) | (static_cast<uint32_t>(s[2 * j + 1]) << 16);
-            *reinterpret_cast<uint4*>(d) = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int i = 0; i < kRepackRows; ++i) {
+                v0[i] = v1[i] = make_uint4(0u, 0u, 0u, 0u);
+                off[i] = 0u;
+                if (r0 + i < r_end) {
+                    const uintptr_t a = reinterpret_cast<uintptr_t>(src + (r0 + i) * ld_src + c);
+                    off[i] = static_cast<uint32_t>(a & 15u);       // bytes past the chunk boundary, even
+                    const uint4* chunk = reinterpret_cast<const uint4*>(a - off[i]);
+                    v0[i] = __ldg(chunk);
+                    if (off[i] != 0u) v1[i] = __ldg(chunk + 1);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kRepackRows; ++i)
+                if (r0 + i < r_end)
+                    *reinterpret_cast<uint4*>(dst + (r0 + i) * ld_dst + c) = repack_cut(v0[i], v1[i], off[i]);
         } else {
-            for (int64_t j = 0; j < cols - c; ++j) d[j] = s[j];
+            for (int64_t r = r0; r < r_end; ++r)
+                for (int64_t j = 0; j < cols - c; ++j) dst[r * ld_dst + c + j] = src[r * ld_src + c + j];
         }
     }
 }

@@ -53,15 +53,27 @@ struct SmemPlanPair {
     static constexpr uint32_t kDynamicBytes = kEnd + 1024;
 };
 
-__device__ __forceinline__ TileCoord tile_coord_bm(int t, int tiles_m, int tiles_n, int group_m, int BM, int BN) {
-    const int per_group = group_m * tiles_n;
-    const int g = t / per_group;
-    const int first_m = g * group_m;
+// Tile t of a tiles_m x tiles_n grid in grouped order: bands of group_m
+// tile-rows, each walked in blocks of group_n tile-columns (the whole width
+// when group_n == 0), column by column inside a block, so a wave of
+// concurrent pairs covers a compact block of tiles that share A row-panels
+// and B column-panels in L2.  With `snake`, odd bands walk their columns from
+// the right: a band starts on the B panels its predecessor ended with.
+__device__ __forceinline__ TileCoord tile_coord_bm(int t, int tiles_m, int tiles_n, int group_m, int BM, int BN,
+                                                   int group_n = 0, int snake = 0) {
+    const int band_tiles = group_m * tiles_n;
+    const int band = t / band_tiles;
+    const int first_m = band * group_m;
     const int rows = min(tiles_m - first_m, group_m);
-    const int r = t - g * per_group;
+    const int r = t - band * band_tiles;           // inside the band: rows x tiles_n tiles
+    const int gn = group_n > 0 ? group_n : tiles_n;
+    const int blk = r / (rows * gn);
+    const int i = r - blk * rows * gn;             // inside the block: rows x (<= gn) tiles
+    int n = blk * gn + i / rows;
+    if (snake && (band & 1)) n = tiles_n - 1 - n;
     TileCoord c;
-    c.m0 = (first_m + r % rows) * BM;
-    c.n0 = (r / rows) * BN;
+    c.m0 = (first_m + i % rows) * BM;
+    c.n0 = n * BN;
     return c;
 }
 
@@ -194,7 +206,7 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             PairUnitIter it = units();
             PairUnit un;
             while (ok && it.next(un)) {
-                const TileCoord tc = tile_coord_bm(un.tile, tiles_m, tiles_n, p.group_m, PM, BN);
+                const TileCoord tc = tile_coord_bm(un.tile, tiles_m, tiles_n, p.group_m, PM, BN, p.group_n, p.snake);
                 const int my_a = a_boxes(tc.m0, rank);
                 // a whole tile: CTA r loads columns n0 + 128r (two boxes); a half
                 // tile h: CTA r loads the one box at n0 + 128h + 64r
@@ -325,7 +337,7 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         PairUnitIter it = units();
         PairUnit un;
         while (it.next(un)) {
-            const TileCoord tc = tile_coord_bm(un.tile, tiles_m, tiles_n, p.group_m, PM, BN);
+            const TileCoord tc = tile_coord_bm(un.tile, tiles_m, tiles_n, p.group_m, PM, BN, p.group_n, p.snake);
             const int half = (warp - 2) >> 2;   // which half of the unit's columns this warp takes
             const int ucols = un.half < 0 ? BN : BN / 2;                       // the unit's width
             const int un0 = un.half < 0 ? tc.n0 : tc.n0 + (BN / 2) * un.half;  // its first column

@@ -187,6 +187,37 @@ def test_unaligned_pointers_use_repack_and_narrow_stores(g, torch_dev, oracle_mo
     assert c[0] == -7.0 and np.all(c[1 + M * N:] == -7.0)
 
 
+@pytest.mark.parametrize("shift", [1, 2, 3, 4, 5, 6, 7])
+def test_repack_every_base_offset_integer_exact(g, torch_dev, oracle_mod, shift):
+    # A and B start `shift` elements (2 * shift bytes) past a 16-byte boundary and
+    # have odd row pitches (lda = K, ldb = N with K, N odd): the repack must cut
+    # every 8-element piece out of its two aligned 16-byte chunks correctly, at
+    # every byte offset, and copy each row's short last piece.  Small integers:
+    # every step is exact, so the result must equal the oracle's bit for bit.
+    torch, dev = torch_dev
+    rng = np.random.default_rng(40 + shift)
+    M, N, K = 136, 203, 77
+    A = rng.integers(-2, 3, (M, K)).astype(np.float16)
+    B = rng.integers(-2, 3, (K, N)).astype(np.float16)
+    bias = rng.integers(-4, 5, N).astype(np.float16)
+    def at_offset(x):
+        buf = torch.zeros(x.size + 16, dtype=torch.float16, device=dev)
+        buf[shift:shift + x.size] = torch.from_numpy(x.ravel()).to(dev)
+        return buf, buf[shift:shift + x.size]
+    bufa, a1 = at_offset(A)
+    bufb, b1 = at_offset(B)
+    plan = g.gemm_f16_plan(M, N, K, "bias", a_addr=a1.data_ptr(), b_addr=b1.data_ptr())
+    assert plan["pack_a"] == 1 and plan["pack_b"] == 1
+    tb = torch.from_numpy(bias).to(dev)
+    C = torch.empty((M, N), dtype=torch.float16, device=dev)
+    assert g.gemm_f16_ptr(a1.data_ptr(), b1.data_ptr(), tb.data_ptr(), C.data_ptr(), M, N, K, "bias",
+                          torch.cuda.current_stream().cuda_stream) == 0
+    st, word = g.gemm_f16_debug_status()
+    assert st == 0, hex(word)
+    ref = oracle_mod.gemm(A, B, bias, "bias")
+    assert np.array_equal(C.cpu().numpy().view(np.uint16), ref.view(np.uint16))
+
+
 def test_odd_k_repacks_a(g, torch_dev, oracle_mod):
     rng = np.random.default_rng(7)
     M, N, K = 150, 264, 77
