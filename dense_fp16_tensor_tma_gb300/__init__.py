@@ -28,7 +28,7 @@ EXPORTS = ("gemm_f16", "gemm_f16_ex", "gemm_f16_status_string", "gemm_f16_last_c
            "gemm_f16_debug_status", "gemm_f16_release_workspace", "gemm_f16_plan", "gemm_f16_plan_ex",
            "gemm_f16_selftest_timeout", "gemm_f16_noalloc", "gemm_f16_force_config", "gemm_f16_set_pdl",
            "gemm_f16_grouped", "attn_f16_fwd", "attn_f16_debug_status", "attn_f16_last_cuda_error",
-           "gemm_f16_debug_inject", "attn_f16_debug_inject")
+           "gemm_f16_debug_inject", "attn_f16_debug_inject", "gemm_f16_force_ksplit")
 GEMM_F16_FAULT_NONE, GEMM_F16_FAULT_SKIP_LOADS, GEMM_F16_FAULT_ENCODE = 0, 1, 2
 CONFIGS = {"auto": 0, "pair256x256": 1, "128x256": 2, "128x128": 3, "128x64": 4, "swap": 5, "pair_whole": 6}
 
@@ -76,6 +76,8 @@ lib.attn_f16_debug_status.restype = _int
 lib.attn_f16_last_cuda_error.restype = _int
 lib.gemm_f16_set_pdl.argtypes = [_int]
 lib.gemm_f16_set_pdl.restype = _int
+lib.gemm_f16_force_ksplit.argtypes = [_int]
+lib.gemm_f16_force_ksplit.restype = _int
 lib.gemm_f16_debug_inject.argtypes = [_int, ctypes.c_uint32]
 lib.gemm_f16_debug_inject.restype = _int
 lib.attn_f16_debug_inject.argtypes = [_int, ctypes.c_uint32]
@@ -272,6 +274,15 @@ def gemm_f16_force_config(config) -> int:
     prev = lib.gemm_f16_force_config(c)
     if prev < 0:
         raise ValueError(f"unknown configuration {config!r}")
+    return prev
+
+
+def gemm_f16_force_ksplit(splits: int) -> int:
+    """Pin the cluster split of K for 128-row tiles (0 automatic, 1 never, 2 or 4
+    CTAs per tile) for later calls; returns the previous setting."""
+    prev = lib.gemm_f16_force_ksplit(int(splits))
+    if prev < 0:
+        raise ValueError(f"unknown split {splits!r}")
     return prev
 
 

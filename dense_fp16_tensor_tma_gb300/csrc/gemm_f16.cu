@@ -82,6 +82,7 @@ EncodeTiledFn g_encode = nullptr;
 // calling thread when it fills kernel parameters
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_force_config{CFG_AUTO};
+std::atomic<int> g_force_ksplit{0};   // 0 automatic, 1 never, 2 / 4 that many CTAs per tile
 // Programmatic dependent launch on every kernel of the library (GEMM_F16_PDL=0
 // in the environment, or gemm_f16_set_pdl(0), turns it off).
 std::atomic<int> g_pdl{-1};   // -1: not yet read from the environment
@@ -136,7 +137,7 @@ struct Plan {
     int tile_m = 0, tile_n = 0, stages = 0, ctas = 0;
     bool pack_a = false, pack_b = false, vec_store = false;
     int64_t lda_packed = 0, ldb_packed = 0;
-    int splits = 1;                        // split-K parts per tile (swap-AB kernel)
+    int splits = 1;                        // swap-AB: split-K parts per tile; 128-row tiles: CTAs per cluster
     int dp_tiles = 0, tail_split = 0;      // CTA pair: whole tiles, then half-tile units
     // scratch layout: [A repack][B repack][split-K partials][split-K counters], each 256-aligned
     size_t a_scratch = 0, b_scratch = 0, p_scratch = 0, c_scratch = 0;
@@ -195,6 +196,58 @@ int check_args(const Operands& op, const void* bias, int64_t M, int64_t N, int64
     return GEMM_OK;
 }
 
+// Single-CTA kernel choice for problems with too few 256 x 256 tiles for
+// the CTA pair (and M > 64): 128-row tiles of width 64, 128 or 256, the
+// narrower two possibly with K split across a cluster of 2 or 4 CTAs.  Each
+// candidate is costed by the operand bytes it moves: the busiest SM's bytes
+// at its intake rate, or every CTA's bytes at the L2's aggregate rate,
+// whichever takes longer, plus a fixed cost for a split's cluster reduction.
+// The rates were fitted on a GB300 to replayed-graph timings of every
+// candidate on 13 shapes: about 88 GB/s per SM, 10.5 TB/s for the L2,
+// 2.5 us per split; 256-wide tiles with a split were never the fastest and
+// are not offered.  A candidate must beat the one before it by 5 %.
+struct Choice {
+    int cfg;
+    int splits;
+};
+
+Choice choose_tiles(int64_t M, int64_t N, int64_t K, int num_sms, int force, bool allow_split) {
+    constexpr double kBytesPerUs = 88.0e3, kL2BytesPerUs = 10.5e6, kSplitUs = 2.5;
+    const int64_t kblocks = (K + kBK - 1) / kBK;
+    const int64_t tiles_m = (M + 127) / 128;
+    const int forced_split = g_force_ksplit.load();
+    Choice best{force == CFG_AUTO ? CFG_128x64 : force, 1};
+    double best_t = 1e300;
+    for (int bn : {64, 128, 256}) {
+        const int cfg = bn == 256 ? CFG_128x256 : (bn == 128 ? CFG_128x128 : CFG_128x64);
+        if (force != CFG_AUTO && cfg != force) continue;
+        const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
+        const double per_k = (128.0 + bn) * 128.0;   // operand bytes per K block of a tile
+        for (int sp : {1, 2, 4}) {
+            if (forced_split == 1 && sp > 1) continue;
+            if (forced_split > 1 && sp != forced_split) continue;
+            double per_sm, total;
+            if (sp > 1) {
+                const int64_t kb_per = (kblocks + sp - 1) / sp;
+                // one tile per cluster, >= 4 K blocks per CTA, no empty part
+                if (!allow_split || tiles * sp > num_sms || kb_per < 4 || kb_per * (sp - 1) >= kblocks) continue;
+                if (bn == 256 && forced_split <= 1) continue;
+                per_sm = per_k * kb_per;
+                total = per_sm * tiles * sp;
+            } else {
+                per_sm = per_k * kblocks * ((tiles + num_sms - 1) / num_sms);
+                total = per_k * kblocks * tiles;
+            }
+            const double t = std::max(per_sm / kBytesPerUs, total / kL2BytesPerUs) + (sp > 1 ? kSplitUs : 0.0);
+            if (t < 0.95 * best_t || (forced_split > 1 && best.splits == 1)) {
+                best_t = t;
+                best = Choice{cfg, sp};
+            }
+        }
+    }
+    return best;
+}
+
 Plan make_plan(const Operands& op, int64_t M, int64_t N, int64_t K, int num_sms, int pair_clusters, int force,
                bool allow_split = true) {
     Plan pl;
@@ -222,17 +275,23 @@ Plan make_plan(const Operands& op, int64_t M, int64_t N, int64_t K, int num_sms,
         cfg = CFG_PAIR_256;
         tail_halves = false;
     }
+    int ksplit = 1;   // 128-row tiles: CTAs per cluster sharing a tile's K
     if (cfg == CFG_AUTO) {
         if (M <= 64) {
             cfg = CFG_SWAP;
-        } else if (pair_tiles >= pair_clusters) {
+        } else if (4 * pair_tiles >= pair_clusters && g_force_ksplit.load() <= 1) {
+            // the CTA pair, also with a partial first wave: it loads half the
+            // operand bytes per output of a 128 x 128 tile per SM (measured
+            // fastest down to a quarter of the pairs busy, e.g. 2048 x 2048 x
+            // 1024: 12.0 us against 13.9 for the best single-CTA tile)
             cfg = CFG_PAIR_256;
         } else {
-            // widest single-CTA tile that still gives every SM a tile; else the narrowest
-            cfg = CFG_128x64;
-            if (tiles_m * ((N + 255) / 256) >= num_sms) cfg = CFG_128x256;
-            else if (tiles_m * ((N + 127) / 128) >= num_sms) cfg = CFG_128x128;
+            const Choice c = choose_tiles(M, N, K, num_sms, CFG_AUTO, allow_split);
+            cfg = c.cfg;
+            ksplit = c.splits;
         }
+    } else if (cfg == CFG_128x256 || cfg == CFG_128x128 || cfg == CFG_128x64) {
+        ksplit = choose_tiles(M, N, K, num_sms, cfg, allow_split).splits;
     }
     pl.cfg = cfg;
     switch (cfg) {
@@ -262,6 +321,7 @@ Plan make_plan(const Operands& op, int64_t M, int64_t N, int64_t K, int num_sms,
         case CFG_128x128: pl.tile_m = 128; pl.tile_n = 128; pl.stages = kStages128; break;
         default: pl.tile_m = 128; pl.tile_n = 64; pl.stages = kStages64; break;
     }
+    if (cfg != CFG_PAIR_256 && cfg != CFG_SWAP) pl.splits = ksplit;
     if (cfg != CFG_PAIR_256) {
         const int64_t tiles = ((M + pl.tile_m - 1) / pl.tile_m) * ((N + pl.tile_n - 1) / pl.tile_n);
         if (cfg == CFG_SWAP && allow_split && tiles < num_sms) {
@@ -275,7 +335,7 @@ Plan make_plan(const Operands& op, int64_t M, int64_t N, int64_t K, int num_sms,
             }
             pl.splits = static_cast<int>(std::max<int64_t>(1, S));
         }
-        if (pl.splits > 1) {
+        if (pl.splits > 1 && cfg == CFG_SWAP) {
             pl.p_scratch = align256(static_cast<size_t>(tiles) * pl.splits * pl.tile_m * pl.tile_n * 4);
             pl.c_scratch = align256(static_cast<size_t>(tiles) * 4 * 4);
         }
@@ -537,7 +597,7 @@ int launch_repack(uint16_t* dst, const void* src, int64_t rows, int64_t cols, in
 template <int BN, int STAGES>
 int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& prm, int ctas, cudaStream_t s) {
     cudaLaunchConfig_t cfg = launch_config(ctas, SmemPlan<BN, STAGES>::kDynamicBytes, s);
-    LaunchAttrs la(1, pdl_enabled());
+    LaunchAttrs la(prm.splits, pdl_enabled());   // split K: clusters of `splits` CTAs
     la.apply(cfg);
     cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_tc_kernel<BN, STAGES>, ta, tb, prm);
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
@@ -785,6 +845,11 @@ int gemm_f16_set_pdl(int enable) {
 int gemm_f16_force_config(int config) {
     if (config < CFG_AUTO || config > CFG_PAIR_256_WHOLE) return -1;
     return g_force_config.exchange(config);
+}
+
+int gemm_f16_force_ksplit(int splits) {
+    if (splits != 0 && splits != 1 && splits != 2 && splits != 4) return -1;
+    return g_force_ksplit.exchange(splits);
 }
 
 int gemm_f16_plan_ex(const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias, const void* C,

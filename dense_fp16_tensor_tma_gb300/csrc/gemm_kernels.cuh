@@ -340,11 +340,97 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams& p, uint32_t t_ba
     epilogue_rows_act<NCOL, EPI_DYNAMIC, true>(p, t_base, row0, n0, stage);
 }
 
+// ---------------------------------------------------------------- split K across a cluster
+// The S CTAs of a cluster compute one tile, each over its share of K.  CTA o
+// finishes rows o * 128 / S .. of the tile: every CTA pushes its partial rows
+// of that slice straight from tensor memory into CTA o's shared memory
+// (remote 16-byte stores; the operand ring, idle by then in every CTA of the
+// cluster), slot `source rank`, and after a cluster barrier CTA o sums its S
+// slots locally, in rank order.  Row pitch (fp32 words) of the received
+// rows: 4 words of padding put a warp's 16-byte stores on different banks.
+template <int BN>
+struct SplitPlan {
+    static constexpr int kPitch = BN + 4;
+    static constexpr uint32_t kBytes = 128u * kPitch * 4u;
+};
+
+// This warp's 32 accumulator rows (row0 = 32 q ..) x BN/2 columns (col0 ..)
+// from tensor memory to the CTA that finishes them.  All 32 rows go to one
+// CTA (a slice is 128 / S >= 32 rows, and slices start at multiples of 32).
+template <int BN>
+__device__ __forceinline__ void split_push(uint32_t recv, uint32_t t_base, int row0, int col0, int rank, int S) {
+    const int lane = threadIdx.x & 31;
+    const int rows = 128 / S;
+    const int row = row0 + lane;
+    const uint32_t owner = static_cast<uint32_t>(row / rows);
+    const int slot_row = rank * rows + row % rows;
+    const uint32_t dst = mapa_shared(recv + static_cast<uint32_t>(slot_row * SplitPlan<BN>::kPitch + col0) * 4u, owner);
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_base + 32u * c, r);
+        tmem_wait_ld(r);
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+            st_shared_cluster_v4(dst + (32u * c + 4u * v) * 4u, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+    }
+}
+
+// After the cluster barrier that follows every push: this CTA's slice of
+// tile tc (rows rank * 128 / S ..), the S received partials summed in rank
+// order (a fixed order), plus bias, activation, fp16, stored (16 bytes where
+// C allows).  tid runs over the 256 epilogue threads; SS is S.
+template <int BN, int SS>
+__device__ __forceinline__ void split_reduce(const GemmParams& p, uint32_t recv, TileCoord tc, int rank, int tid) {
+    constexpr int kGroups = BN / 8;                 // 8-column groups per row
+    constexpr int kRows = 128 / SS;
+    for (int g = tid; g < kRows * kGroups; g += 256) {
+        const int lr = g / kGroups;
+        const int cc = (g % kGroups) * 8;
+        const int row = tc.m0 + rank * kRows + lr, col = tc.n0 + cc;
+        if (row >= p.M || col >= p.N) continue;
+        float4 part[SS][2];
+#pragma unroll
+        for (int src = 0; src < SS; ++src) {
+            const uint32_t a = recv + static_cast<uint32_t>((src * kRows + lr) * SplitPlan<BN>::kPitch + cc) * 4u;
+            part[src][0] = ld_shared_v4(a);
+            part[src][1] = ld_shared_v4(a + 16u);
+        }
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = 0.0f;
+#pragma unroll
+        for (int src = 0; src < SS; ++src) {
+            x[0] += part[src][0].x; x[1] += part[src][0].y; x[2] += part[src][0].z; x[3] += part[src][0].w;
+            x[4] += part[src][1].x; x[5] += part[src][1].y; x[6] += part[src][1].z; x[7] += part[src][1].w;
+        }
+        if (p.epi != EPI_NONE) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (col + i < p.N) x[i] += __half2float(p.bias[col + i]);
+        }
+        uint32_t h[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 hv = __floats2half2_rn(apply_act(x[2 * i], p.epi), apply_act(x[2 * i + 1], p.epi));
+            h[i] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        __half* dst = p.C + static_cast<int64_t>(row) * p.ldc + col;
+        if (p.vec_store && col + 8 <= p.N) {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
+        } else {
+            for (int i = 0; i < 8 && col + i < p.N; ++i)
+                reinterpret_cast<uint16_t*>(dst)[i] = static_cast<uint16_t>(h[i >> 1] >> (16 * (i & 1)));
+        }
+    }
+}
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
     using SP = SmemPlan<BN, STAGES>;
+    static_assert(SplitPlan<BN>::kBytes <= SP::kStage - SP::kA, "a partial tile fits in the operand ring");
     constexpr int kBoxesB = BN / 64;
     constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators, power of two >= 32
     const bool ta = p.trans_a != 0, tb = p.trans_b != 0;
@@ -403,6 +489,17 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     const int num_tiles = tiles_m * tiles_n;
     const int kblocks = (p.K + kBK - 1) / kBK;
     unsigned int* status = &g_status;
+    // Split K across a cluster (p.splits = S > 1, launched as clusters of S
+    // CTAs, one tile per cluster): CTA `rank` multiplies the tile's K blocks
+    // [kb_lo, kb_hi); the S fp32 partial tiles are summed through distributed
+    // shared memory after the mainloop (split_reduce below).
+    const int S = p.splits;
+    const int rank = S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int t_first = static_cast<int>(blockIdx.x) / S;
+    const int t_stride = S > 1 ? num_tiles : static_cast<int>(gridDim.x);   // split: this cluster's tile only
+    const int kb_per = (kblocks + S - 1) / S;
+    const int kb_lo = rank * kb_per;
+    const int kb_hi = min(kblocks, kb_lo + kb_per);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -412,7 +509,7 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             int issued = 0;
             bool ok = true;
             int skip_kb = p.fault_skip_kb;   // -1 except in fault-injection tests
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            for (int t = t_first; ok && t < num_tiles; t += t_stride) {
                 const TileCoord tc = tile_coord(t, tiles_m, tiles_n, p.group_m, BN);
                 // B boxes entirely right of N are skipped: the stale smem they
                 // leave only feeds accumulator columns >= N, which are never stored.
@@ -422,10 +519,10 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 const int a_boxes = ta ? (tc.m0 + 64 < p.M ? 2 : 1) : 1;
                 const uint32_t bytes = (ta ? static_cast<uint32_t>(a_boxes) * kBBoxBytes : kATileBytes) +
                                        static_cast<uint32_t>(live_boxes) * kBBoxBytes;
-                for (int kb = 0; kb < kblocks; ++kb) {
+                for (int kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.timeout_ns, abort_flag, status,
                                            ROLE_PRODUCER, BAR_EMPTY)) { ok = false; break; }
-                    if (kb == skip_kb) {   // injected fault: this stage's loads never come
+                    if (kb - kb_lo == skip_kb) {   // injected fault: this stage's loads never come
                         ++issued;
                         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                         continue;
@@ -465,12 +562,12 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            for (int t = t_first; ok && t < num_tiles; t += t_stride) {
                 if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag, status,
                                        ROLE_MMA, BAR_ACC_EMPTY)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < kblocks; ++kb) {
+                for (int kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait_bounded(full_bar(stage), phase, p.timeout_ns, abort_flag, status,
                                            ROLE_MMA, BAR_FULL)) { ok = false; break; }
                     tc_fence_after();
@@ -479,7 +576,8 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     const uint64_t b_desc = desc_base(sB + stage * SP::kBTileBytes, !tb);
 #pragma unroll
                     for (int k = 0; k < kBK / kUMMA_K; ++k)
-                        tc_mma_f16(d_tmem, a_desc + k * a_step, b_desc + k * b_step, idesc, (kb | k) != 0 ? 1u : 0u);
+                        tc_mma_f16(d_tmem, a_desc + k * a_step, b_desc + k * b_step, idesc,
+                                   (kb != kb_lo || k != 0) ? 1u : 0u);
                     tc_commit(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -497,11 +595,12 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         const int q = warp & 3;            // TMEM lane quarter this warp may access
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        for (int t = t_first; t < num_tiles; t += t_stride) {
             const TileCoord tc = tile_coord(t, tiles_m, tiles_n, p.group_m, BN);
             const int half = (warp - 2) >> 2;   // which half of the tile's columns
             uint32_t* stage = reinterpret_cast<uint32_t*>(base + SP::kStage + (warp - 2) * kStageWarpBytes);
-            if (p.epi != EPI_NONE) stage_bias(p, stage + kStageBlockWords, tc.n0 + half * (BN / 2), BN / 2);
+            if (p.epi != EPI_NONE && S == 1)
+                stage_bias(p, stage + kStageBlockWords, tc.n0 + half * (BN / 2), BN / 2);
             // tcgen05.ld is warp-collective: the go/no-go decision must be warp-uniform.
             const bool ready = mbar_wait_bounded(accf_bar(acc), acc_phase, p.timeout_ns, abort_flag, status,
                                                  ROLE_EPILOGUE, BAR_ACC_FULL);
@@ -509,6 +608,7 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             tc_fence_after();
             const uint32_t t_base = tmem_base + static_cast<uint32_t>(acc * BN + half * (BN / 2)) +
                                     (static_cast<uint32_t>(32 * q) << 16);
+            if (S > 1) break;   // the partial stays in tensor memory until every CTA's ring is idle
             epilogue_rows<BN / 2>(p, t_base, tc.m0 + 32 * q, tc.n0 + half * (BN / 2), stage);
             tc_fence_before();
             __syncwarp();
@@ -518,6 +618,26 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     }
 
     __syncthreads();
+    if (S > 1) {
+        // every CTA of the cluster is done with its operand ring (its MMAs completed)
+        cluster_sync_all();
+        if (warp >= 2) {
+            const int q = warp & 3, half = (warp - 2) >> 2;
+            tc_fence_after();
+            split_push<BN>(base_s + SP::kA, tmem_base + static_cast<uint32_t>(half * (BN / 2)) +
+                                               (static_cast<uint32_t>(32 * q) << 16),
+                           32 * q, half * (BN / 2), rank, S);
+        }
+        // every partial slice has landed where it is summed; no CTA touches a
+        // peer's shared memory after this
+        cluster_sync_all();
+        if (warp >= 2) {
+            const TileCoord tc = tile_coord(t_first, tiles_m, tiles_n, p.group_m, BN);
+            const int tid = static_cast<int>(threadIdx.x) - 64;
+            if (S == 2) split_reduce<BN, 2>(p, base_s + SP::kA, tc, rank, tid);
+            else split_reduce<BN, 4>(p, base_s + SP::kA, tc, rank, tid);
+        }
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);

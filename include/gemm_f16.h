@@ -178,7 +178,8 @@ int gemm_f16_release_workspace(void);
  * 3 swap-AB kernel for M <= 64), tile_m (256 for the CTA-pair kernel),
  * tile_n,
  * pipeline stages, CTAs launched, repack A (0/1), repack B (0/1), vector
- * stores of C (0/1), split-K parts per tile, scratch bytes, and for the CTA
+ * stores of C (0/1), split-K parts per tile (swap-AB: CTAs sharing a tile's
+ * K through scratch; 128-row tiles: CTAs of a cluster), scratch bytes, and for the CTA
  * pair the number of whole tiles before the half-tile units (-1: no split).
  * Returns a status
  * code like gemm_f16 (argument errors only).  Diagnostic; it has no
@@ -208,6 +209,18 @@ int gemm_f16_plan_ex(const void* A, int64_t lda, const void* B, int64_t ldb, con
  * value.  Process-wide; set it while no other host thread is calling.
  */
 int gemm_f16_force_config(int config);
+
+/*
+ * Diagnostic (no counterpart on the pages): pins whether later calls that
+ * run 128-row tiles split K across a cluster of CTAs (each CTA multiplies a
+ * share of the tile's K blocks; the fp32 partial tiles are summed through
+ * distributed shared memory before the epilogue).  0 automatic (the
+ * default: split where it lowers the operand bytes per SM), 1 never, 2 or 4
+ * that many CTAs per tile wherever the problem allows it (one tile per
+ * cluster, at least 4 K blocks per CTA).  Returns the previous setting, or -1
+ * (nothing changed) for another value.  Process-wide.
+ */
+int gemm_f16_force_ksplit(int splits);
 
 /*
  * Programmatic dependent launch (on by default; the environment variable

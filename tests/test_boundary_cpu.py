@@ -82,9 +82,36 @@ def test_plan_large_square_uses_cta_pairs(g):
 
 
 def test_plan_mid_size_uses_single_cta_tiles(g):
-    # 18 pair tiles < 76 pairs: single-CTA 128-row tiles give more CTAs
+    # 18 pair tiles, under a quarter of the 76 pairs: single-CTA 128 x 128 tiles
+    # with K split across clusters of 2 (72 tiles x 2 = 144 CTAs, 32 K blocks each)
     p = g.gemm_f16_plan(1536, 768, 4096, "none", num_sms=152)
-    assert p["tile_m"] == 128 and p["tile_n"] == 64 and p["ctas"] == 144
+    assert (p["tile_m"], p["tile_n"], p["splits"], p["ctas"], p["scratch"]) == (128, 128, 2, 144, 0)
+    # a quarter of the pairs busy or more: the CTA pair (half tiles for a small last wave)
+    p = g.gemm_f16_plan(2048, 1024, 2048, "none", num_sms=152)
+    assert (p["tile_m"], p["ctas"], p["whole_tiles"]) == (256, 128, 0)
+    p = g.gemm_f16_plan(2048, 2048, 1024, "none", num_sms=152)
+    assert (p["tile_m"], p["ctas"], p["whole_tiles"]) == (256, 128, -1)
+    # long K on few tiles: four CTAs per tile
+    p = g.gemm_f16_plan(768, 768, 8192, "none", num_sms=152)
+    assert (p["tile_n"], p["splits"], p["ctas"]) == (128, 4, 144)
+    # 1024^3: 128 x 64 tiles, no split (the reduction would cost more than it saves)
+    p = g.gemm_f16_plan(1024, 1024, 1024, "none", num_sms=152)
+    assert (p["tile_n"], p["splits"], p["ctas"]) == (64, 1, 128)
+
+
+def test_force_ksplit_overrides_and_restores(g):
+    prev = g.gemm_f16_force_ksplit(4)
+    try:
+        p = g.gemm_f16_plan(1024, 1024, 1024, "none", num_sms=152)
+        assert p["splits"] == 4 and p["ctas"] == 4 * (1024 // 128) * (1024 // p["tile_n"])
+        g.gemm_f16_force_ksplit(1)
+        assert g.gemm_f16_plan(768, 768, 8192, "none", num_sms=152)["splits"] == 1
+        g.gemm_f16_force_ksplit(2)
+        assert g.gemm_f16_plan(256, 256, 256, "none", num_sms=152)["splits"] == 1   # K too short to split
+    finally:
+        g.gemm_f16_force_ksplit(prev)
+    with pytest.raises(ValueError):
+        g.gemm_f16_force_ksplit(3)
 
 
 def test_force_config_overrides_and_restores(g):

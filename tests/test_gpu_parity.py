@@ -396,6 +396,60 @@ def test_short_a_split_k_random_and_deterministic(g, torch_dev, oracle_mod, epi)
     assert_parity(c1, oracle_mod.gemm(A, B, bias if epi != "none" else None, epi), epi)
 
 
+# ---------------------------------------------------------------- K split across a cluster (128-row tiles)
+
+@pytest.fixture
+def ksplit(g):
+    prev_cfg = g.gemm_f16_force_config("auto")
+    prev = g.gemm_f16_force_ksplit(0)
+    yield g
+    g.gemm_f16_force_ksplit(prev)
+    g.gemm_f16_force_config(prev_cfg)
+
+
+@pytest.mark.parametrize("S", [2, 4])
+@pytest.mark.parametrize("cfg", ["128x64", "128x128", "128x256"])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 1024), (300, 200, 1000), (129, 264, 1000)])
+def test_ksplit_integer_exact(ksplit, torch_dev, oracle_mod, S, cfg, M, N, K):
+    g = ksplit
+    g.gemm_f16_force_config(cfg)
+    g.gemm_f16_force_ksplit(S)
+    assert g.gemm_f16_plan(M, N, K, "bias")["splits"] == S
+    rng = np.random.default_rng(M * 7 + N + K + S)
+    A = rng.integers(-1, 2, (M, K)).astype(np.float16)
+    B = rng.integers(-1, 2, (K, N)).astype(np.float16)
+    bias = rng.integers(-8, 9, N).astype(np.float16)
+    got = run(g, torch_dev, A, B, bias, "bias")
+    assert np.array_equal(got.view(np.uint16), oracle_mod.gemm(A, B, bias, "bias").view(np.uint16))
+
+
+@pytest.mark.parametrize("epi", EPIS)
+def test_ksplit_every_epilogue_ragged_and_unaligned_c(ksplit, torch_dev, oracle_mod, epi):
+    # N % 8 != 0: B repacked and C rows not 16-byte aligned (element-wise stores)
+    g = ksplit
+    M, N, K = 333, 1003, 2000
+    g.gemm_f16_force_ksplit(4)
+    plan = g.gemm_f16_plan(M, N, K, epi)
+    assert plan["splits"] == 4 and plan["vec_store"] == 0
+    rng = np.random.default_rng(77)
+    A, B, bias = rand16(rng, (M, K), 0.05), rand16(rng, (K, N), 0.05), rand16(rng, N)
+    got = run(g, torch_dev, A, B, bias if epi != "none" else None, epi)
+    assert_parity(got, oracle_mod.gemm(A, B, bias if epi != "none" else None, epi), epi)
+
+
+def test_ksplit_automatic_choice_matches_oracle(ksplit, torch_dev, oracle_mod):
+    g = ksplit
+    for (M, N, K) in [(1024, 1024, 1024), (1536, 768, 4096), (512, 512, 512)]:
+        plan = g.gemm_f16_plan(M, N, K, "bias_gelu_erf")
+        rng = np.random.default_rng(M + K)
+        A, B, bias = rand16(rng, (M, K), 1 / 32), rand16(rng, (K, N), 1 / 32), rand16(rng, N)
+        got = run(g, torch_dev, A, B, bias, "bias_gelu_erf")
+        rows = np.array([0, 1, M // 2, M - 1])
+        assert_parity(got[rows], oracle_mod.gemm_rows(A, B, bias, "bias_gelu_erf", rows), f"{M}x{N}x{K} {plan}")
+        c2 = run(g, torch_dev, A, B, bias, "bias_gelu_erf")
+        assert np.array_equal(got.view(np.uint16), c2.view(np.uint16))   # a fixed summation order
+
+
 # ---------------------------------------------------------------- the device GELU itself
 
 @pytest.mark.parametrize("epi", ["bias_gelu_erf", "bias_gelu_tanh", "bias_sigmoid"])
