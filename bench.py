@@ -59,6 +59,7 @@ def log(*a):
 
 
 ATTN_SOURCES = ("dense_fp16_tensor_tma_gb300/csrc/attn_kernels.cuh",
+                "dense_fp16_tensor_tma_gb300/csrc/attn2_kernels.cuh",
                 "dense_fp16_tensor_tma_gb300/csrc/attn_f16.cu",
                 "dense_fp16_tensor_tma_gb300/csrc/ptx.cuh")
 
@@ -84,6 +85,16 @@ def workload_config(w, epi, layout="nn"):
         "l2": ("inputs larger than L2 (no flush)" if w.alg_bytes() > L2_BYTES
                else "L2 flushed between steps (256 MiB write)"),
     }
+
+
+def attn_kernel_name(w) -> str:
+    """Non-causal problems with an even number of 128-row query tiles run the
+    two-tile kernel (two query tiles per CTA, softmax of one overlapping the
+    other's MMAs); the rest run the one-tile kernel."""
+    nq = (w.S + 127) // 128
+    if not w.causal and nq % 2 == 0:
+        return f"attn_f16_fwd2_kernel<{w.D}>"
+    return f"attn_f16_fwd_kernel<{w.D}>"
 
 
 def kernel_name(plan):
@@ -694,7 +705,7 @@ def run_attention(args, w):
     roof = {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
             "frac": achieved / tensor_peak, "traffic": traffic,
             "peak_source": f"{src} (bf16 burst x fp16/bf16 ratio {FP16_PER_BF16})",
-            "kernel": f"attn_f16_fwd_kernel<{w.D}>", "avg_launch_ms": avg_launch_ms}
+            "kernel": attn_kernel_name(w), "avg_launch_ms": avg_launch_ms}
 
     # ---- end to end: pinned host Q, K, V in and O out through the C ABI every step
     hq, hk, hv = (torch.from_numpy(x).pin_memory() for x in (Q, K, V))

@@ -1,0 +1,446 @@
+// Attention forward, two query tiles per CTA:  O = softmax(scale * Q K^T) V.
+//
+// The method is that of attn_kernels.cuh ("writing-tilelang-kernels", Flash
+// Attention Forward and its Online Softmax pattern; "TileLang: Write,
+// Autotune, and Ship Fused Tensor-Core Kernels from Python", FlashAttention:
+// the FLOP model): blocks of 128 query rows, key blocks of 128 streamed
+// through shared memory, the running maximum and sum kept online, the S x S
+// scores never written to memory.  What differs is the schedule.  With one
+// query tile per CTA the tensor core waits for each block's softmax and the
+// softmax for each block's MMAs.  Here a CTA takes a unit of two query tiles,
+// A and B, of one head; both use every K and V block loaded (half the K/V
+// traffic per query row), each has one score buffer and one output in
+// tensor memory, and the MMA thread issues
+//
+//     S_A(0) S_B(0) | P_A(0)V S_A(1) | P_B(0)V S_B(1) | P_A(1)V S_A(2) | ...
+//
+// so the tensor core computes one tile's P V and next scores while the other
+// tile's softmax warps work.  A tile's P (fp16) is written over its own
+// scores: each softmax warp puts its 64 keys' P into the first 32 columns of
+// its own 64 score columns, after both its passes have read them, so no warp
+// writes columns another warp still reads; S of the next block overwrites
+// the buffer only after the P V that reads that P, both issued by the MMA
+// thread, whose MMAs the tensor pipe executes in issue order.  Pass 2 reads
+// the scores from tensor memory again rather than keeping all 64 in
+// registers (18 warps leave 112 registers per thread).
+//
+// Roles: warp 0 lane 0 loads each unit's two Q tiles and the K blocks,
+// lane 1 the V blocks (two-slot rings; a slot is free once tile B's MMA of
+// the block two back has completed: B's are issued after A's); warp 1
+// allocates tensor memory and issues every MMA from one thread; warps 2..9
+// run tile A's softmax, warps 10..17 tile B's (two warps per TMEM lane
+// quarter, 64 keys each, as in the one-tile kernel).  Every wait is bounded.
+#pragma once
+
+#include "attn_kernels.cuh"
+
+namespace attn_dev {
+
+constexpr int kAttn2Threads = 576;   // producer, MMA, 2 x 8 softmax warps
+
+template <int D>
+struct Attn2Smem {
+    static constexpr uint32_t kTile = (D / 64) * kBox;     // one 128-row tile of Q, K or V
+    static constexpr uint32_t kQ = 0;                        // Q_A, Q_B
+    static constexpr uint32_t kK = kQ + 2 * kTile;           // 2 slots
+    static constexpr uint32_t kV = kK + 2 * kTile;           // 2 slots
+    static constexpr uint32_t kX = kV + 2 * kTile;           // exchange [tile][2 parity][2 half][128]
+    static constexpr uint32_t kBars = kX + 2 * 2 * 2 * 128 * 4;
+    // q_full, k_full[2], v_full[2], s_full[2 tiles][2], p_full[2], pv_done[2][2], o_free[2],
+    // xch[2 tiles][4 quarters][2 parity], drain
+    static constexpr uint32_t kNumBars = 1 + 2 + 2 + 4 + 2 + 4 + 2 + 16 + 1;
+    static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
+    static constexpr uint32_t kAbort = kTmemSlot + 4;
+    static constexpr uint32_t kEnd = kAbort + 4;
+    static constexpr uint32_t kNeed = kEnd + 1024;           // + alignment of the swizzled tiles
+    // one CTA per SM: it allocates all 512 tensor-memory columns
+    static constexpr uint32_t kOnePerSm = 120 * 1024;
+    static constexpr uint32_t kDynamicBytes = kNeed > kOnePerSm ? kNeed : kOnePerSm;
+    static_assert(kDynamicBytes <= kMaxDynSmem, "shared memory plan too large");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kAttn2Threads, 1)
+attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    static_assert(D == 64 || D == 128, "head dimension 64 or 128");
+    using SM = Attn2Smem<D>;
+    constexpr int kDB = D / 64;
+    constexpr uint32_t kTileBytes = SM::kTile;
+    constexpr uint32_t kIdescS = idesc_f16_f32(kQRows, kKeys, /*b_mn_major=*/false);
+    constexpr uint32_t kIdescO = idesc_f16_f32(kQRows, D, /*b_mn_major=*/true);
+    constexpr uint32_t kSCol = 0;             // S_A at 0, S_B at 128
+    constexpr uint32_t kOCol2 = 256;          // O_A at 256, O_B at 256 + D
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t* base = smem_raw + (base_s - raw_s);
+    const uint32_t sQ = base_s + SM::kQ, sK = base_s + SM::kK, sV = base_s + SM::kV;
+    const uint32_t bars = base_s + SM::kBars;
+    const uint32_t q_full = bars;
+    auto k_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto v_full = [&](int s) { return bars + 8u * (3 + s); };
+    auto s_full = [&](int t, int s) { return bars + 8u * (5 + 2 * t + s); };    // S of tile t, block parity s
+    auto p_full = [&](int t) { return bars + 8u * (9 + t); };                   // P of tile t written
+    auto pv_done = [&](int t, int s) { return bars + 8u * (11 + 2 * t + s); };  // P V of tile t completed
+    auto o_free = [&](int t) { return bars + 8u * (15 + t); };                  // tile t's output read out
+    auto xch_bar = [&](int t, int quarter, int b) { return bars + 8u * (17 + 8 * t + 2 * quarter + b); };
+    const uint32_t drain_bar = bars + 8u * 33;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + SM::kTmemSlot);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + SM::kAbort);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Units: pairs of adjacent query tiles (2k, 2k + 1) of one head, head-major
+    // (the units in flight share a few heads, whose K and V stay in L2).  The
+    // host launches this kernel only for non-causal attention with an even
+    // number of query tiles.
+    const int pairs = p.nq >> 1;
+    const int nblk = (p.S + kKeys - 1) / kKeys;    // key blocks per tile (non-causal: all)
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(k_full(s), 1);
+            mbar_init(v_full(s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            for (int s = 0; s < 2; ++s) {
+                mbar_init(s_full(t, s), 1);
+                mbar_init(pv_done(t, s), 1);
+            }
+            mbar_init(p_full(t), 8);
+            mbar_init(o_free(t), 8);
+            for (int q = 0; q < 4; ++q)
+                for (int b = 0; b < 2; ++b) mbar_init(xch_bar(t, q, b), 64);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    grid_dependency_wait();      // set-up above overlaps the previous kernel
+    grid_launch_dependents();
+    unsigned int* status = &g_attn_status;
+
+    // Key blocks are numbered g = 0, 1, ... over all of this CTA's units
+    // (every unit has nblk): block g uses ring slot g & 1 and phase (g >> 1) & 1
+    // of the per-slot barriers, phase g & 1 of p_full; unit n uses phase n & 1
+    // of q_full and o_free.
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane < 2) {
+            const bool is_k = lane == 0;
+            const CUtensorMap* tm = is_k ? &tmK : &tmV;
+            const uint32_t ring = is_k ? sK : sV;
+            const uint32_t which = is_k ? BAR_K : BAR_V;
+            bool ok = true;
+            int g = 0, nu = 0, issued = 0;
+            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+                const int bh = u / pairs;
+                const int qa = 2 * (u % pairs);
+                if (is_k) {
+                    // both Q tiles are operands of every S of the previous unit: reload
+                    // once the last of those (tile B's, issued last) has completed
+                    if (g > 0 && !mbar_wait_bounded(s_full(1, (g - 1) & 1), ((g - 1) >> 1) & 1, p.timeout_ns,
+                                                    abort_flag, status, ROLE_PRODUCER, BAR_Q))
+                        break;
+                    mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
+                    for (int t = 0; t < 2; ++t)
+                        for (int c = 0; c < kDB; ++c)
+                            tma_load_3d(sQ + t * kTileBytes + c * kBox, &tmQ, q_full, 64 * c, (qa + t) * kQRows, bh);
+                }
+                ++nu;
+                for (int j = 0; j < nblk; ++j) {
+                    const int gb = g + j;
+                    const int s = gb & 1;
+                    // slot s is free once tile B's S (for K) or P V (for V) of block
+                    // gb - 2 completed (tile A's were issued before it)
+                    const uint32_t empty = is_k ? s_full(1, s) : pv_done(1, s);
+                    if (!mbar_wait_bounded(empty, static_cast<uint32_t>((gb >> 1) & 1) ^ 1u, p.timeout_ns,
+                                           abort_flag, status, ROLE_PRODUCER, which)) {
+                        ok = false;
+                        break;
+                    }
+                    if (is_k && gb == p.fault_skip_block) continue;   // injected fault: never loaded
+                    const uint32_t full = is_k ? k_full(s) : v_full(s);
+                    mbar_arrive_expect_tx(full, kTileBytes);
+                    for (int c = 0; c < kDB; ++c)
+                        tma_load_3d(ring + (s * kDB + c) * kBox, tm, full, 64 * c, j * kKeys, bh);
+                    issued = gb + 1;
+                }
+                g += nblk;
+            }
+            // every issued load lands before the CTA can exit (the last Q pair and the
+            // last one or two blocks of each ring; earlier ones were waited for by the
+            // MMA thread before it issued what freed their slots)
+            if (is_k && nu > 0)
+                mbar_wait_bounded(q_full, (nu - 1) & 1, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_Q);
+            for (int gb = max(0, issued - 2); gb < issued; ++gb)
+                mbar_wait_bounded(is_k ? k_full(gb & 1) : v_full(gb & 1), (gb >> 1) & 1, p.timeout_ns, nullptr,
+                                  status, ROLE_DRAIN, which);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint64_t k_desc = smem_desc_sw128(sK, 0, 1024);
+            const uint64_t v_desc = smem_desc_sw128(sV, kBox, 1024);   // MN-major: 64-column boxes kBox apart
+            constexpr uint32_t kSlotUnits = kTileBytes >> 4;
+            // S_t of block gb = Q_t K^T into tile t's score buffer
+            auto issue_s = [&](int t, int gb) -> bool {
+                const int s = gb & 1;
+                if (!mbar_wait_bounded(k_full(s), (gb >> 1) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_K))
+                    return false;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + kSCol + static_cast<uint32_t>(t * kKeys);
+                const uint64_t qd = smem_desc_sw128(sQ + t * kTileBytes, 0, 1024);
+                const uint64_t kd = k_desc + static_cast<uint64_t>(s * kSlotUnits);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint64_t off = static_cast<uint64_t>(((k >> 2) * kBox + (k & 3) * 32) >> 4);
+                    tc_mma_f16(d_tmem, qd + off, kd + off, kIdescS, k != 0 ? 1u : 0u);
+                }
+                tc_commit(s_full(t, s));
+                return true;
+            };
+            // O_t += P_t V of block gb (j: its index in the unit, nu: the unit's index)
+            auto issue_pv = [&](int t, int gb, int j, int nu) -> bool {
+                const int s = gb & 1;
+                if (!mbar_wait_bounded(p_full(t), gb & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_P))
+                    return false;
+                // the unit's first P V overwrites O_t: the previous unit's output must be read out
+                if (j == 0 && nu > 0 &&
+                    !mbar_wait_bounded(o_free(t), (nu - 1) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_P))
+                    return false;
+                if (!mbar_wait_bounded(v_full(s), (gb >> 1) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_V))
+                    return false;
+                tc_fence_after();
+                const uint32_t o_tmem = tmem_base + kOCol2 + static_cast<uint32_t>(t * D);
+                const uint32_t pa = tmem_base + kSCol + static_cast<uint32_t>(t * kKeys);
+                const uint64_t vd = v_desc + static_cast<uint64_t>(s * kSlotUnits);
+#pragma unroll
+                for (int k = 0; k < kKeys / 16; ++k) {
+                    // keys 16k..: softmax half k / 4 wrote its P at columns 64 (k / 4) ..
+                    const uint32_t pcol = static_cast<uint32_t>((k >> 2) * 64 + (k & 3) * 8);
+                    tc_mma_f16_ta(o_tmem, pa + pcol, vd + static_cast<uint64_t>(k * 2048 >> 4), kIdescO,
+                                  (j | k) != 0 ? 1u : 0u);
+                }
+                tc_commit(pv_done(t, s));
+                return true;
+            };
+            bool ok = true;
+            int g = 0, nu = 0;
+            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+                ok = mbar_wait_bounded(q_full, nu & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_Q);
+                if (ok) {
+                    tc_fence_after();
+                    ok = issue_s(0, g) && issue_s(1, g);
+                }
+                for (int j = 0; ok && j < nblk; ++j) {
+                    const int gb = g + j;
+                    for (int t = 0; ok && t < 2; ++t) {
+                        ok = issue_pv(t, gb, j, nu);
+                        // S of the next block overwrites this tile's buffer after the P V
+                        // just issued has read its P: the pipe runs them in order
+                        if (ok && j + 1 < nblk) ok = issue_s(t, gb + 1);
+                    }
+                }
+                g += nblk;
+                ++nu;
+            }
+            tc_commit(drain_bar);
+            mbar_wait_bounded(drain_bar, 0, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_DRAIN);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax + output
+        const int t = (warp - 2) >> 3;               // query tile A (0) or B (1)
+        const int local = (warp - 2) & 7;
+        const int quarter = warp & 3;                // TMEM lanes 32 * quarter ..
+        const int half = local >> 2;                 // keys 64 half .. of each block
+        const int r = 32 * quarter + lane;           // this thread's row of the tile
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
+        const uint32_t s_cols = lane_base + kSCol + static_cast<uint32_t>(t * kKeys + 64 * half);
+        volatile float* xch = reinterpret_cast<volatile float*>(base + SM::kX) + t * (2 * 2 * 128);
+        int x = 0;                                   // exchanges so far
+        auto exchange = [&](float mine, float& theirs) -> bool {
+            const int slot = x & 1, use = x >> 1;
+            ++x;
+            xch[(slot * 2 + half) * 128 + r] = mine;
+            mbar_arrive(xch_bar(t, quarter, slot));
+            const bool got = mbar_wait_bounded(xch_bar(t, quarter, slot), use & 1, p.timeout_ns, abort_flag, status,
+                                               ROLE_SOFTMAX, BAR_X);
+            theirs = xch[(slot * 2 + (1 - half)) * 128 + r];
+            return got;
+        };
+        constexpr int kOCols = D / 2;
+        const uint32_t o_cols = lane_base + kOCol2 + static_cast<uint32_t>(t * D + half * kOCols);
+        const bool pos = p.scale_log2 >= 0.0f;
+        const uint32_t lose = __float_as_uint(pos ? -INFINITY : INFINITY);
+        bool ok = true;
+        int g = 0;
+        for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+            const int bh = u / pairs;
+            const int qt = 2 * (u % pairs) + t;
+            const int q = qt * kQRows + r;                // this thread's query index
+            float m = -INFINITY, l = 0.0f;
+            for (int j = 0; j < nblk; ++j) {
+                const int gb = g + j;
+                const int k0 = j * kKeys;
+                ok = mbar_wait_bounded(s_full(t, gb & 1), (gb >> 1) & 1, p.timeout_ns, abort_flag, status,
+                                       ROLE_SOFTMAX, BAR_S);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+                const bool masked_block = k0 + kKeys > p.S;
+                const int key_lim = p.S - k0 - 64 * half;   // valid: col < key_lim
+                // pass 1: the row's largest scaled score over this warp's 64 keys
+                float bm[4];
+                bm[0] = bm[1] = bm[2] = bm[3] = pos ? -INFINITY : INFINITY;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(s_cols + 32u * c, v);
+                    tmem_wait_ld(v);
+                    if (masked_block) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (32 * c + i >= key_lim) v[i] = lose;
+                    }
+                    if (pos) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2)
+                            bm[(i >> 1) & 3] = max3f(bm[(i >> 1) & 3], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2)
+                            bm[(i >> 1) & 3] = min3f(bm[(i >> 1) & 3], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                    }
+                }
+                float bmax = pos ? fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3]))
+                                 : fminf(fminf(bm[0], bm[1]), fminf(bm[2], bm[3]));
+                bmax *= p.scale_log2;
+                float other = -INFINITY;
+                ok = exchange(bmax, other);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                const float bmax2 = fmaxf(bmax, other);
+                float m_new = m;
+                bool raise = false;
+                if (bmax2 > m + kRaise || m == -INFINITY) {
+                    m_new = fmaxf(m, bmax2);
+                    raise = m != -INFINITY && m_new != m;
+                }
+                // O is rescaled only after P V of this tile's previous block has
+                // completed (a raise needs an earlier block of the unit)
+                if (__any_sync(0xffffffffu, raise)) {
+                    ok = mbar_wait_bounded(pv_done(t, (gb - 1) & 1), ((gb - 1) >> 1) & 1, p.timeout_ns, abort_flag,
+                                           status, ROLE_SOFTMAX, BAR_PV);
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    tc_fence_after();
+                    const float alpha = raise ? fast_exp2(m - m_new) : 1.0f;
+                    l *= alpha;
+#pragma unroll 1
+                    for (int c = 0; c < kOCols / 32; ++c) {
+                        uint32_t w[32];
+                        tmem_ld_32x32b_x32(o_cols + 32u * c, w);
+                        tmem_wait_ld(w);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+                        tmem_st_32x32b_x32(o_cols + 32u * c, w);
+                    }
+                    tmem_wait_st();
+                }
+                m = m_new;
+                // pass 2: the scores again, p = 2^(x * scale_log2 - m) as fp16 over the
+                // first 32 of this warp's own 64 score columns (chunk c's P into columns
+                // 16c.., all of which chunk 0 has read before chunk 1's P is written)
+                const float mm = (m == -INFINITY) ? 0.0f : m;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(s_cols + 32u * c, v);
+                    tmem_wait_ld(v);
+                    if (masked_block) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (32 * c + i >= key_lim) v[i] = lose;
+                    }
+                    uint32_t h[16];
+                    float rs0 = 0.0f, rs1 = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 xs = fma2_bc(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]),
+                                                  p.scale_log2, -mm);
+                        const __half2 hv = __floats2half2_rn(fast_exp2(xs.x), fast_exp2(xs.y));
+                        h[i] = *reinterpret_cast<const uint32_t*>(&hv);
+                        if (i & 1) rs1 = add_f16x2_to_f32(rs1, h[i]);
+                        else rs0 = add_f16x2_to_f32(rs0, h[i]);
+                    }
+                    l += rs0 + rs1;
+                    tmem_st_32x32b_x16(s_cols + 16u * c, h);
+                }
+                tmem_wait_st();
+                tc_fence_before();           // P and the O rescale, if any, before the signal
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full(t));
+            }
+            if (!ok) break;
+            // output: O / l after the unit's last P V of this tile
+            const int gl = g + nblk - 1;
+            ok = mbar_wait_bounded(pv_done(t, gl & 1), (gl >> 1) & 1, p.timeout_ns, abort_flag, status,
+                                   ROLE_SOFTMAX, BAR_PV);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            float l_other = 0.0f;
+            ok = exchange(l, l_other);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            const float inv = 1.0f / (l + l_other);
+            __half* orow = p.O + (static_cast<int64_t>(bh) * p.S + q) * D + half * kOCols;
+#pragma unroll 1
+            for (int c = 0; c < kOCols / 32; ++c) {
+                uint32_t w[32];
+                tmem_ld_32x32b_x32(o_cols + 32u * c, w);
+                tmem_wait_ld(w);
+                uint32_t h[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const __half2 hv = __floats2half2_rn(__uint_as_float(w[2 * i]) * inv,
+                                                         __uint_as_float(w[2 * i + 1]) * inv);
+                    h[i] = *reinterpret_cast<const uint32_t*>(&hv);
+                }
+                if (q < p.S) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+                }
+            }
+            tc_fence_before();           // O read out before the next unit may overwrite it
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free(t));
+            g += nblk;
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace attn_dev

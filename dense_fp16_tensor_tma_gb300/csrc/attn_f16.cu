@@ -13,7 +13,11 @@
 #include <mutex>
 
 #include "attn_f16.h"
-#include "attn_kernels.cuh"
+#include "attn2_kernels.cuh"
+
+#ifndef ATTN_PINGPONG
+#define ATTN_PINGPONG 1   // two query tiles per CTA where the problem allows it
+#endif
 
 namespace {
 
@@ -84,6 +88,12 @@ int init_device(int dev) {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(attn_f16_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  AttnSmem<128>::kDynamicBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attn_f16_fwd2_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Attn2Smem<64>::kDynamicBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attn_f16_fwd2_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Attn2Smem<128>::kDynamicBytes);
     if (e != cudaSuccess) return cuda_fail(e);
     if (const char* env = std::getenv("GEMM_F16_TIMEOUT_MS")) {
         const long ms = std::strtol(env, nullptr, 10);
@@ -118,12 +128,12 @@ int encode_3d(CUtensorMap* m, const void* ptr, int64_t D, int64_t S, int64_t BH)
 
 template <int D>
 cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const AttnParams& prm, int ctas,
-                   cudaStream_t s) {
+                   bool two_tiles, cudaStream_t s) {
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(ctas));
-    cfg.blockDim = dim3(kAttnThreads);
-    cfg.dynamicSmemBytes = AttnSmem<D>::kDynamicBytes;
+    cfg.blockDim = dim3(two_tiles ? kAttn2Threads : kAttnThreads);
+    cfg.dynamicSmemBytes = two_tiles ? Attn2Smem<D>::kDynamicBytes : AttnSmem<D>::kDynamicBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     std::memset(attr, 0, sizeof(attr));
@@ -133,6 +143,7 @@ cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
+    if (two_tiles) return cudaLaunchKernelEx(&cfg, attn_f16_fwd2_kernel<D>, q, k, v, prm);
     return cudaLaunchKernelEx(&cfg, attn_f16_fwd_kernel<D>, q, k, v, prm);
 }
 
@@ -181,12 +192,15 @@ int attn_f16_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B
     // of a head's tiles nq - 1 - k and k (equal cost per unit; with fewer tiles
     // pairing would only halve the parallelism).
     const int sms = g_dev[dev].sms;
+    // Non-causal with an even number of query tiles: two tiles per CTA whose
+    // softmax and MMAs interleave (attn_f16_fwd2_kernel); otherwise one tile.
+    const bool two_tiles = ATTN_PINGPONG && !causal && nq % 2 == 0;
     prm.pair = causal && B * H * nq >= 2 * static_cast<int64_t>(sms) ? 1 : 0;
-    const int64_t units = prm.pair ? B * H * ((nq + 1) / 2) : B * H * nq;
+    const int64_t units = two_tiles ? B * H * (nq / 2) : (prm.pair ? B * H * ((nq + 1) / 2) : B * H * nq);
     prm.units = static_cast<int>(units);
     const int ctas = static_cast<int>(std::min<int64_t>(units, sms));
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-    e = D == 64 ? launch<64>(tq, tk, tv, prm, ctas, s) : launch<128>(tq, tk, tv, prm, ctas, s);
+    e = D == 64 ? launch<64>(tq, tk, tv, prm, ctas, two_tiles, s) : launch<128>(tq, tk, tv, prm, ctas, two_tiles, s);
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
 

@@ -74,7 +74,8 @@ def test_attention_prefill_sampled_rows(g, torch_dev, oracle_mod, name):
 # the middle tile alone; ragged S makes every head's last tile partial.
 
 @pytest.mark.parametrize("B,H,S,D,causal", [(4, 32, 1300, 128, True), (4, 32, 1300, 64, True),
-                                            (8, 16, 1000, 128, False), (8, 24, 700, 64, True)])
+                                            (8, 16, 1000, 128, False), (8, 24, 700, 64, True),
+                                            (4, 32, 4096, 64, True), (4, 32, 4096, 64, False)])
 def test_attention_many_tiles_per_cta_sampled_rows(g, torch_dev, oracle_mod, B, H, S, D, causal):
     rng = np.random.default_rng(S + D + 7 * causal)
     Q, K, V = qkv(rng, (B, H, S, D))
@@ -93,7 +94,7 @@ def test_attention_many_tiles_per_cta_sampled_rows(g, torch_dev, oracle_mod, B, 
 
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("S", [1, 7, 127, 128, 129, 300, 513])
+@pytest.mark.parametrize("S", [1, 7, 127, 128, 129, 256, 300, 513, 1000])
 def test_attention_shape_sweep(g, torch_dev, oracle_mod, D, causal, S):
     rng = np.random.default_rng(S * 3 + D + causal)
     Q, K, V = qkv(rng, (2, 3, S, D))
