@@ -17,17 +17,20 @@
 // so the tensor core computes one tile's P V and next scores while the other
 // tile's softmax warps work.  A tile's P (fp16) is written over its own
 // scores: each softmax warp puts its 64 keys' P into the first 32 columns of
-// its own 64 score columns, after both its passes have read them, so no warp
-// writes columns another warp still reads; S of the next block overwrites
-// the buffer only after the P V that reads that P, both issued by the MMA
-// thread, whose MMAs the tensor pipe executes in issue order.  Pass 2 reads
-// the scores from tensor memory again rather than keeping all 64 in
-// registers (18 warps leave 112 registers per thread).
+// its own 64 score columns, after it has read them, so no warp writes
+// columns another warp still reads; S of the next block overwrites the
+// buffer only after the P V that reads that P, both issued by the MMA warp,
+// whose MMAs the tensor pipe executes in issue order.  A softmax warp reads
+// its scores once, computing the block maximum and, speculatively, P under
+// the running maximum it already has, held as packed fp16 in registers; only
+// when the exchanged block maximum raises the running maximum (always in a
+// unit's first block, rarely later) does it read the scores again, which stay
+// in tensor memory until P is stored.
 //
 // Roles: warp 0 lane 0 loads each unit's two Q tiles and the K blocks,
 // lane 1 the V blocks (two-slot rings; a slot is free once tile B's MMA of
 // the block two back has completed: B's are issued after A's); warp 1
-// allocates tensor memory and issues every MMA from one thread; warps 2..9
+// allocates tensor memory and issues every MMA (see a2_mma_ss); warps 2..9
 // run tile A's softmax, warps 10..17 tile B's (two warps per TMEM lane
 // quarter, 64 keys each, as in the one-tile kernel).  Every wait is bounded.
 #pragma once
@@ -37,6 +40,39 @@
 namespace attn_dev {
 
 constexpr int kAttn2Threads = 576;   // producer, MMA, 2 x 8 softmax warps
+
+// MMA issue from a converged warp: the whole MMA warp runs the issue loop, so
+// descriptors and addresses are warp-uniform values, and elect.sync picks the
+// one lane that issues each tcgen05 instruction.  (Issuing from lane 0 alone
+// cost about 60 cycles per MMA here, more than the 32 to 64 cycles an MMA of
+// this kernel keeps the tensor core busy.)
+__device__ __forceinline__ void a2_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void a2_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void a2_commit(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+        ::"r"(bar) : "memory");
+}
 
 template <int D>
 struct Attn2Smem {
@@ -197,7 +233,7 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        {
             const uint64_t k_desc = smem_desc_sw128(sK, 0, 1024);
             const uint64_t v_desc = smem_desc_sw128(sV, kBox, 1024);   // MN-major: 64-column boxes kBox apart
             constexpr uint32_t kSlotUnits = kTileBytes >> 4;
@@ -213,9 +249,9 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint64_t off = static_cast<uint64_t>(((k >> 2) * kBox + (k & 3) * 32) >> 4);
-                    tc_mma_f16(d_tmem, qd + off, kd + off, kIdescS, k != 0 ? 1u : 0u);
+                    a2_mma_ss(d_tmem, qd + off, kd + off, kIdescS, k != 0 ? 1u : 0u);
                 }
-                tc_commit(s_full(t, s));
+                a2_commit(s_full(t, s));
                 return true;
             };
             // O_t += P_t V of block gb (j: its index in the unit, nu: the unit's index)
@@ -237,10 +273,10 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 for (int k = 0; k < kKeys / 16; ++k) {
                     // keys 16k..: softmax half k / 4 wrote its P at columns 64 (k / 4) ..
                     const uint32_t pcol = static_cast<uint32_t>((k >> 2) * 64 + (k & 3) * 8);
-                    tc_mma_f16_ta(o_tmem, pa + pcol, vd + static_cast<uint64_t>(k * 2048 >> 4), kIdescO,
+                    a2_mma_ts(o_tmem, pa + pcol, vd + static_cast<uint64_t>(k * 2048 >> 4), kIdescO,
                                   (j | k) != 0 ? 1u : 0u);
                 }
-                tc_commit(pv_done(t, s));
+                a2_commit(pv_done(t, s));
                 return true;
             };
             bool ok = true;
@@ -263,7 +299,7 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 g += nblk;
                 ++nu;
             }
-            tc_commit(drain_bar);
+            a2_commit(drain_bar);
             mbar_wait_bounded(drain_bar, 0, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_DRAIN);
         }
         __syncwarp();
@@ -278,15 +314,22 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         const uint32_t s_cols = lane_base + kSCol + static_cast<uint32_t>(t * kKeys + 64 * half);
         volatile float* xch = reinterpret_cast<volatile float*>(base + SM::kX) + t * (2 * 2 * 128);
         int x = 0;                                   // exchanges so far
-        auto exchange = [&](float mine, float& theirs) -> bool {
+        // exchange with the warp holding the row's other 64 keys: post, then collect
+        auto xpost = [&](float mine) {
+            xch[((x & 1) * 2 + half) * 128 + r] = mine;
+            mbar_arrive(xch_bar(t, quarter, x & 1));
+        };
+        auto xcollect = [&](float& theirs) -> bool {
             const int slot = x & 1, use = x >> 1;
             ++x;
-            xch[(slot * 2 + half) * 128 + r] = mine;
-            mbar_arrive(xch_bar(t, quarter, slot));
             const bool got = mbar_wait_bounded(xch_bar(t, quarter, slot), use & 1, p.timeout_ns, abort_flag, status,
                                                ROLE_SOFTMAX, BAR_X);
             theirs = xch[(slot * 2 + (1 - half)) * 128 + r];
             return got;
+        };
+        auto exchange = [&](float mine, float& theirs) -> bool {
+            xpost(mine);
+            return xcollect(theirs);
         };
         constexpr int kOCols = D / 2;
         const uint32_t o_cols = lane_base + kOCol2 + static_cast<uint32_t>(t * D + half * kOCols);
@@ -308,11 +351,16 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 tc_fence_after();
                 const bool masked_block = k0 + kKeys > p.S;
                 const int key_lim = p.S - k0 - 64 * half;   // valid: col < key_lim
-                // pass 1: the row's largest scaled score over this warp's 64 keys
+                // one pass over the warp's 64 scores, 32 at a time: the block maximum
+                // and, speculatively, P = 2^(x * scale_log2 - m) with the current
+                // maximum m, packed fp16 in registers.  The scores stay in tensor
+                // memory until P is stored, so a raise of m (always in a unit's first
+                // block, rare once m has settled) recomputes P from them.
                 float bm[4];
                 bm[0] = bm[1] = bm[2] = bm[3] = pos ? -INFINITY : INFINITY;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                uint32_t h[32];
+                float rs0 = 0.0f, rs1 = 0.0f;
+                auto p_chunk = [&](int c, float mx, bool track) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(s_cols + 32u * c, v);
                     tmem_wait_ld(v);
@@ -321,16 +369,30 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                         for (int i = 0; i < 32; ++i)
                             if (32 * c + i >= key_lim) v[i] = lose;
                     }
-                    if (pos) {
+                    if (track) {
+                        if (pos) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 2)
-                            bm[(i >> 1) & 3] = max3f(bm[(i >> 1) & 3], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-                    } else {
+                            for (int i = 0; i < 32; i += 2)
+                                bm[(i >> 1) & 3] = max3f(bm[(i >> 1) & 3], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                        } else {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 2)
-                            bm[(i >> 1) & 3] = min3f(bm[(i >> 1) & 3], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                            for (int i = 0; i < 32; i += 2)
+                                bm[(i >> 1) & 3] = min3f(bm[(i >> 1) & 3], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                        }
                     }
-                }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 xs = fma2_bc(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]),
+                                                  p.scale_log2, -mx);
+                        const __half2 hv = __floats2half2_rn(fast_exp2(xs.x), fast_exp2(xs.y));
+                        h[16 * c + i] = *reinterpret_cast<const uint32_t*>(&hv);
+                        if (i & 1) rs1 = add_f16x2_to_f32(rs1, h[16 * c + i]);
+                        else rs0 = add_f16x2_to_f32(rs0, h[16 * c + i]);
+                    }
+                };
+                const float m_spec = (m == -INFINITY) ? 0.0f : m;
+                p_chunk(0, m_spec, true);
+                p_chunk(1, m_spec, true);
                 float bmax = pos ? fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3]))
                                  : fminf(fminf(bm[0], bm[1]), fminf(bm[2], bm[3]));
                 bmax *= p.scale_log2;
@@ -344,8 +406,6 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     m_new = fmaxf(m, bmax2);
                     raise = m != -INFINITY && m_new != m;
                 }
-                // O is rescaled only after P V of this tile's previous block has
-                // completed (a raise needs an earlier block of the unit)
                 if (__any_sync(0xffffffffu, raise)) {
                     ok = mbar_wait_bounded(pv_done(t, (gb - 1) & 1), ((gb - 1) >> 1) & 1, p.timeout_ns, abort_flag,
                                            status, ROLE_SOFTMAX, BAR_PV);
@@ -362,37 +422,18 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                         for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
                         tmem_st_32x32b_x32(o_cols + 32u * c, w);
                     }
-                    tmem_wait_st();
+                }
+                if (__any_sync(0xffffffffu, m_new != m)) {
+                    rs0 = 0.0f;
+                    rs1 = 0.0f;
+                    const float mm = (m_new == -INFINITY) ? 0.0f : m_new;
+                    p_chunk(0, mm, false);
+                    p_chunk(1, mm, false);
                 }
                 m = m_new;
-                // pass 2: the scores again, p = 2^(x * scale_log2 - m) as fp16 over the
-                // first 32 of this warp's own 64 score columns (chunk c's P into columns
-                // 16c.., all of which chunk 0 has read before chunk 1's P is written)
-                const float mm = (m == -INFINITY) ? 0.0f : m;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(s_cols + 32u * c, v);
-                    tmem_wait_ld(v);
-                    if (masked_block) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (32 * c + i >= key_lim) v[i] = lose;
-                    }
-                    uint32_t h[16];
-                    float rs0 = 0.0f, rs1 = 0.0f;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float2 xs = fma2_bc(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]),
-                                                  p.scale_log2, -mm);
-                        const __half2 hv = __floats2half2_rn(fast_exp2(xs.x), fast_exp2(xs.y));
-                        h[i] = *reinterpret_cast<const uint32_t*>(&hv);
-                        if (i & 1) rs1 = add_f16x2_to_f32(rs1, h[i]);
-                        else rs0 = add_f16x2_to_f32(rs0, h[i]);
-                    }
-                    l += rs0 + rs1;
-                    tmem_st_32x32b_x16(s_cols + 16u * c, h);
-                }
+                l += rs0 + rs1;
+                // P over the first 32 of the warp's 64 score columns
+                tmem_st_32x32b_x32(s_cols, h);
                 tmem_wait_st();
                 tc_fence_before();           // P and the O rescale, if any, before the signal
                 __syncwarp();
