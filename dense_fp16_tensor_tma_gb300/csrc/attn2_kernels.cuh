@@ -30,7 +30,8 @@
 // Roles: warp 0 lane 0 loads each unit's two Q tiles and the K blocks,
 // lane 1 the V blocks (two-slot rings; a slot is free once tile B's MMA of
 // the block two back has completed: B's are issued after A's); warp 1
-// allocates tensor memory and issues every MMA (see a2_mma_ss); warps 2..9
+// allocates tensor memory and issues every MMA (the whole warp runs the
+// loop, one lane elected per instruction: tc_mma_f16); warps 2..9
 // run tile A's softmax, warps 10..17 tile B's (two warps per TMEM lane
 // quarter, 64 keys each, as in the one-tile kernel).  Every wait is bounded.
 #pragma once
@@ -40,39 +41,6 @@
 namespace attn_dev {
 
 constexpr int kAttn2Threads = 576;   // producer, MMA, 2 x 8 softmax warps
-
-// MMA issue from a converged warp: the whole MMA warp runs the issue loop, so
-// descriptors and addresses are warp-uniform values, and elect.sync picks the
-// one lane that issues each tcgen05 instruction.  (Issuing from lane 0 alone
-// cost about 60 cycles per MMA here, more than the 32 to 64 cycles an MMA of
-// this kernel keeps the tensor core busy.)
-__device__ __forceinline__ void a2_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
-        "elect.sync r|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void a2_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
-        "elect.sync r|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void a2_commit(uint32_t bar) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
-        "elect.sync r|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
-        ::"r"(bar) : "memory");
-}
 
 template <int D>
 struct Attn2Smem {
@@ -249,9 +217,9 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint64_t off = static_cast<uint64_t>(((k >> 2) * kBox + (k & 3) * 32) >> 4);
-                    a2_mma_ss(d_tmem, qd + off, kd + off, kIdescS, k != 0 ? 1u : 0u);
+                    tc_mma_f16(d_tmem, qd + off, kd + off, kIdescS, k != 0 ? 1u : 0u);
                 }
-                a2_commit(s_full(t, s));
+                tc_commit(s_full(t, s));
                 return true;
             };
             // O_t += P_t V of block gb (j: its index in the unit, nu: the unit's index)
@@ -273,10 +241,10 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 for (int k = 0; k < kKeys / 16; ++k) {
                     // keys 16k..: softmax half k / 4 wrote its P at columns 64 (k / 4) ..
                     const uint32_t pcol = static_cast<uint32_t>((k >> 2) * 64 + (k & 3) * 8);
-                    a2_mma_ts(o_tmem, pa + pcol, vd + static_cast<uint64_t>(k * 2048 >> 4), kIdescO,
+                    tc_mma_f16_ta(o_tmem, pa + pcol, vd + static_cast<uint64_t>(k * 2048 >> 4), kIdescO,
                                   (j | k) != 0 ? 1u : 0u);
                 }
-                a2_commit(pv_done(t, s));
+                tc_commit(pv_done(t, s));
                 return true;
             };
             bool ok = true;
@@ -299,7 +267,7 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 g += nblk;
                 ++nu;
             }
-            a2_commit(drain_bar);
+            tc_commit(drain_bar);
             mbar_wait_bounded(drain_bar, 0, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_DRAIN);
         }
         __syncwarp();

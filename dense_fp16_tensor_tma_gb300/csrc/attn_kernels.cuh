@@ -142,13 +142,15 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
         : "memory");
 }
 // D[tmem] (+)= A[tmem] * B[smem desc]: A (M x 16, fp16) held in tensor memory,
-// one row per lane, two fp16 per 32-bit column.
+// one row per lane, two fp16 per 32-bit column (issued from a converged warp,
+// as tc_mma_f16).
 __device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                               uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
         ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -368,10 +370,11 @@ attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            // One thread keeps the tensor pipe fed only if the work between two
-            // MMAs (64 cycles each at N = 128) stays short: the descriptors are
-            // built once, and each MMA adds a constant to the start-address
+        {
+            // The whole warp runs this loop and one elected lane issues each MMA
+            // (tc_mma_f16); the tensor pipe stays fed only if the work between
+            // two MMAs (64 cycles each at N = 128) stays short: the descriptors
+            // are built once, and each MMA adds a constant to the start-address
             // field (in 16-byte units; every shared address is below 2^18, so
             // the 14-bit field never carries).
             const uint64_t q_desc = smem_desc_sw128(sQ, 0, 1024);

@@ -554,7 +554,7 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        {
             const uint32_t idesc = idesc_f16_f32(kBM, BN, /*b_mn_major=*/!tb, /*a_mn_major=*/ta);
             const uint64_t a_step = desc_step(ta), b_step = desc_step(!tb);
             int stage = 0;
@@ -564,12 +564,12 @@ gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             bool ok = true;
             for (int t = t_first; ok && t < num_tiles; t += t_stride) {
                 if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag, status,
-                                       ROLE_MMA, BAR_ACC_EMPTY)) { ok = false; break; }
+                                            ROLE_MMA, BAR_ACC_EMPTY)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait_bounded(full_bar(stage), phase, p.timeout_ns, abort_flag, status,
-                                           ROLE_MMA, BAR_FULL)) { ok = false; break; }
+                                                ROLE_MMA, BAR_FULL)) { ok = false; break; }
                     tc_fence_after();
                     // A K-major unless stored K x M; B MN-major unless stored N x K
                     const uint64_t a_desc = desc_base(sA + stage * kATileBytes, ta);

@@ -284,7 +284,7 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (CTA 0 only)
-        if (leader && lane == 0) {
+        if (leader) {
             const uint32_t idesc_whole = idesc_f16_f32(PM, BN, /*b_mn_major=*/!tb, /*a_mn_major=*/ta);
             const uint32_t idesc_half = idesc_f16_f32(PM, BN / 2, !tb, ta);   // 256 x 128 units
             const uint64_t a_step = desc_step(ta), b_step = desc_step(!tb);
@@ -297,13 +297,13 @@ gemm_f16_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             PairUnit un;
             while (ok && it.next(un)) {
                 if (!mbar_wait_cluster_bounded(acce_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag, status,
-                                               ROLE_MMA, BAR_ACC_EMPTY)) { ok = false; break; }
+                                                    ROLE_MMA, BAR_ACC_EMPTY)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 const uint32_t idesc = un.half < 0 ? idesc_whole : idesc_half;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_cluster_bounded(full_bar(stage), phase, p.timeout_ns, abort_flag, status,
-                                                   ROLE_MMA, BAR_FULL)) { ok = false; break; }
+                                                        ROLE_MMA, BAR_FULL)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < KSUB; ++ks) {
@@ -593,7 +593,7 @@ __device__ __forceinline__ void pair_gemm(const Src& src, const GemmParams cp) {
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (CTA 0 only)
-        if (leader && lane == 0) {
+        if (leader) {
             const uint32_t idesc_whole = idesc_f16_f32(PM, BN, /*b_mn_major=*/!tb, /*a_mn_major=*/ta);
             const uint32_t idesc_half = idesc_f16_f32(PM, BN / 2, !tb, ta);   // 256 x 128 units
             const uint64_t a_step = desc_step(ta), b_step = desc_step(!tb);
@@ -607,13 +607,13 @@ __device__ __forceinline__ void pair_gemm(const Src& src, const GemmParams cp) {
             while (ok && it.next(un)) {
                 const int kblocks = kblocks_of(it.params(un.prob));
                 if (!mbar_wait_cluster_bounded(acce_bar(acc), acc_phase ^ 1u, cp.timeout_ns, abort_flag, status,
-                                               ROLE_MMA, BAR_ACC_EMPTY)) { ok = false; break; }
+                                                    ROLE_MMA, BAR_ACC_EMPTY)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 const uint32_t idesc = un.half < 0 ? idesc_whole : idesc_half;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_cluster_bounded(full_bar(stage), phase, cp.timeout_ns, abort_flag, status,
-                                                   ROLE_MMA, BAR_FULL)) { ok = false; break; }
+                                                        ROLE_MMA, BAR_FULL)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < KSUB; ++ks) {

@@ -173,7 +173,7 @@ gemm_f16_swap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        {
             // MMA A = B^T (MN-major unless B is stored N x K), MMA B = A^T (K-major unless A is stored K x M)
             const uint32_t idesc = idesc_f16_f32(TN, MT, /*b_mn_major=*/ta, /*a_mn_major=*/!tb);
             const uint64_t a_step = desc_step(!tb), b_step = desc_step(ta);
@@ -184,13 +184,13 @@ gemm_f16_swap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             bool ok = true;
             for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
                 if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, p.timeout_ns, abort_flag, status,
-                                       ROLE_MMA, BAR_ACC_EMPTY)) { ok = false; break; }
+                                            ROLE_MMA, BAR_ACC_EMPTY)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MT);
                 const int kb0 = kb_begin(u);
                 for (int kb = kb0; kb < kb_end(u); ++kb) {
                     if (!mbar_wait_bounded(full_bar(stage), phase, p.timeout_ns, abort_flag, status,
-                                           ROLE_MMA, BAR_FULL)) { ok = false; break; }
+                                                ROLE_MMA, BAR_FULL)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t st = base_s + stage * SP::kStage;
                     const uint64_t a_desc = desc_base(st, !tb);

@@ -73,6 +73,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return true;
 }
 
+
 // ----------------------------------------------------------------- TMA
 // Programmatic dependent launch.  A kernel launched with programmatic stream
 // serialization may start while the previous kernel in the stream is still
@@ -117,21 +118,38 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// MMA issue from a converged warp.  Every lane of the warp calls these with
+// the same operands (which keeps descriptors and addresses in warp-uniform
+// registers) and elect.sync picks one of the calling lanes to issue the
+// instruction.  Issued from one lane inside divergent code, each MMA cost
+// about 60 cycles of issue, more than a 32- or 64-cycle MMA keeps the tensor
+// core busy.  The MMA warp never splits: it enters its loop converged, and
+// each bounded wait (mbar_wait_bounded) has every lane run the same
+// instructions on the same data (one barrier word, one %globaltimer read,
+// one abort flag), so every lane's answer, and branch, is the same.  (A vote
+// after each wait cost about 2 % of attention throughput; electing among
+// __activemask() lanes cost far more.)
+
 // D[tmem] (+)= A[smem desc] * B[smem desc], f16 inputs, kind::f16, one CTA.
 __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                            uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 op issued so far by this thread has completed.
+// Arrive once on `bar` when every tcgen05 op issued so far by the issuing
+// lane has completed (converged warp, one lane issues).
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                 ::"r"(bar) : "memory");
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+        ::"r"(bar) : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets its lane's 32 columns.
@@ -272,6 +290,7 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t
     return true;
 }
 
+
 // TMA load whose completion may be signalled on the peer CTA's mbarrier
 // (`bar` is a cluster address); destination is this CTA's shared memory.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar,
@@ -306,21 +325,25 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
 
 // D (+)= A * B over the CTA pair: M = 256 (128 rows from each CTA's shared
 // memory), B split by columns between the two CTAs; issued by one thread of
-// the even CTA.
+// the even CTA (from its converged MMA warp, as tc_mma_f16).
 __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                 uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // Arrive once on the mbarrier at offset `bar` in every CTA of `cta_mask`
-// when all pair MMAs issued so far by this thread have completed.
+// when all pair MMAs issued so far by the issuing lane have completed.
 __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-                 ::"r"(bar), "h"(cta_mask) : "memory");
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}"
+        ::"r"(bar), "h"(cta_mask) : "memory");
 }
 
 }  // namespace gemm_f16_dev
