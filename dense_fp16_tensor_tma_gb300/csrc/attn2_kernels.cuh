@@ -97,12 +97,22 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Units: pairs of adjacent query tiles (2k, 2k + 1) of one head, head-major
-    // (the units in flight share a few heads, whose K and V stay in L2).  The
-    // host launches this kernel only for non-causal attention with an even
-    // number of query tiles.
-    const int pairs = p.nq >> 1;
+    // Units: query tiles numbered head-major (tile = head * nq + index), unit u
+    // below pair_units holding tiles 2u and 2u + 1 (adjacent tiles of one head:
+    // the host launches this kernel only for non-causal attention with an even
+    // number of query tiles), each later unit one tile (A alone).  The host
+    // makes the one-tile units the last of at most one per CTA, when the tiles
+    // do not divide evenly into pairs per CTA: 13 pairs and a single rather
+    // than 14 pairs on some CTAs.  Units in flight share a few heads, whose K
+    // and V stay in L2.
     const int nblk = (p.S + kKeys - 1) / kKeys;    // key blocks per tile (non-causal: all)
+    auto unit_tiles = [&](int u, int& bh, int& qa) -> bool {   // true: two tiles
+        const bool two = u < p.pair_units;
+        const int tile = two ? 2 * u : 2 * p.pair_units + (u - p.pair_units);
+        bh = tile / p.nq;
+        qa = tile - bh * p.nq;
+        return two;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -154,27 +164,35 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const uint32_t which = is_k ? BAR_K : BAR_V;
             bool ok = true;
             int g = 0, nu = 0, issued = 0;
+            int pair_end = 0;            // key blocks of the two-tile units so far (they come first)
+            bool prev_two = true;
             for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-                const int bh = u / pairs;
-                const int qa = 2 * (u % pairs);
+                int bh, qa;
+                const bool two = unit_tiles(u, bh, qa);
                 if (is_k) {
-                    // both Q tiles are operands of every S of the previous unit: reload
-                    // once the last of those (tile B's, issued last) has completed
-                    if (g > 0 && !mbar_wait_bounded(s_full(1, (g - 1) & 1), ((g - 1) >> 1) & 1, p.timeout_ns,
-                                                    abort_flag, status, ROLE_PRODUCER, BAR_Q))
+                    // the Q tiles are operands of every S of the previous unit: reload
+                    // once the last of those (tile B's, issued last, or tile A's in a
+                    // one-tile unit) has completed
+                    if (g > 0 && !mbar_wait_bounded(s_full(prev_two ? 1 : 0, (g - 1) & 1), ((g - 1) >> 1) & 1,
+                                                    p.timeout_ns, abort_flag, status, ROLE_PRODUCER, BAR_Q))
                         break;
-                    mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
-                    for (int t = 0; t < 2; ++t)
+                    const int ntiles = two ? 2 : 1;
+                    mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(ntiles) * kTileBytes);
+                    for (int t = 0; t < ntiles; ++t)
                         for (int c = 0; c < kDB; ++c)
                             tma_load_3d(sQ + t * kTileBytes + c * kBox, &tmQ, q_full, 64 * c, (qa + t) * kQRows, bh);
                 }
                 ++nu;
+                if (two) pair_end = g + nblk;
+                prev_two = two;
                 for (int j = 0; j < nblk; ++j) {
                     const int gb = g + j;
                     const int s = gb & 1;
-                    // slot s is free once tile B's S (for K) or P V (for V) of block
-                    // gb - 2 completed (tile A's were issued before it)
-                    const uint32_t empty = is_k ? s_full(1, s) : pv_done(1, s);
+                    // slot s is free once the last MMA reading block gb - 2 completed:
+                    // tile B's S (for K) or P V (for V) in a two-tile unit (tile A's
+                    // were issued before it), tile A's in a one-tile unit
+                    const int tb = gb - 2 < pair_end ? 1 : 0;
+                    const uint32_t empty = is_k ? s_full(tb, s) : pv_done(tb, s);
                     if (!mbar_wait_bounded(empty, static_cast<uint32_t>((gb >> 1) & 1) ^ 1u, p.timeout_ns,
                                            abort_flag, status, ROLE_PRODUCER, which)) {
                         ok = false;
@@ -248,17 +266,19 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 return true;
             };
             bool ok = true;
-            int g = 0, nu = 0;
+            int g = 0, nu = 0, nb = 0;   // nb: two-tile units so far
             for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+                int bh, qa;
+                const int ntiles = unit_tiles(u, bh, qa) ? 2 : 1;
                 ok = mbar_wait_bounded(q_full, nu & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_Q);
                 if (ok) {
                     tc_fence_after();
-                    ok = issue_s(0, g) && issue_s(1, g);
+                    ok = issue_s(0, g) && (ntiles == 1 || issue_s(1, g));
                 }
                 for (int j = 0; ok && j < nblk; ++j) {
                     const int gb = g + j;
-                    for (int t = 0; ok && t < 2; ++t) {
-                        ok = issue_pv(t, gb, j, nu);
+                    for (int t = 0; ok && t < ntiles; ++t) {
+                        ok = issue_pv(t, gb, j, t == 0 ? nu : nb);   // the tile's earlier units
                         // S of the next block overwrites this tile's buffer after the P V
                         // just issued has read its P: the pipe runs them in order
                         if (ok && j + 1 < nblk) ok = issue_s(t, gb + 1);
@@ -266,6 +286,7 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 }
                 g += nblk;
                 ++nu;
+                nb += ntiles - 1;
             }
             tc_commit(drain_bar);
             mbar_wait_bounded(drain_bar, 0, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_DRAIN);
@@ -306,9 +327,9 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         bool ok = true;
         int g = 0;
         for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-            const int bh = u / pairs;
-            const int qt = 2 * (u % pairs) + t;
-            const int q = qt * kQRows + r;                // this thread's query index
+            int bh, qa;
+            if (!unit_tiles(u, bh, qa) && t == 1) break;  // tile B's warps sit out the one-tile units
+            const int q = (qa + t) * kQRows + r;          // this thread's query index
             float m = -INFINITY, l = 0.0f;
             for (int j = 0; j < nblk; ++j) {
                 const int gb = g + j;
@@ -374,24 +395,25 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     m_new = fmaxf(m, bmax2);
                     raise = m != -INFINITY && m_new != m;
                 }
-                if (__any_sync(0xffffffffu, raise)) {
-                    ok = mbar_wait_bounded(pv_done(t, (gb - 1) & 1), ((gb - 1) >> 1) & 1, p.timeout_ns, abort_flag,
-                                           status, ROLE_SOFTMAX, BAR_PV);
-                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                    tc_fence_after();
-                    const float alpha = raise ? fast_exp2(m - m_new) : 1.0f;
-                    l *= alpha;
-#pragma unroll 1
-                    for (int c = 0; c < kOCols / 32; ++c) {
-                        uint32_t w[32];
-                        tmem_ld_32x32b_x32(o_cols + 32u * c, w);
-                        tmem_wait_ld(w);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
-                        tmem_st_32x32b_x32(o_cols + 32u * c, w);
-                    }
-                }
+                // a raise implies a new maximum: one vote covers the common case
                 if (__any_sync(0xffffffffu, m_new != m)) {
+                    if (__any_sync(0xffffffffu, raise)) {
+                        ok = mbar_wait_bounded(pv_done(t, (gb - 1) & 1), ((gb - 1) >> 1) & 1, p.timeout_ns,
+                                               abort_flag, status, ROLE_SOFTMAX, BAR_PV);
+                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                        tc_fence_after();
+                        const float alpha = raise ? fast_exp2(m - m_new) : 1.0f;
+                        l *= alpha;
+#pragma unroll 1
+                        for (int c = 0; c < kOCols / 32; ++c) {
+                            uint32_t w[32];
+                            tmem_ld_32x32b_x32(o_cols + 32u * c, w);
+                            tmem_wait_ld(w);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+                            tmem_st_32x32b_x32(o_cols + 32u * c, w);
+                        }
+                    }
                     rs0 = 0.0f;
                     rs1 = 0.0f;
                     const float mm = (m_new == -INFINITY) ? 0.0f : m_new;
@@ -413,33 +435,39 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             ok = mbar_wait_bounded(pv_done(t, gl & 1), (gl >> 1) & 1, p.timeout_ns, abort_flag, status,
                                    ROLE_SOFTMAX, BAR_PV);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            // this warp's O columns into registers first, then O's tensor memory is
+            // released to the next unit's first P V; the row sums are exchanged and
+            // the output normalised and stored after that
+            tc_fence_after();
+            uint32_t w0[32], w1[32];
+            tmem_ld_32x32b_x32(o_cols, w0);
+            if constexpr (kOCols == 64) tmem_ld_32x32b_x32(o_cols + 32u, w1);
+            tmem_wait_ld(w0);
+            if constexpr (kOCols == 64) tmem_wait_ld(w1);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free(t));
             float l_other = 0.0f;
             ok = exchange(l, l_other);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            tc_fence_after();
             const float inv = 1.0f / (l + l_other);
-            __half* orow = p.O + (static_cast<int64_t>(bh) * p.S + q) * D + half * kOCols;
-#pragma unroll 1
-            for (int c = 0; c < kOCols / 32; ++c) {
-                uint32_t w[32];
-                tmem_ld_32x32b_x32(o_cols + 32u * c, w);
-                tmem_wait_ld(w);
-                uint32_t h[16];
+            if (q < p.S) {
+                __half* orow = p.O + (static_cast<int64_t>(bh) * p.S + q) * D + half * kOCols;
+                auto store32 = [&](const uint32_t (&w)[32], int c) {
+                    uint32_t h[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const __half2 hv = __floats2half2_rn(__uint_as_float(w[2 * i]) * inv,
-                                                         __uint_as_float(w[2 * i + 1]) * inv);
-                    h[i] = *reinterpret_cast<const uint32_t*>(&hv);
-                }
-                if (q < p.S) {
+                    for (int i = 0; i < 16; ++i) {
+                        const __half2 hv = __floats2half2_rn(__uint_as_float(w[2 * i]) * inv,
+                                                             __uint_as_float(w[2 * i + 1]) * inv);
+                        h[i] = *reinterpret_cast<const uint32_t*>(&hv);
+                    }
                     uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-                }
+                };
+                store32(w0, 0);
+                if constexpr (kOCols == 64) store32(w1, 1);
             }
-            tc_fence_before();           // O read out before the next unit may overwrite it
-            __syncwarp();
-            if (lane == 0) mbar_arrive(o_free(t));
             g += nblk;
         }
         tc_fence_before();

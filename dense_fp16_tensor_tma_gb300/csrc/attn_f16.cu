@@ -196,7 +196,20 @@ int attn_f16_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B
     // softmax and MMAs interleave (attn_f16_fwd2_kernel); otherwise one tile.
     const bool two_tiles = ATTN_PINGPONG && !causal && nq % 2 == 0;
     prm.pair = causal && B * H * nq >= 2 * static_cast<int64_t>(sms) ? 1 : 0;
-    const int64_t units = two_tiles ? B * H * (nq / 2) : (prm.pair ? B * H * ((nq + 1) / 2) : B * H * nq);
+    int64_t units = prm.pair ? B * H * ((nq + 1) / 2) : B * H * nq;
+    prm.pair_units = 0;
+    if (two_tiles) {
+        // Two tiles per unit; when the tiles left over after k full rounds of
+        // pairs (k per CTA) fit one per CTA, they run as one-tile units (k pairs
+        // and at most one single per CTA instead of k + 1 pairs on some CTAs);
+        // otherwise every unit is a pair.
+        const int64_t tiles = B * H * nq;
+        const int64_t k = tiles / (2 * static_cast<int64_t>(sms));
+        const int64_t rest = tiles - 2 * k * sms;
+        const int64_t pairs = rest <= sms ? k * sms : tiles / 2;
+        prm.pair_units = static_cast<int>(pairs);
+        units = pairs + (tiles - 2 * pairs);
+    }
     prm.units = static_cast<int>(units);
     const int ctas = static_cast<int>(std::min<int64_t>(units, sms));
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);

@@ -74,6 +74,7 @@ struct AttnParams {
     int causal;
     int units;          // work units: query tiles, or pairs of query tiles
     int pair;           // causal, with at least two tiles per SM: a unit is a pair of tiles
+    int pair_units;     // two-tile kernel: units below this hold two tiles, the rest one
     float scale_log2;   // softmax scale * log2(e)
     uint64_t timeout_ns;
     // Fault injection for the tests of the bounded waits (-1 in every normal

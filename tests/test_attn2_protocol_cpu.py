@@ -1,7 +1,9 @@
 """A model of the two-tile attention kernel's barrier protocol, run on the CPU.
 
 attn_f16_fwd2_kernel (csrc/attn2_kernels.cuh) gives each CTA units of two
-query tiles (A and B) of one head that share the K and V rings.  Each tile
+query tiles (A and B) of one head that share the K and V rings, and, when
+the tiles do not divide evenly into two per CTA, a last unit of one tile
+(A alone) on some CTAs.  Each tile
 has one score buffer in tensor memory, which its P overwrites, and its own
 output; the MMA thread issues S_A, S_B, then per key block P_A V, the next
 S_A, P_B V, the next S_B, so one tile's MMAs run while the other tile's
@@ -15,7 +17,10 @@ S writing a tile's score buffer while a softmax warp may still read it, and
 no load overwriting a K or V ring slot that a queued or running MMA still
 reads.  That P V of block j has read its P (in the score buffer) before S of
 block j + 1 writes there rests on the tensor pipe executing one thread's
-MMAs in issue order, which the model assumes as the kernel does.
+MMAs in issue order, which the model assumes as the kernel does.  Across
+the switch from two-tile to one-tile units a ring slot's previous block may
+have been read last by tile B's MMA; the producer then frees it on tile B's
+barrier, later ones on tile A's.
 """
 import random
 
@@ -46,10 +51,16 @@ class Barrier:
 
 
 def run_protocol2(units, seed, nsoft=2, defect=None):
-    """`units`: key blocks of each unit this CTA walks.  nsoft softmax warps per
-    tile stand for the eight.  `defect` plants a mistake: "early_s" (the MMA
-    thread issues the next S of a tile before that tile's P is written) or
-    "k_slot_a" (the producer frees a K slot on tile A's S instead of B's)."""
+    """`units`: the units this CTA walks, each a number of key blocks (a unit
+    of two tiles) or a pair (key blocks, False) for a unit of tile A alone; the
+    one-tile units come last.  nsoft softmax warps per tile stand for the eight.
+    `defect` plants a mistake: "early_s" (the MMA thread issues the next S of a
+    tile before that tile's P is written), "k_slot_a" (the producer frees a K
+    slot on tile A's S instead of B's), or "single_slot_a" (once the one-tile
+    units begin, every slot is freed on tile A's barriers, also a slot whose
+    previous block belonged to a two-tile unit)."""
+    units = [(u, True) if isinstance(u, int) else u for u in units]
+    assert all(a[1] or not b[1] for a, b in zip(units, units[1:])), "one-tile units come last"
     rnd = random.Random(seed)
     q_full, drain = Barrier("q_full", 1), Barrier("drain", 1)
     k_full = [Barrier(f"k_full{i}", 1) for i in range(2)]
@@ -68,20 +79,30 @@ def run_protocol2(units, seed, nsoft=2, defect=None):
 
     def producer(is_k):
         g = 0
-        for u, nblk in enumerate(units):
+        pair_end = 0                  # blocks of the two-tile units so far (they come first)
+        prev_pair = True
+        for u, (nblk, pair) in enumerate(units):
             if is_k:
-                if g > 0:   # the previous unit's last S (S_B, issued after S_A) has read both Q tiles
-                    yield wait(s_full["B"][(g - 1) & 1], (g - 1) >> 1, "producer Q")
-                q_full.arrive(tx=2)
-                tma.append(q_full)
-                tma.append(q_full)
+                if g > 0:   # the previous unit's last S (S_B, issued after S_A, or S_A alone) has read Q
+                    yield wait(s_full["B" if prev_pair else "A"][(g - 1) & 1], (g - 1) >> 1, "producer Q")
+                ntiles = 2 if pair else 1
+                q_full.arrive(tx=ntiles)
+                for _ in range(ntiles):
+                    tma.append(q_full)
+            if pair:
+                pair_end = g + nblk       # blocks below this one belong to two-tile units
             for j in range(nblk):
                 gb = g + j
                 s = gb & 1
                 # the slot's previous block gb - 2 is done: both S (K) or both P V (V);
-                # tile B's are issued after tile A's, so B's commits cover both
-                t = "A" if (is_k and defect == "k_slot_a") else "B"
-                yield wait(s_full[t][s] if is_k else pv_done["B"][s], (gb >> 1) - 1, "producer slot")
+                # tile B's are issued after tile A's, so B's commits cover both; a
+                # block of a one-tile unit was read by tile A alone
+                t = "B" if gb - 2 < pair_end else "A"
+                if is_k and defect == "k_slot_a":
+                    t = "A"
+                if defect == "single_slot_a" and not pair:
+                    t = "A"
+                yield wait(s_full[t][s] if is_k else pv_done[t][s], (gb >> 1) - 1, "producer slot")
                 # the load overwrites ring slot s: no MMA reading its previous block may remain
                 for op, _, gq in pipe:
                     assert not (gq is not None and gq & 1 == s and gq < gb and op == ("s" if is_k else "pv")), \
@@ -90,6 +111,7 @@ def run_protocol2(units, seed, nsoft=2, defect=None):
                 full.arrive(tx=1)
                 tma.append(full)
             g += nblk
+            prev_pair = pair
 
     def mma():
         g = 0
@@ -99,32 +121,38 @@ def run_protocol2(units, seed, nsoft=2, defect=None):
             # no earlier P V may still read the P in it (the pipe is in order)
             pipe.append(("s", t, gb))
 
-        for u, nblk in enumerate(units):
+        nb = 0                        # two-tile units so far
+        for u, (nblk, pair) in enumerate(units):
+            tiles = "AB" if pair else "A"
             yield wait(q_full, u, "mma Q")
             yield wait(k_full[g & 1], g >> 1, "mma K")
-            issue_s("A", g)
-            issue_s("B", g)
+            for t in tiles:
+                issue_s(t, g)
             for j in range(nblk):
                 gb = g + j
-                for t in "AB":
+                for t in tiles:
                     if defect == "early_s" and t == "A" and j + 1 < nblk:
                         yield wait(k_full[(gb + 1) & 1], (gb + 1) >> 1, "mma K")
                         issue_s("A", gb + 1)
                     yield wait(p_full[t], gb, f"mma P{t}")
-                    if j == 0 and u > 0:
-                        yield wait(o_free[t], u - 1, f"mma O{t} free")
+                    done = u if t == "A" else nb      # this tile's earlier units
+                    if j == 0 and done > 0:
+                        yield wait(o_free[t], done - 1, f"mma O{t} free")
                     yield wait(v_full[gb & 1], gb >> 1, "mma V")
                     pipe.append(("pv", t, gb))
                     if j + 1 < nblk and not (defect == "early_s" and t == "A"):
                         yield wait(k_full[(gb + 1) & 1], (gb + 1) >> 1, "mma K")
                         issue_s(t, gb + 1)
             g += nblk
+            nb += pair
         pipe.append(("drain", None, None))
         yield wait(drain, 0, "mma drain")
 
     def softmax(t):
         g = x = 0
-        for u, nblk in enumerate(units):
+        for u, (nblk, pair) in enumerate(units):
+            if t == "B" and not pair:
+                break                                # tile B's warps sit out the one-tile units
             for j in range(nblk):
                 gb = g + j
                 yield wait(s_full[t][gb & 1], gb >> 1, f"softmax{t} S")
@@ -191,7 +219,9 @@ def run_protocol2(units, seed, nsoft=2, defect=None):
     raise AssertionError("no progress bound reached")
 
 
-CASES = [[1], [2], [5], [2, 2], [8, 8, 8], [32, 32], [3, 1, 4], [1, 1, 1, 1]]
+CASES = [[1], [2], [5], [2, 2], [8, 8, 8], [32, 32], [3, 1, 4], [1, 1, 1, 1],
+         [(1, False)], [(5, False)], [(3, False), (3, False)], [4, (4, False)], [8, 8, (8, False)],
+         [1, (1, False)], [2, 2, (2, False), (2, False)], [32, 32, (32, False)]]
 
 
 @pytest.mark.parametrize("units", CASES)
@@ -205,3 +235,11 @@ def test_attention2_model_catches_planted_defects(defect):
     with pytest.raises(AssertionError):
         for seed in range(60):
             run_protocol2([4, 4, 3], seed, defect=defect)
+
+
+def test_attention2_model_catches_slot_freed_on_the_wrong_tile_at_the_switch():
+    # the last two-tile unit's blocks are read last by tile B: freeing their
+    # slots on tile A's barriers lets a load overwrite K or V under S_B / P_B V
+    with pytest.raises(AssertionError):
+        for seed in range(200):
+            run_protocol2([4, 4, (3, False)], seed, defect="single_slot_a")

@@ -75,7 +75,8 @@ def test_attention_prefill_sampled_rows(g, torch_dev, oracle_mod, name):
 
 @pytest.mark.parametrize("B,H,S,D,causal", [(4, 32, 1300, 128, True), (4, 32, 1300, 64, True),
                                             (8, 16, 1000, 128, False), (8, 24, 700, 64, True),
-                                            (4, 32, 4096, 64, True), (4, 32, 4096, 64, False)])
+                                            (4, 32, 4096, 64, True), (4, 32, 4096, 64, False),
+                                            (16, 16, 1024, 128, False)])
 def test_attention_many_tiles_per_cta_sampled_rows(g, torch_dev, oracle_mod, B, H, S, D, causal):
     rng = np.random.default_rng(S + D + 7 * causal)
     Q, K, V = qkv(rng, (B, H, S, D))
