@@ -267,7 +267,6 @@ Plan make_plan(const Operands& op, int64_t M, int64_t N, int64_t K, int num_sms,
     pl.a_scratch = pl.pack_a ? align256(static_cast<size_t>(op.a_rows(M, K) * pl.lda_packed * 2)) : 0;
     pl.b_scratch = pl.pack_b ? align256(static_cast<size_t>(op.b_rows(N, K) * pl.ldb_packed * 2)) : 0;
     pl.vec_store = aligned(op.C, 16) && op.ldc % 8 == 0;
-    const int64_t tiles_m = (M + 127) / 128;
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     int cfg = force;
     bool tail_halves = true;
