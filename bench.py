@@ -87,12 +87,14 @@ def workload_config(w, epi, layout="nn"):
     }
 
 
-def attn_kernel_name(w) -> str:
-    """Non-causal problems with an even number of 128-row query tiles run the
-    two-tile kernel (two query tiles per CTA, softmax of one overlapping the
-    other's MMAs); the rest run the one-tile kernel."""
+def attn_kernel_name(w, sms: int) -> str:
+    """Problems with an even number of 128-row query tiles run the two-tile
+    kernel (two query tiles per CTA, softmax of one overlapping the other's
+    MMAs), causal ones from 16 tiles per head and with a step of two tile
+    pairs per SM; the rest run the one-tile kernel."""
     nq = (w.S + 127) // 128
-    if not w.causal and nq % 2 == 0:
+    steps = w.B * w.H * ((nq // 2 + 1) // 2)
+    if nq % 2 == 0 and (not w.causal or (nq >= 16 and steps >= sms)):
         return f"attn_f16_fwd2_kernel<{w.D}>"
     return f"attn_f16_fwd_kernel<{w.D}>"
 
@@ -705,7 +707,7 @@ def run_attention(args, w):
     roof = {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
             "frac": achieved / tensor_peak, "traffic": traffic,
             "peak_source": f"{src} (bf16 burst x fp16/bf16 ratio {FP16_PER_BF16})",
-            "kernel": attn_kernel_name(w), "avg_launch_ms": avg_launch_ms}
+            "kernel": attn_kernel_name(w, props.multi_processor_count), "avg_launch_ms": avg_launch_ms}
 
     # ---- end to end: pinned host Q, K, V in and O out through the C ABI every step
     hq, hk, hv = (torch.from_numpy(x).pin_memory() for x in (Q, K, V))

@@ -97,21 +97,54 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Units: query tiles numbered head-major (tile = head * nq + index), unit u
-    // below pair_units holding tiles 2u and 2u + 1 (adjacent tiles of one head:
-    // the host launches this kernel only for non-causal attention with an even
-    // number of query tiles), each later unit one tile (A alone).  The host
-    // makes the one-tile units the last of at most one per CTA, when the tiles
-    // do not divide evenly into pairs per CTA: 13 pairs and a single rather
-    // than 14 pairs on some CTAs.  Units in flight share a few heads, whose K
-    // and V stay in L2.
-    const int nblk = (p.S + kKeys - 1) / kKeys;    // key blocks per tile (non-causal: all)
-    auto unit_tiles = [&](int u, int& bh, int& qa) -> bool {   // true: two tiles
-        const bool two = u < p.pair_units;
-        const int tile = two ? 2 * u : 2 * p.pair_units + (u - p.pair_units);
-        bh = tile / p.nq;
-        qa = tile - bh * p.nq;
-        return two;
+    // Units.  Non-causal: query tiles numbered head-major (tile = head * nq +
+    // index), unit u below pair_units holding tiles 2u and 2u + 1 (adjacent tiles
+    // of one head: the host launches this kernel only for an even number of
+    // query tiles), each later unit one tile (A alone); the host makes the
+    // one-tile units the last of at most one per CTA, when the tiles do not
+    // divide evenly into pairs per CTA (13 pairs and a single rather than 14
+    // pairs on some CTAs).  Causal: units of tiles 2k and 2k + 1 of one head;
+    // tile A reads key blocks 0..2k, tile B 0..2k + 1 (every block the unit
+    // loads); a CTA takes them two at a time from one head, pair np - 1 - m and
+    // then pair m (np pairs per head, the middle pair of an odd np alone), so
+    // every such step costs the same.  Units in flight share a few heads, whose
+    // K and V stay in L2.
+    const int nblk = (p.S + kKeys - 1) / kKeys;    // key blocks per tile, non-causal
+    const int np = p.nq >> 1;                       // pairs per head
+    const int sp = (np + 1) >> 1;                   // causal steps per head
+    struct UnitWalk {
+        int U, i;                                   // step (unit) index, unit within a causal step
+        // the next unit: head, tile A's index, key blocks of A and of B (0: A alone)
+        __device__ bool next(const AttnParams& p, int nblk, int np, int sp, int& bh, int& qa, int& na, int& nb) {
+            if (U >= p.units) return false;
+            if (!p.causal) {
+                const int u = U;
+                U += static_cast<int>(gridDim.x);
+                const bool two = u < p.pair_units;
+                const int tile = two ? 2 * u : 2 * p.pair_units + (u - p.pair_units);
+                bh = tile / p.nq;
+                qa = tile - bh * p.nq;
+                na = nblk;
+                nb = two ? nblk : 0;
+                return true;
+            }
+            bh = U / sp;
+            const int m = U - bh * sp;
+            int k;
+            if (i == 0) {
+                k = np - 1 - m;
+                if (k == m) U += static_cast<int>(gridDim.x);   // the middle pair: a step of one unit
+                else i = 1;
+            } else {
+                k = m;
+                i = 0;
+                U += static_cast<int>(gridDim.x);
+            }
+            qa = 2 * k;
+            na = 2 * k + 1;
+            nb = 2 * k + 2;
+            return true;
+        }
     };
 
     if (threadIdx.x == 0) {
@@ -151,10 +184,12 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     grid_launch_dependents();
     unsigned int* status = &g_attn_status;
 
-    // Key blocks are numbered g = 0, 1, ... over all of this CTA's units
-    // (every unit has nblk): block g uses ring slot g & 1 and phase (g >> 1) & 1
-    // of the per-slot barriers, phase g & 1 of p_full; unit n uses phase n & 1
-    // of q_full and o_free.
+    // Key blocks loaded are numbered g = 0, 1, ... over all of this CTA's units:
+    // block g uses ring slot g & 1 and phase (g >> 1) & 1 of the ring barriers.
+    // Each tile numbers the blocks it reads (A fewer than loaded in causal
+    // units): its block b uses phase (b >> 1) & 1 of its s_full(t, b & 1) and
+    // pv_done(t, b & 1), phase b & 1 of p_full(t).  Unit n uses phase n & 1 of
+    // q_full, each tile's own unit count the phases of its o_free.
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane < 2) {
@@ -166,9 +201,11 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             int g = 0, nu = 0, issued = 0;
             int pair_end = 0;            // key blocks of the two-tile units so far (they come first)
             bool prev_two = true;
-            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-                int bh, qa;
-                const bool two = unit_tiles(u, bh, qa);
+            UnitWalk walk{static_cast<int>(blockIdx.x), 0};
+            int bh, qa, na, nb;
+            while (ok && walk.next(p, nblk, np, sp, bh, qa, na, nb)) {
+                const bool two = nb > 0;
+                const int nr = two ? nb : na;   // blocks loaded: all of B's (B reads every one), or A's
                 if (is_k) {
                     // the Q tiles are operands of every S of the previous unit: reload
                     // once the last of those (tile B's, issued last, or tile A's in a
@@ -183,14 +220,17 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                             tma_load_3d(sQ + t * kTileBytes + c * kBox, &tmQ, q_full, 64 * c, (qa + t) * kQRows, bh);
                 }
                 ++nu;
-                if (two) pair_end = g + nblk;
+                if (two) pair_end = g + nr;
                 prev_two = two;
-                for (int j = 0; j < nblk; ++j) {
+                for (int j = 0; j < nr; ++j) {
                     const int gb = g + j;
                     const int s = gb & 1;
                     // slot s is free once the last MMA reading block gb - 2 completed:
                     // tile B's S (for K) or P V (for V) in a two-tile unit (tile A's
-                    // were issued before it), tile A's in a one-tile unit
+                    // were issued before it), tile A's in a one-tile unit.  Tile B
+                    // reads every block of a two-tile unit and the two-tile units come
+                    // first, so B's count of that block is gb - 2; one-tile units
+                    // come only without causal masking, where A reads every block.
                     const int tb = gb - 2 < pair_end ? 1 : 0;
                     const uint32_t empty = is_k ? s_full(tb, s) : pv_done(tb, s);
                     if (!mbar_wait_bounded(empty, static_cast<uint32_t>((gb >> 1) & 1) ^ 1u, p.timeout_ns,
@@ -205,7 +245,7 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                         tma_load_3d(ring + (s * kDB + c) * kBox, tm, full, 64 * c, j * kKeys, bh);
                     issued = gb + 1;
                 }
-                g += nblk;
+                g += nr;
             }
             // every issued load lands before the CTA can exit (the last Q pair and the
             // last one or two blocks of each ring; earlier ones were waited for by the
@@ -223,10 +263,10 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const uint64_t k_desc = smem_desc_sw128(sK, 0, 1024);
             const uint64_t v_desc = smem_desc_sw128(sV, kBox, 1024);   // MN-major: 64-column boxes kBox apart
             constexpr uint32_t kSlotUnits = kTileBytes >> 4;
-            // S_t of block gb = Q_t K^T into tile t's score buffer
-            auto issue_s = [&](int t, int gb) -> bool {
-                const int s = gb & 1;
-                if (!mbar_wait_bounded(k_full(s), (gb >> 1) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_K))
+            // S_t of loaded block rb (tile t's block tb) = Q_t K^T into t's score buffer
+            auto issue_s = [&](int t, int rb, int tb) -> bool {
+                const int s = rb & 1;
+                if (!mbar_wait_bounded(k_full(s), (rb >> 1) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_K))
                     return false;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + kSCol + static_cast<uint32_t>(t * kKeys);
@@ -237,19 +277,20 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     const uint64_t off = static_cast<uint64_t>(((k >> 2) * kBox + (k & 3) * 32) >> 4);
                     tc_mma_f16(d_tmem, qd + off, kd + off, kIdescS, k != 0 ? 1u : 0u);
                 }
-                tc_commit(s_full(t, s));
+                tc_commit(s_full(t, tb & 1));
                 return true;
             };
-            // O_t += P_t V of block gb (j: its index in the unit, nu: the unit's index)
-            auto issue_pv = [&](int t, int gb, int j, int nu) -> bool {
-                const int s = gb & 1;
-                if (!mbar_wait_bounded(p_full(t), gb & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_P))
+            // O_t += P_t V of loaded block rb (tile t's block tb; j: its index in the
+            // unit, nu: the tile's earlier units)
+            auto issue_pv = [&](int t, int rb, int tb, int j, int nu) -> bool {
+                const int s = rb & 1;
+                if (!mbar_wait_bounded(p_full(t), tb & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_P))
                     return false;
                 // the unit's first P V overwrites O_t: the previous unit's output must be read out
                 if (j == 0 && nu > 0 &&
                     !mbar_wait_bounded(o_free(t), (nu - 1) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_P))
                     return false;
-                if (!mbar_wait_bounded(v_full(s), (gb >> 1) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_V))
+                if (!mbar_wait_bounded(v_full(s), (rb >> 1) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_V))
                     return false;
                 tc_fence_after();
                 const uint32_t o_tmem = tmem_base + kOCol2 + static_cast<uint32_t>(t * D);
@@ -262,31 +303,39 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     tc_mma_f16_ta(o_tmem, pa + pcol, vd + static_cast<uint64_t>(k * 2048 >> 4), kIdescO,
                                   (j | k) != 0 ? 1u : 0u);
                 }
-                tc_commit(pv_done(t, s));
+                tc_commit(pv_done(t, tb & 1));
                 return true;
             };
             bool ok = true;
-            int g = 0, nu = 0, nb = 0;   // nb: two-tile units so far
-            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-                int bh, qa;
-                const int ntiles = unit_tiles(u, bh, qa) ? 2 : 1;
+            int g = 0, gA = 0, gB = 0;   // blocks loaded; blocks tile A and tile B read
+            int nu = 0, nuB = 0;         // units; units with a tile B
+            UnitWalk walk{static_cast<int>(blockIdx.x), 0};
+            int bh, qa, na, nb;
+            while (ok && walk.next(p, nblk, np, sp, bh, qa, na, nb)) {
+                const int nr = nb > 0 ? nb : na;
                 ok = mbar_wait_bounded(q_full, nu & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_Q);
                 if (ok) {
                     tc_fence_after();
-                    ok = issue_s(0, g) && (ntiles == 1 || issue_s(1, g));
+                    ok = issue_s(0, g, gA) && (nb == 0 || issue_s(1, g, gB));
                 }
-                for (int j = 0; ok && j < nblk; ++j) {
-                    const int gb = g + j;
-                    for (int t = 0; ok && t < ntiles; ++t) {
-                        ok = issue_pv(t, gb, j, t == 0 ? nu : nb);   // the tile's earlier units
-                        // S of the next block overwrites this tile's buffer after the P V
-                        // just issued has read its P: the pipe runs them in order
-                        if (ok && j + 1 < nblk) ok = issue_s(t, gb + 1);
+                // S of a tile's next block overwrites its buffer after the P V just
+                // issued has read its P: the pipe runs them in order.  In a causal
+                // unit tile A has no last block.
+                for (int j = 0; ok && j < nr; ++j) {
+                    if (j < na) {
+                        ok = issue_pv(0, g + j, gA + j, j, nu);
+                        if (ok && j + 1 < na) ok = issue_s(0, g + j + 1, gA + j + 1);
+                    }
+                    if (ok && j < nb) {
+                        ok = issue_pv(1, g + j, gB + j, j, nuB);
+                        if (ok && j + 1 < nb) ok = issue_s(1, g + j + 1, gB + j + 1);
                     }
                 }
-                g += nblk;
+                g += nr;
+                gA += na;
+                gB += nb;
                 ++nu;
-                nb += ntiles - 1;
+                nuB += nb > 0 ? 1 : 0;
             }
             tc_commit(drain_bar);
             mbar_wait_bounded(drain_bar, 0, p.timeout_ns, nullptr, status, ROLE_DRAIN, BAR_DRAIN);
@@ -326,20 +375,24 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         const uint32_t lose = __float_as_uint(pos ? -INFINITY : INFINITY);
         bool ok = true;
         int g = 0;
-        for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-            int bh, qa;
-            if (!unit_tiles(u, bh, qa) && t == 1) break;  // tile B's warps sit out the one-tile units
+        UnitWalk walk{static_cast<int>(blockIdx.x), 0};
+        int bh, qa, na, nb;
+        while (ok && walk.next(p, nblk, np, sp, bh, qa, na, nb)) {
+            if (t == 1 && nb == 0) break;                 // tile B's warps sit out the one-tile units
+            const int n = t == 0 ? na : nb;               // key blocks this tile reads
             const int q = (qa + t) * kQRows + r;          // this thread's query index
+            // keys past S, and (causal) keys after this query, do not count
+            const int key_end = p.causal ? min(p.S, q + 1) : p.S;
             float m = -INFINITY, l = 0.0f;
-            for (int j = 0; j < nblk; ++j) {
-                const int gb = g + j;
+            for (int j = 0; j < n; ++j) {
+                const int gb = g + j;                     // this tile's block number
                 const int k0 = j * kKeys;
                 ok = mbar_wait_bounded(s_full(t, gb & 1), (gb >> 1) & 1, p.timeout_ns, abort_flag, status,
                                        ROLE_SOFTMAX, BAR_S);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
-                const bool masked_block = k0 + kKeys > p.S;
-                const int key_lim = p.S - k0 - 64 * half;   // valid: col < key_lim
+                const bool masked_block = k0 + kKeys > p.S || (p.causal && j == n - 1);
+                const int key_lim = key_end - k0 - 64 * half;   // valid: col < key_lim
                 // one pass over the warp's 64 scores, 32 at a time: the block maximum
                 // and, speculatively, P = 2^(x * scale_log2 - m) with the current
                 // maximum m, packed fp16 in registers.  The scores stay in tensor
@@ -431,7 +484,7 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             }
             if (!ok) break;
             // output: O / l after the unit's last P V of this tile
-            const int gl = g + nblk - 1;
+            const int gl = g + n - 1;
             ok = mbar_wait_bounded(pv_done(t, gl & 1), (gl >> 1) & 1, p.timeout_ns, abort_flag, status,
                                    ROLE_SOFTMAX, BAR_PV);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -468,7 +521,7 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 store32(w0, 0);
                 if constexpr (kOCols == 64) store32(w1, 1);
             }
-            g += nblk;
+            g += n;
         }
         tc_fence_before();
     }

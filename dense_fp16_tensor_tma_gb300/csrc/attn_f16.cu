@@ -18,6 +18,9 @@
 #ifndef ATTN_PINGPONG
 #define ATTN_PINGPONG 1   // two query tiles per CTA where the problem allows it
 #endif
+#ifndef ATTN_CAUSAL_PAIRS
+#define ATTN_CAUSAL_PAIRS 1   // causal problems too
+#endif
 
 namespace {
 
@@ -192,13 +195,24 @@ int attn_f16_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B
     // of a head's tiles nq - 1 - k and k (equal cost per unit; with fewer tiles
     // pairing would only halve the parallelism).
     const int sms = g_dev[dev].sms;
-    // Non-causal with an even number of query tiles: two tiles per CTA whose
-    // softmax and MMAs interleave (attn_f16_fwd2_kernel); otherwise one tile.
-    const bool two_tiles = ATTN_PINGPONG && !causal && nq % 2 == 0;
-    prm.pair = causal && B * H * nq >= 2 * static_cast<int64_t>(sms) ? 1 : 0;
+    // An even number of query tiles: two tiles per CTA whose softmax and MMAs
+    // interleave (attn_f16_fwd2_kernel); causal, only from 16 tiles per head
+    // (shorter heads ran faster one tile per CTA, nq - 1 - k paired with k:
+    // 16x16x1024 702 against 730 TFLOP/s) and with at least one step of two
+    // pairs per SM (fewer leave SMs idle that single tiles would use);
+    // otherwise one tile per CTA.
+    const int64_t causal_steps = B * H * ((nq / 2 + 1) / 2);
+    const bool two_tiles = ATTN_PINGPONG && nq % 2 == 0 &&
+                           (!causal || (ATTN_CAUSAL_PAIRS && nq >= 16 && causal_steps >= static_cast<int64_t>(sms)));
+    prm.pair = !two_tiles && causal && B * H * nq >= 2 * static_cast<int64_t>(sms) ? 1 : 0;
     int64_t units = prm.pair ? B * H * ((nq + 1) / 2) : B * H * nq;
     prm.pair_units = 0;
-    if (two_tiles) {
+    if (two_tiles && causal) {
+        // steps of two pairs of one head (np - 1 - m, then m; the middle one of
+        // an odd count alone)
+        units = causal_steps;
+        prm.pair_units = static_cast<int>(units);
+    } else if (two_tiles) {
         // Two tiles per unit; when the tiles left over after k full rounds of
         // pairs (k per CTA) fit one per CTA, they run as one-tile units (k pairs
         // and at most one single per CTA instead of k + 1 pairs on some CTAs);

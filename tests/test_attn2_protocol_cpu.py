@@ -52,14 +52,21 @@ class Barrier:
 
 def run_protocol2(units, seed, nsoft=2, defect=None):
     """`units`: the units this CTA walks, each a number of key blocks (a unit
-    of two tiles) or a pair (key blocks, False) for a unit of tile A alone; the
-    one-tile units come last.  nsoft softmax warps per tile stand for the eight.
+    of two tiles), a pair (key blocks, False) for a unit of tile A alone, or a
+    pair (blocks of A, blocks of B) with B's one more (causal: tile A = 2k reads
+    key blocks 0..2k, tile B = 2k + 1 reads 0..2k + 1, so B reads every block
+    the unit loads); the one-tile units come last.  nsoft softmax warps per tile stand for the eight.
     `defect` plants a mistake: "early_s" (the MMA thread issues the next S of a
     tile before that tile's P is written), "k_slot_a" (the producer frees a K
-    slot on tile A's S instead of B's), or "single_slot_a" (once the one-tile
+    slot on tile A's S instead of B's), "single_slot_a" (once the one-tile
     units begin, every slot is freed on tile A's barriers, also a slot whose
-    previous block belonged to a two-tile unit)."""
-    units = [(u, True) if isinstance(u, int) else u for u in units]
+    previous block belonged to a two-tile unit), or "a_ring_phase" (the MMA
+    thread takes tile A's barrier phases from the count of blocks loaded, which
+    runs ahead of A's own count in causal units)."""
+    # normalise to (blocks of A, blocks of B), B's 0 for a one-tile unit
+    units = [(u, u) if isinstance(u, int) else (u[0], u[0] if u[1] is True else (0 if u[1] is False else u[1]))
+             for u in units]
+    assert all(b == 0 or b >= a for a, b in units), "tile B reads every block of a two-tile unit"
     assert all(a[1] or not b[1] for a, b in zip(units, units[1:])), "one-tile units come last"
     rnd = random.Random(seed)
     q_full, drain = Barrier("q_full", 1), Barrier("drain", 1)
@@ -81,7 +88,9 @@ def run_protocol2(units, seed, nsoft=2, defect=None):
         g = 0
         pair_end = 0                  # blocks of the two-tile units so far (they come first)
         prev_pair = True
-        for u, (nblk, pair) in enumerate(units):
+        for u, (na, nbk) in enumerate(units):
+            pair = nbk > 0
+            nblk = nbk if pair else na      # blocks loaded: every block B reads, or A's
             if is_k:
                 if g > 0:   # the previous unit's last S (S_B, issued after S_A, or S_A alone) has read Q
                     yield wait(s_full["B" if prev_pair else "A"][(g - 1) & 1], (g - 1) >> 1, "producer Q")
@@ -104,9 +113,9 @@ def run_protocol2(units, seed, nsoft=2, defect=None):
                     t = "A"
                 yield wait(s_full[t][s] if is_k else pv_done[t][s], (gb >> 1) - 1, "producer slot")
                 # the load overwrites ring slot s: no MMA reading its previous block may remain
-                for op, _, gq in pipe:
-                    assert not (gq is not None and gq & 1 == s and gq < gb and op == ("s" if is_k else "pv")), \
-                        f"load of block {gb} into {'K' if is_k else 'V'} slot {s} while block {gq}'s MMA reads it"
+                for op, _, _, rq in pipe:
+                    assert not (rq is not None and rq & 1 == s and rq < gb and op == ("s" if is_k else "pv")), \
+                        f"load of block {gb} into {'K' if is_k else 'V'} slot {s} while block {rq}'s MMA reads it"
                 full = k_full[s] if is_k else v_full[s]
                 full.arrive(tx=1)
                 tma.append(full)
@@ -114,45 +123,56 @@ def run_protocol2(units, seed, nsoft=2, defect=None):
             prev_pair = pair
 
     def mma():
-        g = 0
+        g = 0                          # ring blocks (every block loaded)
+        gt = {"A": 0, "B": 0}          # each tile's own blocks: the phases of its barriers
 
-        def issue_s(t, gb):
+        def issue_s(t, rb, tb):
             # S overwrites tile t's score buffer: no softmax may still read it and
             # no earlier P V may still read the P in it (the pipe is in order)
-            pipe.append(("s", t, gb))
+            pipe.append(("s", t, tb, rb))
 
         nb = 0                        # two-tile units so far
-        for u, (nblk, pair) in enumerate(units):
-            tiles = "AB" if pair else "A"
+        for u, (na, nbk) in enumerate(units):
+            n = {"A": na, "B": nbk}
+            tiles = "AB" if nbk else "A"
+            nr = max(na, nbk)
             yield wait(q_full, u, "mma Q")
             yield wait(k_full[g & 1], g >> 1, "mma K")
             for t in tiles:
-                issue_s(t, g)
-            for j in range(nblk):
-                gb = g + j
+                issue_s(t, g, gt[t])
+            for j in range(nr):
+                rb = g + j
                 for t in tiles:
-                    if defect == "early_s" and t == "A" and j + 1 < nblk:
-                        yield wait(k_full[(gb + 1) & 1], (gb + 1) >> 1, "mma K")
-                        issue_s("A", gb + 1)
-                    yield wait(p_full[t], gb, f"mma P{t}")
+                    if j >= n[t]:
+                        continue                   # tile A has no last block in a causal unit
+                    tb = gt[t] + j
+                    if defect == "a_ring_phase" and t == "A":
+                        tb = rb
+                    if defect == "early_s" and t == "A" and j + 1 < n[t]:
+                        yield wait(k_full[(rb + 1) & 1], (rb + 1) >> 1, "mma K")
+                        issue_s("A", rb + 1, tb + 1)
+                    yield wait(p_full[t], tb, f"mma P{t}")
                     done = u if t == "A" else nb      # this tile's earlier units
                     if j == 0 and done > 0:
                         yield wait(o_free[t], done - 1, f"mma O{t} free")
-                    yield wait(v_full[gb & 1], gb >> 1, "mma V")
-                    pipe.append(("pv", t, gb))
-                    if j + 1 < nblk and not (defect == "early_s" and t == "A"):
-                        yield wait(k_full[(gb + 1) & 1], (gb + 1) >> 1, "mma K")
-                        issue_s(t, gb + 1)
-            g += nblk
-            nb += pair
-        pipe.append(("drain", None, None))
+                    yield wait(v_full[rb & 1], rb >> 1, "mma V")
+                    pipe.append(("pv", t, tb, rb))
+                    if j + 1 < n[t] and not (defect == "early_s" and t == "A"):
+                        yield wait(k_full[(rb + 1) & 1], (rb + 1) >> 1, "mma K")
+                        issue_s(t, rb + 1, tb + 1)
+            g += nr
+            for t in tiles:
+                gt[t] += n[t]
+            nb += nbk > 0
+        pipe.append(("drain", None, None, None))
         yield wait(drain, 0, "mma drain")
 
     def softmax(t):
-        g = x = 0
-        for u, (nblk, pair) in enumerate(units):
-            if t == "B" and not pair:
+        g = x = 0                                    # g: this tile's blocks
+        for u, (na, nbk) in enumerate(units):
+            if t == "B" and not nbk:
                 break                                # tile B's warps sit out the one-tile units
+            nblk = na if t == "A" else nbk
             for j in range(nblk):
                 gb = g + j
                 yield wait(s_full[t][gb & 1], gb >> 1, f"softmax{t} S")
@@ -203,7 +223,7 @@ def run_protocol2(units, seed, nsoft=2, defect=None):
         if kind == "tma":
             tma.pop(rnd.randrange(len(tma))).complete_tx(1)
         elif kind == "pipe":
-            op, t, gb = pipe.pop(0)        # the tensor pipe completes in issue order
+            op, t, gb, _ = pipe.pop(0)     # the tensor pipe completes in issue order (gb: the tile's block)
             if op == "s":
                 assert s_readers[t] == 0, f"S_{t} of block {gb} overwrote a score buffer a softmax still reads"
                 s_full[t][gb & 1].arrive()
@@ -221,7 +241,9 @@ def run_protocol2(units, seed, nsoft=2, defect=None):
 
 CASES = [[1], [2], [5], [2, 2], [8, 8, 8], [32, 32], [3, 1, 4], [1, 1, 1, 1],
          [(1, False)], [(5, False)], [(3, False), (3, False)], [4, (4, False)], [8, 8, (8, False)],
-         [1, (1, False)], [2, 2, (2, False), (2, False)], [32, 32, (32, False)]]
+         [1, (1, False)], [2, 2, (2, False), (2, False)], [32, 32, (32, False)],
+         # causal units: tile A 2k + 1 blocks, tile B 2k + 2 (two pairs of one head, heavy then light)
+         [(1, 2)], [(3, 4), (1, 2)], [(31, 32), (1, 2), (29, 30), (3, 4)], [(5, 6), (5, 6)], [(1, 2), (1, 2), (1, 2)]]
 
 
 @pytest.mark.parametrize("units", CASES)
@@ -243,3 +265,11 @@ def test_attention2_model_catches_slot_freed_on_the_wrong_tile_at_the_switch():
     with pytest.raises(AssertionError):
         for seed in range(200):
             run_protocol2([4, 4, (3, False)], seed, defect="single_slot_a")
+
+
+def test_attention2_model_catches_tile_a_phases_from_the_ring_count():
+    # in causal units tile A reads one block fewer than is loaded: its barrier
+    # phases must follow its own block count
+    with pytest.raises(AssertionError):
+        for seed in range(50):
+            run_protocol2([(3, 4), (1, 2), (5, 6)], seed, defect="a_ring_phase")
