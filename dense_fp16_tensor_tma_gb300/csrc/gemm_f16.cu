@@ -196,23 +196,28 @@ int check_args(const Operands& op, const void* bias, int64_t M, int64_t N, int64
     return GEMM_OK;
 }
 
-// Single-CTA kernel choice for problems with too few 256 x 256 tiles for
-// the CTA pair (and M > 64): 128-row tiles of width 64, 128 or 256, the
-// narrower two possibly with K split across a cluster of 2 or 4 CTAs.  Each
-// candidate is costed by the operand bytes it moves: the busiest SM's bytes
-// at its intake rate, or every CTA's bytes at the L2's aggregate rate,
-// whichever takes longer, plus a fixed cost for a split's cluster reduction.
+// Kernel choice for problems with too few 256 x 256 tiles for the CTA pair to
+// take them by rule (and M > 64): 128-row tiles of width 64, 128 or 256,
+// possibly with K split across a cluster of 2 or 4 CTAs, and, with at least 32
+// K blocks, the CTA pair itself.  Each candidate is costed by the operand bytes
+// it moves: the busiest SM's bytes at its intake rate, or every SM's bytes at
+// the L2's aggregate rate, whichever takes longer, plus a fixed cost per call
+// and, for a split, the cluster reduction (proportional to the tile's width).
 // The rates were fitted on a GB300 to replayed-graph timings of every
-// candidate on 13 shapes: about 88 GB/s per SM, 10.5 TB/s for the L2,
-// 2.5 us per split; 256-wide tiles with a split were never the fastest and
-// are not offered.  A candidate must beat the one before it by 5 %.
+// candidate on 26 shapes (per SM: 98.7 GB/s single-CTA, 134.4 GB/s in the
+// pair; L2 12.2 TB/s; 4.0 us fixed, 5.1 in the pair; 2.5 us per split of a
+// 128-wide tile), with the MMAs issued from a converged warp; the fitted model
+// then picked the fastest candidate on all 26 and on 7 of 8 further shapes
+// (the eighth 3 % slower).  The pair at fewer than 32 K blocks was slower than
+// the best single-CTA tile on every shape measured.
 struct Choice {
     int cfg;
     int splits;
 };
 
-Choice choose_tiles(int64_t M, int64_t N, int64_t K, int num_sms, int force, bool allow_split) {
-    constexpr double kBytesPerUs = 88.0e3, kL2BytesPerUs = 10.5e6, kSplitUs = 2.5;
+Choice choose_tiles(int64_t M, int64_t N, int64_t K, int num_sms, int pair_clusters, int force, bool allow_split) {
+    constexpr double kBytesPerUs = 98.7e3, kPairBytesPerUs = 134.4e3, kL2BytesPerUs = 12.19e6;
+    constexpr double kFixedUs = 4.0, kPairFixedUs = 5.14, kSplitUs = 2.5;
     const int64_t kblocks = (K + kBK - 1) / kBK;
     const int64_t tiles_m = (M + 127) / 128;
     const int forced_split = g_force_ksplit.load();
@@ -231,19 +236,36 @@ Choice choose_tiles(int64_t M, int64_t N, int64_t K, int num_sms, int force, boo
                 const int64_t kb_per = (kblocks + sp - 1) / sp;
                 // one tile per cluster, >= 4 K blocks per CTA, no empty part
                 if (!allow_split || tiles * sp > num_sms || kb_per < 4 || kb_per * (sp - 1) >= kblocks) continue;
-                if (bn == 256 && forced_split <= 1) continue;
                 per_sm = per_k * kb_per;
                 total = per_sm * tiles * sp;
             } else {
                 per_sm = per_k * kblocks * ((tiles + num_sms - 1) / num_sms);
                 total = per_k * kblocks * tiles;
             }
-            const double t = std::max(per_sm / kBytesPerUs, total / kL2BytesPerUs) + (sp > 1 ? kSplitUs : 0.0);
-            if (t < 0.95 * best_t || (forced_split > 1 && best.splits == 1)) {
+            const double t = std::max(per_sm / kBytesPerUs, total / kL2BytesPerUs) + kFixedUs +
+                             (sp > 1 ? kSplitUs * bn / 128.0 : 0.0);
+            if (t < best_t || (forced_split > 1 && best.splits == 1)) {
                 best_t = t;
                 best = Choice{cfg, sp};
             }
         }
+    }
+    if (force == CFG_AUTO && forced_split <= 1 && kblocks >= 32 && pair_clusters > 0) {
+        // the pair's units: whole 256 x 256 tiles, a partial last wave of R <= G/2
+        // tiles as 2R half tiles (256 x 128), as make_plan lays them out; per SM
+        // and K block a whole tile moves 128 rows of A and 128 columns of B, a
+        // half tile 128 rows and 64 columns
+        const int64_t G = pair_clusters;
+        const int64_t T = ((M + 255) / 256) * ((N + 255) / 256);
+        const int64_t R = T % G;
+        const int64_t halves = (R > 0 && 2 * R <= G) ? 2 * R : 0;
+        const int64_t whole = T - halves / 2;
+        const double per_sm = static_cast<double>(kblocks) *
+                              (32768.0 * static_cast<double>((whole + G - 1) / G) + (halves ? 24576.0 : 0.0));
+        const double total = static_cast<double>(kblocks) *
+                             (65536.0 * static_cast<double>(whole) + 49152.0 * static_cast<double>(halves));
+        const double t = std::max(per_sm / kPairBytesPerUs, total / kL2BytesPerUs) + kPairFixedUs;
+        if (t < best_t) best = Choice{CFG_PAIR_256, 1};
     }
     return best;
 }
@@ -285,12 +307,12 @@ Plan make_plan(const Operands& op, int64_t M, int64_t N, int64_t K, int num_sms,
             // 1024: 12.0 us against 13.9 for the best single-CTA tile)
             cfg = CFG_PAIR_256;
         } else {
-            const Choice c = choose_tiles(M, N, K, num_sms, CFG_AUTO, allow_split);
+            const Choice c = choose_tiles(M, N, K, num_sms, pair_clusters, CFG_AUTO, allow_split);
             cfg = c.cfg;
             ksplit = c.splits;
         }
     } else if (cfg == CFG_128x256 || cfg == CFG_128x128 || cfg == CFG_128x64) {
-        ksplit = choose_tiles(M, N, K, num_sms, cfg, allow_split).splits;
+        ksplit = choose_tiles(M, N, K, num_sms, pair_clusters, cfg, allow_split).splits;
     }
     pl.cfg = cfg;
     switch (cfg) {
