@@ -7,10 +7,12 @@
 // through shared memory, the running maximum and sum kept online, the S x S
 // scores never written to memory.  What differs is the schedule.  With one
 // query tile per CTA the tensor core waits for each block's softmax and the
-// softmax for each block's MMAs.  Here a CTA takes a unit of two query tiles,
-// A and B, of one head; both use every K and V block loaded (half the K/V
-// traffic per query row), each has one score buffer and one output in
-// tensor memory, and the MMA thread issues
+// softmax for each block's MMAs.  Here a CTA takes a unit of two adjacent
+// query tiles, A and B, of one head (or, for a tail of the work, tile A
+// alone); both read the K and V blocks loaded for the unit (half the K/V
+// traffic per query row; causal: tile B reads one block more than A), each
+// has one score buffer and one output in tensor memory, and the MMA warp
+// issues
 //
 //     S_A(0) S_B(0) | P_A(0)V S_A(1) | P_B(0)V S_B(1) | P_A(1)V S_A(2) | ...
 //
@@ -27,9 +29,10 @@
 // unit's first block, rarely later) does it read the scores again, which stay
 // in tensor memory until P is stored.
 //
-// Roles: warp 0 lane 0 loads each unit's two Q tiles and the K blocks,
-// lane 1 the V blocks (two-slot rings; a slot is free once tile B's MMA of
-// the block two back has completed: B's are issued after A's); warp 1
+// Roles: warp 0 lane 0 loads each unit's Q tiles and the K blocks, lane 1
+// the V blocks (two-slot rings; a slot is free once the last MMA reading the
+// block two back has completed: tile B's, issued after A's, or tile A's in a
+// one-tile unit); warp 1
 // allocates tensor memory and issues every MMA (the whole warp runs the
 // loop, one lane elected per instruction: tc_mma_f16); warps 2..9
 // run tile A's softmax, warps 10..17 tile B's (two warps per TMEM lane
