@@ -17,33 +17,32 @@
 //     S_A(0) S_B(0) | P_A(0)V S_A(1) | P_B(0)V S_B(1) | P_A(1)V S_A(2) | ...
 //
 // so the tensor core computes one tile's P V and next scores while the other
-// tile's softmax warps work.  A tile's P (fp16) is written over its own
-// scores: each softmax warp puts its 64 keys' P into the first 32 columns of
-// its own 64 score columns, after it has read them, so no warp writes
-// columns another warp still reads; S of the next block overwrites the
-// buffer only after the P V that reads that P, both issued by the MMA warp,
-// whose MMAs the tensor pipe executes in issue order.  A softmax warp reads
-// its scores once, computing the block maximum and, speculatively, P under
-// the running maximum it already has, held as packed fp16 in registers; only
-// when the exchanged block maximum raises the running maximum (always in a
-// unit's first block, rarely later) does it read the scores again, which stay
-// in tensor memory until P is stored.
+// tile's softmax warps work.  Each softmax warp owns 32 whole rows of its
+// tile (one TMEM lane quarter): a thread reads all 128 scores of its row's
+// block into registers once, takes the exact block maximum before any
+// exponential (no partner warp, no exchange), and writes its row's P (fp16,
+// 64 columns) over the first half of its row's score columns, after it has
+// read them; S of the next block overwrites the buffer only after the P V
+// that reads that P, both issued by the MMA warp, whose MMAs the tensor pipe
+// executes in issue order.  (Two warps per row, 64 keys each, exchanging
+// their block maxima through shared memory with P computed speculatively
+// meanwhile, measured the same at D = 128 and 2-4 % slower elsewhere.)
 //
 // Roles: warp 0 lane 0 loads each unit's Q tiles and the K blocks, lane 1
 // the V blocks (two-slot rings; a slot is free once the last MMA reading the
 // block two back has completed: tile B's, issued after A's, or tile A's in a
 // one-tile unit); warp 1
 // allocates tensor memory and issues every MMA (the whole warp runs the
-// loop, one lane elected per instruction: tc_mma_f16); warps 2..9
-// run tile A's softmax, warps 10..17 tile B's (two warps per TMEM lane
-// quarter, 64 keys each, as in the one-tile kernel).  Every wait is bounded.
+// loop, one lane elected per instruction: tc_mma_f16); warps 2..5 run tile
+// A's softmax, warps 6..9 tile B's (one warp per TMEM lane quarter); 320
+// threads leave 168 registers per thread.  Every wait is bounded.
 #pragma once
 
 #include "attn_kernels.cuh"
 
 namespace attn_dev {
 
-constexpr int kAttn2Threads = 576;   // producer, MMA, 2 x 8 softmax warps
+constexpr int kAttn2Threads = 320;   // producer, MMA, 2 x 4 softmax warps
 
 template <int D>
 struct Attn2Smem {
@@ -51,11 +50,9 @@ struct Attn2Smem {
     static constexpr uint32_t kQ = 0;                        // Q_A, Q_B
     static constexpr uint32_t kK = kQ + 2 * kTile;           // 2 slots
     static constexpr uint32_t kV = kK + 2 * kTile;           // 2 slots
-    static constexpr uint32_t kX = kV + 2 * kTile;           // exchange [tile][2 parity][2 half][128]
-    static constexpr uint32_t kBars = kX + 2 * 2 * 2 * 128 * 4;
-    // q_full, k_full[2], v_full[2], s_full[2 tiles][2], p_full[2], pv_done[2][2], o_free[2],
-    // xch[2 tiles][4 quarters][2 parity], drain
-    static constexpr uint32_t kNumBars = 1 + 2 + 2 + 4 + 2 + 4 + 2 + 16 + 1;
+    static constexpr uint32_t kBars = kV + 2 * kTile;
+    // q_full, k_full[2], v_full[2], s_full[2 tiles][2], p_full[2], pv_done[2][2], o_free[2], drain
+    static constexpr uint32_t kNumBars = 1 + 2 + 2 + 4 + 2 + 4 + 2 + 1;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kEnd = kAbort + 4;
@@ -92,8 +89,7 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     auto p_full = [&](int t) { return bars + 8u * (9 + t); };                   // P of tile t written
     auto pv_done = [&](int t, int s) { return bars + 8u * (11 + 2 * t + s); };  // P V of tile t completed
     auto o_free = [&](int t) { return bars + 8u * (15 + t); };                  // tile t's output read out
-    auto xch_bar = [&](int t, int quarter, int b) { return bars + 8u * (17 + 8 * t + 2 * quarter + b); };
-    const uint32_t drain_bar = bars + 8u * 33;
+    const uint32_t drain_bar = bars + 8u * 17;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + SM::kTmemSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + SM::kAbort);
 
@@ -161,10 +157,8 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 mbar_init(s_full(t, s), 1);
                 mbar_init(pv_done(t, s), 1);
             }
-            mbar_init(p_full(t), 8);
-            mbar_init(o_free(t), 8);
-            for (int q = 0; q < 4; ++q)
-                for (int b = 0; b < 2; ++b) mbar_init(xch_bar(t, q, b), 64);
+            mbar_init(p_full(t), 4);
+            mbar_init(o_free(t), 4);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -301,8 +295,8 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 const uint64_t vd = v_desc + static_cast<uint64_t>(s * kSlotUnits);
 #pragma unroll
                 for (int k = 0; k < kKeys / 16; ++k) {
-                    // keys 16k..: softmax half k / 4 wrote its P at columns 64 (k / 4) ..
-                    const uint32_t pcol = static_cast<uint32_t>((k >> 2) * 64 + (k & 3) * 8);
+                    // keys 16k..: P at columns 8k .. 8k + 7 of the tile's score buffer
+                    const uint32_t pcol = static_cast<uint32_t>(k * 8);
                     tc_mma_f16_ta(o_tmem, pa + pcol, vd + static_cast<uint64_t>(k * 2048 >> 4), kIdescO,
                                   (j | k) != 0 ? 1u : 0u);
                 }
@@ -346,34 +340,12 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + output
-        const int t = (warp - 2) >> 3;               // query tile A (0) or B (1)
-        const int local = (warp - 2) & 7;
-        const int quarter = warp & 3;                // TMEM lanes 32 * quarter ..
-        const int half = local >> 2;                 // keys 64 half .. of each block
+        const int t = (warp - 2) >> 2;               // query tile A (0) or B (1)
+        const int quarter = warp & 3;                // TMEM lanes 32 * quarter ..: this warp's rows
         const int r = 32 * quarter + lane;           // this thread's row of the tile
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
-        const uint32_t s_cols = lane_base + kSCol + static_cast<uint32_t>(t * kKeys + 64 * half);
-        volatile float* xch = reinterpret_cast<volatile float*>(base + SM::kX) + t * (2 * 2 * 128);
-        int x = 0;                                   // exchanges so far
-        // exchange with the warp holding the row's other 64 keys: post, then collect
-        auto xpost = [&](float mine) {
-            xch[((x & 1) * 2 + half) * 128 + r] = mine;
-            mbar_arrive(xch_bar(t, quarter, x & 1));
-        };
-        auto xcollect = [&](float& theirs) -> bool {
-            const int slot = x & 1, use = x >> 1;
-            ++x;
-            const bool got = mbar_wait_bounded(xch_bar(t, quarter, slot), use & 1, p.timeout_ns, abort_flag, status,
-                                               ROLE_SOFTMAX, BAR_X);
-            theirs = xch[(slot * 2 + (1 - half)) * 128 + r];
-            return got;
-        };
-        auto exchange = [&](float mine, float& theirs) -> bool {
-            xpost(mine);
-            return xcollect(theirs);
-        };
-        constexpr int kOCols = D / 2;
-        const uint32_t o_cols = lane_base + kOCol2 + static_cast<uint32_t>(t * D + half * kOCols);
+        const uint32_t s_cols = lane_base + kSCol + static_cast<uint32_t>(t * kKeys);
+        const uint32_t o_cols = lane_base + kOCol2 + static_cast<uint32_t>(t * D);
         const bool pos = p.scale_log2 >= 0.0f;
         const uint32_t lose = __float_as_uint(pos ? -INFINITY : INFINITY);
         bool ok = true;
@@ -394,135 +366,122 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                                        ROLE_SOFTMAX, BAR_S);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
-                const bool masked_block = k0 + kKeys > p.S || (p.causal && j == n - 1);
-                const int key_lim = key_end - k0 - 64 * half;   // valid: col < key_lim
-                // one pass over the warp's 64 scores, 32 at a time: the block maximum
-                // and, speculatively, P = 2^(x * scale_log2 - m) with the current
-                // maximum m, packed fp16 in registers.  The scores stay in tensor
-                // memory until P is stored, so a raise of m (always in a unit's first
-                // block, rare once m has settled) recomputes P from them.
+                // the row's 128 scores of the block, all in registers
+                uint32_t v[128];
+                uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(v);
+                uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 32);
+                uint32_t (&v2)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 64);
+                uint32_t (&v3)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 96);
+                tmem_ld_32x32b_x32(s_cols, v0);
+                tmem_ld_32x32b_x32(s_cols + 32u, v1);
+                tmem_ld_32x32b_x32(s_cols + 64u, v2);
+                tmem_ld_32x32b_x32(s_cols + 96u, v3);
+                tmem_wait_ld(v0);
+                tmem_wait_ld(v1);
+                tmem_wait_ld(v2);
+                tmem_wait_ld(v3);
+                if (k0 + kKeys > p.S || (p.causal && j == n - 1)) {
+                    const int key_lim = key_end - k0;         // valid: column < key_lim
+#pragma unroll
+                    for (int i = 0; i < 128; ++i)
+                        if (i >= key_lim) v[i] = lose;
+                }
                 float bm[4];
                 bm[0] = bm[1] = bm[2] = bm[3] = pos ? -INFINITY : INFINITY;
-                uint32_t h[32];
-                float rs0 = 0.0f, rs1 = 0.0f;
-                auto p_chunk = [&](int c, float mx, bool track) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(s_cols + 32u * c, v);
-                    tmem_wait_ld(v);
-                    if (masked_block) {
+                if (pos) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (32 * c + i >= key_lim) v[i] = lose;
-                    }
-                    if (track) {
-                        if (pos) {
+                    for (int i = 0; i < 128; i += 2)
+                        bm[(i >> 1) & 3] = max3f(bm[(i >> 1) & 3], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                } else {
 #pragma unroll
-                            for (int i = 0; i < 32; i += 2)
-                                bm[(i >> 1) & 3] = max3f(bm[(i >> 1) & 3], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; i += 2)
-                                bm[(i >> 1) & 3] = min3f(bm[(i >> 1) & 3], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-                        }
-                    }
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float2 xs = fma2_bc(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]),
-                                                  p.scale_log2, -mx);
-                        const __half2 hv = __floats2half2_rn(fast_exp2(xs.x), fast_exp2(xs.y));
-                        h[16 * c + i] = *reinterpret_cast<const uint32_t*>(&hv);
-                        if (i & 1) rs1 = add_f16x2_to_f32(rs1, h[16 * c + i]);
-                        else rs0 = add_f16x2_to_f32(rs0, h[16 * c + i]);
-                    }
-                };
-                const float m_spec = (m == -INFINITY) ? 0.0f : m;
-                p_chunk(0, m_spec, true);
-                p_chunk(1, m_spec, true);
+                    for (int i = 0; i < 128; i += 2)
+                        bm[(i >> 1) & 3] = min3f(bm[(i >> 1) & 3], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                }
                 float bmax = pos ? fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3]))
                                  : fminf(fminf(bm[0], bm[1]), fminf(bm[2], bm[3]));
                 bmax *= p.scale_log2;
-                float other = -INFINITY;
-                ok = exchange(bmax, other);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                const float bmax2 = fmaxf(bmax, other);
                 float m_new = m;
                 bool raise = false;
-                if (bmax2 > m + kRaise || m == -INFINITY) {
-                    m_new = fmaxf(m, bmax2);
+                if (bmax > m + kRaise || m == -INFINITY) {
+                    m_new = fmaxf(m, bmax);
                     raise = m != -INFINITY && m_new != m;
                 }
-                // a raise implies a new maximum: one vote covers the common case
-                if (__any_sync(0xffffffffu, m_new != m)) {
-                    if (__any_sync(0xffffffffu, raise)) {
-                        ok = mbar_wait_bounded(pv_done(t, (gb - 1) & 1), ((gb - 1) >> 1) & 1, p.timeout_ns,
-                                               abort_flag, status, ROLE_SOFTMAX, BAR_PV);
-                        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                        tc_fence_after();
-                        const float alpha = raise ? fast_exp2(m - m_new) : 1.0f;
-                        l *= alpha;
-#pragma unroll 1
-                        for (int c = 0; c < kOCols / 32; ++c) {
-                            uint32_t w[32];
-                            tmem_ld_32x32b_x32(o_cols + 32u * c, w);
-                            tmem_wait_ld(w);
+                // P = 2^(x * scale_log2 - m) as fp16 over the first 64 of the row's
+                // score columns (keys 32c .. 32c + 31 into columns 16c ..), and its sum
+                // over the fp16 values the tensor core multiplies
+                const float mm = (m_new == -INFINITY) ? 0.0f : m_new;
+                float rs0 = 0.0f, rs1 = 0.0f;
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
-                            tmem_st_32x32b_x32(o_cols + 32u * c, w);
-                        }
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t h[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 xs = fma2_bc(__uint_as_float(v[32 * c + 2 * i]), __uint_as_float(v[32 * c + 2 * i + 1]),
+                                                  p.scale_log2, -mm);
+                        const __half2 hv = __floats2half2_rn(fast_exp2(xs.x), fast_exp2(xs.y));
+                        h[i] = *reinterpret_cast<const uint32_t*>(&hv);
+                        if (i & 1) rs1 = add_f16x2_to_f32(rs1, h[i]);
+                        else rs0 = add_f16x2_to_f32(rs0, h[i]);
                     }
-                    rs0 = 0.0f;
-                    rs1 = 0.0f;
-                    const float mm = (m_new == -INFINITY) ? 0.0f : m_new;
-                    p_chunk(0, mm, false);
-                    p_chunk(1, mm, false);
+                    tmem_st_32x32b_x16(s_cols + 16u * c, h);
+                }
+                // O rescaled (a raise needs an earlier block of the unit) after the
+                // tile's previous P V has completed
+                if (__any_sync(0xffffffffu, raise)) {
+                    ok = mbar_wait_bounded(pv_done(t, (gb - 1) & 1), ((gb - 1) >> 1) & 1, p.timeout_ns, abort_flag,
+                                           status, ROLE_SOFTMAX, BAR_PV);
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    tc_fence_after();
+                    const float alpha = raise ? fast_exp2(m - m_new) : 1.0f;
+                    l *= alpha;
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t w[32];
+                        tmem_ld_32x32b_x32(o_cols + 32u * c, w);
+                        tmem_wait_ld(w);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+                        tmem_st_32x32b_x32(o_cols + 32u * c, w);
+                    }
                 }
                 m = m_new;
                 l += rs0 + rs1;
-                // P over the first 32 of the warp's 64 score columns
-                tmem_st_32x32b_x32(s_cols, h);
                 tmem_wait_st();
                 tc_fence_before();           // P and the O rescale, if any, before the signal
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_full(t));
             }
             if (!ok) break;
-            // output: O / l after the unit's last P V of this tile
+            // output: O / l after the unit's last P V of this tile; O read into
+            // registers and its tensor memory released before the stores
             const int gl = g + n - 1;
             ok = mbar_wait_bounded(pv_done(t, gl & 1), (gl >> 1) & 1, p.timeout_ns, abort_flag, status,
                                    ROLE_SOFTMAX, BAR_PV);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            // this warp's O columns into registers first, then O's tensor memory is
-            // released to the next unit's first P V; the row sums are exchanged and
-            // the output normalised and stored after that
             tc_fence_after();
-            uint32_t w0[32], w1[32];
-            tmem_ld_32x32b_x32(o_cols, w0);
-            if constexpr (kOCols == 64) tmem_ld_32x32b_x32(o_cols + 32u, w1);
-            tmem_wait_ld(w0);
-            if constexpr (kOCols == 64) tmem_wait_ld(w1);
+            uint32_t w[D];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c)
+                tmem_ld_32x32b_x32(o_cols + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(w + 32 * c));
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(w + 32 * c));
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free(t));
-            float l_other = 0.0f;
-            ok = exchange(l, l_other);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            const float inv = 1.0f / (l + l_other);
+            const float inv = 1.0f / l;
             if (q < p.S) {
-                __half* orow = p.O + (static_cast<int64_t>(bh) * p.S + q) * D + half * kOCols;
-                auto store32 = [&](const uint32_t (&w)[32], int c) {
-                    uint32_t h[16];
+                uint4* dst = reinterpret_cast<uint4*>(p.O + (static_cast<int64_t>(bh) * p.S + q) * D);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const __half2 hv = __floats2half2_rn(__uint_as_float(w[2 * i]) * inv,
-                                                             __uint_as_float(w[2 * i + 1]) * inv);
-                        h[i] = *reinterpret_cast<const uint32_t*>(&hv);
+                for (int i = 0; i < D / 8; ++i) {
+                    uint32_t hh[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __half2 hv = __floats2half2_rn(__uint_as_float(w[8 * i + 2 * e]) * inv,
+                                                             __uint_as_float(w[8 * i + 2 * e + 1]) * inv);
+                        hh[e] = *reinterpret_cast<const uint32_t*>(&hv);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-                };
-                store32(w0, 0);
-                if constexpr (kOCols == 64) store32(w1, 1);
+                    dst[i] = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+                }
             }
             g += n;
         }

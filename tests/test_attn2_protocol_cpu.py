@@ -55,7 +55,7 @@ def run_protocol2(units, seed, nsoft=2, defect=None):
     of two tiles), a pair (key blocks, False) for a unit of tile A alone, or a
     pair (blocks of A, blocks of B) with B's one more (causal: tile A = 2k reads
     key blocks 0..2k, tile B = 2k + 1 reads 0..2k + 1, so B reads every block
-    the unit loads); the one-tile units come last.  nsoft softmax warps per tile stand for the eight.
+    the unit loads); the one-tile units come last.  nsoft softmax warps per tile stand for the four.
     `defect` plants a mistake: "early_s" (the MMA thread issues the next S of a
     tile before that tile's P is written), "k_slot_a" (the producer frees a K
     slot on tile A's S instead of B's), "single_slot_a" (once the one-tile
@@ -76,7 +76,6 @@ def run_protocol2(units, seed, nsoft=2, defect=None):
     p_full = {t: Barrier(f"p_full{t}", nsoft) for t in "AB"}
     pv_done = {"A": [Barrier(f"pv_doneA{i}", 1) for i in range(2)], "B": [Barrier(f"pv_doneB{i}", 1) for i in range(2)]}
     o_free = {t: Barrier(f"o_free{t}", nsoft) for t in "AB"}
-    xch = {t: [Barrier(f"xch{t}{i}", nsoft) for i in range(2)] for t in "AB"}
     tma, pipe = [], []
     # tensor-memory hazard: softmax warps that may still read each tile's score buffer
     s_readers = {"A": 0, "B": 0}
@@ -168,7 +167,7 @@ def run_protocol2(units, seed, nsoft=2, defect=None):
         yield wait(drain, 0, "mma drain")
 
     def softmax(t):
-        g = x = 0                                    # g: this tile's blocks
+        g = 0                                        # this tile's blocks
         for u, (na, nbk) in enumerate(units):
             if t == "B" and not nbk:
                 break                                # tile B's warps sit out the one-tile units
@@ -177,22 +176,14 @@ def run_protocol2(units, seed, nsoft=2, defect=None):
                 gb = g + j
                 yield wait(s_full[t][gb & 1], gb >> 1, f"softmax{t} S")
                 s_readers[t] += 1
-                slot, use = x & 1, x >> 1
-                x += 1
-                xch[t][slot].arrive()
-                yield wait(xch[t][slot], use, f"softmax{t} exchange")
+                yield None                           # S read into registers, P written over it
                 if j >= 1 and rnd.random() < 0.3:   # a raise: O rescaled after the previous P V
                     yield wait(pv_done[t][(gb - 1) & 1], (gb - 1) >> 1, f"softmax{t} rescale")
-                yield None                           # pass 2 reads S again and writes P into it
                 s_readers[t] -= 1
                 p_full[t].arrive()
             gl = g + nblk - 1
             yield wait(pv_done[t][gl & 1], gl >> 1, f"softmax{t} output")
-            slot, use = x & 1, x >> 1
-            x += 1
-            xch[t][slot].arrive()
-            yield wait(xch[t][slot], use, f"softmax{t} row sum")
-            o_free[t].arrive()
+            o_free[t].arrive()                       # O read out of tensor memory
             g += nblk
 
     roles = [producer(True), producer(False), mma()] + [softmax(t) for t in "AB" for _ in range(nsoft)]
