@@ -90,11 +90,13 @@ def workload_config(w, epi, layout="nn"):
 def attn_kernel_name(w, sms: int) -> str:
     """Problems with an even number of 128-row query tiles run the two-tile
     kernel (two query tiles per CTA, softmax of one overlapping the other's
-    MMAs), causal ones from 16 tiles per head and with a step of two tile
-    pairs per SM; the rest run the one-tile kernel."""
+    MMAs), causal ones with a multiple of 4 tiles per head, at least 12, a step
+    of two tile pairs per SM and steps that split over the SMs no worse than the
+    one-tile kernel's units; the rest run the one-tile kernel."""
     nq = (w.S + 127) // 128
-    steps = w.B * w.H * ((nq // 2 + 1) // 2)
-    if nq % 2 == 0 and (not w.causal or (nq >= 16 and steps >= sms)):
+    steps = w.B * w.H * (nq // 4)
+    balanced = 2 * -(-steps // sms) * (80 if w.D == 64 else 85) < 100 * -(-2 * steps // sms)
+    if nq % 2 == 0 and (not w.causal or (nq % 4 == 0 and nq >= 12 and steps >= sms and balanced)):
         return f"attn_f16_fwd2_kernel<{w.D}>"
     return f"attn_f16_fwd_kernel<{w.D}>"
 

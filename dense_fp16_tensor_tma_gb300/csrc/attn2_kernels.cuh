@@ -105,12 +105,13 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     // pairs on some CTAs).  Causal: units of tiles 2k and 2k + 1 of one head;
     // tile A reads key blocks 0..2k, tile B 0..2k + 1 (every block the unit
     // loads); a CTA takes them two at a time from one head, pair np - 1 - m and
-    // then pair m (np pairs per head, the middle pair of an odd np alone), so
-    // every such step costs the same.  Units in flight share a few heads, whose
-    // K and V stay in L2.
+    // then pair m (np pairs per head, even: the host launches causal problems
+    // here only with a multiple of 4 query tiles per head), so every such step
+    // costs the same.  Units in flight share a few heads, whose K and V stay
+    // in L2.
     const int nblk = (p.S + kKeys - 1) / kKeys;    // key blocks per tile, non-causal
     const int np = p.nq >> 1;                       // pairs per head
-    const int sp = (np + 1) >> 1;                   // causal steps per head
+    const int sp = np >> 1;                         // causal steps per head
     struct UnitWalk {
         int U, i;                                   // step (unit) index, unit within a causal step
         // the next unit: head, tile A's index, key blocks of A and of B (0: A alone)
@@ -132,8 +133,7 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             int k;
             if (i == 0) {
                 k = np - 1 - m;
-                if (k == m) U += static_cast<int>(gridDim.x);   // the middle pair: a step of one unit
-                else i = 1;
+                i = 1;
             } else {
                 k = m;
                 i = 0;
