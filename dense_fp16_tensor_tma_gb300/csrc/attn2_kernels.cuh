@@ -47,10 +47,13 @@ constexpr int kAttn2Threads = 320;   // producer, MMA, 2 x 4 softmax warps
 template <int D>
 struct Attn2Smem {
     static constexpr uint32_t kTile = (D / 64) * kBox;     // one 128-row tile of Q, K or V
+    // D = 64: a V slot is the block's 64 columns and then a box of fp16 ones,
+    // columns 64.. of the P V operand, so O's column 64 accumulates the row sum
+    static constexpr uint32_t kVSlot = D == 64 ? 2 * kBox : kTile;
     static constexpr uint32_t kQ = 0;                        // Q_A, Q_B
     static constexpr uint32_t kK = kQ + 2 * kTile;           // 2 slots
     static constexpr uint32_t kV = kK + 2 * kTile;           // 2 slots
-    static constexpr uint32_t kBars = kV + 2 * kTile;
+    static constexpr uint32_t kBars = kV + 2 * kVSlot;
     // q_full, k_full[2], v_full[2], s_full[2 tiles][2], p_full[2], pv_done[2][2], o_free[2], drain
     static constexpr uint32_t kNumBars = 1 + 2 + 2 + 4 + 2 + 4 + 2 + 1;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
@@ -71,10 +74,16 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     using SM = Attn2Smem<D>;
     constexpr int kDB = D / 64;
     constexpr uint32_t kTileBytes = SM::kTile;
+    // D = 64: the P V MMA also multiplies P by a column of ones (N = 80), so the
+    // tensor core sums each row's fp16 P into O's column 64 in fp32, rescaled
+    // with O; D = 128 leaves no tensor-memory columns for it and the softmax
+    // warps sum P themselves
+    constexpr bool kSumByMma = D == 64;
+    constexpr int kON = kSumByMma ? D + 16 : D;
     constexpr uint32_t kIdescS = idesc_f16_f32(kQRows, kKeys, /*b_mn_major=*/false);
-    constexpr uint32_t kIdescO = idesc_f16_f32(kQRows, D, /*b_mn_major=*/true);
+    constexpr uint32_t kIdescO = idesc_f16_f32(kQRows, kON, /*b_mn_major=*/true);
     constexpr uint32_t kSCol = 0;             // S_A at 0, S_B at 128
-    constexpr uint32_t kOCol2 = 256;          // O_A at 256, O_B at 256 + D
+    constexpr uint32_t kOCol2 = 256;          // O_A at 256, O_B at 384 (kON <= 128 columns each)
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -164,6 +173,15 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         *abort_flag = 0;
         fence_mbarrier_init();
     }
+    if constexpr (kSumByMma) {
+        // the boxes of ones after each V slot, written once; never loaded over
+        for (int s = 0; s < 2; ++s) {
+            uint4* ones = reinterpret_cast<uint4*>(base + SM::kV + s * SM::kVSlot + kBox);
+            for (int i = threadIdx.x; i < static_cast<int>(kBox / 16); i += kAttn2Threads)
+                ones[i] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);   // fp16 1.0
+        }
+        fence_proxy_async_smem();
+    }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
@@ -193,6 +211,7 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const bool is_k = lane == 0;
             const CUtensorMap* tm = is_k ? &tmK : &tmV;
             const uint32_t ring = is_k ? sK : sV;
+            const uint32_t slot_bytes = is_k ? kTileBytes : SM::kVSlot;
             const uint32_t which = is_k ? BAR_K : BAR_V;
             bool ok = true;
             int g = 0, nu = 0, issued = 0;
@@ -239,7 +258,7 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     const uint32_t full = is_k ? k_full(s) : v_full(s);
                     mbar_arrive_expect_tx(full, kTileBytes);
                     for (int c = 0; c < kDB; ++c)
-                        tma_load_3d(ring + (s * kDB + c) * kBox, tm, full, 64 * c, j * kKeys, bh);
+                        tma_load_3d(ring + s * slot_bytes + c * kBox, tm, full, 64 * c, j * kKeys, bh);
                     issued = gb + 1;
                 }
                 g += nr;
@@ -260,6 +279,7 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const uint64_t k_desc = smem_desc_sw128(sK, 0, 1024);
             const uint64_t v_desc = smem_desc_sw128(sV, kBox, 1024);   // MN-major: 64-column boxes kBox apart
             constexpr uint32_t kSlotUnits = kTileBytes >> 4;
+            constexpr uint32_t kVSlotUnits = SM::kVSlot >> 4;
             // S_t of loaded block rb (tile t's block tb) = Q_t K^T into t's score buffer
             auto issue_s = [&](int t, int rb, int tb) -> bool {
                 const int s = rb & 1;
@@ -290,9 +310,9 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 if (!mbar_wait_bounded(v_full(s), (rb >> 1) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_V))
                     return false;
                 tc_fence_after();
-                const uint32_t o_tmem = tmem_base + kOCol2 + static_cast<uint32_t>(t * D);
+                const uint32_t o_tmem = tmem_base + kOCol2 + static_cast<uint32_t>(t * 128);
                 const uint32_t pa = tmem_base + kSCol + static_cast<uint32_t>(t * kKeys);
-                const uint64_t vd = v_desc + static_cast<uint64_t>(s * kSlotUnits);
+                const uint64_t vd = v_desc + static_cast<uint64_t>(s * kVSlotUnits);
 #pragma unroll
                 for (int k = 0; k < kKeys / 16; ++k) {
                     // keys 16k..: P at columns 8k .. 8k + 7 of the tile's score buffer
@@ -345,7 +365,7 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         const int r = 32 * quarter + lane;           // this thread's row of the tile
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
         const uint32_t s_cols = lane_base + kSCol + static_cast<uint32_t>(t * kKeys);
-        const uint32_t o_cols = lane_base + kOCol2 + static_cast<uint32_t>(t * D);
+        const uint32_t o_cols = lane_base + kOCol2 + static_cast<uint32_t>(t * 128);
         const bool pos = p.scale_log2 >= 0.0f;
         const uint32_t lose = __float_as_uint(pos ? -INFINITY : INFINITY);
         bool ok = true;
@@ -407,8 +427,8 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     raise = m != -INFINITY && m_new != m;
                 }
                 // P = 2^(x * scale_log2 - m) as fp16 over the first 64 of the row's
-                // score columns (keys 32c .. 32c + 31 into columns 16c ..), and its sum
-                // over the fp16 values the tensor core multiplies
+                // score columns (keys 32c .. 32c + 31 into columns 16c ..), and (D =
+                // 128) its sum over the fp16 values the tensor core multiplies
                 const float mm = (m_new == -INFINITY) ? 0.0f : m_new;
                 float rs0 = 0.0f, rs1 = 0.0f;
 #pragma unroll
@@ -420,8 +440,10 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                                                   p.scale_log2, -mm);
                         const __half2 hv = __floats2half2_rn(fast_exp2(xs.x), fast_exp2(xs.y));
                         h[i] = *reinterpret_cast<const uint32_t*>(&hv);
-                        if (i & 1) rs1 = add_f16x2_to_f32(rs1, h[i]);
-                        else rs0 = add_f16x2_to_f32(rs0, h[i]);
+                        if constexpr (!kSumByMma) {
+                            if (i & 1) rs1 = add_f16x2_to_f32(rs1, h[i]);
+                            else rs0 = add_f16x2_to_f32(rs0, h[i]);
+                        }
                     }
                     tmem_st_32x32b_x16(s_cols + 16u * c, h);
                 }
@@ -434,8 +456,9 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     tc_fence_after();
                     const float alpha = raise ? fast_exp2(m - m_new) : 1.0f;
                     l *= alpha;
+                    // D = 64: columns 64..95, the row sum among them
 #pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int c = 0; c < (kSumByMma ? D / 32 + 1 : D / 32); ++c) {
                         uint32_t w[32];
                         tmem_ld_32x32b_x32(o_cols + 32u * c, w);
                         tmem_wait_ld(w);
@@ -445,7 +468,7 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     }
                 }
                 m = m_new;
-                l += rs0 + rs1;
+                if constexpr (!kSumByMma) l += rs0 + rs1;
                 tmem_wait_st();
                 tc_fence_before();           // P and the O rescale, if any, before the signal
                 __syncwarp();
@@ -463,8 +486,14 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 #pragma unroll
             for (int c = 0; c < D / 32; ++c)
                 tmem_ld_32x32b_x32(o_cols + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(w + 32 * c));
+            uint32_t lw[16];
+            if constexpr (kSumByMma) tmem_ld_32x32b_x16(o_cols + D, lw);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(w + 32 * c));
+            if constexpr (kSumByMma) {
+                tmem_wait_ld(lw);
+                l = __uint_as_float(lw[0]);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free(t));

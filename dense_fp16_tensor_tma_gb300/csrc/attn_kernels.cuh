@@ -166,6 +166,12 @@ __device__ __forceinline__ float add_f16x2_to_f32(float acc, uint32_t w) {
     return acc;
 }
 
+// Generic-proxy writes to shared memory made visible to the async proxy (the
+// tensor core, TMA) before a barrier that orders them with its reads.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Three-input maximum / minimum (one instruction on sm_100 and later).
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float m;
