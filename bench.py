@@ -60,6 +60,7 @@ def log(*a):
 
 ATTN_SOURCES = ("dense_fp16_tensor_tma_gb300/csrc/attn_kernels.cuh",
                 "dense_fp16_tensor_tma_gb300/csrc/attn2_kernels.cuh",
+                "dense_fp16_tensor_tma_gb300/csrc/attn3_kernels.cuh",
                 "dense_fp16_tensor_tma_gb300/csrc/attn_f16.cu",
                 "dense_fp16_tensor_tma_gb300/csrc/ptx.cuh")
 
@@ -90,14 +91,15 @@ def workload_config(w, epi, layout="nn"):
 def attn_kernel_name(w, sms: int) -> str:
     """Problems with an even number of 128-row query tiles run the two-tile
     kernel (two query tiles per CTA, softmax of one overlapping the other's
-    MMAs), causal ones with a multiple of 4 tiles per head, at least 12, a step
-    of two tile pairs per SM and steps that split over the SMs no worse than the
-    one-tile kernel's units; the rest run the one-tile kernel."""
+    MMAs; at D = 64 with P buffers of their own, so the next S overlaps the
+    softmax), causal ones with a multiple of 4 tiles per head, at least 12, a
+    step of two tile pairs per SM and steps that split over the SMs no worse
+    than the one-tile kernel's units; the rest run the one-tile kernel."""
     nq = (w.S + 127) // 128
     steps = w.B * w.H * (nq // 4)
     balanced = 2 * -(-steps // sms) * (80 if w.D == 64 else 85) < 100 * -(-2 * steps // sms)
     if nq % 2 == 0 and (not w.causal or (nq % 4 == 0 and nq >= 12 and steps >= sms and balanced)):
-        return f"attn_f16_fwd2_kernel<{w.D}>"
+        return "attn_f16_fwd3_kernel<64>" if w.D == 64 else f"attn_f16_fwd2_kernel<{w.D}>"
     return f"attn_f16_fwd_kernel<{w.D}>"
 
 

@@ -44,6 +44,53 @@ namespace attn_dev {
 
 constexpr int kAttn2Threads = 320;   // producer, MMA, 2 x 4 softmax warps
 
+// Units of the two-tile kernels.  Non-causal: query tiles numbered head-major
+// (tile = head * nq + index), unit u below pair_units holding tiles 2u and
+// 2u + 1 (adjacent tiles of one head: the host launches these kernels only for
+// an even number of query tiles), each later unit one tile (A alone); the host
+// makes the one-tile units the last of at most one per CTA, when the tiles do
+// not divide evenly into pairs per CTA (13 pairs and a single rather than 14
+// pairs on some CTAs).  Causal: units of tiles 2k and 2k + 1 of one head; tile
+// A reads key blocks 0..2k, tile B 0..2k + 1 (every block the unit loads); a
+// CTA takes them two at a time from one head, pair np - 1 - m and then pair m
+// (np pairs per head, even: the host launches causal problems here only with a
+// multiple of 4 query tiles per head), so every such step costs the same.
+// Units in flight share a few heads, whose K and V stay in L2.
+struct UnitWalk {
+    int U, i;                                   // step (unit) index, unit within a causal step
+    // the next unit: head, tile A's index, key blocks of A and of B (0: A alone);
+    // nblk key blocks per tile (non-causal), np pairs and sp causal steps per head
+    __device__ bool next(const AttnParams& p, int nblk, int np, int sp, int& bh, int& qa, int& na, int& nb) {
+        if (U >= p.units) return false;
+        if (!p.causal) {
+            const int u = U;
+            U += static_cast<int>(gridDim.x);
+            const bool two = u < p.pair_units;
+            const int tile = two ? 2 * u : 2 * p.pair_units + (u - p.pair_units);
+            bh = tile / p.nq;
+            qa = tile - bh * p.nq;
+            na = nblk;
+            nb = two ? nblk : 0;
+            return true;
+        }
+        bh = U / sp;
+        const int m = U - bh * sp;
+        int k;
+        if (i == 0) {
+            k = np - 1 - m;
+            i = 1;
+        } else {
+            k = m;
+            i = 0;
+            U += static_cast<int>(gridDim.x);
+        }
+        qa = 2 * k;
+        na = 2 * k + 1;
+        nb = 2 * k + 2;
+        return true;
+    }
+};
+
 template <int D>
 struct Attn2Smem {
     static constexpr uint32_t kTile = (D / 64) * kBox;     // one 128-row tile of Q, K or V
@@ -105,55 +152,9 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Units.  Non-causal: query tiles numbered head-major (tile = head * nq +
-    // index), unit u below pair_units holding tiles 2u and 2u + 1 (adjacent tiles
-    // of one head: the host launches this kernel only for an even number of
-    // query tiles), each later unit one tile (A alone); the host makes the
-    // one-tile units the last of at most one per CTA, when the tiles do not
-    // divide evenly into pairs per CTA (13 pairs and a single rather than 14
-    // pairs on some CTAs).  Causal: units of tiles 2k and 2k + 1 of one head;
-    // tile A reads key blocks 0..2k, tile B 0..2k + 1 (every block the unit
-    // loads); a CTA takes them two at a time from one head, pair np - 1 - m and
-    // then pair m (np pairs per head, even: the host launches causal problems
-    // here only with a multiple of 4 query tiles per head), so every such step
-    // costs the same.  Units in flight share a few heads, whose K and V stay
-    // in L2.
     const int nblk = (p.S + kKeys - 1) / kKeys;    // key blocks per tile, non-causal
     const int np = p.nq >> 1;                       // pairs per head
     const int sp = np >> 1;                         // causal steps per head
-    struct UnitWalk {
-        int U, i;                                   // step (unit) index, unit within a causal step
-        // the next unit: head, tile A's index, key blocks of A and of B (0: A alone)
-        __device__ bool next(const AttnParams& p, int nblk, int np, int sp, int& bh, int& qa, int& na, int& nb) {
-            if (U >= p.units) return false;
-            if (!p.causal) {
-                const int u = U;
-                U += static_cast<int>(gridDim.x);
-                const bool two = u < p.pair_units;
-                const int tile = two ? 2 * u : 2 * p.pair_units + (u - p.pair_units);
-                bh = tile / p.nq;
-                qa = tile - bh * p.nq;
-                na = nblk;
-                nb = two ? nblk : 0;
-                return true;
-            }
-            bh = U / sp;
-            const int m = U - bh * sp;
-            int k;
-            if (i == 0) {
-                k = np - 1 - m;
-                i = 1;
-            } else {
-                k = m;
-                i = 0;
-                U += static_cast<int>(gridDim.x);
-            }
-            qa = 2 * k;
-            na = 2 * k + 1;
-            nb = 2 * k + 2;
-            return true;
-        }
-    };
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);

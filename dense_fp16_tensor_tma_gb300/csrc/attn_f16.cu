@@ -13,7 +13,7 @@
 #include <mutex>
 
 #include "attn_f16.h"
-#include "attn2_kernels.cuh"
+#include "attn3_kernels.cuh"
 
 #ifndef ATTN_PINGPONG
 #define ATTN_PINGPONG 1   // two query tiles per CTA where the problem allows it
@@ -23,6 +23,9 @@
 #endif
 #ifndef ATTN_CAUSAL_PAIRS
 #define ATTN_CAUSAL_PAIRS 1   // causal problems too
+#endif
+#ifndef ATTN_SPLIT_P
+#define ATTN_SPLIT_P 1   // D = 64: the two-tile kernel with P buffers of its own (attn_f16_fwd3_kernel)
 #endif
 
 namespace {
@@ -94,9 +97,15 @@ int init_device(int dev) {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(attn_f16_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  AttnSmem<128>::kDynamicBytes);
+#if ATTN_SPLIT_P
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attn_f16_fwd3_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Attn3Smem<64>::kDynamicBytes);
+#else
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(attn_f16_fwd2_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Attn2Smem<64>::kDynamicBytes);
+#endif
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(attn_f16_fwd2_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Attn2Smem<128>::kDynamicBytes);
@@ -135,11 +144,13 @@ int encode_3d(CUtensorMap* m, const void* ptr, int64_t D, int64_t S, int64_t BH)
 template <int D>
 cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const AttnParams& prm, int ctas,
                    bool two_tiles, cudaStream_t s) {
+    constexpr bool split_p = D == 64 && ATTN_SPLIT_P;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(ctas));
     cfg.blockDim = dim3(two_tiles ? kAttn2Threads : kAttnThreads);
-    cfg.dynamicSmemBytes = two_tiles ? Attn2Smem<D>::kDynamicBytes : AttnSmem<D>::kDynamicBytes;
+    if constexpr (split_p) cfg.dynamicSmemBytes = two_tiles ? Attn3Smem<D>::kDynamicBytes : AttnSmem<D>::kDynamicBytes;
+    else cfg.dynamicSmemBytes = two_tiles ? Attn2Smem<D>::kDynamicBytes : AttnSmem<D>::kDynamicBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     std::memset(attr, 0, sizeof(attr));
@@ -149,7 +160,11 @@ cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    if (two_tiles) return cudaLaunchKernelEx(&cfg, attn_f16_fwd2_kernel<D>, q, k, v, prm);
+    if constexpr (split_p) {
+        if (two_tiles) return cudaLaunchKernelEx(&cfg, attn_f16_fwd3_kernel<D>, q, k, v, prm);
+    } else {
+        if (two_tiles) return cudaLaunchKernelEx(&cfg, attn_f16_fwd2_kernel<D>, q, k, v, prm);
+    }
     return cudaLaunchKernelEx(&cfg, attn_f16_fwd_kernel<D>, q, k, v, prm);
 }
 
