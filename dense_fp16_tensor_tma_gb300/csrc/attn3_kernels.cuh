@@ -17,13 +17,21 @@
 // 0 and 128, P_A, P_B (fp16 pairs) at 256 and 320, O_A, O_B at 384 and 448:
 // all 512 columns, which is why this schedule is for D = 64 only.
 //
-// K and V blocks sit in rings of three slots; the MMA warp frees a slot by a
-// commit to its k_empty / v_empty barrier after the last MMA that reads it
-// (tile B's in a two-tile unit: B reads every block the unit loads, and its
-// MMAs are issued after A's), and frees the Q tiles by a commit to q_empty
-// after a unit's last S.  A unit's first P V overwrites O without a barrier of
-// its own: each softmax warp arrives on p_full of the unit's first block only
-// after it has read the previous unit's O out.  The protocol (every wait's
+// Each tile has an MMA warp of its own (warps 1 and 2): one warp issuing all
+// 24 MMAs of a block pair spent most of its time issuing (about 75 cycles an
+// MMA with its commits) and held back the other tile's next P V.  Per block a
+// tile's warp issues S of the next block (once the softmax has read this
+// block's) and then P V of this block; the tensor pipe runs each warp's MMAs
+// in order and may interleave the two warps'.  K and V blocks sit in rings of
+// three slots.  A commit covers only its own warp's MMAs, so a slot's k_empty
+// / v_empty barrier and the Q tiles' q_empty take one commit from each tile's
+// warp after its last MMA reading them; in a one-tile unit tile A's warp
+// commits twice, and in a causal unit, whose last block tile A does not read,
+// tile A's warp arrives for that block once it has landed (earlier, the
+// arrival could count toward the slot's previous block).  A unit's first P V
+// overwrites O without a barrier of its own: each softmax warp arrives on
+// p_full of the unit's first block only after it has read the previous
+// unit's O out.  The protocol (every wait's
 // phase, no deadlock, no write over data still to be read, planted defects
 // caught) is checked by a CPU model in tests/test_attn3_protocol_cpu.py.
 //
@@ -37,6 +45,7 @@
 namespace attn_dev {
 
 constexpr int kAttn3Stages = 3;
+constexpr int kAttn3Threads = 352;   // producer, two MMA warps, 2 x 4 softmax warps
 
 template <int D>
 struct Attn3Smem {
@@ -59,7 +68,7 @@ struct Attn3Smem {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kAttn2Threads, 1)
+__global__ void __launch_bounds__(kAttn3Threads, 1)
 attn_f16_fwd3_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
     static_assert(D == 64, "separate P buffers leave tensor memory for D = 64 only");
@@ -99,12 +108,12 @@ attn_f16_fwd3_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
+        mbar_init(q_empty, 2);                       // one commit from each tile's MMA warp
         for (int s = 0; s < kSt; ++s) {
             mbar_init(k_full(s), 1);
-            mbar_init(k_empty(s), 1);
+            mbar_init(k_empty(s), 2);
             mbar_init(v_full(s), 1);
-            mbar_init(v_empty(s), 1);
+            mbar_init(v_empty(s), 2);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(s_full(t), 1);
@@ -112,7 +121,7 @@ attn_f16_fwd3_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             mbar_init(p_full(t), 4);
             mbar_init(pv_done(t), 1);
         }
-        mbar_init(drain_bar, 1);
+        mbar_init(drain_bar, 2);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -189,44 +198,45 @@ attn_f16_fwd3_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                                   status, ROLE_DRAIN, which);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp <= 2) {
+        // ------------------------------------------------------------ MMA issuers, one per tile
         {
+            const int t = warp - 1;
             const uint64_t k_desc = smem_desc_sw128(sK, 0, 1024);
             const uint64_t v_desc = smem_desc_sw128(sV, kBox, 1024);   // MN-major, one 64-column box
+            const uint64_t qd = smem_desc_sw128(sQ + t * kTileBytes, 0, 1024);
+            const uint32_t s_tmem = tmem_base + kSCol + static_cast<uint32_t>(t * kKeys);
+            const uint32_t o_tmem = tmem_base + kOCol + static_cast<uint32_t>(t * D);
+            const uint32_t pa = tmem_base + kPCol + static_cast<uint32_t>(t * (kKeys / 2));
             constexpr uint32_t kSlotUnits = kTileBytes >> 4;
-            // S_t of loaded block rb (tile t's block tb) = Q_t K^T into t's score
-            // buffer; the commits free the K slot (last reader) and the Q tiles
-            // (the unit's last S)
-            auto issue_s = [&](int t, int rb, bool free_k, bool free_q) -> bool {
+            // S_t of loaded block rb = Q_t K^T into the tile's score buffer; the
+            // commits free the K slot and, after the tile's last S of the unit, the
+            // Q tiles (reps: 2 in a one-tile unit, arriving for tile B's warp too)
+            auto issue_s = [&](int rb, bool last_s, int reps) -> bool {
                 const int s = rb % kSt;
                 if (!mbar_wait_bounded(k_full(s), (rb / kSt) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_K))
                     return false;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + kSCol + static_cast<uint32_t>(t * kKeys);
-                const uint64_t qd = smem_desc_sw128(sQ + t * kTileBytes, 0, 1024);
                 const uint64_t kd = k_desc + static_cast<uint64_t>(s * kSlotUnits);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint64_t off = static_cast<uint64_t>((k * 32) >> 4);
-                    tc_mma_f16(d_tmem, qd + off, kd + off, kIdescS, k != 0 ? 1u : 0u);
+                    tc_mma_f16(s_tmem, qd + off, kd + off, kIdescS, k != 0 ? 1u : 0u);
                 }
                 tc_commit(s_full(t));
-                if (free_k) tc_commit(k_empty(s));
-                if (free_q) tc_commit(q_empty);
+                for (int r = 0; r < reps; ++r) tc_commit(k_empty(s));
+                if (last_s)
+                    for (int r = 0; r < reps; ++r) tc_commit(q_empty);
                 return true;
             };
-            // O_t += P_t V of loaded block rb (tile t's block tb; j: its index in
-            // the unit); the commits report it and free the V slot (last reader)
-            auto issue_pv = [&](int t, int rb, int tb, int j, bool free_v) -> bool {
+            // O_t += P_t V of loaded block rb (the tile's block tb, j-th of the unit)
+            auto issue_pv = [&](int rb, int tb, int j, int reps) -> bool {
                 const int s = rb % kSt;
                 if (!mbar_wait_bounded(p_full(t), tb & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_P))
                     return false;
                 if (!mbar_wait_bounded(v_full(s), (rb / kSt) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_V))
                     return false;
                 tc_fence_after();
-                const uint32_t o_tmem = tmem_base + kOCol + static_cast<uint32_t>(t * D);
-                const uint32_t pa = tmem_base + kPCol + static_cast<uint32_t>(t * (kKeys / 2));
                 const uint64_t vd = v_desc + static_cast<uint64_t>(s * kSlotUnits);
 #pragma unroll
                 for (int k = 0; k < kKeys / 16; ++k) {
@@ -235,45 +245,51 @@ attn_f16_fwd3_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                                   kIdescO, (j | k) != 0 ? 1u : 0u);
                 }
                 tc_commit(pv_done(t));
-                if (free_v) tc_commit(v_empty(s));
+                for (int r = 0; r < reps; ++r) tc_commit(v_empty(s));
                 return true;
             };
             bool ok = true;
-            int g = 0, nu = 0;
-            int gt[2] = {0, 0};          // blocks tile A and tile B read
+            int g = 0, gt = 0, nu = 0;   // blocks loaded, blocks this tile read, units
             UnitWalk walk{static_cast<int>(blockIdx.x), 0};
             int bh, qa, na, nb;
             while (ok && walk.next(p, nblk, np, sp, bh, qa, na, nb)) {
-                const int n[2] = {na, nb};
-                const int nt = nb > 0 ? 2 : 1;        // tiles of the unit; the last, nt - 1, reads every block
-                const int nr = n[nt - 1];
+                if (t == 1 && nb == 0) break;         // tile B's warp sits out the one-tile units
+                const int n = t == 0 ? na : nb;       // blocks this tile reads
+                const int nr = nb > 0 ? nb : na;      // blocks loaded
+                const int reps = nb > 0 ? 1 : 2;
                 ok = mbar_wait_bounded(q_full, nu & 1, p.timeout_ns, abort_flag, status, ROLE_MMA, BAR_Q);
-                if (ok) tc_fence_after();
-                for (int t = 0; ok && t < nt; ++t) {
-                    const bool last = t == nt - 1;
-                    ok = issue_s(t, g, last, last && n[t] == 1);
+                if (ok) {
+                    tc_fence_after();
+                    ok = issue_s(g, n == 1, reps);
                 }
-                for (int j = 0; ok && j < nr; ++j) {
+                for (int j = 0; ok && j < n; ++j) {
                     const int rb = g + j;
-                    // the next S of each tile, once its softmax warps have read this one
-                    for (int t = 0; ok && t < nt; ++t) {
-                        if (j + 1 >= n[t]) continue;
-                        ok = mbar_wait_bounded(s_free(t), (gt[t] + j) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA,
+                    // the next S, once the softmax warps have read this one
+                    if (j + 1 < n) {
+                        ok = mbar_wait_bounded(s_free(t), (gt + j) & 1, p.timeout_ns, abort_flag, status, ROLE_MMA,
                                                BAR_S);
                         if (ok) {
                             tc_fence_after();
-                            const bool last = t == nt - 1;
-                            ok = issue_s(t, rb + 1, last, last && j + 2 == n[t]);
+                            ok = issue_s(rb + 1, j + 2 == n, reps);
                         }
                     }
-                    for (int t = 0; ok && t < nt; ++t) {
-                        if (j >= n[t]) continue;       // tile A has no last block in a causal unit
-                        ok = issue_pv(t, rb, gt[t] + j, j, t == nt - 1);
+                    if (ok) ok = issue_pv(rb, gt + j, j, reps);
+                }
+                if (ok && n < nr) {
+                    // causal: tile A does not read the unit's last block; it arrives
+                    // for that block's ring slots once the block has landed
+                    const int lb = g + nr - 1;
+                    ok = mbar_wait_bounded(k_full(lb % kSt), (lb / kSt) & 1, p.timeout_ns, abort_flag, status,
+                                           ROLE_MMA, BAR_K) &&
+                         mbar_wait_bounded(v_full(lb % kSt), (lb / kSt) & 1, p.timeout_ns, abort_flag, status,
+                                           ROLE_MMA, BAR_V);
+                    if (ok) {
+                        tc_commit(k_empty(lb % kSt));
+                        tc_commit(v_empty(lb % kSt));
                     }
                 }
                 g += nr;
-                gt[0] += na;
-                gt[1] += nb;
+                gt += n;
                 ++nu;
             }
             tc_commit(drain_bar);
@@ -282,7 +298,7 @@ attn_f16_fwd3_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + output
-        const int t = (warp - 2) >> 2;               // query tile A (0) or B (1)
+        const int t = (warp - 3) >> 2;               // query tile A (0, warps 3..6) or B (1, warps 7..10)
         const int quarter = warp & 3;                // TMEM lanes 32 * quarter ..: this warp's rows
         const int r = 32 * quarter + lane;           // this thread's row of the tile
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
@@ -352,34 +368,32 @@ attn_f16_fwd3_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     m_new = fmaxf(m, bmax);
                     raise = m != -INFINITY && m_new != m;
                 }
-                // the P buffer is free, and O settled for a rescale, once the
-                // tile's previous P V has completed (a unit's first block: the
-                // previous unit's output already waited for its last one)
+                // P = 2^(x * scale_log2 - m) as fp16 pairs, all in registers (each
+                // pair replaces two scores), and its sum over the fp16 values the
+                // tensor core multiplies
+                const float mm = (m_new == -INFINITY) ? 0.0f : m_new;
+                float rs0 = 0.0f, rs1 = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    const float2 xs = fma2_bc(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), p.scale_log2, -mm);
+                    const __half2 hv = __floats2half2_rn(fast_exp2(xs.x), fast_exp2(xs.y));
+                    v[i] = *reinterpret_cast<const uint32_t*>(&hv);
+                    if (i & 1) rs1 = add_f16x2_to_f32(rs1, v[i]);
+                    else rs0 = add_f16x2_to_f32(rs0, v[i]);
+                }
+                // into the P buffer (keys 32c .. 32c + 31 at columns 16c ..) once the
+                // tile's previous P V, which reads it, has completed; O is then
+                // settled for a rescale too (a unit's first block: the previous
+                // unit's output already waited for its last P V)
                 if (j > 0) {
                     ok = mbar_wait_bounded(pv_done(t), (gb - 1) & 1, p.timeout_ns, abort_flag, status, ROLE_SOFTMAX,
                                            BAR_PV);
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                     tc_fence_after();
                 }
-                // P = 2^(x * scale_log2 - m) as fp16 pairs into the P buffer (keys
-                // 32c .. 32c + 31 into columns 16c ..), and its sum over the fp16
-                // values the tensor core multiplies
-                const float mm = (m_new == -INFINITY) ? 0.0f : m_new;
-                float rs0 = 0.0f, rs1 = 0.0f;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t h[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float2 xs = fma2_bc(__uint_as_float(v[32 * c + 2 * i]), __uint_as_float(v[32 * c + 2 * i + 1]),
-                                                  p.scale_log2, -mm);
-                        const __half2 hv = __floats2half2_rn(fast_exp2(xs.x), fast_exp2(xs.y));
-                        h[i] = *reinterpret_cast<const uint32_t*>(&hv);
-                        if (i & 1) rs1 = add_f16x2_to_f32(rs1, h[i]);
-                        else rs0 = add_f16x2_to_f32(rs0, h[i]);
-                    }
-                    tmem_st_32x32b_x16(p_cols + 16u * c, h);
-                }
+                for (int c = 0; c < 4; ++c)
+                    tmem_st_32x32b_x16(p_cols + 16u * c, *reinterpret_cast<const uint32_t(*)[16]>(v + 16 * c));
                 // O rescaled on a raise (which needs an earlier block of the unit)
                 if (__any_sync(0xffffffffu, raise)) {
                     const float alpha = raise ? fast_exp2(m - m_new) : 1.0f;

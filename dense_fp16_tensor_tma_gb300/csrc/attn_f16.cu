@@ -148,7 +148,7 @@ cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(ctas));
-    cfg.blockDim = dim3(two_tiles ? kAttn2Threads : kAttnThreads);
+    cfg.blockDim = dim3(!two_tiles ? kAttnThreads : split_p ? kAttn3Threads : kAttn2Threads);
     if constexpr (split_p) cfg.dynamicSmemBytes = two_tiles ? Attn3Smem<D>::kDynamicBytes : AttnSmem<D>::kDynamicBytes;
     else cfg.dynamicSmemBytes = two_tiles ? Attn2Smem<D>::kDynamicBytes : AttnSmem<D>::kDynamicBytes;
     cfg.stream = s;

@@ -8,9 +8,15 @@ of block j + 1 may overwrite the score buffer as soon as the tile's softmax
 warps have read S of block j into registers (they arrive on s_free), and it
 runs on the tensor core while they compute P of block j.  A softmax warp
 writes P of block j only once P V of block j - 1, which reads the P buffer,
-has completed (pv_done).  K and V sit in rings of three slots; the MMA warp
-frees a slot with a commit to its k_empty / v_empty barrier after the last
-MMA that reads it (tile B's in a two-tile unit, which reads every block).
+has completed (pv_done).  Each tile has an MMA warp of its own, whose MMAs the
+tensor pipe runs in order; the two warps' MMAs interleave in any order, and a
+commit arrives once its own warp's earlier MMAs have completed.  K and V sit in
+rings of three slots, each freed by one commit from each tile's warp to its
+k_empty / v_empty barrier (count two) after its last MMA reading the slot; in
+a one-tile unit tile A's warp commits twice, and in a causal unit tile A's
+warp arrives for the last block, which it does not read, once that block has
+landed.  The Q tiles are freed the same way (q_empty, after each tile's last
+S of the unit).
 
 Every role is written as the sequence of its mbarrier waits and arrivals in
 the kernel's order and with its phase arithmetic; a scheduler runs the roles,
@@ -24,9 +30,9 @@ of its own: each softmax warp arrives on p_full of a unit's first block only
 after reading the previous unit's O, so that P V's wait on p_full covers
 it), a K or V
 slot loaded while a queued MMA reads its previous block, Q reloaded under a
-queued S (the Q reload waits for q_empty, committed after a unit's last S:
-a single s_full barrier per tile could be up to three phases behind the
-producer).  Four planted defects must each fail.
+queued S (the Q reload waits for q_empty: a single s_full barrier per tile
+could be up to three phases behind the producer), an MMA reading a ring slot
+that holds another block.  Five planted defects must each fail.
 """
 import random
 
@@ -63,37 +69,45 @@ def run_protocol3(units, seed, nsoft=2, defect=None):
     (n, False) (tile A alone, last), or (a, b) with b = a + 1 (causal).
     `defect`: "s_before_free" (the next S issued without waiting for s_free),
     "p_unguarded" (P written without waiting for the previous P V),
-    "k_empty_a" (a K slot of a two-tile unit freed after tile A's S, not B's),
-    "q_unguarded" (Q reloaded without waiting for the previous unit's last S)."""
+    "k_empty_b_only" (tile A's MMA warp never arrives on k_empty, whose count
+    is still two), "q_unguarded" (Q reloaded without waiting for q_empty), or
+    "early_extra" (tile A's extra arrival for the last block of a causal unit,
+    which it does not read, made without waiting for that block's load)."""
     units = [(u, u) if isinstance(u, int) else (u[0], 0 if u[1] is False else u[1]) for u in units]
     assert all(b == 0 or b >= a for a, b in units)
     assert all(a[1] or not b[1] for a, b in zip(units, units[1:])), "one-tile units come last"
     rnd = random.Random(seed)
-    q_full, q_empty, drain = Barrier("q_full", 1), Barrier("q_empty", 1), Barrier("drain", 1)
+    q_full, q_empty, drain = Barrier("q_full", 1), Barrier("q_empty", 2), Barrier("drain", 2)
     k_full = [Barrier(f"k_full{i}", 1) for i in range(STAGES)]
     v_full = [Barrier(f"v_full{i}", 1) for i in range(STAGES)]
-    k_empty = [Barrier(f"k_empty{i}", 1) for i in range(STAGES)]
-    v_empty = [Barrier(f"v_empty{i}", 1) for i in range(STAGES)]
+    k_empty = [Barrier(f"k_empty{i}", 2) for i in range(STAGES)]
+    v_empty = [Barrier(f"v_empty{i}", 2) for i in range(STAGES)]
     s_full = {t: Barrier(f"s_full{t}", 1) for t in "AB"}
     s_free = {t: Barrier(f"s_free{t}", nsoft) for t in "AB"}
     p_full = {t: Barrier(f"p_full{t}", nsoft) for t in "AB"}
     pv_done = {t: Barrier(f"pv_done{t}", 1) for t in "AB"}
-    tma, pipe = [], []
+    tma = []
+    # tensor pipe: each MMA warp's operations complete in its issue order; the two
+    # warps' operations interleave in any order.  A commit arrives once every
+    # earlier operation of its warp has completed.
+    ops = {"A": [], "B": []}
     s_readers = {"A": 0, "B": 0}      # softmax warps reading each tile's score buffer
     reads = {"A": {}, "B": {}}        # per tile and unit: softmax warps that have read O out
     outputs_read = {"A": 0, "B": 0}   # units whose O every softmax warp of the tile has read out
     q_unit = [None]                   # the unit whose Q tiles shared memory holds (or is loading)
+    slot_block = {"k": [None] * STAGES, "v": [None] * STAGES}   # block each ring slot holds
 
     def wait(bar, index, who):
         return (bar, index & 1, who, index)
 
-    def queued(op, t=None, slot=None, before=None):
-        for e in pipe:
-            if e[0] != op or (t is not None and e[1] != t):
-                continue
-            if slot is not None and not (e[3] % STAGES == slot and e[3] < before):
-                continue
-            return True
+    def queued(kind, t=None, slot=None, before=None):
+        for w in "AB":
+            for e in ops[w]:
+                if e[0] != kind or (t is not None and e[1] != t):
+                    continue
+                if slot is not None and not (e[3] % STAGES == slot and e[3] < before):
+                    continue
+                return True
         return False
 
     def producer(is_k):
@@ -102,10 +116,10 @@ def run_protocol3(units, seed, nsoft=2, defect=None):
             nr = nb if nb else na
             if is_k:
                 if u > 0 and defect != "q_unguarded":
-                    # the previous unit's last S has read Q (a commit after it)
+                    # both tiles' last S of the previous unit have read Q
                     yield wait(q_empty, u - 1, "producer Q")
                     assert not queued("s"), "Q reloaded under a queued S"
-                q_unit[0] = u                         # the Q tiles in shared memory from here on
+                q_unit[0] = u
                 ntiles = 2 if nb else 1
                 q_full.arrive(tx=ntiles)
                 for _ in range(ntiles):
@@ -117,67 +131,75 @@ def run_protocol3(units, seed, nsoft=2, defect=None):
                     yield wait(k_empty[s] if is_k else v_empty[s], gb // STAGES - 1, "producer slot")
                 assert not queued("s" if is_k else "pv", slot=s, before=gb), \
                     f"{'K' if is_k else 'V'} block {gb} loaded into slot {s} under a queued MMA"
+                slot_block["k" if is_k else "v"][s] = gb
                 full = k_full[s] if is_k else v_full[s]
                 full.arrive(tx=1)
                 tma.append(full)
             g += nr
 
-    def mma():
-        g = 0
-        gt = {"A": 0, "B": 0}
-        nu = {"A": 0, "B": 0}
+    def mma(t):
+        """Tile t's MMA warp: the S and P V of every unit the tile takes part in,
+        per block S of the next block (once the softmax has read this one's)
+        before P V of this one."""
+        g = 0                      # blocks loaded
+        gt = 0                     # blocks this tile reads
+        nu = 0                     # units this tile took part in
 
-        def issue(op, t, tb, rb, commits, outputs_needed=None):
-            if op == "s":
+        def issue(kind, tb, rb, commits, outputs_needed=None, unit=None):
+            if kind == "s":
                 assert s_readers[t] == 0, f"S_{t} of block {tb} issued while a softmax warp reads the buffer"
-            pipe.append((op, t, tb, rb, commits, outputs_needed, unit[0]))
+            ops[t].append((kind, t, tb, rb, list(commits), outputs_needed, unit))
 
-        unit = [0]
+        def commit_now(bars):
+            # a commit arrives once the warp's earlier operations complete (at once if none)
+            if ops[t]:
+                ops[t][-1][4].extend(bars)
+            else:
+                for b in bars:
+                    b.arrive()
+
         for u, (na, nb) in enumerate(units):
-            unit[0] = u
-            n = {"A": na, "B": nb}
-            tiles = "AB" if nb else "A"
-            last = tiles[-1]                      # the last reader of every block of the unit
+            if t == "B" and not nb:
+                break                                  # tile B's MMA warp sits out the one-tile units
+            n = na if t == "A" else nb
             nr = max(na, nb)
-            yield wait(q_full, u, "mma Q")
-            yield wait(k_full[g % STAGES], g // STAGES, "mma K")
-            for t in tiles:
-                commits = [s_full[t]]
-                k_last = "A" if defect == "k_empty_a" else last
-                if t == k_last:
-                    commits.append(k_empty[g % STAGES])
-                if n[t] == 1 and t == last:
-                    commits.append(q_empty)           # the unit's last S
-                issue("s", t, gt[t], g, commits)
-            for j in range(nr):
+            reps = 2 if nb == 0 else 1                 # a one-tile unit: tile A arrives for both warps
+            yield wait(q_full, u, f"mma{t} Q")
+
+            def s_commits(j):
+                c = [s_full[t]]
+                if not (defect == "k_empty_b_only" and t == "A"):
+                    c += [k_empty[(g + j) % STAGES]] * reps
+                if j == n - 1:
+                    c += [q_empty] * reps              # the tile's last S of the unit has read Q
+                return c
+
+            yield wait(k_full[g % STAGES], g // STAGES, f"mma{t} K")
+            issue("s", gt, g, s_commits(0), unit=u)
+            for j in range(n):
                 rb = g + j
-                for t in tiles:
-                    if j + 1 < n[t]:
-                        if defect != "s_before_free":
-                            yield wait(s_free[t], gt[t] + j, f"mma S{t} free")
-                        yield wait(k_full[(rb + 1) % STAGES], (rb + 1) // STAGES, "mma K")
-                        commits = [s_full[t]]
-                        k_last = "A" if defect == "k_empty_a" else last
-                        if t == k_last:
-                            commits.append(k_empty[(rb + 1) % STAGES])
-                        if j + 2 == n[t] and t == last:
-                            commits.append(q_empty)   # the unit's last S
-                        issue("s", t, gt[t] + j + 1, rb + 1, commits)
-                for t in tiles:
-                    if j < n[t]:
-                        yield wait(p_full[t], gt[t] + j, f"mma P{t}")
-                        yield wait(v_full[rb % STAGES], rb // STAGES, "mma V")
-                        commits = [pv_done[t]]
-                        if t == last:
-                            commits.append(v_empty[rb % STAGES])
-                        # a unit's first P V overwrites O: every earlier output must be read out
-                        issue("pv", t, gt[t] + j, rb, commits, nu[t] if j == 0 else None)
+                if j + 1 < n:
+                    if defect != "s_before_free":
+                        yield wait(s_free[t], gt + j, f"mma{t} S free")
+                    yield wait(k_full[(rb + 1) % STAGES], (rb + 1) // STAGES, f"mma{t} K")
+                    issue("s", gt + j + 1, rb + 1, s_commits(j + 1), unit=u)
+                yield wait(p_full[t], gt + j, f"mma{t} P")
+                yield wait(v_full[rb % STAGES], rb // STAGES, f"mma{t} V")
+                issue("pv", gt + j, rb, [pv_done[t]] + [v_empty[rb % STAGES]] * reps, nu if j == 0 else None)
+            if n < nr:
+                # causal: tile A does not read the unit's last block; it arrives for
+                # that block's slots once the block has landed (an earlier arrival
+                # could count toward the slot's previous block)
+                lb = g + nr - 1
+                if defect != "early_extra":
+                    yield wait(k_full[lb % STAGES], lb // STAGES, f"mma{t} K extra")
+                    yield wait(v_full[lb % STAGES], lb // STAGES, f"mma{t} V extra")
+                commit_now([k_empty[lb % STAGES], v_empty[lb % STAGES]])
             g += nr
-            for t in tiles:
-                gt[t] += n[t]
-                nu[t] += 1
-        pipe.append(("drain", None, None, -1, [drain], None, None))
-        yield wait(drain, 0, "mma drain")
+            gt += n
+            nu += 1
+        commit_now([drain])
+        yield wait(drain, 0, f"mma{t} drain")
 
     def softmax(t):
         g = 0
@@ -208,7 +230,7 @@ def run_protocol3(units, seed, nsoft=2, defect=None):
                 outputs_read[t] += 1
             g += n
 
-    roles = [producer(True), producer(False), mma()] + [softmax(t) for t in "AB" for _ in range(nsoft)]
+    roles = [producer(True), producer(False), mma("A"), mma("B")] + [softmax(t) for t in "AB" for _ in range(nsoft)]
     current = [None] * len(roles)
     live = [True] * len(roles)
     for _ in range(2_000_000):
@@ -226,8 +248,9 @@ def run_protocol3(units, seed, nsoft=2, defect=None):
                 ready.append(("role", i))
         if tma:
             ready.append(("tma", None))
-        if pipe:
-            ready.append(("pipe", None))
+        for w in "AB":
+            if ops[w]:
+                ready.append(("pipe", w))
         if not ready:
             stuck = [f"{current[i][2]} on {current[i][0].name}" for i in range(len(roles)) if live[i]]
             assert not stuck, "deadlock: " + "; ".join(stuck)
@@ -236,10 +259,13 @@ def run_protocol3(units, seed, nsoft=2, defect=None):
         if kind == "tma":
             tma.pop(rnd.randrange(len(tma))).complete_tx(1)
         elif kind == "pipe":
-            op, t, tb, rb, commits, outputs_needed, u = pipe.pop(0)     # in issue order
+            op, t, tb, rb, commits, outputs_needed, u = ops[i].pop(0)     # this warp's oldest operation
             if op == "s":
                 assert s_readers[t] == 0, f"S_{t} of block {tb} overwrote a score buffer a softmax still reads"
                 assert q_unit[0] == u, f"S_{t} of unit {u} read the Q tiles of unit {q_unit[0]}"
+                assert slot_block["k"][rb % STAGES] == rb, f"S_{t} read K slot {rb % STAGES} holding another block"
+            if op == "pv":
+                assert slot_block["v"][rb % STAGES] == rb, f"P V_{t} read V slot {rb % STAGES} holding another block"
             if outputs_needed is not None:
                 assert outputs_read[t] >= outputs_needed, f"P V of tile {t} overwrote O before it was read out"
             for bar in commits:
@@ -264,8 +290,10 @@ def test_attention3_barrier_protocol(units):
         run_protocol3(units, seed)
 
 
-@pytest.mark.parametrize("defect", ["s_before_free", "p_unguarded", "k_empty_a", "q_unguarded"])
-def test_attention3_model_catches_planted_defects(defect):
+@pytest.mark.parametrize("defect,units", [("s_before_free", [4, 4, 3]), ("p_unguarded", [4, 4, 3]),
+                                          ("k_empty_b_only", [4, 4, 3]), ("q_unguarded", [4, 4, 3]),
+                                          ("early_extra", [(5, 6), (1, 2), (3, 4)])])
+def test_attention3_model_catches_planted_defects(defect, units):
     with pytest.raises(AssertionError):
-        for seed in range(100):
-            run_protocol3([4, 4, 3], seed, defect=defect)
+        for seed in range(200):
+            run_protocol3(units, seed, defect=defect)

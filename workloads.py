@@ -195,4 +195,6 @@ ATTN_WORKLOADS = {
     "attn_ragged_causal": AttnWorkload("attn_ragged_causal", 2, 3, 1000, 128, True, 12, "full"),
     "attn_prefill": AttnWorkload("attn_prefill", 4, 32, 4096, 128, False, 13, "sampled"),
     "attn_prefill_causal": AttnWorkload("attn_prefill_causal", 4, 32, 4096, 128, True, 14, "sampled"),
+    "attn_prefill_d64": AttnWorkload("attn_prefill_d64", 4, 32, 4096, 64, False, 15, "sampled"),
+    "attn_prefill_d64_causal": AttnWorkload("attn_prefill_d64_causal", 4, 32, 4096, 64, True, 16, "sampled"),
 }
