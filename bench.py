@@ -59,6 +59,7 @@ def log(*a):
 
 
 ATTN_SOURCES = ("dense_fp16_tensor_tma_gb300/csrc/attn_kernels.cuh",
+                "dense_fp16_tensor_tma_gb300/csrc/attn4_kernels.cuh",
                 "dense_fp16_tensor_tma_gb300/csrc/attn2_kernels.cuh",
                 "dense_fp16_tensor_tma_gb300/csrc/attn3_kernels.cuh",
                 "dense_fp16_tensor_tma_gb300/csrc/attn_f16.cu",
@@ -100,7 +101,7 @@ def attn_kernel_name(w, sms: int) -> str:
     balanced = 2 * -(-steps // sms) * (80 if w.D == 64 else 85) < 100 * -(-2 * steps // sms)
     if nq % 2 == 0 and (not w.causal or (nq % 4 == 0 and nq >= 12 and steps >= sms and balanced)):
         return "attn_f16_fwd3_kernel<64>" if w.D == 64 else f"attn_f16_fwd2_kernel<{w.D}>"
-    return f"attn_f16_fwd_kernel<{w.D}>"
+    return f"attn_f16_fwd4_kernel<{w.D}>"
 
 
 def kernel_name(plan):

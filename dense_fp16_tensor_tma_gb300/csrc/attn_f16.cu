@@ -1,6 +1,7 @@
 // C-ABI boundary of the attention forward (declared in include/attn_f16.h):
 // argument checks, device check, 3-D TMA tensor maps over (D, S, B*H), and
-// the launch of attn_f16_fwd_kernel on the caller's stream.
+// and the launch of the attention kernel the problem's shape selects on the
+// caller's stream.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -14,6 +15,7 @@
 
 #include "attn_f16.h"
 #include "attn3_kernels.cuh"
+#include "attn4_kernels.cuh"
 
 #ifndef ATTN_PINGPONG
 #define ATTN_PINGPONG 1   // two query tiles per CTA where the problem allows it
@@ -92,11 +94,11 @@ int init_device(int dev) {
             return cuda_fail(e != cudaSuccess ? e : cudaErrorSymbolNotFound);
         g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    e = cudaFuncSetAttribute(attn_f16_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             AttnSmem<64>::kDynamicBytes);
+    e = cudaFuncSetAttribute(attn_f16_fwd4_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Attn4Smem<64>::kDynamicBytes);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(attn_f16_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 AttnSmem<128>::kDynamicBytes);
+        e = cudaFuncSetAttribute(attn_f16_fwd4_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Attn4Smem<128>::kDynamicBytes);
 #if ATTN_SPLIT_P
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(attn_f16_fwd3_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -145,12 +147,14 @@ template <int D>
 cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const AttnParams& prm, int ctas,
                    bool two_tiles, cudaStream_t s) {
     constexpr bool split_p = D == 64 && ATTN_SPLIT_P;
+    constexpr int one_threads = kAttn4Threads;
+    constexpr uint32_t one_smem = Attn4Smem<D>::kDynamicBytes;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(ctas));
-    cfg.blockDim = dim3(!two_tiles ? kAttnThreads : split_p ? kAttn3Threads : kAttn2Threads);
-    if constexpr (split_p) cfg.dynamicSmemBytes = two_tiles ? Attn3Smem<D>::kDynamicBytes : AttnSmem<D>::kDynamicBytes;
-    else cfg.dynamicSmemBytes = two_tiles ? Attn2Smem<D>::kDynamicBytes : AttnSmem<D>::kDynamicBytes;
+    cfg.blockDim = dim3(!two_tiles ? one_threads : split_p ? kAttn3Threads : kAttn2Threads);
+    if constexpr (split_p) cfg.dynamicSmemBytes = two_tiles ? Attn3Smem<D>::kDynamicBytes : one_smem;
+    else cfg.dynamicSmemBytes = two_tiles ? Attn2Smem<D>::kDynamicBytes : one_smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     std::memset(attr, 0, sizeof(attr));
@@ -165,7 +169,7 @@ cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap
     } else {
         if (two_tiles) return cudaLaunchKernelEx(&cfg, attn_f16_fwd2_kernel<D>, q, k, v, prm);
     }
-    return cudaLaunchKernelEx(&cfg, attn_f16_fwd_kernel<D>, q, k, v, prm);
+    return cudaLaunchKernelEx(&cfg, attn_f16_fwd4_kernel<D>, q, k, v, prm);
 }
 
 }  // namespace

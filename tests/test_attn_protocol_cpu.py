@@ -1,6 +1,7 @@
 """A model of the attention kernel's barrier protocol, run on the CPU.
 
-Each role of attn_f16_fwd_kernel (csrc/attn_kernels.cuh) is written here as
+Each role of the one-tile attention kernel attn_f16_fwd4_kernel
+(csrc/attn4_kernels.cuh) is written here as
 the sequence of its mbarrier waits, arrivals, expect-tx arrivals, TMA loads
 and tensor-core commits, in the kernel's order and with its phase-parity
 arithmetic; a scheduler runs the roles, the TMA completions (any order) and
@@ -71,7 +72,6 @@ def run_protocol(tiles, seed, nsoft=2, misnumbered_producer=False):
     s_full = [Barrier(f"s_full{i}", 1) for i in range(2)]
     p_full = [Barrier(f"p_full{i}", nsoft) for i in range(2)]
     pv_done = [Barrier(f"pv_done{i}", 1) for i in range(2)]
-    xch = [Barrier(f"xch{i}", nsoft) for i in range(2)]
     tma, pipe = [], []
 
     def wait(bar, index, who):
@@ -128,25 +128,18 @@ def run_protocol(tiles, seed, nsoft=2, misnumbered_producer=False):
         yield wait(drain, 0, "mma drain")
 
     def softmax():
-        g = x = 0
+        g = 0
         for qt, nblk in tiles:
             for j in range(nblk):
                 gb = g + j
                 s = gb & 1
                 yield wait(s_full[s], gb >> 1, "softmax S")
-                slot, use = x & 1, x >> 1
-                x += 1
-                xch[slot].arrive()
-                yield wait(xch[slot], use, "softmax exchange")
+                yield None                           # S read, P computed in registers
                 if j >= 1 and rnd.random() < 0.3:   # a raise of the running maximum
                     yield wait(pv_done[(gb - 1) & 1], (gb - 1) >> 1, "softmax rescale")
                 p_full[s].arrive()
             gl = g + nblk - 1
             yield wait(pv_done[gl & 1], gl >> 1, "softmax output")
-            slot, use = x & 1, x >> 1
-            x += 1
-            xch[slot].arrive()
-            yield wait(xch[slot], use, "softmax row sum")
             o_free.arrive()
             g += nblk
 
