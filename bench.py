@@ -93,13 +93,13 @@ def attn_kernel_name(w, sms: int) -> str:
     """Problems with an even number of 128-row query tiles run the two-tile
     kernel (two query tiles per CTA, softmax of one overlapping the other's
     MMAs; at D = 64 with P buffers of their own, so the next S overlaps the
-    softmax), causal ones with a multiple of 4 tiles per head, at least 12, a
+    softmax), causal ones with a multiple of 4 tiles per head, at least 8, a
     step of two tile pairs per SM and steps that split over the SMs no worse
     than the one-tile kernel's units; the rest run the one-tile kernel."""
     nq = (w.S + 127) // 128
     steps = w.B * w.H * (nq // 4)
-    balanced = 2 * -(-steps // sms) * (80 if w.D == 64 else 85) < 100 * -(-2 * steps // sms)
-    if nq % 2 == 0 and (not w.causal or (nq % 4 == 0 and nq >= 12 and steps >= sms and balanced)):
+    balanced = 2 * -(-steps // sms) * (75 if w.D == 64 else 92) < 100 * -(-2 * steps // sms)
+    if nq % 2 == 0 and (not w.causal or (nq % 4 == 0 and nq >= 8 and steps >= sms and balanced)):
         return "attn_f16_fwd3_kernel<64>" if w.D == 64 else f"attn_f16_fwd2_kernel<{w.D}>"
     return f"attn_f16_fwd4_kernel<{w.D}>"
 

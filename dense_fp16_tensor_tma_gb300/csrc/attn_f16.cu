@@ -21,7 +21,7 @@
 #define ATTN_PINGPONG 1   // two query tiles per CTA where the problem allows it
 #endif
 #ifndef ATTN_CAUSAL_MIN_TILES
-#define ATTN_CAUSAL_MIN_TILES 12   // causal heads of fewer query tiles run one tile per CTA
+#define ATTN_CAUSAL_MIN_TILES 8   // causal heads of fewer query tiles run one tile per CTA
 #endif
 #ifndef ATTN_CAUSAL_PAIRS
 #define ATTN_CAUSAL_PAIRS 1   // causal problems too
@@ -218,22 +218,24 @@ int attn_f16_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B
     // pairing would only halve the parallelism).
     const int sms = g_dev[dev].sms;
     // An even number of query tiles: two tiles per CTA whose softmax and MMAs
-    // interleave (attn_f16_fwd2_kernel).  Causal: with a multiple of 4 tiles
-    // per head (an even number of pairs, so every step of two pairs costs the
-    // same; with an odd number the cheaper one-pair steps fell on the same CTAs:
-    // 4x32x1792x128 827 against 935 TFLOP/s one tile per CTA), from 12 tiles
-    // per head (8: 725 against 729, 4: 484 against 489, 12: 856 against 764),
-    // with at least one step per SM, and only where the busiest CTA's steps
-    // cost less than its share of the one-tile kernel's units (tiles k and
-    // nq - 1 - k, half a step's key blocks each).  A key block of the two-tile
-    // kernel took 0.85 (D = 128) and 0.80 (D = 64) of the one-tile kernel's time
-    // where both split evenly (4x32x4096, 4x32x1536); 2x32x1500x64 (192 steps:
-    // 2 on some CTAs, against 3 units) ran 390 against 412 TFLOP/s.  Otherwise
-    // one tile per CTA.
+    // interleave (attn_f16_fwd2_kernel; at D = 64 attn_f16_fwd3_kernel).
+    // Causal (same-box A/B against the one-tile kernel, attn_f16_fwd4_kernel,
+    // which pairs tiles k and nq - 1 - k, so its units cost half a step each):
+    // with a multiple of 4 tiles per head (an even number of pairs, so every
+    // step of two pairs costs the same; with an odd number the cheaper one-pair
+    // steps fell on the same CTAs: 4x32x1792x128 827 against 935 TFLOP/s), from
+    // 8 tiles per head (4x32x1024: 687 against 627 at D = 128, 574 against 414
+    // at D = 64), with at least one step per SM, and only where the busiest
+    // CTA's steps cost less than its share of the one-tile kernel's units.  A
+    // key block of the two-tile kernels took 0.92 (D = 128) and 0.75 (D = 64)
+    // of the one-tile kernel's time where both split evenly (4x32x4096 413.1
+    // against 450.7 us and 285.5 against 391.1 us, 1x32x16384 0.94 and 0.75);
+    // 4x32x2048x128 (512 steps: 4 on some CTAs, against 7 units) ran 984
+    // against 999.  Otherwise one tile per CTA.
     const int64_t causal_steps = B * H * (nq / 4);
     const int64_t steps_busiest = (causal_steps + sms - 1) / sms;
     const int64_t units1_busiest = (2 * causal_steps + sms - 1) / sms;
-    const int64_t block_cost_pct = D == 64 ? 80 : 85;
+    const int64_t block_cost_pct = D == 64 ? 75 : 92;
     const bool two_tiles = ATTN_PINGPONG && nq % 2 == 0 &&
                            (!causal || (ATTN_CAUSAL_PAIRS && nq % 4 == 0 && nq >= ATTN_CAUSAL_MIN_TILES &&
                                         causal_steps >= static_cast<int64_t>(sms) &&

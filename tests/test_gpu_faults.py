@@ -135,12 +135,16 @@ def _attn_inputs(torch, dev, shape, seed):
     return (Q, K, V), [torch.from_numpy(x).to(dev) for x in (Q, K, V)]
 
 
-# (1,1,256,64): the two-tile kernel with one-tile units only; (4,40,256,64): its
-# two-tile units then one-tile units (152 + 16); (1,76,2048,64) causal: its
-# causal pairs (16 tiles per head, 304 steps); (1,2,384,128) causal: the
-# one-tile kernel (3 tiles per head)
+# D = 64, the two-tile kernel with P buffers of its own: (1,1,256,64) with
+# one-tile units only; (4,40,256,64) two-tile units then one-tile units
+# (152 + 16); (1,76,2048,64) causal pairs (16 tiles per head, 304 steps).
+# D = 128, the two-tile kernel with P over the scores: the same two non-causal
+# cases and (1,76,1024,128) causal pairs (8 tiles per head, 152 steps).
+# (1,2,384,128) causal: the one-tile kernel (3 tiles per head).
 @pytest.mark.parametrize("shape,causal", [((1, 1, 256, 64), False), ((4, 40, 256, 64), False),
-                                          ((1, 76, 2048, 64), True), ((1, 2, 384, 128), True)])
+                                          ((1, 76, 2048, 64), True), ((1, 1, 256, 128), False),
+                                          ((4, 40, 256, 128), False), ((1, 76, 1024, 128), True),
+                                          ((1, 2, 384, 128), True)])
 def test_attention_skipped_key_block_times_out_and_the_context_survives(env, shape, causal):
     torch, dev, g, oracle = env
     (Q, K, V), (tq, tk, tv) = _attn_inputs(torch, dev, shape, 3)
