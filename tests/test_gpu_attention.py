@@ -59,7 +59,7 @@ def test_attention_workloads_full(g, torch_dev, oracle_mod, name):
 
 
 @pytest.mark.parametrize("name", ["attn_prefill", "attn_prefill_causal", "attn_prefill_d64",
-                                  "attn_prefill_d64_causal"])
+                                  "attn_prefill_d64_causal", "attn_odd_causal"])
 def test_attention_prefill_sampled_rows(g, torch_dev, oracle_mod, name):
     w = workloads.ATTN_WORKLOADS[name]
     Q, K, V = w.make()

@@ -197,4 +197,6 @@ ATTN_WORKLOADS = {
     "attn_prefill_causal": AttnWorkload("attn_prefill_causal", 4, 32, 4096, 128, True, 14, "sampled"),
     "attn_prefill_d64": AttnWorkload("attn_prefill_d64", 4, 32, 4096, 64, False, 15, "sampled"),
     "attn_prefill_d64_causal": AttnWorkload("attn_prefill_d64_causal", 4, 32, 4096, 64, True, 16, "sampled"),
+    # an odd number of query tiles per head (11): the one-tile kernel, causal pairs
+    "attn_odd_causal": AttnWorkload("attn_odd_causal", 8, 16, 1300, 128, True, 17, "sampled"),
 }
