@@ -44,13 +44,13 @@ namespace attn_dev {
 
 constexpr int kAttn2Threads = 320;   // producer, MMA, 2 x 4 softmax warps
 
-// Units of the two-tile kernels.  Non-causal: query tiles numbered head-major
-// (tile = head * nq + index), unit u below pair_units holding tiles 2u and
-// 2u + 1 (adjacent tiles of one head: the host launches these kernels only for
-// an even number of query tiles), each later unit one tile (A alone); the host
-// makes the one-tile units the last of at most one per CTA, when the tiles do
-// not divide evenly into pairs per CTA (13 pairs and a single rather than 14
-// pairs on some CTAs).  Causal: units of tiles 2k and 2k + 1 of one head; tile
+// Units of the two-tile kernels.  Non-causal: a head's query tiles form pairs
+// (2k, 2k + 1), numbered head-major; unit u below pair_units holds pair u, each
+// later unit one tile (A alone): first the tiles of the pairs not taken as
+// pairs, then, with an odd number of tiles per head, each head's last tile.
+// The host takes the pairs in whole rounds over the CTAs and leaves the rest
+// as one-tile units when they fit one per CTA (13 pairs and a single rather
+// than 14 pairs on some CTAs).  Causal: units of tiles 2k and 2k + 1 of one head; tile
 // A reads key blocks 0..2k, tile B 0..2k + 1 (every block the unit loads); a
 // CTA takes them two at a time from one head, pair np - 1 - m and then pair m
 // (np pairs per head, even: the host launches causal problems here only with a
@@ -65,12 +65,27 @@ struct UnitWalk {
         if (!p.causal) {
             const int u = U;
             U += static_cast<int>(gridDim.x);
-            const bool two = u < p.pair_units;
-            const int tile = two ? 2 * u : 2 * p.pair_units + (u - p.pair_units);
-            bh = tile / p.nq;
-            qa = tile - bh * p.nq;
+            const int pph = p.nq >> 1;                  // pairs (2k, 2k + 1) per head
             na = nblk;
-            nb = two ? nblk : 0;
+            if (u < p.pair_units) {                     // pair u
+                bh = u / pph;
+                qa = 2 * (u - bh * pph);
+                nb = nblk;
+                return true;
+            }
+            // the tiles of the pairs not taken as pairs, then (odd nq) each
+            // head's last tile
+            nb = 0;
+            const int s = u - p.pair_units;
+            const int split = 2 * (p.BH * pph - p.pair_units);
+            if (s < split) {
+                const int pi = p.pair_units + (s >> 1);
+                bh = pi / pph;
+                qa = 2 * (pi - bh * pph) + (s & 1);
+            } else {
+                bh = s - split;
+                qa = p.nq - 1;
+            }
             return true;
         }
         bh = U / sp;

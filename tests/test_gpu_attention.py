@@ -70,18 +70,21 @@ def test_attention_prefill_sampled_rows(g, torch_dev, oracle_mod, name):
 
 
 # ---------------------------------------------------------------- many tiles per CTA
-# More query tiles than SMs, so every CTA walks several tiles.  An even tile
-# count runs two tiles per CTA (causal with a multiple of 4 tiles per head, at
-# least 8: adjacent pairs, two pairs of a head per step; S 1500: 12 tiles,
-# S 1000: 8, the last partial);
-# otherwise one tile per CTA, causal tiles paired nq - 1 - k with k (S 1300: 11
-# tiles, the middle one alone); ragged S makes every head's last tile partial.
+# More query tiles than SMs, so every CTA walks several tiles.  Non-causal
+# problems run two tiles per CTA (S 2100: 17 tiles per head, the last one
+# alone; S 1300: 11 tiles, alone at D = 64, one tile per CTA at D = 128);
+# causal ones too with a multiple of 4 tiles per head, at least 8 (adjacent
+# pairs, two pairs of a head per step; S 1500: 12 tiles, S 1000: 8, the last
+# partial); otherwise one tile per CTA, causal tiles paired nq - 1 - k with k
+# (S 1300: 11 tiles, the middle one alone); ragged S makes every head's last
+# tile partial.
 
 @pytest.mark.parametrize("B,H,S,D,causal", [(4, 32, 1300, 128, True), (4, 32, 1300, 64, True),
                                             (8, 16, 1000, 128, False), (8, 24, 700, 64, True),
                                             (4, 32, 4096, 64, True), (4, 32, 4096, 64, False),
                                             (16, 16, 1024, 128, False), (4, 32, 1500, 64, True),
-                                            (2, 76, 1000, 128, True)])
+                                            (2, 76, 1000, 128, True), (4, 32, 1300, 128, False),
+                                            (4, 32, 1300, 64, False), (4, 16, 2100, 128, False)])
 def test_attention_many_tiles_per_cta_sampled_rows(g, torch_dev, oracle_mod, B, H, S, D, causal):
     rng = np.random.default_rng(S + D + 7 * causal)
     Q, K, V = qkv(rng, (B, H, S, D))
