@@ -1,0 +1,81 @@
+"""Seeded random attention problems on the GPU against the fp64 oracle.
+
+The host routes each problem to one of three kernels (one query tile per
+CTA; two tiles per CTA with P over the scores at D = 128; two tiles with P
+buffers of their own at D = 64), chooses how many tile pairs to form and,
+causal, whether to pair steps of a head; those choices turn on the batch and
+head counts, the number of 128-row query tiles per head (odd or even, a
+multiple of 4 or not, ragged last tile) and the SM count.  Forty problems
+drawn over those dimensions, and eight causal ones aimed at the two-tile path,
+exercise the combinations a fixed list misses.
+Bar: the oracle.compare tolerance on sampled rows (each head's first and last
+query tile rows and a seeded sample), and every output row written (O starts
+as NaN).  Inputs: seeded normal fp16 Q, K, V.
+"""
+import numpy as np
+import pytest
+
+from oracle.compare import parity
+
+pytestmark = pytest.mark.gpu
+
+
+def problems(count=40, seed=2024):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        S = int(rng.choice([int(rng.integers(1, 400)), int(rng.integers(400, 1800)), int(rng.integers(1800, 3200))]))
+        D = int(rng.choice([64, 128]))
+        causal = bool(rng.integers(0, 2))
+        # batch x heads from a handful of heads to a few hundred, capped so a
+        # problem stays under ~0.4 GB of inputs
+        bh_cap = max(1, int(2e8 // (S * D * 2 * 3)))
+        bh = int(min(bh_cap, rng.choice([int(rng.integers(1, 8)), int(rng.integers(8, 160)),
+                                         int(rng.integers(160, 400))])))
+        B = int(rng.integers(1, 5))
+        H = max(1, bh // B)
+        out.append((B, H, S, D, causal))
+    # causal problems aimed at the two-tile path: a multiple of 4 query tiles
+    # per head (the last one ragged) and enough heads for a step per SM
+    for _ in range(count // 5):
+        nq = 4 * int(rng.integers(2, 7))
+        S = 128 * nq - int(rng.integers(0, 128))
+        D = int(rng.choice([64, 128]))
+        bh = int(rng.integers(152 // (nq // 4) + 1, max(152 // (nq // 4) + 2, int(2e8 // (S * D * 2 * 3)))))
+        B = int(rng.integers(1, 5))
+        out.append((B, max(1, bh // B), S, D, True))
+    return out
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import dense_fp16_tensor_tma_gb300 as g
+    return torch, torch.device("cuda:0"), g
+
+
+@pytest.mark.parametrize("case", list(enumerate(problems())), ids=lambda c: "B{1[0]}H{1[1]}S{1[2]}D{1[3]}{2}".format(
+    c[0], c[1], "c" if c[1][4] else "n"))
+def test_random_attention_problem(env, oracle_mod, case):
+    torch, dev, g = env
+    i, (B, H, S, D, causal) = case
+    rng = np.random.default_rng(1000 + i)
+    Q, K, V = (rng.standard_normal((B, H, S, D)).astype(np.float16) for _ in range(3))
+    tq, tk, tv = (torch.from_numpy(x).to(dev) for x in (Q, K, V))
+    O = torch.full(tq.shape, float("nan"), dtype=torch.float16, device=dev)
+    g.attn_f16_fwd(tq, tk, tv, O, causal)
+    st, word = g.attn_f16_debug_status()
+    assert st == 0, f"device status {st} word {word:#x}"
+    got = O.cpu().numpy().reshape(-1, D)
+    assert np.isfinite(got).all(), "a query row was never written"
+    heads = B * H
+    picks = []
+    for h in sorted({0, heads // 2, heads - 1}):
+        for r in (0, min(127, S - 1), max(0, S - 128), S - 1):
+            picks.append(h * S + r)
+    rows = np.unique(np.concatenate([np.array(picks, np.int64), rng.integers(0, heads * S, 96)]))
+    ref = oracle_mod.attention_rows(Q, K, V, causal, 1.0 / np.sqrt(D), rows)
+    res = parity(got[rows], ref)
+    assert res["ok"], f"B{B} H{H} S{S} D{D} causal={causal}: {res}"
