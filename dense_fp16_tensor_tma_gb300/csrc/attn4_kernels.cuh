@@ -95,9 +95,10 @@ attn_f16_fwd4_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 
     // Work units in head-major order: unit u is query tile nq - 1 - u % nq of
     // head u / nq (causal: the heaviest tiles of a head first), or, when causal
-    // tiles are paired, tiles nq - 1 - k and k of head u / npairs (k = u %
-    // npairs; the middle tile of an odd count alone), so that every unit costs
-    // the same nq + 1 key blocks.  The units in flight belong to a few heads,
+    // tiles are paired, tiles nq - 1 - k and k of a head, so that every unit
+    // costs the same nq + 1 key blocks, the pairs of every head first and then,
+    // with an odd nq, each head's middle tile alone (half a unit: dealt last,
+    // they fall on the CTAs with one pair fewer).  The units in flight belong to a few heads,
     // whose K and V stay in L2 (ordering by tile across heads made every query
     // tile read its head's K and V from HBM again: 7.4 GB per launch at B 4,
     // H 32, S 4096, D 128).
@@ -109,15 +110,18 @@ attn_f16_fwd4_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             qt = p.nq - 1 - u % p.nq;
             return true;
         }
-        const int npairs = (p.nq + 1) >> 1;
-        bh = u / npairs;
-        const int k = u % npairs;
-        if (i == 0) {
-            qt = p.nq - 1 - k;
+        // pairs of every head first, then (odd nq) each head's middle tile
+        const int hp = p.nq >> 1;                  // pairs per head
+        const int pair_units = p.BH * hp;
+        if (u >= pair_units) {
+            if (i > 0) return false;
+            bh = u - pair_units;
+            qt = hp;                                // the middle tile (nq - 1) / 2
             return true;
         }
-        if (k == p.nq - 1 - k) return false;
-        qt = k;
+        bh = u / hp;
+        const int k = u - bh * hp;
+        qt = i == 0 ? p.nq - 1 - k : k;
         return true;
     };
     auto blocks_of = [&](int qt) { return p.causal ? min(kblocks_all, qt + 1) : kblocks_all; };
