@@ -245,9 +245,9 @@ int attn_f16_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B
     // TFLOP/s, 4x16x2100 622 -> 808, 4x32x300 215 -> 244, 2x32x513 235 -> 267);
     // at D = 128 on 17 tiles per head (4x16x2100 1071 -> 1133) but not on 11
     // (8x16x1300 927 against 880, 16x16x1300 980 against 959), where the
-    // model now keeps the one-tile kernel.  The pairs taken are chosen among
-    // whole rounds over the CTAs and all of them, for the least busy busiest
-    // CTA (the last three whole rounds are tried).
+    // model now keeps the one-tile kernel.  The number of pairs taken (all of
+    // them, or one of the last three whole rounds over the CTAs) is the one that
+    // leaves the busiest CTA the least work.
     const int64_t tiles_all = B * H * nq;
     const int64_t head_pairs = B * H * (nq / 2);
     // the busiest CTA's cost with p pair units first and then s one-tile units,
@@ -291,8 +291,7 @@ int attn_f16_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B
     int64_t units = prm.pair ? B * H * ((nq + 1) / 2) : B * H * nq;
     prm.pair_units = 0;
     if (two_tiles && causal) {
-        // steps of two pairs of one head (np - 1 - m, then m; the middle one of
-        // an odd count alone)
+        // steps of two pairs of one head (np - 1 - m, then m; np is even here)
         units = causal_steps;
         prm.pair_units = static_cast<int>(units);
     } else if (two_tiles) {
