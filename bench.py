@@ -89,50 +89,14 @@ def workload_config(w, epi, layout="nn"):
     }
 
 
-def odd_two_tiles(bh: int, nq: int, D: int, sms: int) -> bool:
-    """Whether a non-causal problem of an odd number of query tiles per head runs
-    the two-tile kernel: the busiest CTA's units (pairs 1, one-tile units 0.6)
-    cost less than its tiles on the one-tile kernel (0.51 each at D = 128, 0.654
-    at D = 64), for the best number of pairs among all of them and the last
-    three whole rounds over the CTAs (the library's own rule)."""
-    tiles, head_pairs = bh * nq, bh * (nq // 2)
-
-    def busiest(p, s1):
-        g = min(p + s1, sms)
-        worst = 0.0
-        for c in range(g):
-            pc = p // g + (1 if c < p % g else 0)
-            first = (c - p % g) % g
-            sc = -(-(s1 - first) // g) if first < s1 else 0
-            worst = max(worst, pc + 0.6 * sc)
-        return worst
-
-    best = busiest(head_pairs, tiles - 2 * head_pairs)
-    rounds = tiles // (2 * sms)
-    for j in range(max(0, rounds - 2), rounds + 1):
-        if j * sms >= head_pairs:
-            break
-        best = min(best, busiest(j * sms, tiles - 2 * j * sms))
-    return best < -(-tiles // sms) * (0.654 if D == 64 else 0.51)
-
-
 def attn_kernel_name(w, sms: int) -> str:
-    """Non-causal problems run the two-tile kernel (two query tiles per CTA, a
-    head's last tile alone when it has an odd number; softmax of one overlapping the other's
-    MMAs; at D = 64 with P buffers of their own, so the next S overlaps the
-    softmax), causal ones with a multiple of 4 tiles per head, at least 8, a
-    step of two tile pairs per SM and steps that split over the SMs no worse
-    than the one-tile kernel's units; the rest run the one-tile kernel."""
-    nq = (w.S + 127) // 128
-    steps = w.B * w.H * (nq // 4)
-    balanced = 2 * -(-steps // sms) * (75 if w.D == 64 else 92) < 100 * -(-2 * steps // sms)
-    if w.causal:
-        two = nq % 4 == 0 and nq >= 8 and steps >= sms and balanced
-    else:
-        two = nq % 2 == 0 or (nq >= 3 and odd_two_tiles(w.B * w.H, nq, w.D, sms))
-    if two:
-        return "attn_f16_fwd3_kernel<64>" if w.D == 64 else f"attn_f16_fwd2_kernel<{w.D}>"
-    return f"attn_f16_fwd4_kernel<{w.D}>"
+    """The attention kernel the library's plan picks for this workload (its
+    host-only attn_f16_plan: the two-tile kernels for non-causal problems and
+    for causal ones with a multiple of 4 tiles per head that split evenly, the
+    one-tile kernel otherwise)."""
+    import dense_fp16_tensor_tma_gb300 as g
+    name = g.attn_f16_plan(w.B, w.H, w.S, w.D, w.causal, sms)["kernel_name"]
+    return f"{name}<{w.D}>"
 
 
 def kernel_name(plan):

@@ -28,7 +28,7 @@ EXPORTS = ("gemm_f16", "gemm_f16_ex", "gemm_f16_status_string", "gemm_f16_last_c
            "gemm_f16_debug_status", "gemm_f16_release_workspace", "gemm_f16_plan", "gemm_f16_plan_ex",
            "gemm_f16_selftest_timeout", "gemm_f16_noalloc", "gemm_f16_force_config", "gemm_f16_set_pdl",
            "gemm_f16_grouped", "attn_f16_fwd", "attn_f16_debug_status", "attn_f16_last_cuda_error",
-           "gemm_f16_debug_inject", "attn_f16_debug_inject", "gemm_f16_force_ksplit")
+           "gemm_f16_debug_inject", "attn_f16_debug_inject", "gemm_f16_force_ksplit", "attn_f16_plan")
 GEMM_F16_FAULT_NONE, GEMM_F16_FAULT_SKIP_LOADS, GEMM_F16_FAULT_ENCODE = 0, 1, 2
 CONFIGS = {"auto": 0, "pair256x256": 1, "128x256": 2, "128x128": 3, "128x64": 4, "swap": 5, "pair_whole": 6}
 
@@ -74,6 +74,8 @@ lib.attn_f16_fwd.restype = _int
 lib.attn_f16_debug_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
 lib.attn_f16_debug_status.restype = _int
 lib.attn_f16_last_cuda_error.restype = _int
+lib.attn_f16_plan.argtypes = [_i64, _i64, _i64, _i64, _int, _int, ctypes.POINTER(ctypes.c_int64)]
+lib.attn_f16_plan.restype = _int
 lib.gemm_f16_set_pdl.argtypes = [_int]
 lib.gemm_f16_set_pdl.restype = _int
 lib.gemm_f16_force_ksplit.argtypes = [_int]
@@ -351,6 +353,21 @@ def attn_f16_fwd(Q, K, V, O, causal=False, scale=None, stream=None):
     if st != GEMM_OK:
         raise GemmError(st, "attn_f16_fwd")
     return O
+
+
+ATTN_KERNELS = {0: None, 1: "attn_f16_fwd4_kernel", 2: "attn_f16_fwd2_kernel", 3: "attn_f16_fwd3_kernel"}
+
+
+def attn_f16_plan(B, H, S, D, causal=False, num_sms=152):
+    """Host-only: the kernel and work split attn_f16_fwd would use (dict),
+    without touching a device."""
+    out = (ctypes.c_int64 * 5)()
+    st = lib.attn_f16_plan(int(B), int(H), int(S), int(D), 1 if causal else 0, int(num_sms), out)
+    if st != GEMM_OK:
+        raise GemmError(st, "attn_f16_plan")
+    d = dict(zip(("kernel", "units", "pair_units", "causal_pairs", "ctas"), list(out)))
+    d["kernel_name"] = ATTN_KERNELS[d["kernel"]]
+    return d
 
 
 def attn_f16_debug_status(stream=None):

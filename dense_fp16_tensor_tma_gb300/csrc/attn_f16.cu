@@ -146,6 +146,114 @@ int encode_3d(CUtensorMap* m, const void* ptr, int64_t D, int64_t S, int64_t BH)
     return GEMM_OK;
 }
 
+// The kernel and the work units of one call: 1 attn_f16_fwd4_kernel (one query
+// tile per CTA), 2 attn_f16_fwd2_kernel (two tiles, P over the scores, D = 128),
+// 3 attn_f16_fwd3_kernel (two tiles, P buffers of its own, D = 64).  Host only.
+struct AttnPlan {
+    int kernel = 1;
+    int64_t units = 0, pair_units = 0;
+    int pair = 0;        // one-tile kernel: causal pairs of tiles nq - 1 - k and k
+    int ctas = 0;
+};
+
+AttnPlan plan_attention(int64_t B, int64_t H, int64_t nq, int64_t D, bool causal, int sms) {
+    AttnPlan pl;
+    // Work units: query tiles, or, causal with at least two tiles per SM, pairs
+    // of a head's tiles nq - 1 - k and k (equal cost per unit; with fewer tiles
+    // pairing would only halve the parallelism).
+    // Non-causal: two tiles per CTA whose softmax and MMAs interleave
+    // (attn_f16_fwd2_kernel; at D = 64 attn_f16_fwd3_kernel), a head's tiles
+    // paired (2k, 2k + 1) and, with an odd number per head, its last tile run
+    // alone.  Causal (same-box A/B against the one-tile kernel, attn_f16_fwd4_kernel,
+    // which pairs tiles k and nq - 1 - k, so its units cost half a step each):
+    // with a multiple of 4 tiles per head (an even number of pairs, so every
+    // step of two pairs costs the same; with an odd number the cheaper one-pair
+    // steps fell on the same CTAs: 4x32x1792x128 827 against 935 TFLOP/s), from
+    // 8 tiles per head (4x32x1024: 687 against 627 at D = 128, 574 against 414
+    // at D = 64), with at least one step per SM, and only where the busiest
+    // CTA's steps cost less than its share of the one-tile kernel's units.  A
+    // key block of the two-tile kernels took 0.92 (D = 128) and 0.75 (D = 64)
+    // of the one-tile kernel's time where both split evenly (4x32x4096 413.1
+    // against 450.7 us and 285.5 against 391.1 us, 1x32x16384 0.94 and 0.75);
+    // 4x32x2048x128 (512 steps: 4 on some CTAs, against 7 units) ran 984
+    // against 999.  Otherwise one tile per CTA.
+    // Non-causal with an odd number of tiles per head (at least 3): pairs of a
+    // head's tiles and its last tile alone, where the busiest CTA's units cost
+    // less than the one-tile kernel's tiles.  Costs in pair units: a one-tile
+    // unit of the two-tile kernels 0.6, a tile of the one-tile kernel 0.51 at
+    // D = 128 and 0.654 at D = 64, fitted to same-box A/B runs: at D = 64 the
+    // two-tile kernel won on every odd shape tried (8x16x1300 551 -> 670
+    // TFLOP/s, 4x16x2100 622 -> 808, 4x32x300 215 -> 244, 2x32x513 235 -> 267);
+    // at D = 128 on 17 tiles per head (4x16x2100 1071 -> 1133) but not on 11
+    // (8x16x1300 927 against 880, 16x16x1300 980 against 959), where the
+    // model now keeps the one-tile kernel.  The number of pairs taken (all of
+    // them, or one of the last three whole rounds over the CTAs) is the one that
+    // leaves the busiest CTA the least work.
+    const int64_t tiles_all = B * H * nq;
+    const int64_t head_pairs = B * H * (nq / 2);
+    // the busiest CTA's cost with p pair units first and then s one-tile units,
+    // dealt round-robin to min(p + s, sms) CTAs
+    auto busiest = [&](int64_t p, int64_t s1) -> double {
+        const int64_t G = std::min<int64_t>(p + s1, sms);
+        double worst = 0.0;
+        for (int64_t c = 0; c < G; ++c) {
+            const int64_t pc = p / G + (c < p % G ? 1 : 0);
+            const int64_t first = (c - p % G + G) % G;   // the first one-tile unit dealt to CTA c
+            const int64_t sc = first < s1 ? (s1 - first + G - 1) / G : 0;
+            worst = std::max(worst, static_cast<double>(pc) + 0.6 * static_cast<double>(sc));
+        }
+        return worst;
+    };
+    int64_t odd_pairs = head_pairs;
+    bool odd_two = false;
+    if (!causal && nq % 2 == 1 && nq >= 3 && ATTN_ODD_TILES) {
+        double best = busiest(head_pairs, tiles_all - 2 * head_pairs);
+        const int64_t rounds = tiles_all / (2 * static_cast<int64_t>(sms));   // whole rounds of pairs that fit
+        for (int64_t j = std::max<int64_t>(0, rounds - 2); j <= rounds && j * sms < head_pairs; ++j) {
+            const double c = busiest(j * sms, tiles_all - 2 * j * sms);
+            if (c < best) {
+                best = c;
+                odd_pairs = j * sms;
+            }
+        }
+        const int64_t one_tile = (tiles_all + sms - 1) / sms;
+        odd_two = best < static_cast<double>(one_tile) * (D == 64 ? 0.654 : 0.51);
+    }
+    const int64_t causal_steps = B * H * (nq / 4);
+    const int64_t steps_busiest = (causal_steps + sms - 1) / sms;
+    const int64_t units1_busiest = (2 * causal_steps + sms - 1) / sms;
+    const int64_t block_cost_pct = D == 64 ? 75 : 92;
+    const bool two_tiles = ATTN_PINGPONG &&
+                           (causal ? (ATTN_CAUSAL_PAIRS && nq % 4 == 0 && nq >= ATTN_CAUSAL_MIN_TILES &&
+                                      causal_steps >= static_cast<int64_t>(sms) &&
+                                      2 * steps_busiest * block_cost_pct < 100 * units1_busiest)
+                                   : (nq % 2 == 0 || odd_two));
+    pl.pair = !two_tiles && causal && B * H * nq >= 2 * static_cast<int64_t>(sms) ? 1 : 0;
+    int64_t units = pl.pair ? B * H * ((nq + 1) / 2) : B * H * nq;
+    pl.pair_units = 0;
+    if (two_tiles && causal) {
+        // steps of two pairs of one head (np - 1 - m, then m; np is even here)
+        units = causal_steps;
+        pl.pair_units = units;
+    } else if (two_tiles) {
+        // Two tiles per unit; when the tiles left over after k full rounds of
+        // pairs (k per CTA) fit one per CTA, they run as one-tile units (k pairs
+        // and at most one single per CTA instead of k + 1 pairs on some CTAs);
+        // otherwise every pair a head has is a unit (and, with an odd number of
+        // tiles per head, each head's last tile runs alone).
+        const int64_t tiles = tiles_all;
+        const int64_t k = tiles / (2 * static_cast<int64_t>(sms));
+        const int64_t rest = tiles - 2 * k * sms;
+        const int64_t pairs = nq % 2 == 1 ? odd_pairs : (rest <= sms ? k * sms : head_pairs);
+        pl.pair_units = pairs;
+        units = pairs + (tiles - 2 * pairs);
+    }
+    pl.kernel = !two_tiles ? 1 : (D == 64 ? 3 : 2);
+    pl.units = units;
+    pl.ctas = static_cast<int>(std::min<int64_t>(units, sms));
+    return pl;
+}
+
 template <int D>
 cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const AttnParams& prm, int ctas,
                    bool two_tiles, cudaStream_t s) {
@@ -216,102 +324,34 @@ int attn_f16_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B
         prm.fault_skip_block = 1;
         prm.timeout_ns = g_fault_wait_ns.load(std::memory_order_relaxed);
     }
-    // Work units: query tiles, or, causal with at least two tiles per SM, pairs
-    // of a head's tiles nq - 1 - k and k (equal cost per unit; with fewer tiles
-    // pairing would only halve the parallelism).
-    const int sms = g_dev[dev].sms;
-    // Non-causal: two tiles per CTA whose softmax and MMAs interleave
-    // (attn_f16_fwd2_kernel; at D = 64 attn_f16_fwd3_kernel), a head's tiles
-    // paired (2k, 2k + 1) and, with an odd number per head, its last tile run
-    // alone.  Causal (same-box A/B against the one-tile kernel, attn_f16_fwd4_kernel,
-    // which pairs tiles k and nq - 1 - k, so its units cost half a step each):
-    // with a multiple of 4 tiles per head (an even number of pairs, so every
-    // step of two pairs costs the same; with an odd number the cheaper one-pair
-    // steps fell on the same CTAs: 4x32x1792x128 827 against 935 TFLOP/s), from
-    // 8 tiles per head (4x32x1024: 687 against 627 at D = 128, 574 against 414
-    // at D = 64), with at least one step per SM, and only where the busiest
-    // CTA's steps cost less than its share of the one-tile kernel's units.  A
-    // key block of the two-tile kernels took 0.92 (D = 128) and 0.75 (D = 64)
-    // of the one-tile kernel's time where both split evenly (4x32x4096 413.1
-    // against 450.7 us and 285.5 against 391.1 us, 1x32x16384 0.94 and 0.75);
-    // 4x32x2048x128 (512 steps: 4 on some CTAs, against 7 units) ran 984
-    // against 999.  Otherwise one tile per CTA.
-    // Non-causal with an odd number of tiles per head (at least 3): pairs of a
-    // head's tiles and its last tile alone, where the busiest CTA's units cost
-    // less than the one-tile kernel's tiles.  Costs in pair units: a one-tile
-    // unit of the two-tile kernels 0.6, a tile of the one-tile kernel 0.51 at
-    // D = 128 and 0.654 at D = 64, fitted to same-box A/B runs: at D = 64 the
-    // two-tile kernel won on every odd shape tried (8x16x1300 551 -> 670
-    // TFLOP/s, 4x16x2100 622 -> 808, 4x32x300 215 -> 244, 2x32x513 235 -> 267);
-    // at D = 128 on 17 tiles per head (4x16x2100 1071 -> 1133) but not on 11
-    // (8x16x1300 927 against 880, 16x16x1300 980 against 959), where the
-    // model now keeps the one-tile kernel.  The number of pairs taken (all of
-    // them, or one of the last three whole rounds over the CTAs) is the one that
-    // leaves the busiest CTA the least work.
-    const int64_t tiles_all = B * H * nq;
-    const int64_t head_pairs = B * H * (nq / 2);
-    // the busiest CTA's cost with p pair units first and then s one-tile units,
-    // dealt round-robin to min(p + s, sms) CTAs
-    auto busiest = [&](int64_t p, int64_t s1) -> double {
-        const int64_t G = std::min<int64_t>(p + s1, sms);
-        double worst = 0.0;
-        for (int64_t c = 0; c < G; ++c) {
-            const int64_t pc = p / G + (c < p % G ? 1 : 0);
-            const int64_t first = (c - p % G + G) % G;   // the first one-tile unit dealt to CTA c
-            const int64_t sc = first < s1 ? (s1 - first + G - 1) / G : 0;
-            worst = std::max(worst, static_cast<double>(pc) + 0.6 * static_cast<double>(sc));
-        }
-        return worst;
-    };
-    int64_t odd_pairs = head_pairs;
-    bool odd_two = false;
-    if (!causal && nq % 2 == 1 && nq >= 3 && ATTN_ODD_TILES) {
-        double best = busiest(head_pairs, tiles_all - 2 * head_pairs);
-        const int64_t rounds = tiles_all / (2 * static_cast<int64_t>(sms));   // whole rounds of pairs that fit
-        for (int64_t j = std::max<int64_t>(0, rounds - 2); j <= rounds && j * sms < head_pairs; ++j) {
-            const double c = busiest(j * sms, tiles_all - 2 * j * sms);
-            if (c < best) {
-                best = c;
-                odd_pairs = j * sms;
-            }
-        }
-        const int64_t one_tile = (tiles_all + sms - 1) / sms;
-        odd_two = best < static_cast<double>(one_tile) * (D == 64 ? 0.654 : 0.51);
-    }
-    const int64_t causal_steps = B * H * (nq / 4);
-    const int64_t steps_busiest = (causal_steps + sms - 1) / sms;
-    const int64_t units1_busiest = (2 * causal_steps + sms - 1) / sms;
-    const int64_t block_cost_pct = D == 64 ? 75 : 92;
-    const bool two_tiles = ATTN_PINGPONG &&
-                           (causal ? (ATTN_CAUSAL_PAIRS && nq % 4 == 0 && nq >= ATTN_CAUSAL_MIN_TILES &&
-                                      causal_steps >= static_cast<int64_t>(sms) &&
-                                      2 * steps_busiest * block_cost_pct < 100 * units1_busiest)
-                                   : (nq % 2 == 0 || odd_two));
-    prm.pair = !two_tiles && causal && B * H * nq >= 2 * static_cast<int64_t>(sms) ? 1 : 0;
-    int64_t units = prm.pair ? B * H * ((nq + 1) / 2) : B * H * nq;
-    prm.pair_units = 0;
-    if (two_tiles && causal) {
-        // steps of two pairs of one head (np - 1 - m, then m; np is even here)
-        units = causal_steps;
-        prm.pair_units = static_cast<int>(units);
-    } else if (two_tiles) {
-        // Two tiles per unit; when the tiles left over after k full rounds of
-        // pairs (k per CTA) fit one per CTA, they run as one-tile units (k pairs
-        // and at most one single per CTA instead of k + 1 pairs on some CTAs);
-        // otherwise every pair a head has is a unit (and, with an odd number of
-        // tiles per head, each head's last tile runs alone).
-        const int64_t tiles = tiles_all;
-        const int64_t k = tiles / (2 * static_cast<int64_t>(sms));
-        const int64_t rest = tiles - 2 * k * sms;
-        const int64_t pairs = nq % 2 == 1 ? odd_pairs : (rest <= sms ? k * sms : head_pairs);
-        prm.pair_units = static_cast<int>(pairs);
-        units = pairs + (tiles - 2 * pairs);
-    }
-    prm.units = static_cast<int>(units);
-    const int ctas = static_cast<int>(std::min<int64_t>(units, sms));
+    const AttnPlan pl = plan_attention(B, H, nq, D, causal != 0, g_dev[dev].sms);
+    prm.pair = pl.pair;
+    prm.pair_units = static_cast<int>(pl.pair_units);
+    prm.units = static_cast<int>(pl.units);
+    const int ctas = pl.ctas;
+    const bool two_tiles = pl.kernel != 1;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     e = D == 64 ? launch<64>(tq, tk, tv, prm, ctas, two_tiles, s) : launch<128>(tq, tk, tv, prm, ctas, two_tiles, s);
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+}
+
+int attn_f16_plan(int64_t B, int64_t H, int64_t S, int64_t D, int causal, int num_sms, int64_t plan[5]) {
+    if (plan == nullptr || num_sms <= 0) return GEMM_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || S < 0) return GEMM_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return GEMM_ERR_INVALID_ARG;
+    if (S >= (int64_t(1) << 31) || B >= (int64_t(1) << 31) || H >= (int64_t(1) << 31)) return GEMM_ERR_INVALID_ARG;
+    if (B * H >= (int64_t(1) << 31)) return GEMM_ERR_INVALID_ARG;
+    for (int i = 0; i < 5; ++i) plan[i] = 0;
+    if (B == 0 || H == 0 || S == 0) return GEMM_OK;
+    const int64_t nq = (S + kQRows - 1) / kQRows;
+    if (B * H * nq >= (int64_t(1) << 31)) return GEMM_ERR_INVALID_ARG;
+    const AttnPlan pl = plan_attention(B, H, nq, D, causal != 0, num_sms);
+    plan[0] = pl.kernel;
+    plan[1] = pl.units;
+    plan[2] = pl.pair_units;
+    plan[3] = pl.pair;
+    plan[4] = pl.ctas;
+    return GEMM_OK;
 }
 
 int attn_f16_last_cuda_error(void) { return t_last_cuda_error; }

@@ -54,6 +54,26 @@ extern "C" {
 int attn_f16_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B, int64_t H, int64_t S,
                  int64_t D, int causal, float scale, void* cuda_stream);
 
+/*
+ * attn_f16_plan -- host only, touches no device (a diagnostic with no
+ * counterpart on the pages): the kernel and work split attn_f16_fwd would use
+ * for these arguments on a device of `num_sms` SMs.  On GEMM_OK,
+ *
+ *   plan[0]  kernel: 1 one query tile per CTA (attn_f16_fwd4_kernel);
+ *            2 two tiles per CTA, P over the scores (attn_f16_fwd2_kernel,
+ *            D = 128); 3 two tiles per CTA, P buffers of its own
+ *            (attn_f16_fwd3_kernel, D = 64); 0 for an empty problem
+ *   plan[1]  work units (a unit: one tile, a pair of tiles, or, causal on a
+ *            two-tile kernel, a step of two pairs of one head)
+ *   plan[2]  two-tile kernels: units that hold two tiles (or causal steps)
+ *   plan[3]  one-tile kernel: 1 when causal tiles run in pairs nq - 1 - k, k
+ *   plan[4]  CTAs launched (persistent: min(units, SMs))
+ *
+ * `plan` is caller-owned, 5 entries.  GEMM_ERR_INVALID_ARG for a null plan,
+ * num_sms <= 0 or the argument errors of attn_f16_fwd (pointers aside).
+ */
+int attn_f16_plan(int64_t B, int64_t H, int64_t S, int64_t D, int causal, int num_sms, int64_t plan[5]);
+
 /* cudaError_t value behind the calling thread's most recent GEMM_ERR_CUDA from attn_f16_fwd. */
 int attn_f16_last_cuda_error(void);
 
