@@ -18,7 +18,10 @@
 // of 64 keys, 320 threads, exchanging maxima and sums through shared memory;
 // same-box A/B at 4x32x4096x128: 1215 -> 1316 TFLOP/s, 4x32x4096x64 701 ->
 // 800, causal 1058 -> 1124).  It computes all of P in registers before storing
-// it.  192 threads: warp 0 the TMA producer, warp 1 the MMA warp, warps 2..5
+// it, each pair of scores' registers then holding their P; where a block's sum
+// of P calls for the exact maximum, the thread reads the block's scores from
+// tensor memory again (the buffer is overwritten only after P is signalled).
+// 192 threads: warp 0 the TMA producer, warp 1 the MMA warp, warps 2..5
 // the softmax.  (Keeping P in tensor memory instead of shared memory measured
 // 3 % faster and frees 64 KiB of shared memory; spending that on a third K
 // and V ring slot did not pay.)
@@ -320,63 +323,93 @@ attn_f16_fwd4_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                                            BAR_S);
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                     tc_fence_after();
-                    // the row's 128 scores of the block, all in registers
+                    // the row's 128 scores of the block, all in registers.  The largest
+                    // scaled score comes from the largest raw score when the scale is
+                    // positive and from the smallest when it is negative; keys that do
+                    // not count get the raw score that loses that comparison, so their
+                    // weight is 2^-inf = 0.
                     uint32_t v[128];
-                    uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(v);
-                    uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 32);
-                    uint32_t (&v2)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 64);
-                    uint32_t (&v3)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 96);
-                    tmem_ld_32x32b_x32(s_cols, v0);
-                    tmem_ld_32x32b_x32(s_cols + 32u, v1);
-                    tmem_ld_32x32b_x32(s_cols + 64u, v2);
-                    tmem_ld_32x32b_x32(s_cols + 96u, v3);
-                    tmem_wait_ld(v0);
-                    tmem_wait_ld(v1);
-                    tmem_wait_ld(v2);
-                    tmem_wait_ld(v3);
-                    // The largest scaled score comes from the largest raw score when the
-                    // scale is positive and from the smallest when it is negative; keys
-                    // that do not count get the raw score that loses that comparison, so
-                    // their weight is 2^-inf = 0.
-                    if (k0 + kKeys > p.S || (p.causal && j == nblk - 1)) {
-                        const int key_lim = key_end - k0;         // valid: column < key_lim
+                    auto load_scores = [&]() {
+                        uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(v);
+                        uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 32);
+                        uint32_t (&v2)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 64);
+                        uint32_t (&v3)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 96);
+                        tmem_ld_32x32b_x32(s_cols, v0);
+                        tmem_ld_32x32b_x32(s_cols + 32u, v1);
+                        tmem_ld_32x32b_x32(s_cols + 64u, v2);
+                        tmem_ld_32x32b_x32(s_cols + 96u, v3);
+                        tmem_wait_ld(v0);
+                        tmem_wait_ld(v1);
+                        tmem_wait_ld(v2);
+                        tmem_wait_ld(v3);
+                        if (k0 + kKeys > p.S || (p.causal && j == nblk - 1)) {
+                            const int key_lim = key_end - k0;         // valid: column < key_lim
 #pragma unroll
-                        for (int t = 0; t < 128; ++t)
-                            if (t >= key_lim) v[t] = lose;
-                    }
-                    float bm[4];
-                    bm[0] = bm[1] = bm[2] = bm[3] = pos ? -INFINITY : INFINITY;
-                    if (pos) {
+                            for (int t = 0; t < 128; ++t)
+                                if (t >= key_lim) v[t] = lose;
+                        }
+                    };
+                    // the largest scaled score (log2 units); -inf if no key counts
+                    auto block_max = [&]() -> float {
+                        float bm[4];
+                        bm[0] = bm[1] = bm[2] = bm[3] = pos ? -INFINITY : INFINITY;
+                        if (pos) {
 #pragma unroll
-                        for (int t = 0; t < 128; t += 2)
-                            bm[(t >> 1) & 3] = max3f(bm[(t >> 1) & 3], __uint_as_float(v[t]), __uint_as_float(v[t + 1]));
-                    } else {
+                            for (int t = 0; t < 128; t += 2)
+                                bm[(t >> 1) & 3] = max3f(bm[(t >> 1) & 3], __uint_as_float(v[t]), __uint_as_float(v[t + 1]));
+                        } else {
 #pragma unroll
-                        for (int t = 0; t < 128; t += 2)
-                            bm[(t >> 1) & 3] = min3f(bm[(t >> 1) & 3], __uint_as_float(v[t]), __uint_as_float(v[t + 1]));
-                    }
-                    float bmax = pos ? fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3]))
-                                     : fminf(fminf(bm[0], bm[1]), fminf(bm[2], bm[3]));
-                    bmax *= p.scale_log2;   // the largest scaled score (log2 units); -inf if no key counts
+                            for (int t = 0; t < 128; t += 2)
+                                bm[(t >> 1) & 3] = min3f(bm[(t >> 1) & 3], __uint_as_float(v[t]), __uint_as_float(v[t + 1]));
+                        }
+                        const float b = pos ? fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3]))
+                                            : fminf(fminf(bm[0], bm[1]), fminf(bm[2], bm[3]));
+                        return b * p.scale_log2;
+                    };
+                    // P = 2^(x * scale_log2 - mm) as fp16 pairs, all in registers (each
+                    // pair replaces two scores); returns the block's sum of those fp16
+                    // values, in fp32
+                    auto p_pass = [&](float mm) -> float {
+                        float rs0 = 0.0f, rs1 = 0.0f;
+#pragma unroll
+                        for (int t = 0; t < 64; ++t) {
+                            const float2 xs = fma2_bc(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]),
+                                                      p.scale_log2, -mm);
+                            const __half2 hv = __floats2half2_rn(fast_exp2(xs.x), fast_exp2(xs.y));
+                            v[t] = *reinterpret_cast<const uint32_t*>(&hv);
+                            if (t & 1) rs1 = add_f16x2_to_f32(rs1, v[t]);
+                            else rs0 = add_f16x2_to_f32(rs0, v[t]);
+                        }
+                        return rs0 + rs1;
+                    };
+                    // The running maximum m is raised when the block maximum exceeds it
+                    // by more than kRaise, so that every P stays within 2^kRaise.  At a
+                    // tile's first block (m not yet set) the maximum is taken first.
+                    // Otherwise P is formed with m at once and its sum decides: a sum
+                    // within 2^kRaise bounds every P, so the maximum cannot have exceeded
+                    // the limit; above it the scores are read again from tensor memory,
+                    // the maximum taken and P formed again (with the raised maximum,
+                    // where there is a raise).
+                    load_scores();
                     float m_new = m;
                     bool raise = false;
-                    if (bmax > m + kRaise || m == -INFINITY) {
-                        m_new = fmaxf(m, bmax);
-                        raise = m != -INFINITY && m_new != m;
+                    const bool first = __any_sync(0xffffffffu, m == -INFINITY);
+                    if (first) {
+                        const float bmax = block_max();
+                        if (bmax > m + kRaise || m == -INFINITY) {
+                            m_new = fmaxf(m, bmax);
+                            raise = m != -INFINITY && m_new != m;
+                        }
                     }
-                    // P = 2^(x * scale_log2 - m) as fp16 pairs, all in registers (each
-                    // pair replaces two scores), and its sum over the fp16 values the
-                    // tensor core multiplies
-                    const float mm = (m_new == -INFINITY) ? 0.0f : m_new;
-                    float rs0 = 0.0f, rs1 = 0.0f;
-#pragma unroll
-                    for (int t = 0; t < 64; ++t) {
-                        const float2 xs = fma2_bc(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]),
-                                                  p.scale_log2, -mm);
-                        const __half2 hv = __floats2half2_rn(fast_exp2(xs.x), fast_exp2(xs.y));
-                        v[t] = *reinterpret_cast<const uint32_t*>(&hv);
-                        if (t & 1) rs1 = add_f16x2_to_f32(rs1, v[t]);
-                        else rs0 = add_f16x2_to_f32(rs0, v[t]);
+                    float bsum = p_pass((m_new == -INFINITY) ? 0.0f : m_new);
+                    if (!first && __any_sync(0xffffffffu, bsum > kRaiseSum)) {
+                        load_scores();
+                        const float bmax = block_max();
+                        if (bmax > m + kRaise) {
+                            m_new = fmaxf(m, bmax);
+                            raise = m_new != m;
+                        }
+                        bsum = p_pass(m_new);
                     }
                     // O is rescaled only after P V of block gb - 1 (of this tile: a raise
                     // needs an earlier block) has finished.  P V of block gb - 3 was issued
@@ -401,7 +434,7 @@ attn_f16_fwd4_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                         }
                     }
                     m = m_new;
-                    l += rs0 + rs1;
+                    l += bsum;
                     // P buffer s (keys 32c .. 32c + 31 at columns 16c ..) was last read by
                     // P V of block gb - 2, issued before S of block gb: complete
 #pragma unroll

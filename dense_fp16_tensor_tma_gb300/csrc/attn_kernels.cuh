@@ -19,14 +19,20 @@
 // O += P_j V_j (M = 128, N = D, K = 128; P read by the tensor core straight
 // from tensor memory, V MN-major from shared memory); softmax warps, one
 // query row per thread (its TMEM lane), which read the row's 128 scores of a
-// block into registers, take the block maximum, form p = 2^(s * scale *
-// log2 e - m) in fp32, sum it and write it as fp16 pairs into tensor memory
-// (the layout the MMA reads its A operand in).  The running maximum m is
+// block into registers, form p = 2^(s * scale * log2 e - m) in fp32, write it
+// as fp16 pairs into tensor memory (the layout the MMA reads its A operand in)
+// and sum, in fp32, the fp16 values the tensor core multiplies (so that O / l
+// is exactly V where V is constant over the keys). The running maximum m is
 // raised only when a block's maximum exceeds it by more than 8 (in log2
 // units); O and the running sum l are then rescaled in place (TMEM load,
-// multiply, store).  Between raises p stays below 2^8, which fp16 and the fp32
-// sums hold exactly enough, and the final O / l is the same ratio.  After a
-// unit's last block: O / l rounded to fp16, 16-byte stores of each thread's row.
+// multiply, store). Between raises p stays within 2^8, which fp16 and the fp32
+// sums hold exactly enough, and the final O / l is the same ratio. The two-
+// tile kernels take each block's maximum before its exponentials; the one-tile
+// kernel does so only at a tile's first block, later forming P with m at once
+// and taking the maximum only when the block's sum of P exceeds 2^8 (below
+// that no p can, so no raise is due), then forming P again. After a
+// unit's last block: O / l rounded to fp16, 16-byte stores of each thread's
+// row.
 //
 // The kernels: attn_f16_fwd4_kernel (attn4_kernels.cuh: one query tile per
 // CTA, two score and two P buffers), attn_f16_fwd2_kernel (attn2_kernels.cuh:
@@ -55,6 +61,7 @@ constexpr uint32_t kMaxDynSmem = 232448;  // 227 KiB: the most dynamic shared me
 constexpr uint32_t kBox = 64 * 128 * 2;  // one 64 (D or keys) x 128 (rows) fp16 box: 16 KiB
 constexpr uint32_t kTmemCols = 512;      // every attention CTA allocates all of tensor memory
 constexpr float kRaise = 8.0f;           // raise the running max only past 2^8 growth
+constexpr float kRaiseSum = 256.0f;      // 2^kRaise: a block sum of P within it bounds every P
 
 enum : uint32_t { ROLE_SOFTMAX = 6, BAR_Q = 7, BAR_K = 8, BAR_V = 9, BAR_S = 10, BAR_P = 11, BAR_PV = 12,
                   BAR_X = 13, BAR_ALIGN = 14 };

@@ -7,8 +7,12 @@ and tensor-core commits, in the kernel's order and with its phase-parity
 arithmetic; a scheduler runs the roles, the TMA completions (any order) and
 the tensor pipe (in issue order) in seeded random interleavings.  Checked:
 no deadlock, no barrier receiving more arrivals than its count in one phase,
-and every parity wait finding its barrier at exactly the phase it means (a
-barrier one phase behind or two ahead would pass or block wrongly).  The
+every parity wait finding its barrier at exactly the phase it means (a
+barrier one phase behind or two ahead would pass or block wrongly), and no
+score buffer overwritten while a softmax warp reads it: a block's scores are
+read once after its S commit and, when the block's sum of P exceeds 2^8 (the
+maximum then taken exactly), a second time before P is signalled; the MMA
+thread issues the next S into that buffer only after the signal.  The
 work lists are those the kernel walks: one tile per unit (head-major,
 heaviest causal tile first) or causal pairs (tile nq-1-k, then tile k).
 
@@ -60,11 +64,12 @@ def work_list(units, grid, cta, nq, causal, paired):
     return [(qt, min(nq, qt + 1) if causal else nq) for qt in tiles]
 
 
-def run_protocol(tiles, seed, nsoft=2, misnumbered_producer=False):
+def run_protocol(tiles, seed, nsoft=2, misnumbered_producer=False, early_s=False):
     """One CTA: producer K and V lanes, the MMA thread and `nsoft` softmax warps
-    (standing for the eight, which all arrive on the same barriers).
+    (standing for the four, which all arrive on the same barriers).
     `misnumbered_producer` plants a defect an early build had: the producer
-    advanced its block count inside the block loop."""
+    advanced its block count inside the block loop.  `early_s` plants another:
+    the MMA thread issues S of block gb + 2 before P of block gb is signalled."""
     rnd = random.Random(seed)
     q_full, drain, o_free = Barrier("q_full", 1), Barrier("drain", 1), Barrier("o_free", nsoft)
     k_full = [Barrier(f"k_full{i}", 1) for i in range(2)]
@@ -73,6 +78,7 @@ def run_protocol(tiles, seed, nsoft=2, misnumbered_producer=False):
     p_full = [Barrier(f"p_full{i}", nsoft) for i in range(2)]
     pv_done = [Barrier(f"pv_done{i}", 1) for i in range(2)]
     tma, pipe = [], []
+    s_block = [None, None]       # the block whose S the MMA thread last issued into each buffer
 
     def wait(bar, index, who):
         # the phase the wait means and the parity the kernel passes for it
@@ -105,6 +111,7 @@ def run_protocol(tiles, seed, nsoft=2, misnumbered_producer=False):
 
         def issue_s(gb):
             yield wait(k_full[gb & 1], gb >> 1, "mma K")
+            s_block[gb & 1] = gb
             pipe.append(s_full[gb & 1])
 
         for qt, nblk in tiles:
@@ -115,12 +122,14 @@ def run_protocol(tiles, seed, nsoft=2, misnumbered_producer=False):
             for j in range(nblk):
                 gb = g + j
                 s = gb & 1
+                if early_s and j + 2 < nblk:
+                    yield from issue_s(gb + 2)
                 yield wait(p_full[s], gb >> 1, "mma P")
                 if j == 0 and ntile > 0:
                     yield wait(o_free, ntile - 1, "mma O free")
                 yield wait(v_full[s], gb >> 1, "mma V")
                 pipe.append(pv_done[s])
-                if j + 2 < nblk:
+                if j + 2 < nblk and not early_s:
                     yield from issue_s(gb + 2)
             g += nblk
             ntile += 1
@@ -134,7 +143,11 @@ def run_protocol(tiles, seed, nsoft=2, misnumbered_producer=False):
                 gb = g + j
                 s = gb & 1
                 yield wait(s_full[s], gb >> 1, "softmax S")
+                assert s_block[s] == gb, f"score buffer {s} overwritten while block {gb} is read"
                 yield None                           # S read, P computed in registers
+                if j >= 1 and rnd.random() < 0.3:   # a block sum above 2^8: the scores read again
+                    yield None
+                    assert s_block[s] == gb, f"score buffer {s} overwritten before block {gb} is read again"
                 if j >= 1 and rnd.random() < 0.3:   # a raise of the running maximum
                     yield wait(pv_done[(gb - 1) & 1], (gb - 1) >> 1, "softmax rescale")
                 p_full[s].arrive()
@@ -207,3 +220,13 @@ def test_protocol_model_catches_a_misnumbered_producer():
     tiles = work_list(2, 1, 0, 3, False, False)
     with pytest.raises(AssertionError):
         run_protocol(tiles, 0, misnumbered_producer=True)
+
+
+def test_protocol_model_catches_an_early_score_issue():
+    # S of block gb + 2 issued into the buffer of block gb before that block's
+    # P is signalled would overwrite scores the softmax may still be reading
+    tiles = work_list(1, 1, 0, 4, False, False)
+    with pytest.raises(AssertionError):
+        for seed in range(20):
+            run_protocol(tiles, seed, early_s=True)
+

@@ -167,6 +167,47 @@ def test_attention_running_max_raised_every_block(g, torch_dev, oracle_mod, D):
         check(got, oracle_mod.attention(Q, K, V, causal, scale=scale), f"ramp causal={causal}")
 
 
+# Score levels (log2 units) of successive key blocks for the even query rows:
+# after block 0 sets the running maximum m = 0, block 1's P sum 128 * 2^6 and
+# block 2's 128 * 2^7.75 exceed 2^8 with no raise due (the exact maximum is
+# taken and the first P kept), block 3 raises m to 9, blocks 4, 5 and 9 again
+# sum above 2^8 without a raise, block 6 raises to 20, block 7's P is tiny,
+# block 8's sum is exactly 2^8 (no second look) and block 10 raises to 30.
+# The odd rows see the negated scores and never leave the first pass, in the
+# same warps.
+SUM_CHECK_LEVELS = [0.0, 6.0, 7.75, 9.0, 14.0, 12.0, 20.0, 1.0, 21.0, 27.0, 30.0]
+
+
+@pytest.mark.parametrize("B,H,S,D,causal,kernel", [
+    (1, 2, 1024, 128, False, "attn_f16_fwd2_kernel"),
+    (1, 76, 1024, 128, True, "attn_f16_fwd2_kernel"),
+    (1, 3, 1300, 128, False, "attn_f16_fwd4_kernel"),
+    (1, 3, 1300, 128, True, "attn_f16_fwd4_kernel"),
+    (1, 2, 1300, 64, True, "attn_f16_fwd4_kernel"),
+    (1, 2, 1300, 64, False, "attn_f16_fwd3_kernel"),
+])
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_attention_block_sum_check(g, torch_dev, oracle_mod, B, H, S, D, causal, kernel, sign):
+    # Q = +-1 and every key of block b equal to SUM_CHECK_LEVELS[b]: with scale
+    # ln 2 / D the log2-unit score of a key is +-its level.  A negative scale
+    # (Q negated with it) takes the kernels' minimum-score branch.
+    assert g.attn_f16_plan(B, H, S, D, causal)["kernel_name"] == kernel
+    rng = np.random.default_rng(86)
+    row_sign = np.where(np.arange(S) % 2 == 0, 1.0, -1.0) * sign
+    Q = np.broadcast_to((row_sign[:, None] * np.ones(D))[None, None], (B, H, S, D)).astype(np.float16)
+    level = np.array(SUM_CHECK_LEVELS)[np.arange(S) // 128]
+    K = np.broadcast_to((level[:, None] * np.ones(D))[None, None], (B, H, S, D)).astype(np.float16)
+    V = rng.standard_normal((B, H, S, D)).astype(np.float16)
+    scale = sign * np.log(2.0) / D
+    got = run_attn(g, torch_dev, Q, K, V, causal, scale).reshape(B * H * S, D)
+    assert np.isfinite(got).all()
+    heads = B * H
+    rows = np.unique(np.concatenate([h * S + np.arange(S) for h in sorted({0, heads - 1})] +
+                                    [rng.integers(0, heads * S, 256)]))
+    ref = oracle_mod.attention_rows(Q, K, V, causal, scale, rows)
+    check(got[rows], ref, f"levels {B}x{H}x{S}x{D} causal={causal} sign={sign}")
+
+
 @pytest.mark.parametrize("scale", [0.05, -0.1, 0.3, -1.0])
 def test_attention_explicit_scale(g, torch_dev, oracle_mod, scale):
     rng = np.random.default_rng(84)
