@@ -110,27 +110,42 @@ def kernel_name(plan):
     return f"gemm_f16_tc_kernel<{plan['tile_n']}, {plan['stages']}>"
 
 
-def read_peaks():
-    """(fp16 tensor TFLOP/s, HBM GB/s, source): the measured burst figures, else the fallbacks."""
+# A timed window at least this long runs under the board's power cap (the
+# clock record of a 1000-step 8192^3 run shows sw_power_cap within it), so its
+# kernels are measured against the sustained tensor peak; shorter windows
+# against the burst peak.
+SUSTAINED_WINDOW_S = 0.25
+FALLBACK_TENSOR_SUSTAINED_TFLOPS = 1700.0
+
+
+def read_peaks(window_s=0.0):
+    """(fp16 tensor TFLOP/s, HBM GB/s, source): the measured figures (the
+    sustained tensor peak for a timed window of SUSTAINED_WINDOW_S or more,
+    else the burst one), else the fallbacks."""
+    sustained = window_s >= SUSTAINED_WINDOW_S
+    kind = "sustained" if sustained else "burst"
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             pk = json.load(f)
-        return float(pk["bf16_tflops"]) * FP16_PER_BF16, float(pk["hbm_gbs"]), "measured"
+        tflops = float(pk["bf16_tflops_sustained" if sustained else "bf16_tflops"])
+        return tflops * FP16_PER_BF16, float(pk["hbm_gbs"]), f"measured bf16 {kind}"
     except (OSError, KeyError, ValueError):
-        return FALLBACK_TENSOR_TFLOPS, FALLBACK_HBM_GBS, "fallback"
+        tflops = FALLBACK_TENSOR_SUSTAINED_TFLOPS if sustained else FALLBACK_TENSOR_TFLOPS
+        return tflops, FALLBACK_HBM_GBS, f"fallback {kind}"
 
 
-def roofline(w, avg_launch_ms, traffic, plan):
+def roofline(w, avg_launch_ms, traffic, plan, window_s):
     """Roofline of the dominant kernel: tensor-bound when the workload's
     arithmetic intensity (algorithmic FLOPs per algorithmic byte) is above the
-    ridge point of the two peaks, else HBM-bound."""
-    tensor_peak, hbm_peak, src = read_peaks()
+    ridge point of the two peaks, else HBM-bound.  window_s: the timed
+    window's length (selects the burst or sustained tensor peak)."""
+    tensor_peak, hbm_peak, src = read_peaks(window_s)
     intensity = w.flops() / w.alg_bytes()
     ridge = tensor_peak * 1e12 / (hbm_peak * 1e9)
     if intensity >= ridge:
         achieved, peak, unit, bound = w.flops() / (avg_launch_ms * 1e-3) / 1e12, tensor_peak, "TFLOP/s", "tensor"
-        peak_src = f"{src} (bf16 burst x fp16/bf16 ratio {FP16_PER_BF16})"
+        peak_src = f"{src} (x fp16/bf16 ratio {FP16_PER_BF16})"
     else:
         achieved, peak, unit, bound = w.alg_bytes() / (avg_launch_ms * 1e-3) / 1e9, hbm_peak, "GB/s", "hbm"
         peak_src = f"{src} (copy bandwidth)"
@@ -466,8 +481,8 @@ def run_ours(args, w, epi):
     value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
     avg_launch_ms = statistics.mean(per_launch_ms)
     traffic = committed_traffic(w.name if args.layout == "nn" else f"{w.name}:{args.layout}")
-    roof = roofline(w, avg_launch_ms, traffic, plan)
-    tensor_peak = read_peaks()[0]
+    roof = roofline(w, avg_launch_ms, traffic, plan, elapsed_ms * 1e-3)
+    tensor_peak = read_peaks(elapsed_ms * 1e-3)[0]
 
     # ---- end to end: pinned host buffers through the C ABI, copies inside the timed region
     hA = torch.from_numpy(A_st).pin_memory()
@@ -701,12 +716,12 @@ def run_attention(args, w):
     flops = w.flops()
     value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
     avg_launch_ms = statistics.mean(per_launch_ms)
-    tensor_peak, _, src = read_peaks()
+    tensor_peak, _, src = read_peaks(elapsed_ms * 1e-3)
     achieved = flops / (avg_launch_ms * 1e-3) / 1e12
     traffic = committed_traffic(w.name, ATTN_SOURCES)
     roof = {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
             "frac": achieved / tensor_peak, "traffic": traffic,
-            "peak_source": f"{src} (bf16 burst x fp16/bf16 ratio {FP16_PER_BF16})",
+            "peak_source": f"{src} (x fp16/bf16 ratio {FP16_PER_BF16})",
             "kernel": attn_kernel_name(w, props.multi_processor_count), "avg_launch_ms": avg_launch_ms}
 
     # ---- end to end: pinned host Q, K, V in and O out through the C ABI every step

@@ -18,14 +18,14 @@ import workloads    # noqa: E402
 
 
 def fixed_peaks(monkeypatch, tflops=2000.0, gbs=8000.0):
-    monkeypatch.setattr(bench, "read_peaks", lambda: (tflops, gbs, "test"))
+    monkeypatch.setattr(bench, "read_peaks", lambda window_s=0.0: (tflops, gbs, "test"))
 
 
 def test_roofline_tensor_bound_square(monkeypatch):
     fixed_peaks(monkeypatch)
     w = workloads.WORKLOADS["fused8192"]
     ms = 0.55
-    r = bench.roofline(w, ms, None, {"path": 2, "stages": 3, "tile_m": 256, "tile_n": 256})
+    r = bench.roofline(w, ms, None, {"path": 2, "stages": 3, "tile_m": 256, "tile_n": 256}, 0.01)
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
     assert r["achieved"] == pytest.approx(2 * 8192 ** 3 / (ms * 1e-3) / 1e12)
     assert r["frac"] == pytest.approx(r["achieved"] / 2000.0)
@@ -37,7 +37,7 @@ def test_roofline_hbm_bound_skinny(monkeypatch):
     fixed_peaks(monkeypatch)
     w = workloads.WORKLOADS["skinny16x8192x8192"]
     ms = 0.03
-    r = bench.roofline(w, ms, 1.0e8, {"path": 3, "stages": 12, "tile_m": 16, "tile_n": 128})
+    r = bench.roofline(w, ms, 1.0e8, {"path": 3, "stages": 12, "tile_m": 16, "tile_n": 128}, 0.01)
     assert r["bound"] == "hbm" and r["unit"] == "GB/s"
     assert r["achieved"] == pytest.approx(w.alg_bytes() / (ms * 1e-3) / 1e9)
     assert r["frac"] == pytest.approx(r["achieved"] / 8000.0)
@@ -47,10 +47,18 @@ def test_roofline_hbm_bound_skinny(monkeypatch):
 def test_read_peaks_falls_back_without_measurements(monkeypatch, tmp_path):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     tf, gb, src = bench.read_peaks()
-    assert src == "fallback" and tf == bench.FALLBACK_TENSOR_TFLOPS and gb == bench.FALLBACK_HBM_GBS
-    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"bf16_tflops": 1900.0, "hbm_gbs": 7000.0}))
+    assert src == "fallback burst" and tf == bench.FALLBACK_TENSOR_TFLOPS and gb == bench.FALLBACK_HBM_GBS
+    tf, gb, src = bench.read_peaks(bench.SUSTAINED_WINDOW_S)
+    assert src == "fallback sustained" and tf == bench.FALLBACK_TENSOR_SUSTAINED_TFLOPS
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                                                              "hbm_gbs": 7000.0}))
     tf, gb, src = bench.read_peaks()
-    assert src == "measured" and tf == pytest.approx(1900.0 * bench.FP16_PER_BF16) and gb == 7000.0
+    assert src == "measured bf16 burst" and tf == pytest.approx(1900.0 * bench.FP16_PER_BF16) and gb == 7000.0
+    # a timed window long enough to run under the power cap: the sustained peak
+    tf, gb, src = bench.read_peaks(0.7)
+    assert src == "measured bf16 sustained" and tf == pytest.approx(1700.0 * bench.FP16_PER_BF16)
+    tf, _, _ = bench.read_peaks(0.012)
+    assert tf == pytest.approx(1900.0 * bench.FP16_PER_BF16)
 
 
 def test_committed_traffic_only_for_the_profiled_sources(monkeypatch, tmp_path):
