@@ -281,7 +281,7 @@ int gemm_f16_selftest_timeout(void* cuda_stream, uint32_t timeout_us);
 
 /*
  * gemm_f16_noalloc -- the same operation as gemm_f16, for callers that must
- * not allocate device memory.  The paper has no counterpart; this entry
+ * not allocate device memory.  The tutorial pages have no counterpart; this entry
  * point exists for the library's users.
  *
  * Who needs it: code that runs inside a host framework which owns the
