@@ -10,8 +10,12 @@ drawn over those dimensions, and eight causal ones aimed at the two-tile path,
 exercise the combinations a fixed list misses.
 Bar: the oracle.compare tolerance on sampled rows (each head's first and last
 query tile rows and a seeded sample), and every output row written (O starts
-as NaN).  Inputs: seeded normal fp16 Q, K, V.
+as NaN).  Inputs: seeded normal fp16 Q, K, V.  RANDOM_ATTN_PROBLEMS and
+RANDOM_SEED in the environment draw a longer or different sample (a soak run);
+the defaults are 40 + 8 problems from seed 2024.
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -20,7 +24,8 @@ from oracle.compare import parity
 pytestmark = pytest.mark.gpu
 
 
-def problems(count=40, seed=2024):
+def problems(count=int(os.environ.get("RANDOM_ATTN_PROBLEMS", "40")),
+             seed=int(os.environ.get("RANDOM_SEED", "2024"))):
     rng = np.random.default_rng(seed)
     out = []
     for _ in range(count):

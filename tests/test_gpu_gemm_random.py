@@ -10,7 +10,11 @@ padded pitch, or stored transposed), C pitches and the six epilogues exercise
 the combinations a fixed list misses.  Bar: the oracle.compare tolerance on
 sampled elements (2048 seeded positions and the first and last row and column).
 Inputs: A ~ U(-1, 1), B ~ N(0, 1) / sqrt(K), bias ~ N(0, 1), seeded.
+RANDOM_GEMM_PROBLEMS and RANDOM_SEED in the environment draw a longer or
+different sample (a soak run); the defaults are 40 problems from seed 7.
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -21,7 +25,8 @@ pytestmark = pytest.mark.gpu
 EPILOGUES = ["none", "bias", "bias_relu", "bias_gelu_erf", "bias_sigmoid", "bias_gelu_tanh"]
 
 
-def problems(count=40, seed=7):
+def problems(count=int(os.environ.get("RANDOM_GEMM_PROBLEMS", "40")),
+             seed=int(os.environ.get("RANDOM_SEED", "7"))):
     rng = np.random.default_rng(seed)
     out = []
     for _ in range(count):
