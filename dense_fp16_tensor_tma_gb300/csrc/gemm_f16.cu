@@ -1049,7 +1049,14 @@ int gemm_f16_grouped(const gemm_f16_problem_t* problems, int count, int epilogue
     auto flush = [&]() -> int {
         if (gp.count == 0) return GEMM_OK;
         const int tiles = gp.tile_start[gp.count];
-        const int ctas = 2 * std::min(tiles, std::max(1, ds.pair_clusters));
+        const int G = std::max(1, ds.pair_clusters);
+        // a partial last wave of R tiles (R <= G/2) runs as 2R half tiles, as
+        // for one problem
+        const int R = tiles % G;
+        const bool halves = R > 0 && 2 * R <= G;
+        gp.dp_tiles = halves ? tiles - R : tiles;
+        gp.tail_split = halves ? 1 : 0;
+        const int ctas = 2 * std::min(gp.dp_tiles + (halves ? 2 * R : 0), G);
         const int r = launch_grouped(gp, ctas, s);
         gp.count = 0;
         return r;

@@ -383,8 +383,10 @@ struct PairJob {
 
 // Independent problems of one grouped launch (at most kMaxGroupProblems, all
 // with the same epilogue and operand layouts), passed by value as the kernel
-// parameter: their tensor maps, their GemmParams, and the prefix sums of
-// their 256 x 256 tile counts.
+// parameter: their tensor maps, their GemmParams, the prefix sums of their
+// 256 x 256 tile counts, and how the concatenated tiles split into whole
+// tiles and half tiles (as for one problem: the tiles from dp_tiles on run as
+// two 256 x 128 halves when tail_split is set).
 constexpr int kMaxGroupProblems = 64;
 struct GroupedParams {
     CUtensorMap tmA[kMaxGroupProblems];
@@ -392,27 +394,44 @@ struct GroupedParams {
     GemmParams prob[kMaxGroupProblems];
     int tile_start[kMaxGroupProblems + 1];
     int count;
+    int dp_tiles;
+    int tail_split;
 };
 
 // Work source of a grouped launch: the concatenated tile lists of all
-// problems, strided over the CTA pairs (whole tiles only).
+// problems, strided over the CTA pairs, whole tiles below dp_tiles and then
+// (tail_split) half tiles of the rest, in the order PairUnitIter gives one
+// problem's units.  Tile indices only grow along the sequence, so the
+// problem of each is found by a forward scan of the prefix sums.
 struct GroupedPairSource {
     const GroupedParams* gp;
-    int t, G, g;
-    __device__ GroupedPairSource(const GroupedParams* gp_, int cid, int G_) : gp(gp_), t(cid), G(G_), g(0) {}
+    int t, u, G, g, halves;
+    __device__ GroupedPairSource(const GroupedParams* gp_, int cid, int G_)
+        : gp(gp_), t(cid), u(cid), G(G_), g(0),
+          halves(gp_->tail_split ? 2 * (gp_->tile_start[gp_->count] - gp_->dp_tiles) : 0) {}
     __device__ bool next(PairJob& j) {
-        if (t >= gp->tile_start[gp->count]) return false;
-        while (t >= gp->tile_start[g + 1]) ++g;
+        int tile, half;
+        if (t < gp->dp_tiles) {
+            tile = t;
+            half = -1;
+            t += G;
+        } else if (u < halves) {
+            tile = gp->dp_tiles + (u >> 1);
+            half = u & 1;
+            u += G;
+        } else {
+            return false;
+        }
+        while (tile >= gp->tile_start[g + 1]) ++g;
         const GemmParams& q = gp->prob[g];
-        const TileCoord tc = tile_coord_bm(t - gp->tile_start[g], (q.M + 255) / 256, (q.N + 255) / 256, q.group_m,
+        const TileCoord tc = tile_coord_bm(tile - gp->tile_start[g], (q.M + 255) / 256, (q.N + 255) / 256, q.group_m,
                                            256, 256);
         j.tmA = &gp->tmA[g];
         j.tmB = &gp->tmB[g];
         j.prob = g;
         j.m0 = tc.m0;
         j.n0 = tc.n0;
-        j.half = -1;
-        t += G;
+        j.half = half;
         return true;
     }
     __device__ const GemmParams& params(int g) const { return gp->prob[g]; }

@@ -144,7 +144,8 @@ typedef struct gemm_f16_problem {
  * argument error returns before anything is enqueued.  Problems with M or N
  * of 0 are skipped; K == 0 problems get C_g = epilogue(bias_g).  The tiles of
  * all problems (256 x 256, CTA pairs) are scheduled together, up to 64
- * problems per launch (more take further launches on the same stream).
+ * problems per launch (more take further launches on the same stream); a
+ * partial last wave of at most half the pairs runs as 256 x 128 half tiles.
  * Problems must not write each other's C or read another problem's C.
  * No counterpart beyond the name on the pages; the numerics are gemm_f16's.
  */

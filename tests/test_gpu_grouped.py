@@ -82,6 +82,19 @@ def test_grouped_random_every_epilogue(g, torch_dev, oracle_mod, epi):
         assert res["ok"], f"problem {i} {shapes[i]} {epi}: {res}"
 
 
+@pytest.mark.parametrize("layout", ["nn", "tt"])
+def test_grouped_whole_and_half_tiles(g, torch_dev, oracle_mod, layout):
+    # 100 tiles of 256 x 256 over ten problems: with 76 CTA pairs (152 SMs)
+    # the first 76 run whole and the last 24 as 48 halves of 256 x 128, the
+    # halves spanning three problems; integer operands, so bit-exact
+    rng = np.random.default_rng(66)
+    shapes = [(512, 1280, 64)] * 7 + [(300, 1100, 72), (512, 1280, 64), (257, 1203, 64)]
+    probs = [(ints(rng, (M, K)), ints(rng, (K, N)), ints(rng, N, -8, 9)) for M, N, K in shapes]
+    got = run_grouped(g, torch_dev, probs, "bias", layout)
+    for i, (c, r) in enumerate(zip(got, oracle_mod.gemm_grouped(probs, "bias"))):
+        assert np.array_equal(c, r), f"problem {i} {shapes[i]} {layout}"
+
+
 def test_grouped_k_zero_and_repacked_operands(g, torch_dev, oracle_mod):
     rng = np.random.default_rng(61)
     shapes = [(100, 60, 0), (300, 1003, 136), (257, 300, 61), (64, 64, 64)]   # K=0; N % 8; K % 8
