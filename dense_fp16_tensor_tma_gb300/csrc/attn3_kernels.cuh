@@ -327,18 +327,8 @@ attn_f16_fwd3_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 // the row's 128 scores of the block into registers; then the score
                 // buffer is free for the next block's S
                 uint32_t v[128];
-                uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(v);
-                uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 32);
-                uint32_t (&v2)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 64);
-                uint32_t (&v3)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 96);
-                tmem_ld_32x32b_x32(s_cols, v0);
-                tmem_ld_32x32b_x32(s_cols + 32u, v1);
-                tmem_ld_32x32b_x32(s_cols + 64u, v2);
-                tmem_ld_32x32b_x32(s_cols + 96u, v3);
-                tmem_wait_ld(v0);
-                tmem_wait_ld(v1);
-                tmem_wait_ld(v2);
-                tmem_wait_ld(v3);
+                tmem_ld_32x32b_x128(s_cols, v);   // one load: four 32-column loads took longer
+                tmem_wait_ld(v);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(s_free(t));
@@ -422,11 +412,8 @@ attn_f16_fwd3_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             uint32_t w[D];
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c)
-                tmem_ld_32x32b_x32(o_cols + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(w + 32 * c));
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(w + 32 * c));
+            tmem_ld_row<D>(o_cols, w);
+            tmem_wait_ld(w);
             tc_fence_before();           // O read before this warp's next p_full arrival
             const float inv = 1.0f / l;
             if (q < p.S) {
