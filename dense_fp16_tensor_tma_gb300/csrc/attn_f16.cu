@@ -32,6 +32,21 @@
 #ifndef ATTN_SPLIT_P
 #define ATTN_SPLIT_P 1   // D = 64: the two-tile kernel with P buffers of its own (attn_f16_fwd3_kernel)
 #endif
+// Routing costs (see plan_attention): a causal key block of the two-tile kernels
+// in percent of the one-tile kernel's, and a tile of the one-tile kernel in
+// thousandths of a two-tile unit, at D = 128 and D = 64
+#ifndef ATTN_CAUSAL_PCT_D128
+#define ATTN_CAUSAL_PCT_D128 89
+#endif
+#ifndef ATTN_CAUSAL_PCT_D64
+#define ATTN_CAUSAL_PCT_D64 73
+#endif
+#ifndef ATTN_ODD_TILE_MILLI_D128
+#define ATTN_ODD_TILE_MILLI_D128 525
+#endif
+#ifndef ATTN_ODD_TILE_MILLI_D64
+#define ATTN_ODD_TILE_MILLI_D64 640
+#endif
 
 namespace {
 
@@ -172,23 +187,22 @@ AttnPlan plan_attention(int64_t B, int64_t H, int64_t nq, int64_t D, bool causal
     // 8 tiles per head (4x32x1024: 687 against 627 at D = 128, 574 against 414
     // at D = 64), with at least one step per SM, and only where the busiest
     // CTA's steps cost less than its share of the one-tile kernel's units.  A
-    // key block of the two-tile kernels took 0.92 (D = 128) and 0.75 (D = 64)
-    // of the one-tile kernel's time where both split evenly (4x32x4096 413.1
-    // against 450.7 us and 285.5 against 391.1 us, 1x32x16384 0.94 and 0.75);
-    // 4x32x2048x128 (512 steps: 4 on some CTAs, against 7 units) ran 984
-    // against 999.  Otherwise one tile per CTA.
+    // key block of the two-tile kernels takes 0.89 (D = 128) and 0.73 (D = 64)
+    // of the one-tile kernel's time, fitted to same-box A/B runs of both
+    // kernels forced in turn (D = 128: 4x32x3072 1183 against 1149 TFLOP/s,
+    // 2x32x3072 1162 against 1068, 8x16x1536 933 against 844, 4x32x2048 1059
+    // against 1055, which the rule leaves to the one-tile kernel; D = 64:
+    // 4x32x3072 828 against 671, 4x32x2048 749 against 622, 2x32x1500 473
+    // against 454).  Otherwise one tile per CTA.
     // Non-causal with an odd number of tiles per head (at least 3): pairs of a
     // head's tiles and its last tile alone, where the busiest CTA's units cost
     // less than the one-tile kernel's tiles.  Costs in pair units: a one-tile
-    // unit of the two-tile kernels 0.6, a tile of the one-tile kernel 0.51 at
-    // D = 128 and 0.654 at D = 64, fitted to same-box A/B runs: at D = 64 the
-    // two-tile kernel won on every odd shape tried (8x16x1300 551 -> 670
-    // TFLOP/s, 4x16x2100 622 -> 808, 4x32x300 215 -> 244, 2x32x513 235 -> 267);
-    // at D = 128 on 17 tiles per head (4x16x2100 1071 -> 1133) but not on 11
-    // (8x16x1300 927 against 880, 16x16x1300 980 against 959), where the
-    // model now keeps the one-tile kernel.  The number of pairs taken (all of
-    // them, or one of the last three whole rounds over the CTAs) is the one that
-    // leaves the busiest CTA the least work.
+    // unit of the two-tile kernels 0.6, a tile of the one-tile kernel 0.525 at
+    // D = 128 and 0.64 at D = 64, fitted to the same runs (D = 128: 4x16x2100
+    // 1225 against 1143, 16x16x1300 1014 against 999, 8x16x1300 988 against
+    // 986; D = 64: 8x16x1300 703 against 575, 4x32x300 251 against 214).  The
+    // number of pairs taken (all of them, or one of the last three whole rounds
+    // over the CTAs) is the one that leaves the busiest CTA the least work.
     const int64_t tiles_all = B * H * nq;
     const int64_t head_pairs = B * H * (nq / 2);
     // the busiest CTA's cost with p pair units first and then s one-tile units,
@@ -217,12 +231,13 @@ AttnPlan plan_attention(int64_t B, int64_t H, int64_t nq, int64_t D, bool causal
             }
         }
         const int64_t one_tile = (tiles_all + sms - 1) / sms;
-        odd_two = best < static_cast<double>(one_tile) * (D == 64 ? 0.654 : 0.51);
+        odd_two = best < static_cast<double>(one_tile) *
+                             (D == 64 ? ATTN_ODD_TILE_MILLI_D64 : ATTN_ODD_TILE_MILLI_D128) / 1000.0;
     }
     const int64_t causal_steps = B * H * (nq / 4);
     const int64_t steps_busiest = (causal_steps + sms - 1) / sms;
     const int64_t units1_busiest = (2 * causal_steps + sms - 1) / sms;
-    const int64_t block_cost_pct = D == 64 ? 75 : 92;
+    const int64_t block_cost_pct = D == 64 ? ATTN_CAUSAL_PCT_D64 : ATTN_CAUSAL_PCT_D128;
     const bool two_tiles = ATTN_PINGPONG &&
                            (causal ? (ATTN_CAUSAL_PAIRS && nq % 4 == 0 && nq >= ATTN_CAUSAL_MIN_TILES &&
                                       causal_steps >= static_cast<int64_t>(sms) &&

@@ -28,13 +28,14 @@ def plan(B, H, S, D, causal, sms=152):
     (4, 32, 4096, 64, True, TWO64),
     (4, 32, 1024, 128, True, TWO128),      # 8 tiles per head (687 against 627 TFLOP/s)
     (4, 32, 1792, 128, True, ONE),         # 14 tiles: an odd pair count (827 against 935)
-    (4, 32, 2048, 128, True, ONE),         # 512 steps split unevenly (984 against 999)
-    (2, 32, 1500, 64, True, ONE),          # 192 steps: two on some CTAs against three units
+    (4, 32, 2048, 128, True, ONE),         # 512 steps split unevenly (1059 against 1055: a tie)
+    (4, 32, 3072, 128, True, TWO128),      # 768 steps (1183 against 1149)
+    (2, 32, 1500, 64, True, TWO64),        # 192 steps: two on some CTAs against three units (473 against 454)
     (4, 32, 512, 128, True, ONE),          # 4 tiles per head: below the minimum of 8
-    (8, 16, 1300, 64, False, TWO64),       # odd tiles at D = 64 (551 -> 670)
-    (4, 16, 2100, 128, False, TWO128),     # 17 tiles at D = 128 (1071 -> 1133)
-    (8, 16, 1300, 128, False, ONE),        # 11 tiles at D = 128 (927 against 880)
-    (16, 16, 1300, 128, False, ONE),       # (980 against 959)
+    (8, 16, 1300, 64, False, TWO64),       # odd tiles at D = 64 (703 against 575)
+    (4, 16, 2100, 128, False, TWO128),     # 17 tiles at D = 128 (1225 against 1143)
+    (8, 16, 1300, 128, False, TWO128),     # 11 tiles at D = 128 (988 against 986)
+    (16, 16, 1300, 128, False, TWO128),    # (1014 against 999)
     (2, 3, 100, 64, False, ONE),           # one tile per head
 ])
 def test_measured_routing(B, H, S, D, causal, kernel):
