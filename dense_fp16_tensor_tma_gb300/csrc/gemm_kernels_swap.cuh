@@ -35,6 +35,47 @@ namespace gemm_f16_dev {
 
 constexpr int kSwapThreads = 192;   // producer, MMA, 4 epilogue warps
 
+// The 64 accumulator columns of this thread's TMEM lane in one load, and its
+// wait (the registers as read-write operands: no use is scheduled before it).
+__device__ __forceinline__ void swap_tmem_ld_x64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
+        "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+        "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63"
+        "}, [%64];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void swap_tmem_wait_ld_x64(uint32_t (&r)[64]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+          "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+          "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+          "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]),
+          "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]),
+          "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]),
+          "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]),
+          "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63]) : : "memory");
+}
+// This thread's MT accumulator columns in one load (MT / 16 loads, each waited
+// for in turn, measured the same or up to 4 % slower: 48x4096x4096 20.4 -> 19.5 us).
+template <int MT>
+__device__ __forceinline__ void swap_ld_acc(uint32_t taddr, uint32_t (&r)[MT]) {
+    if constexpr (MT == 16) tmem_ld_32x32b_x16(taddr, r);
+    else if constexpr (MT == 32) tmem_ld_32x32b_x32(taddr, r);
+    else swap_tmem_ld_x64(taddr, r);
+    if constexpr (MT == 64) swap_tmem_wait_ld_x64(r);
+    else tmem_wait_ld(r);
+}
+
 template <int MT, int STAGES>
 struct SmemPlanSwap {
     static constexpr uint32_t kBtBytes = 2 * kBBoxBytes;       // 128 columns of B x 64 K
@@ -227,13 +268,11 @@ gemm_f16_swap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             tc_fence_after();
             const uint32_t t_base = tmem_base + static_cast<uint32_t>(acc * MT) + (static_cast<uint32_t>(32 * q) << 16);
             float v[MT];
+            {
+                uint32_t r[MT];
+                swap_ld_acc<MT>(t_base, r);
 #pragma unroll
-            for (int j = 0; j < MT / 16; ++j) {
-                uint32_t r[16];
-                tmem_ld_32x32b_x16(t_base + 16u * j, r);
-                tmem_wait_ld(r);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[16 * j + i] = __uint_as_float(r[i]);
+                for (int i = 0; i < MT; ++i) v[i] = __uint_as_float(r[i]);
             }
             // the accumulator is in registers now: hand the TMEM buffer back
             tc_fence_before();
