@@ -437,21 +437,29 @@ attn_f16_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 // 128) its sum over the fp16 values the tensor core multiplies
                 const float mm = (m_new == -INFINITY) ? 0.0f : m_new;
                 float rs0 = 0.0f, rs1 = 0.0f;
+                // P written 32 columns (keys 64 c2 ..) at a time: one 64-column store
+                // after the whole pass measured 1 % faster non-causal and 3 % slower
+                // causal, four 16-column stores 1-2 % slower than this
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t h[16];
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t h2[32];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float2 xs = fma2_bc(__uint_as_float(v[32 * c + 2 * i]), __uint_as_float(v[32 * c + 2 * i + 1]),
-                                                  p.scale_log2, -mm);
-                        const __half2 hv = __floats2half2_rn(fast_exp2(xs.x), fast_exp2(xs.y));
-                        h[i] = *reinterpret_cast<const uint32_t*>(&hv);
-                        if constexpr (!kSumByMma) {
-                            if (i & 1) rs1 = add_f16x2_to_f32(rs1, h[i]);
-                            else rs0 = add_f16x2_to_f32(rs0, h[i]);
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c = 2 * c2 + cc;
+                        uint32_t (&h)[16] = *reinterpret_cast<uint32_t(*)[16]>(h2 + 16 * cc);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float2 xs = fma2_bc(__uint_as_float(v[32 * c + 2 * i]),
+                                                      __uint_as_float(v[32 * c + 2 * i + 1]), p.scale_log2, -mm);
+                            const __half2 hv = __floats2half2_rn(fast_exp2(xs.x), fast_exp2(xs.y));
+                            h[i] = *reinterpret_cast<const uint32_t*>(&hv);
+                            if constexpr (!kSumByMma) {
+                                if (i & 1) rs1 = add_f16x2_to_f32(rs1, h[i]);
+                                else rs0 = add_f16x2_to_f32(rs0, h[i]);
+                            }
                         }
                     }
-                    tmem_st_32x32b_x16(s_cols + 16u * c, h);
+                    tmem_st_32x32b_x32(s_cols + 32u * c2, h2);
                 }
                 // O rescaled (a raise needs an earlier block of the unit) after the
                 // tile's previous P V has completed
